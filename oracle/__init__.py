@@ -1,0 +1,185 @@
+"""The oracle: a plain, slow, single-threaded CPU reference of the ops, in C
+(``oracle.c``), loaded through ctypes.
+
+TEST INFRASTRUCTURE.  Only ``tests/``, the ``smoke()`` check in
+``__graft_entry__.py`` and the ``cpu_baseline`` leg (and ``--impl reference``
+arm) of ``bench.py`` may import this package.  The product path never does,
+and it shares no code with the CUDA sources.
+
+Every function takes and returns numpy arrays: f32 inputs as ``float32``;
+bf16 data is widened with :func:`bf16_widen` first and the f32 results are
+rounded with :func:`bf16_round` where a test needs storage bits.  Each op is
+the definition the pages give, written out step by step in f32; the
+citations sit beside each function in ``oracle.c``.
+
+``Oracle(mutant=k)`` loads a build with the k-th planted mistake of the
+pages' pitfalls table (s01..s15), so tests can show that the pins reject it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math"]
+_lock = threading.Lock()
+_cache: dict[int, "Oracle"] = {}
+
+
+class OracleError(ValueError):
+    pass
+
+
+def lib_path(mutant: int = 0) -> str:
+    return os.path.join(_HERE, "liboracle.so" if mutant == 0 else f"liboracle_m{mutant:02d}.so")
+
+
+def build(mutant: int = 0, force: bool = False) -> str:
+    path = lib_path(mutant)
+    stale = (not os.path.exists(path)) or os.path.getmtime(path) < os.path.getmtime(_SRC)
+    if force or stale:
+        flags = list(CFLAGS) + ([f"-DORACLE_MUTANT={mutant}"] if mutant else [])
+        tmp = path + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", *flags, "-o", tmp, _SRC, "-lm"], check=True)
+        os.replace(tmp, path)
+    return path
+
+
+def _f32(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.float32)
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data
+
+
+class Oracle:
+    def __init__(self, mutant: int = 0):
+        self.mutant = mutant
+        lib = ctypes.CDLL(build(mutant))
+        i64, f32, vp, i32 = ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_int
+        sig = {
+            "orc_rmsnorm": [vp, vp, vp, i64, i64, f32],
+            "orc_add": [vp, vp, vp, i64],
+            "orc_add_rmsnorm": [vp, vp, vp, vp, vp, i64, i64, f32, i32],
+            "orc_rope": [vp, vp, vp, i64, i64, i64, i64, vp, f32, i32],
+            "orc_silu_mul": [vp, vp, vp, i64],
+            "orc_embedding": [vp, vp, vp, i64, i64, i64],
+            "orc_argmax": [vp, i64],
+            "orc_argmax_rows": [vp, vp, i64, i64],
+            "orc_bf16_widen": [vp, vp, i64],
+            "orc_bf16_round": [vp, vp, i64],
+            "orc_mutant": [],
+        }
+        for name, args in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_int32 if name == "orc_argmax" else (
+                None if name.startswith("orc_bf16") else ctypes.c_int)
+        assert lib.orc_mutant() == mutant
+        self.lib = lib
+
+    @staticmethod
+    def _check(st: int, what: str):
+        if st != 0:
+            raise OracleError(f"{what}: oracle status {st}")
+
+    # -- storage -------------------------------------------------------------
+    def bf16_widen(self, bits: np.ndarray) -> np.ndarray:
+        bits = np.ascontiguousarray(bits, dtype=np.uint16)
+        out = np.empty(bits.shape, dtype=np.float32)
+        self.lib.orc_bf16_widen(_ptr(bits), _ptr(out), bits.size)
+        return out
+
+    def bf16_round(self, x: np.ndarray) -> np.ndarray:
+        x = _f32(x)
+        out = np.empty(x.shape, dtype=np.uint16)
+        self.lib.orc_bf16_round(_ptr(x), _ptr(out), x.size)
+        return out
+
+    # -- ops -------------------------------------------------------------------
+    def rmsnorm(self, x, w, eps: float, out: np.ndarray | None = None) -> np.ndarray:
+        x, w = _f32(x), _f32(w)
+        d = x.shape[-1]
+        rows = x.size // d if d else 0
+        if w.size != d:
+            raise OracleError("rmsnorm: w must have d entries")
+        y = np.empty_like(x) if out is None else out
+        self._check(self.lib.orc_rmsnorm(_ptr(x), _ptr(w), _ptr(y), rows, d, eps), "rmsnorm")
+        return y
+
+    def add(self, a, b) -> np.ndarray:
+        a, b = _f32(a), _f32(b)
+        if a.shape != b.shape:
+            raise OracleError("add: shapes differ")
+        y = np.empty_like(a)
+        self._check(self.lib.orc_add(_ptr(a), _ptr(b), _ptr(y), a.size), "add")
+        return y
+
+    def add_rmsnorm(self, x, residual, w, eps: float, h_bf16: bool = False):
+        x, r, w = _f32(x), _f32(residual), _f32(w)
+        d = x.shape[-1]
+        y = np.empty_like(x)
+        h = np.empty_like(x)
+        self._check(self.lib.orc_add_rmsnorm(_ptr(x), _ptr(r), _ptr(w), _ptr(y), _ptr(h),
+                                             x.size // d, d, eps, int(h_bf16)), "add_rmsnorm")
+        return y, h
+
+    def rope(self, x, pos, inv_freq, r: int, mu: float, layout: int,
+             in_place: bool = False) -> np.ndarray:
+        x = _f32(x) if not in_place else x
+        if in_place and (x.dtype != np.float32 or not x.flags.c_contiguous):
+            raise OracleError("rope in place needs a contiguous float32 array")
+        T, H, D = x.shape
+        pos = np.ascontiguousarray(pos, dtype=np.int32)
+        om = _f32(inv_freq)
+        if pos.size != T or om.size < r // 2:
+            raise OracleError("rope: pos needs T entries and inv_freq r/2")
+        y = x if in_place else np.empty_like(x)
+        self._check(self.lib.orc_rope(_ptr(x), _ptr(y), _ptr(pos), T, H, D, r, _ptr(om), mu,
+                                      layout), "rope")
+        return y
+
+    def silu_mul(self, gate, up) -> np.ndarray:
+        g, u = _f32(gate), _f32(up)
+        y = np.empty_like(g)
+        self._check(self.lib.orc_silu_mul(_ptr(g), _ptr(u), _ptr(y), g.size), "silu_mul")
+        return y
+
+    def embedding(self, table, ids) -> np.ndarray:
+        table = _f32(table)
+        V, d = table.shape
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        out = np.empty((ids.size, d), dtype=np.float32)
+        self._check(self.lib.orc_embedding(_ptr(table), _ptr(ids), _ptr(out), ids.size, d, V),
+                    "embedding")
+        return out
+
+    def argmax(self, x) -> np.ndarray:
+        x = _f32(x)
+        if x.ndim == 1:
+            x = x.reshape(1, -1)
+        rows, n = x.shape
+        out = np.empty(rows, dtype=np.int32)
+        st = self.lib.orc_argmax_rows(_ptr(x), _ptr(out), rows, n)
+        if st == -3:
+            raise OracleError("argmax: empty row")
+        self._check(st, "argmax")
+        return out
+
+    def argmax_one(self, x) -> int:
+        """The pages' single-row routine as written, -1 for an empty row too."""
+        x = _f32(x).reshape(-1)
+        return int(self.lib.orc_argmax(_ptr(x), x.size))
+
+
+def get(mutant: int = 0) -> Oracle:
+    with _lock:
+        if mutant not in _cache:
+            _cache[mutant] = Oracle(mutant)
+        return _cache[mutant]

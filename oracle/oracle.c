@@ -1,0 +1,257 @@
+/*
+ * oracle.c -- the plain, slow, single-threaded CPU reference of the
+ * elementwise and row-wise transformer ops.
+ *
+ * TEST INFRASTRUCTURE.  Only the tests, the smoke check of the package entry
+ * file and the CPU-baseline leg of bench.py may load or run this code.  The
+ * product (the CUDA library and its Python binding) never calls it and
+ * shares no code with it: nothing here is included by, or includes, the CUDA
+ * sources.
+ *
+ * What it follows.  The two pages define every op in f32:
+ *   [Ops]  "Operations" (glia runtime spec): section 1 (Argmax, Add),
+ *          section 2 (RmsNorm), section 3 (Rope, TokenEmbed), section 4
+ *          (Silu), section 10 (FusedSkipNorm).  Its CPU reference computes
+ *          everything in f32.
+ *   [L9.6] "Elementwise kernels in C: RMSNorm, RoPE, SiLU-mul, embedding,
+ *          add, argmax": section 2 (principles and the symbol table),
+ *          section 2.1 to 2.4, section 3 (worked examples), section 4 (the
+ *          interface), section 5 (pitfalls).
+ * Each op is written as those sections define it, one operation at a time in
+ * the order they state.  The file is compiled with -ffp-contract=off and
+ * without fast-math, so every + - * / rounds on its own in f32, exactly as
+ * written.  Where the pages leave a step open the reading taken is named in
+ * the function's comment.
+ *
+ * Planted mistakes.  Building with -DORACLE_MUTANT=k (1..15) swaps in the
+ * k-th wrong variant of the pitfalls table of [L9.6] section 5 (s01..s15).
+ * The tests build those variants on the CPU to show that their pins reject
+ * each one.  A normal build (ORACLE_MUTANT undefined) contains none of them.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#ifndef ORACLE_MUTANT
+#define ORACLE_MUTANT 0
+#endif
+#define MUT(k) (ORACLE_MUTANT == (k))
+
+enum { ORC_OK = 0, ORC_ERR_ARG = -1, ORC_ERR_ID = -2, ORC_ERR_EMPTY = -3 };
+
+int orc_mutant(void) { return ORACLE_MUTANT; }
+
+/* ---- bf16 storage ----------------------------------------------------------
+ * bf16 is the top half of an f32.  Widening is exact (bits << 16); narrowing
+ * rounds to nearest, ties to even, and keeps NaN a (quiet) NaN.            */
+
+void orc_bf16_widen(const uint16_t *in, float *out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) {
+        uint32_t u = (uint32_t)in[i] << 16;
+        memcpy(&out[i], &u, 4);
+    }
+}
+
+static uint16_t orc_round_one(float f) {
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if ((u & 0x7FFFFFFFu) > 0x7F800000u) return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t keep = u >> 16, rest = u & 0xFFFFu;
+    if (rest > 0x8000u || (rest == 0x8000u && (keep & 1u))) keep += 1u;
+    return (uint16_t)keep;
+}
+
+void orc_bf16_round(const float *in, uint16_t *out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_round_one(in[i]);
+}
+
+/* ---- RMSNorm ---------------------------------------------------------------
+ * [L9.6] 2.1 and [Ops] 2: y_i = x_i / sqrt(mean(x^2) + eps) * w_i over one row,
+ * eps inside the root.  Per row: sum the squares in f32 in increasing i, divide
+ * by d, add eps, take the root, invert, then write x_i * inv * w_i.
+ * Readings: [Ops] writes (x / rms) * g while [L9.6] writes x * inv * w; the
+ * latter is taken.  [L9.6] inverts with the course's own Newton rsqrt, which
+ * the pages do not specify; here 1 / sqrtf, both correctly rounded.
+ * y may be x: a row's sum is complete before its first write.                */
+int orc_rmsnorm(const float *x, const float *w, float *y, int64_t rows, int64_t d, float eps) {
+    if (rows < 0 || d <= 0) return ORC_ERR_ARG;
+#if ORACLE_MUTANT == 15
+    float ss = 0.0f; /* s15: one sum for the whole call instead of one per row */
+#endif
+    for (int64_t r = 0; r < rows; ++r) {
+        const float *xr = x + r * d;
+        float *yr = y + r * d;
+#if ORACLE_MUTANT != 15
+        float ss = 0.0f;
+#endif
+        for (int64_t i = 0; i < d; ++i) {
+            float sq = xr[i] * xr[i];
+            ss = ss + sq;
+        }
+        float ms = MUT(2) ? ss : ss / (float)d;      /* s02: no division by d */
+        float inv;
+        if (MUT(1))
+            inv = 1.0f / (sqrtf(ms) + eps);            /* s01: eps outside the root */
+        else
+            inv = 1.0f / sqrtf(ms + eps);
+        for (int64_t i = 0; i < d; ++i) {
+            float t = xr[i] * inv;
+            yr[i] = MUT(3) ? t : t * w[i];             /* s03: gain forgotten */
+        }
+    }
+    return ORC_OK;
+}
+
+/* ---- Add -------------------------------------------------------------------
+ * [Ops] 1 (Add) and [L9.6] 2.4: y_i = a_i + b_i, usually in place (y == a).   */
+int orc_add(const float *a, const float *b, float *y, int64_t n) {
+    if (n < 0) return ORC_ERR_ARG;
+    for (int64_t i = 0; i < n; ++i) y[i] = a[i] + b[i];
+    return ORC_OK;
+}
+
+/* ---- Fused residual add + RMSNorm -----------------------------------------
+ * [Ops] 10 (FusedSkipNorm): returns RmsNorm(x + skip) and x + skip, and must
+ * equal the unfused composition.  Reading: the unfused composition stores the
+ * sum in the storage type before the norm reads it, so with h_bf16 != 0 the
+ * sum is rounded to bf16 first and the norm runs on the rounded h.  In f32
+ * the two readings coincide.  h and y are written as f32 values (the caller
+ * rounds them to bf16 storage where that applies).                          */
+int orc_add_rmsnorm(const float *x, const float *res, const float *w, float *y, float *h,
+                    int64_t rows, int64_t d, float eps, int h_bf16) {
+    if (rows < 0 || d <= 0) return ORC_ERR_ARG;
+    int st = orc_add(x, res, h, rows * d);
+    if (st != ORC_OK) return st;
+    if (h_bf16) {
+        for (int64_t i = 0; i < rows * d; ++i) {
+            uint16_t b = orc_round_one(h[i]);
+            orc_bf16_widen(&b, &h[i], 1);
+        }
+    }
+    return orc_rmsnorm(h, w, y, rows, d, eps);
+}
+
+/* ---- RoPE --------------------------------------------------------------------
+ * [L9.6] 2.2 and 4, [Ops] 3.  x is [T, H, D]; pair i (0 <= i < r/2) of token t
+ * turns by theta = p_t * omega_i:  a' = mu (a cos - b sin),
+ * b' = mu (a sin + b cos).  Layout 0 ("half") pairs entries (i, i + r/2),
+ * layout 1 ("interleaved") pairs (2i, 2i + 1).  Entries r .. D-1 pass through.
+ * The angle is the double product rounded to f32 (equal to the f32 product of
+ * float(p_t) and omega_i below 2^24).  One angle serves every head.  Both
+ * members of a pair are read before either is written, so y may be x.
+ * Readings: the pages do not say how cos and sin are evaluated; here they are
+ * the double cos / sin of the f32 angle, rounded to f32.  mu multiplies the
+ * rotated pair from outside, as the matrix form writes it.                   */
+int orc_rope(const float *x, float *y, const int32_t *pos, int64_t T, int64_t H, int64_t D,
+             int64_t r, const float *inv_freq, float mu, int layout) {
+    if (T < 0 || H < 0 || D <= 0 || r < 0 || r > D || (r & 1) || (layout != 0 && layout != 1))
+        return ORC_ERR_ARG;
+    const int64_t half = r / 2;
+    int64_t npairs = half;
+    if (MUT(7)) npairs = D / 2; /* s07: every entry rotates, tail included */
+    int lay = layout;
+    if (MUT(4)) lay = 1 - layout; /* s04: the two layouts swapped */
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t i = 0; i < npairs; ++i) {
+            int64_t fi = i < half ? i : half - 1; /* s07 keeps its reads inside inv_freq */
+            float theta = (float)((double)pos[t] * (double)inv_freq[fi]);
+            if (MUT(5)) theta = -theta; /* s05: turned the other way */
+            float c = (float)cos((double)theta);
+            float s = (float)sin((double)theta);
+            float m = MUT(8) ? 1.0f : mu; /* s08: attention scaling ignored */
+            int64_t span = MUT(7) ? D / 2 : half;
+            for (int64_t h = 0; h < H; ++h) {
+                const float *xv = x + (t * H + h) * D;
+                float *yv = y + (t * H + h) * D;
+                int64_t ia = lay == 0 ? i : 2 * i;
+                int64_t ib = lay == 0 ? i + span : 2 * i + 1;
+                float a = xv[ia];
+                float b = xv[ib];
+                float ac = a * c, bs = b * s;
+                float a2 = m * (ac - bs);
+                float as, bc;
+                if (MUT(6))
+                    as = a2 * s; /* s06: b' built from the new a' */
+                else
+                    as = a * s;
+                bc = b * c;
+                float b2 = m * (as + bc);
+                yv[ia] = a2;
+                yv[ib] = b2;
+            }
+        }
+        if (y != x && !MUT(7)) {
+            for (int64_t h = 0; h < H; ++h)
+                for (int64_t j = r; j < D; ++j) y[(t * H + h) * D + j] = x[(t * H + h) * D + j];
+        }
+    }
+    return ORC_OK;
+}
+
+/* ---- SiLU-mul ----------------------------------------------------------------
+ * [L9.6] 2.3 and [Ops] 4 (Silu): y = g / (1 + e^-g) * u, silu first, then the
+ * product with u.  Written this way it saturates: for g -> -inf, e^-g
+ * overflows to +inf and the quotient is -0; for g -> +inf the quotient is g.
+ * Reading: libm expf replaces the course's own saturating exp (both overflow
+ * to +inf above about 88.7).                                                  */
+int orc_silu_mul(const float *g, const float *u, float *y, int64_t n) {
+    if (n < 0) return ORC_ERR_ARG;
+    for (int64_t i = 0; i < n; ++i) {
+        float e, silu;
+        if (MUT(10))
+            e = expf(g[i]); /* s10: e^g instead of e^-g */
+        else
+            e = expf(-g[i]);
+        float den = 1.0f + e;
+        if (MUT(9))
+            silu = 1.0f / den; /* s09: the sigmoid alone */
+        else
+            silu = g[i] / den;
+        y[i] = silu * u[i];
+    }
+    return ORC_OK;
+}
+
+/* ---- Embedding ---------------------------------------------------------------
+ * [L9.6] 2.4 and [Ops] 3 (TokenEmbed): out row t is row ids[t] of the [V, d]
+ * table, which starts at element ids[t] * d.  The pages leave the id check to
+ * the caller; the oracle reports an id outside [0, V) as an error.           */
+int orc_embedding(const float *table, const int32_t *ids, float *out, int64_t n, int64_t d,
+                  int64_t V) {
+    if (n < 0 || d <= 0 || V < 0) return ORC_ERR_ARG;
+    for (int64_t t = 0; t < n; ++t) {
+        int64_t id = ids[t];
+        if (id < 0 || id >= V) return ORC_ERR_ID;
+        int64_t start = MUT(11) ? id : id * d; /* s11: offset ids[t], not ids[t] * d */
+        for (int64_t j = 0; j < d; ++j) out[t * d + j] = table[start + j];
+    }
+    return ORC_OK;
+}
+
+/* ---- Greedy argmax -------------------------------------------------------------
+ * [L9.6] 2.4 and 4, [Ops] 1 (Argmax) and 8 (greedy sampling): scan forward,
+ * skip NaN, keep an entry only if it is strictly greater than the best so
+ * far, so equal values go to the lowest index; -1 when the row holds no
+ * number.  -0 and +0 compare equal and so tie.  +inf is a number; a row of
+ * -inf gives 0.  n == 0 also gives -1 here; orc_argmax_rows rejects it.      */
+int32_t orc_argmax(const float *x, int64_t n) {
+    int32_t best = -1;
+    float bv = 0.0f;
+    for (int64_t i = 0; i < n; ++i) {
+        float v = x[i];
+        if (!MUT(13) && v != v) continue;                 /* s13: no NaN check */
+        if (best < 0 || (MUT(12) ? v >= bv : v > bv)) {   /* s12: >= instead of > */
+            best = (int32_t)i;
+            bv = v;
+        }
+    }
+    if (MUT(14) && best < 0) return 0; /* s14: 0 for an empty or all-NaN row */
+    return best;
+}
+
+int orc_argmax_rows(const float *x, int32_t *out, int64_t rows, int64_t n) {
+    if (rows < 0 || n < 0 || n > INT32_MAX) return ORC_ERR_ARG;
+    if (n == 0 && rows > 0) return ORC_ERR_EMPTY;
+    for (int64_t r = 0; r < rows; ++r) out[r] = orc_argmax(x + r * n, n);
+    return ORC_OK;
+}

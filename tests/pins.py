@@ -1,0 +1,352 @@
+"""Pins of the oracle: checks that tie it to something other than itself.
+
+Each ``pin_*`` takes an oracle handle and raises AssertionError when the oracle
+breaks the fact it checks.  The facts come from the pages (worked examples and
+the test catalog of "Elementwise kernels in C", section 3 and 4), from the
+mathematics (closed forms, invariants, brute force in float64), and from
+library routines that reduce to the same definition (torch float64
+``rms_norm`` / ``silu``, ``numpy.nanargmax``, numpy fancy indexing, torch's
+bf16 rounding).  ``KILLS`` names, for each planted mistake s01..s15 of the
+pages' pitfalls table (section 5), the pin that the table says must reject it.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from golden_io import load, printed_close
+
+RNG = np.random.default_rng(1234)  # pins draw their own small cases
+
+
+def _rand(*shape, scale=1.0):
+    return (RNG.standard_normal(shape) * scale).astype(np.float32)
+
+
+def _bits(a):
+    return np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
+
+
+def _same_bits(a, b) -> bool:
+    return np.array_equal(_bits(a), _bits(b))
+
+
+# ---- RMSNorm -------------------------------------------------------------------
+
+def pin_hand_example(o):
+    g = load("rmsnorm_worked_example.txt")
+    y = o.rmsnorm(g["x"].reshape(1, -1), g["w"], g["eps"])
+    assert printed_close(y.ravel(), g["y"], 7), ("rmsnorm worked example", y)
+    for name in ("rope_half_worked_example.txt", "rope_interleaved_worked_example.txt"):
+        g = load(name)
+        x = g["x"].astype(np.float32).reshape(1, 1, -1)
+        y = o.rope(x, [g["pos"]], g["inv_freq"], g["r"], g["mu"], g["layout"])
+        assert printed_close(y.ravel(), g["y"], 7), (name, y)
+    g = load("silu_mul_worked_example.txt")
+    y = o.silu_mul(g["gate"], g["up"])
+    assert printed_close(y, g["y"], 7), ("silu_mul worked example", y)
+    g = load("argmax_worked_example.txt")
+    assert int(o.argmax(g["x"])[0]) == g["index"]
+
+
+def pin_rmsnorm_eps_is_inside_the_root(o):
+    g = load("rmsnorm_eps_inside_root.txt")
+    y = o.rmsnorm(g["x"].reshape(1, -1), g["w"], g["eps"])
+    assert printed_close(y.ravel(), g["y"], 4), y
+    z = o.rmsnorm(np.zeros((2, 33), np.float32), np.full(33, 1.25, np.float32), 1e-5)
+    assert not np.isnan(z).any() and np.all(z == 0.0)
+
+
+def pin_rmsnorm_rows_are_independent_and_in_place(o):
+    d = 37
+    w = RNG.uniform(0.5, 1.5, d).astype(np.float32)
+    batch = _rand(12, d)
+    batch[5] *= 1e-3
+    batch[7] *= 1e3
+    full = o.rmsnorm(batch, w, 1e-5)
+    for b in range(1, 13):
+        part = o.rmsnorm(batch[:b], w, 1e-5)
+        assert _same_bits(part, full[:b]), f"batch of {b}"
+    for r in range(12):
+        alone = o.rmsnorm(batch[r:r + 1], w, 1e-5)
+        assert _same_bits(alone, full[r:r + 1]), f"row {r} alone"
+    x = batch.copy()
+    o.rmsnorm(x, w, 1e-5, out=x)
+    assert _same_bits(x, full)
+
+
+def pin_rmsnorm_library(o):
+    for d in (1, 7, 64, 1000, 4096):
+        x = _rand(5, d, scale=3.0)
+        w = RNG.uniform(0.5, 1.5, d).astype(np.float32)
+        y = o.rmsnorm(x, w, 1e-5).astype(np.float64)
+        ref = torch.nn.functional.rms_norm(torch.from_numpy(x).double(), (d,),
+                                           torch.from_numpy(w).double(), 1e-5).numpy()
+        err = np.abs(y - ref) / np.maximum(np.abs(ref), 1e-30)
+        assert err.max() <= 2e-6, (d, err.max())
+
+
+def pin_rmsnorm_closed_forms(o):
+    x = _rand(6, 257)
+    w = RNG.uniform(0.5, 1.5, 257).astype(np.float32)
+    base = o.rmsnorm(x, w, 0.0)
+    for k in (-20, -3, 1, 9, 30):  # power-of-two scale: exact at eps = 0
+        assert _same_bits(o.rmsnorm(x * np.float32(2.0 ** k), w, 0.0), base), k
+    for c in (0.37, 11.0):
+        y = o.rmsnorm(x * np.float32(c), w, 0.0)
+        assert np.allclose(y, base, rtol=2e-6, atol=0)
+    rms = np.sqrt(np.mean((base.astype(np.float64) / w) ** 2, axis=1))
+    assert np.allclose(rms, 1.0, atol=2e-6), rms
+
+
+def pin_add_rmsnorm_composition(o):
+    d = 300
+    x, r = _rand(4, d), _rand(4, d)
+    w = RNG.uniform(0.5, 1.5, d).astype(np.float32)
+    y, h = o.add_rmsnorm(x, r, w, 1e-5)
+    assert _same_bits(h, x + r)  # numpy's f32 add is the IEEE sum
+    ref = torch.nn.functional.rms_norm(torch.from_numpy(x + r).double(), (d,),
+                                       torch.from_numpy(w).double(), 1e-5).numpy()
+    assert np.allclose(y, ref, rtol=2e-6, atol=0)
+    yb, hb = o.add_rmsnorm(x, r, w, 1e-5, h_bf16=True)
+    hb_ref = torch.from_numpy(x + r).bfloat16().float().numpy()
+    assert _same_bits(hb, hb_ref)
+    ref = torch.nn.functional.rms_norm(torch.from_numpy(hb_ref).double(), (d,),
+                                       torch.from_numpy(w).double(), 1e-5).numpy()
+    assert np.allclose(yb, ref, rtol=2e-6, atol=0)
+
+
+# ---- RoPE ----------------------------------------------------------------------
+
+def _brute_rope(x, pos, om, r, mu, layout):
+    """float64 2x2 rotation matrices on each pair, the angle taken as the f32
+    product of the position and the frequency."""
+    x = x.astype(np.float64)
+    y = x.copy()
+    T, H, D = x.shape
+    for t in range(T):
+        for i in range(r // 2):
+            th = float(np.float32(np.float32(pos[t]) * np.float32(om[i])))
+            R = mu * np.array([[np.cos(th), -np.sin(th)], [np.sin(th), np.cos(th)]])
+            ia, ib = (i, i + r // 2) if layout == 0 else (2 * i, 2 * i + 1)
+            for h in range(H):
+                y[t, h, [ia, ib]] = R @ x[t, h, [ia, ib]]
+    return y
+
+
+def _pair_idx(r, layout):
+    i = np.arange(r // 2)
+    return (i, i + r // 2) if layout == 0 else (2 * i, 2 * i + 1)
+
+
+def pin_rope_interleaved_layout_and_position_zero(o):
+    g = load("rope_interleaved_worked_example.txt")
+    y = o.rope(g["x"].astype(np.float32).reshape(1, 1, -1), [g["pos"]], g["inv_freq"], g["r"],
+               g["mu"], g["layout"])
+    assert printed_close(y.ravel(), g["y"], 7), y
+    x = _rand(3, 2, 12)
+    om = RNG.uniform(0.001, 2.0, 5).astype(np.float32)
+    for layout in (0, 1):
+        y = o.rope(x, [0, 0, 0], om, 10, 1.0, layout)
+        assert _same_bits(y, x), layout
+
+
+def pin_rope_partial_rotary_and_scaling(o):
+    T, H, D, r = 5, 3, 24, 10
+    x = _rand(T, H, D)
+    pos = RNG.integers(0, 5000, T).astype(np.int32)
+    om = RNG.uniform(0.001, 1.0, r // 2).astype(np.float32)
+    for layout in (0, 1):
+        y1 = o.rope(x, pos, om, r, 1.0, layout)
+        assert _same_bits(y1[..., r:], x[..., r:]), "tail must pass through"
+        y2 = o.rope(x, pos, om, r, 2.0, layout)
+        assert _same_bits(y2[..., :r], (y1[..., :r] * np.float32(2.0))), "mu = 2 doubles"
+        ref = _brute_rope(x, pos, om, r, 1.0, layout)  # [T, H, D] indexing, per token
+        a, b = _pair_idx(r, layout)
+        norm = np.sqrt(x[..., a].astype(np.float64) ** 2 + x[..., b].astype(np.float64) ** 2)
+        for idx in (a, b):
+            assert np.all(np.abs(y1[..., idx] - ref[..., idx]) <= 2e-6 * norm + 1e-30)
+        xi = x.copy()
+        o.rope(xi, pos, om, r, 1.0, layout, in_place=True)
+        assert _same_bits(xi, y1), "in place equals out of place"
+
+
+def pin_rope_is_a_rotation(o):
+    for trial in range(8):
+        T, H = int(RNG.integers(1, 6)), int(RNG.integers(1, 5))
+        r = 2 * int(RNG.integers(1, 9))
+        D = r + int(RNG.integers(0, 5))
+        layout = trial % 2
+        mu = float(RNG.choice([1.0, 1.2, 0.5]))
+        x = _rand(T, H, D)
+        pos = RNG.integers(0, 1 << 20, T).astype(np.int32)
+        om = RNG.uniform(1e-4, 1.5, r // 2).astype(np.float32)
+        y = o.rope(x, pos, om, r, mu, layout)
+        a, b = _pair_idx(r, layout)
+        n0 = np.hypot(x[..., a].astype(np.float64), x[..., b].astype(np.float64))
+        n1 = np.hypot(y[..., a].astype(np.float64), y[..., b].astype(np.float64))
+        assert np.all(np.abs(n1 - mu * n0) <= 1e-6 * mu * n0 + 1e-30), (trial, layout)
+
+
+def pin_rope_brute_force(o):
+    for layout in (0, 1):
+        x = _rand(4, 3, 10)
+        pos = np.array([0, 3, 77, 4095], np.int32)
+        om = RNG.uniform(1e-3, 1.0, 4).astype(np.float32)
+        y = o.rope(x, pos, om, 8, 1.2, layout)
+        ref = _brute_rope(x, pos, om, 8, 1.2, layout)
+        a, b = _pair_idx(8, layout)
+        norm = np.hypot(x[..., a].astype(np.float64), x[..., b].astype(np.float64))
+        for idx in (a, b):
+            assert np.all(np.abs(y[..., idx] - ref[..., idx]) <= 2e-6 * 1.2 * norm + 1e-30)
+
+
+def pin_rope_relative_position(o):
+    D, r = 16, 16
+    om = (10000.0 ** (-2.0 * np.arange(8) / 16)).astype(np.float32)
+    q, k = _rand(1, 1, D), _rand(1, 1, D)
+    for layout in (0, 1):
+        dots = []
+        for shift in (0, 5, 20, 50):  # angles stay below 100 rad, where their f32 rounding is < 4e-6
+            qr = o.rope(q, [37 + shift], om, r, 1.0, layout).astype(np.float64)
+            kr = o.rope(k, [12 + shift], om, r, 1.0, layout).astype(np.float64)
+            dots.append(float(np.sum(qr * kr)))
+        scale = np.linalg.norm(q) * np.linalg.norm(k)
+        assert max(dots) - min(dots) <= 2e-5 * scale, (layout, dots)
+        # and the dot product does change with the offset itself
+        qr = o.rope(q, [38], om, r, 1.0, layout).astype(np.float64)
+        kr = o.rope(k, [12], om, r, 1.0, layout).astype(np.float64)
+        assert abs(float(np.sum(qr * kr)) - dots[0]) > 1e-4 * scale
+
+
+def pin_rope_layout_equivalence(o):
+    T, H, D, r = 3, 2, 12, 8
+    x = _rand(T, H, D)
+    pos = np.array([1, 9, 300], np.int32)
+    om = RNG.uniform(1e-3, 1.0, r // 2).astype(np.float32)
+    perm = np.arange(D)  # P: entry 2i -> i, 2i+1 -> i + r/2 (rotated part only)
+    perm[:r] = np.concatenate([np.arange(0, r, 2), np.arange(1, r, 2)])
+    inter = o.rope(x, pos, om, r, 1.0, 1)
+    half = o.rope(np.ascontiguousarray(x[..., perm]), pos, om, r, 1.0, 0)
+    back = np.empty_like(half)
+    back[..., perm] = half
+    assert _same_bits(back, inter)
+
+
+# ---- SiLU-mul ------------------------------------------------------------------
+
+def pin_silu_mul_saturates_without_nan(o):
+    g = np.array([-1e4, -1e4, 100.0, -100.0, 1e4, -88.0, 0.0], np.float32)
+    u = np.array([2.0, -3.0, 1.5, 2.0, 0.25, 1.0, 7.0], np.float32)
+    y = o.silu_mul(g, u)
+    assert not np.isnan(y).any()
+    assert y[0] == 0 and np.signbit(y[0]), "silu(-1e4) * u (u > 0) is -0"
+    assert y[1] == 0 and not np.signbit(y[1]), "silu(-1e4) * u (u < 0) is +0"
+    assert y[2] == np.float32(150.0), "large gate: y = g * u"
+    assert y[3] == 0 and np.signbit(y[3])
+    assert y[4] == np.float32(2500.0)
+    assert 0 > y[5] > -1e-35
+    assert y[6] == 0
+
+
+def pin_silu_library(o):
+    g = RNG.uniform(-80, 80, 4000).astype(np.float32)
+    g[:100] = RNG.uniform(-1, 1, 100)
+    u = _rand(4000, scale=2.0)
+    y = o.silu_mul(g, u).astype(np.float64)
+    ref = (torch.nn.functional.silu(torch.from_numpy(g).double()) * torch.from_numpy(u).double()).numpy()
+    err = np.abs(y - ref) / np.maximum(np.abs(ref), 1e-300)
+    assert err.max() <= 1e-6, err.max()
+
+
+# ---- Embedding / add / argmax / bf16 ---------------------------------------------
+
+def pin_embedding_gathers_rows(o):
+    table = _rand(50, 9)
+    ids = np.array([7, 7, 0, 49, 3, 7, 12], np.int32)  # repeated and out of order
+    out = o.embedding(table, ids)
+    assert _same_bits(out, table[ids])
+    for bad in ([50], [-1]):
+        try:
+            o.embedding(table, np.array(bad, np.int32))
+        except ValueError:
+            pass
+        else:
+            raise AssertionError("an id outside [0, V) must be reported")
+
+
+def pin_add_in_place(o):
+    a, b = _rand(1000), _rand(1000)
+    assert _same_bits(o.add(a, b), a + b)
+    ta = torch.from_numpy(a).bfloat16()
+    tb = torch.from_numpy(b).bfloat16()
+    wide_a, wide_b = ta.float().numpy(), tb.float().numpy()
+    got = o.bf16_round(o.add(wide_a, wide_b))
+    want = (ta + tb).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, want), "bf16 add: f32 sum rounded to nearest even"
+
+
+def pin_bf16_storage(o):
+    specials = np.array([0.0, -0.0, 1.0, -1.0, np.inf, -np.inf, np.nan, 3.4e38, -3.4e38,
+                         1e-40, -1e-40, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, 1.0 + 2 ** -9,
+                         1.0 + 2 ** -8 + 2 ** -9, 65504.0, 2.0 ** -126], np.float32)
+    vals = np.concatenate([specials, _rand(20000, scale=100.0),
+                           (np.arange(1, 5000, dtype=np.uint32) << 15).view(np.float32)])
+    got = o.bf16_round(vals)
+    want = torch.from_numpy(vals).bfloat16().view(torch.int16).numpy().view(np.uint16)
+    finite = ~np.isnan(vals)
+    assert np.array_equal(got[finite], want[finite])
+    assert np.all(np.isnan(o.bf16_widen(got[~finite])))
+    back = o.bf16_widen(want)
+    assert _same_bits(back[finite],
+                      torch.from_numpy(want.view(np.int16)).view(torch.bfloat16).float().numpy()[finite])
+
+
+def pin_argmax_ties_nan_and_empty(o):
+    nan, inf = np.nan, np.inf
+    assert list(o.argmax(np.array([[3, 9, 9, 1], [9, 3, 9, 9]], np.float32))) == [1, 0]
+    assert int(o.argmax(np.array([nan, 1, 2, 2], np.float32))[0]) == 2
+    assert int(o.argmax(np.array([nan, nan], np.float32))[0]) == -1
+    assert int(o.argmax(np.array([-inf, -inf, -inf], np.float32))[0]) == 0
+    assert int(o.argmax(np.array([nan, -inf, nan], np.float32))[0]) == 1
+    assert int(o.argmax(np.array([-0.0, 0.0], np.float32))[0]) == 0
+    assert int(o.argmax(np.array([0.0, -0.0], np.float32))[0]) == 0
+    assert int(o.argmax(np.array([1, inf, nan, inf], np.float32))[0]) == 1
+    assert o.argmax_one(np.zeros(0, np.float32)) == -1
+    try:
+        o.argmax(np.zeros((3, 0), np.float32))
+    except ValueError:
+        pass
+    else:
+        raise AssertionError("an empty row must be rejected")
+
+
+def pin_argmax_library(o):
+    x = _rand(40, 513)
+    x[RNG.random(x.shape) < 0.05] = np.nan
+    x[3, 100] = x[3, 300] = 50.0
+    x[4, :] = np.round(x[4] * 2) / 2  # many exact ties
+    got = o.argmax(x)
+    assert np.array_equal(got, np.nanargmax(x, axis=1)), "nanargmax: first max, NaN ignored"
+
+
+PINS = {name[4:]: fn for name, fn in dict(globals()).items() if name.startswith("pin_")}
+
+# planted mistake (pitfalls table, section 5) -> the pin that must reject it
+KILLS = {
+    1: "rmsnorm_eps_is_inside_the_root",
+    2: "rmsnorm_eps_is_inside_the_root",
+    3: "hand_example",
+    4: "rope_interleaved_layout_and_position_zero",
+    5: "rope_interleaved_layout_and_position_zero",
+    6: "rope_is_a_rotation",
+    7: "rope_partial_rotary_and_scaling",
+    8: "rope_partial_rotary_and_scaling",
+    9: "silu_mul_saturates_without_nan",
+    10: "silu_mul_saturates_without_nan",
+    11: "embedding_gathers_rows",
+    12: "argmax_ties_nan_and_empty",
+    13: "argmax_ties_nan_and_empty",
+    14: "argmax_ties_nan_and_empty",
+    15: "rmsnorm_rows_are_independent_and_in_place",
+}
