@@ -1,0 +1,503 @@
+"""Throughput of the elementwise / row-op library on one GB300.
+
+One step is one pass of every op of the library over one batch of synthetic
+inputs at Llama-3-8B prefill shapes (T = 8192 tokens, bf16 storage, f32
+math):  embedding gather (table [128256, 4096]), fused residual add + RMSNorm
+[8192, 4096], RoPE half layout on q [8192, 32, 128] and k [8192, 8, 128],
+the same in the interleaved layout (separate copies, so no call reads what
+another left in L2), SiLU-mul [8192, 14336], residual add [8192, 4096], RMSNorm
+[8192, 4096] and greedy argmax over logits [8192, 128256].  Every op reads
+its inputs from HBM once and writes its outputs once; a step moves ~3.9 GB,
+so the inputs are far larger than the 129 MB L2.
+
+The metric is achieved HBM GB/s: the algorithmic bytes of the step (what the
+ops must read plus what they must write) over the measured time.  Printed as
+one JSON line (rank 0).  `--impl reference` times the CPU oracle instead, on
+a bounded sample of the same workload.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+       (N > 1: one process per GPU under torch.distributed.run; each rank runs
+       its own replica of the step, no collective on the data path)
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "achieved HBM GB/s and % of GB300 peak per op; rows/sec at Llama-8B shapes"
+WORKLOAD = "llama3-8b-prefill-T8192-bf16"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+# op name -> (workload case, C entry point) in step order
+STEP = [
+    ("embedding", "embedding"),
+    ("add_rmsnorm", "add_rmsnorm"),
+    ("rope_q_half", "rope_q"),
+    ("rope_k_half", "rope_k"),
+    ("rope_q_interleaved", "rope_q_interleaved"),
+    ("rope_k_interleaved", "rope_k_interleaved"),
+    ("silu_mul", "silu_mul"),
+    ("add", "add"),
+    ("rmsnorm", "rmsnorm"),
+    ("argmax", "argmax"),
+]
+KERNEL_OF = {  # op -> the kernel it launches (names as ncu lists them)
+    "embedding": "embedding_rows", "add_rmsnorm": "rmsnorm_rows", "rope_q_half": "rope_tokens",
+    "rope_k_half": "rope_tokens", "rope_q_interleaved": "rope_tokens", "rope_k_interleaved": "rope_tokens",
+    "silu_mul": "pointwise_vec", "add": "pointwise_vec", "rmsnorm": "rmsnorm_rows", "argmax": "argmax_rows1",
+}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---- algorithmic bytes ------------------------------------------------------------
+
+def op_bytes(op: str, arrays: dict, params: dict) -> tuple[int, int]:
+    """(bytes the op must read + write, rows it processes)."""
+    nb = lambda a: int(a.nbytes)
+    if op == "embedding":
+        n, d = params["n"], params["d"]
+        es = arrays["table"].itemsize
+        return 2 * n * d * es + nb(arrays["ids"]), n
+    if op == "add_rmsnorm":
+        return 4 * nb(arrays["x"]) + nb(arrays["w"]), params["rows"]
+    if op.startswith("rope"):
+        x = arrays["x"]
+        T, H, D, r = params["T"], params["H"], params["D"], params["r"]
+        moved = x.nbytes if r == D or not params.get("in_place") else T * H * r * x.itemsize
+        return 2 * moved + nb(arrays["pos"]) + 4 * (r // 2), T
+    if op in ("silu_mul", "add"):
+        k = "gate" if op == "silu_mul" else "a"
+        a = arrays[k]
+        return 3 * nb(a), a.shape[0]
+    if op == "rmsnorm":
+        return 2 * nb(arrays["x"]) + nb(arrays["w"]), params["rows"]
+    if op == "argmax":
+        return nb(arrays["x"]) + 4 * params["rows"], params["rows"]
+    raise KeyError(op)
+
+
+# ---- clocks sampled during the timed region -------------------------------------
+
+class Clocks:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [s.strip() for s in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        loaded = [s for s in sm if mx and s >= 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ---- our arm: the CUDA library ------------------------------------------------------
+
+def build_inputs(rank_seed_offset: int = 0):
+    from synth import workloads as W
+    cases = W.cases(W.PREFILL)
+    data = {}
+    for op, case in STEP:
+        arrays, params = cases[case]()
+        data[op] = (arrays, params)
+    return data
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import elementwise_row_rmsnorm_gb300 as gbe
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    gbe.lib()
+
+    data = build_inputs()
+
+    def to_dev(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(a).to(dev)
+
+    # device buffers: inputs (a separate copy per op), outputs
+    bufs = {}
+    for op, (arrays, params) in data.items():
+        ins = {k: to_dev(v) for k, v in arrays.items()}
+        bufs[op] = ins
+    out = {
+        "embedding": torch.empty((8192, 4096), dtype=torch.bfloat16, device=dev),
+        "add_rmsnorm": (torch.empty((8192, 4096), dtype=torch.bfloat16, device=dev),
+                        torch.empty((8192, 4096), dtype=torch.bfloat16, device=dev)),
+        "silu_mul": torch.empty_like(bufs["silu_mul"]["gate"]),
+        "add": torch.empty_like(bufs["add"]["a"]),
+        "rmsnorm": torch.empty_like(bufs["rmsnorm"]["x"]),
+        "argmax": torch.empty((8192,), dtype=torch.int32, device=dev),
+    }
+    for op in ("rope_q_half", "rope_k_half", "rope_q_interleaved", "rope_k_interleaved"):
+        out[op] = torch.empty_like(bufs[op]["x"])
+
+    def call(op, b=None, o=None):
+        b = bufs[op] if b is None else b
+        o = out[op] if o is None else o
+        p = data[op][1]
+        if op == "embedding":
+            gbe.gbe_embedding(b["table"], b["ids"], o)
+        elif op == "add_rmsnorm":
+            gbe.gbe_add_rmsnorm(b["x"], b["residual"], b["w"], o[0], o[1], p["eps"])
+        elif op.startswith("rope"):
+            gbe.gbe_rope(b["x"], o, b["pos"], b["inv_freq"], p["r"], p["mu"], p["layout"])
+        elif op == "silu_mul":
+            gbe.gbe_silu_mul(b["gate"], b["up"], o)
+        elif op == "add":
+            gbe.gbe_add(b["a"], b["b"], o)
+        elif op == "rmsnorm":
+            gbe.gbe_rmsnorm(b["x"], b["w"], o, p["eps"])
+        elif op == "argmax":
+            gbe.gbe_argmax(b["x"], o)
+
+    nbytes = {op: op_bytes(op, *data[op]) for op in data}
+    step_bytes = sum(b for b, _ in nbytes.values())
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        for op, _c in STEP:
+            call(op)
+    barrier()
+
+    clocks = Clocks(local)
+    clocks.start()
+    ev = {op: [] for op, _ in STEP}
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    t0.record(stream)
+    for _ in range(args.steps):
+        for op, _c in STEP:
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            call(op)
+            b.record(stream)
+            ev[op].append((a, b))
+    t1.record(stream)
+    barrier()
+    clk = clocks.stop()
+    elapsed_ms = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+    per_op = {}
+    for op, _ in STEP:
+        ms = [a.elapsed_time(b) for a, b in ev[op]]
+        mean = sum(ms) / len(ms)
+        bts, rows = nbytes[op]
+        per_op[op] = {"bytes": bts, "ms": round(mean, 5), "ms_min": round(min(ms), 5),
+                      "gbs": round(bts / (mean * 1e-3) / 1e9, 1), "rows_per_s": round(rows / (mean * 1e-3), 1)}
+
+    # e2e: the same step from pinned host buffers, copies inside the timed region
+    e2e = run_e2e(args, gbe, torch, dev, data, bufs, out, call, nbytes, step_bytes) if not args.no_e2e else None
+
+    peak, peak_kind = peaks()
+    for op in per_op:
+        per_op[op]["frac_of_peak"] = round(per_op[op]["gbs"] / peak, 4)
+        per_op[op]["frac_of_8tbs"] = round(per_op[op]["gbs"] / NOMINAL_HBM_GBS, 4)
+    # dominant kernel: the op with the largest share of the step's time
+    dom = max(per_op, key=lambda o: per_op[o]["ms"])
+    traffic = dram_traffic(dom)
+    value = step_bytes * args.steps * world / (elapsed_ms * 1e-3) / 1e9
+
+    result = None
+    if rank == 0:
+        cpu = cpu_baseline(data) if (world == 1 and not args.no_cpu) else None
+        result = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(elapsed_ms / args.steps, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded splitmix64; Llama-3-8B shapes)",
+            "config": {"workload": WORKLOAD, "storage": "bf16", "tokens": 8192, "hidden": 4096,
+                       "ffn": 14336, "heads_q": 32, "heads_kv": 8, "head_dim": 128, "vocab": 128256,
+                       "bytes_per_step": step_bytes,
+                       "l2": "inputs larger than L2 (each step moves ~3.9 GB through distinct buffers)",
+                       "parallelism": f"replicas{world}"},
+            "roofline": {"bound": "hbm", "kernel": KERNEL_OF[dom], "op": dom,
+                         "achieved": per_op[dom]["gbs"], "peak": peak, "unit": "GB/s",
+                         "frac": round(per_op[dom]["gbs"] / peak, 4), "peak_source": peak_kind,
+                         "traffic": traffic},
+            "per_op": per_op,
+            "e2e": e2e,
+            "gpu_launches": len(STEP) * args.steps,
+            "clocks": clk,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return result
+
+
+def run_e2e(args, gbe, torch, dev, data, bufs, out, call, nbytes, step_bytes):
+    """Each step: copy every op's per-step inputs from pinned host memory, run
+    the step, copy every result back; weights (the embedding table, RMSNorm
+    gains, RoPE frequencies) stay resident.  Timed with CUDA events."""
+    weights = {("embedding", "table"), ("add_rmsnorm", "w"), ("rmsnorm", "w")}
+    weights |= {(op, "inv_freq") for op in bufs if op.startswith("rope")}
+    host_in, h2d = {}, 0
+    for op, b in bufs.items():
+        for k, t in b.items():
+            if (op, k) in weights:
+                continue
+            h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+            h.copy_(t)
+            host_in[(op, k)] = h
+            h2d += t.numel() * t.element_size()
+    host_out, d2h = {}, 0
+    for op, o in out.items():
+        for i, t in enumerate(o if isinstance(o, tuple) else (o,)):
+            host_out[(op, i)] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+            d2h += t.numel() * t.element_size()
+    stream = torch.cuda.current_stream()
+    steps = max(1, min(args.steps, 5))
+
+    def one():
+        for (op, k), h in host_in.items():
+            bufs[op][k].copy_(h, non_blocking=True)
+        for op, _c in STEP:
+            call(op)
+        for (op, i), h in host_out.items():
+            o = out[op]
+            h.copy_((o if isinstance(o, tuple) else (o,))[i], non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    return {"value": round(step_bytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(ms, 3),
+            "steps": steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def dram_traffic(op: str):
+    """DRAM bytes per launch of the op's kernel from the committed ncu summary,
+    or None when there is none or the kernel sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    want = sources_hash()
+    for line in open(path):
+        parts = line.split()
+        if len(parts) == 3 and not line.startswith("#") and parts[0] == op and parts[2] == want:
+            return int(parts[1])
+    return None
+
+
+def sources_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "elementwise_row_rmsnorm_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+# ---- the oracle on the host cores -------------------------------------------------------
+
+SAMPLE_FRACTION = 4  # the CPU runs the first quarter of each op's rows
+CPU_SECONDS = 10.0   # and repeats that sample for about this long
+
+ROW_KEYS = ("x", "residual", "ids", "gate", "up", "a", "b", "pos")
+
+
+def slice_rows(arrays: dict, params: dict, rows: int):
+    """The first `rows` rows (tokens, ids, logits rows) of an op case."""
+    out = {k: (v[:rows] if k in ROW_KEYS else v) for k, v in arrays.items()}
+    p = dict(params)
+    for k in ("rows", "T"):
+        if k in p:
+            p[k] = rows
+    if "n" in p:
+        lead = out.get("ids", out.get("gate", out.get("a", out.get("x"))))
+        p["n"] = int(lead.shape[0]) if "ids" in out else int(lead.size)
+    return out, p
+
+
+def oracle_sample(data=None, fraction=SAMPLE_FRACTION):
+    """A bounded sample of the step: the first 1/fraction of the rows of every
+    op (from the full inputs when given, else drawn from the same streams),
+    widened to the f32 the oracle reads."""
+    from synth import workloads as W
+    import oracle
+    o = oracle.get()
+    cases = W.cases(W.PREFILL)
+    sample = []
+    rows = max(1, 8192 // fraction)
+    for op, case in STEP:
+        if data is not None:
+            arrays, params = slice_rows(*data[op], rows)
+        else:
+            arrays, params = cases[case](rows=(0, rows))
+        bts, _ = op_bytes(op, arrays, params)
+        f32 = {k: (o.bf16_widen(v) if v.dtype == np.uint16 else np.ascontiguousarray(v))
+               for k, v in arrays.items()}
+        sample.append((op, f32, params, bts, rows))
+    return sample
+
+
+def oracle_step(sample):
+    import oracle
+    o = oracle.get()
+    for op, a, p, _b, _r in sample:
+        if op == "embedding":
+            o.embedding(a["table"], a["ids"])
+        elif op == "add_rmsnorm":
+            o.add_rmsnorm(a["x"], a["residual"], a["w"], p["eps"], h_bf16=True)
+        elif op.startswith("rope"):
+            o.rope(a["x"], a["pos"], a["inv_freq"], p["r"], p["mu"], p["layout"])
+        elif op == "silu_mul":
+            o.silu_mul(a["gate"], a["up"])
+        elif op == "add":
+            o.add(a["a"], a["b"])
+        elif op == "rmsnorm":
+            o.rmsnorm(a["x"], a["w"], p["eps"])
+        elif op == "argmax":
+            o.argmax(a["x"])
+
+
+def cpu_baseline(data=None):
+    """The oracle, as it stands, on the host: one thread, the sample repeated
+    for about CPU_SECONDS."""
+    sample = oracle_sample(data)
+    bts = sum(s[3] for s in sample)
+    reps, t = 0, time.perf_counter()
+    while True:
+        oracle_step(sample)
+        reps += 1
+        dt = time.perf_counter() - t
+        if dt >= CPU_SECONDS:
+            break
+    return {"value": round(bts * reps / dt / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "seconds": round(dt, 2), "repeats": reps,
+            "sample": f"first 1/{SAMPLE_FRACTION} of the rows of every op of the step "
+                      f"({bts / 1e6:.0f} MB algorithmic), single-threaded C in f32, repeated for "
+                      f"{dt:.1f} s"}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    sample = oracle_sample()
+    bts = sum(s[3] for s in sample)
+    for _ in range(args.warmup):
+        oracle_step(sample)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(sample)
+    dt = time.perf_counter() - t
+    value = bts * args.steps / dt / 1e9
+    result = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded splitmix64; Llama-3-8B shapes)",
+        "config": {"workload": WORKLOAD, "storage": "bf16", "sample_fraction": SAMPLE_FRACTION,
+                   "bytes_per_step": bts, "parallelism": "host, 1 thread"},
+        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"first 1/{SAMPLE_FRACTION} of the rows of every op per step"},
+        "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(result), flush=True)
+    return result
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,227 @@
+"""Python binding of the C ABI (include/gbe_elementwise.h).
+
+Argument marshalling only: each ``gbe_*`` function takes torch tensors that
+already live on the current CUDA device, checks that their shapes and dtypes
+agree with one another, and passes their pointers, sizes and the current
+stream to the C entry point of the same name.  Every step of every op runs
+in the CUDA library; there is no other code path.  If the library is not
+built, the first call raises :class:`LibraryMissing`.
+
+The functions without the ``gbe_`` prefix (``rmsnorm``, ``rope``, ...) are
+conveniences that allocate the outputs with torch and call the ``gbe_``
+function.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "lib", "libgbe_elementwise.so")
+
+GBE_F32, GBE_BF16 = 0, 1
+_DTYPES = {torch.float32: GBE_F32, torch.bfloat16: GBE_BF16}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class LibraryMissing(RuntimeError):
+    pass
+
+
+class GbeError(RuntimeError):
+    def __init__(self, op: str, status: int, message: str, cuda_error: int = 0):
+        super().__init__(f"{op}: status {status} ({message})"
+                         + (f", cudaError {cuda_error}" if cuda_error else ""))
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (raises LibraryMissing when it is not built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise LibraryMissing(
+                    f"{LIB_PATH} is not built; run elementwise_row_rmsnorm_gb300.build() "
+                    "(nvcc, sm_103a) first")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i64, f32, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int
+            sigs = {
+                "gbe_rmsnorm": [vp, vp, vp, i64, i64, f32, i32, vp],
+                "gbe_add_rmsnorm": [vp, vp, vp, vp, vp, i64, i64, f32, i32, vp],
+                "gbe_rope": [vp, vp, vp, i64, i64, i64, i64, vp, f32, i32, i32, vp],
+                "gbe_silu_mul": [vp, vp, vp, i64, i32, vp],
+                "gbe_add": [vp, vp, vp, i64, i32, vp],
+                "gbe_embedding": [vp, vp, vp, i64, i64, i64, vp, i32, vp],
+                "gbe_argmax": [vp, vp, i64, i64, i32, vp],
+                "gbe_version": [],
+                "gbe_last_cuda_error": [],
+                "gbe_status_string": [i32],
+            }
+            for name, args in sigs.items():
+                fn = getattr(L, name)
+                fn.argtypes = args
+                fn.restype = ctypes.c_char_p if name == "gbe_status_string" else ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().gbe_status_string(status).decode()
+
+
+def _check(op: str, st: int):
+    if st != 0:
+        L = lib()
+        raise GbeError(op, st, status_string(st), L.gbe_last_cuda_error() if st == 11 else 0)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dt(*ts) -> int:
+    dt = ts[0].dtype
+    for t in ts:
+        if t.dtype != dt:
+            raise TypeError(f"all float tensors of one call share a dtype ({dt} vs {t.dtype})")
+    if dt not in _DTYPES:
+        raise TypeError(f"unsupported dtype {dt} (float32 or bfloat16)")
+    return _DTYPES[dt]
+
+
+def _dev(*ts):
+    for t in ts:
+        if not t.is_cuda:
+            raise ValueError("tensors must be on the CUDA device")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+# ---- the C entry points, one to one -----------------------------------------------
+
+def gbe_rmsnorm(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor, eps: float, stream=None) -> None:
+    _dev(x, w, y)
+    d = x.shape[-1]
+    if y.shape != x.shape or w.numel() != d:
+        raise ValueError("rmsnorm: y must match x and w must have x.shape[-1] entries")
+    _check("gbe_rmsnorm", lib().gbe_rmsnorm(_ptr(x), _ptr(w), _ptr(y), x.numel() // d if d else 0, d,
+                                            eps, _dt(x, w, y), _stream(stream)))
+
+
+def gbe_add_rmsnorm(x, residual, w, y, h, eps: float, stream=None) -> None:
+    _dev(x, residual, w, y, h)
+    d = x.shape[-1]
+    if not (residual.shape == y.shape == h.shape == x.shape) or w.numel() != d:
+        raise ValueError("add_rmsnorm: x, residual, y, h must share a shape; w has x.shape[-1] entries")
+    _check("gbe_add_rmsnorm", lib().gbe_add_rmsnorm(
+        _ptr(x), _ptr(residual), _ptr(w), _ptr(y), _ptr(h), x.numel() // d if d else 0, d, eps,
+        _dt(x, residual, w, y, h), _stream(stream)))
+
+
+def gbe_rope(x, y, pos, inv_freq, r: int, mu: float = 1.0, layout: int = 0, stream=None) -> None:
+    _dev(x, y, pos, inv_freq)
+    if x.dim() != 3 or y.shape != x.shape:
+        raise ValueError("rope: x is [T, H, D] and y matches it")
+    T, H, D = x.shape
+    if pos.dtype != torch.int32 or pos.numel() != T:
+        raise ValueError("rope: pos is int32[T]")
+    if inv_freq.dtype != torch.float32 or inv_freq.numel() < r // 2:
+        raise ValueError("rope: inv_freq is float32[r/2]")
+    _check("gbe_rope", lib().gbe_rope(_ptr(x), _ptr(y), _ptr(pos), T, H, D, r, _ptr(inv_freq), mu, layout,
+                                      _dt(x, y), _stream(stream)))
+
+
+def gbe_silu_mul(gate, up, y, stream=None) -> None:
+    _dev(gate, up, y)
+    if not (gate.shape == up.shape == y.shape):
+        raise ValueError("silu_mul: gate, up, y must share a shape")
+    _check("gbe_silu_mul", lib().gbe_silu_mul(_ptr(gate), _ptr(up), _ptr(y), gate.numel(),
+                                              _dt(gate, up, y), _stream(stream)))
+
+
+def gbe_add(a, b, y, stream=None) -> None:
+    _dev(a, b, y)
+    if not (a.shape == b.shape == y.shape):
+        raise ValueError("add: a, b, y must share a shape")
+    _check("gbe_add", lib().gbe_add(_ptr(a), _ptr(b), _ptr(y), a.numel(), _dt(a, b, y), _stream(stream)))
+
+
+def gbe_embedding(table, ids, out, bad_id_count=None, stream=None) -> None:
+    _dev(table, ids, out)
+    if bad_id_count is not None:
+        _dev(bad_id_count)
+        if bad_id_count.dtype != torch.int32 or bad_id_count.numel() != 1:
+            raise ValueError("embedding: bad_id_count is one int32")
+    if table.dim() != 2 or ids.dtype != torch.int32:
+        raise ValueError("embedding: table is [V, d], ids int32")
+    V, d = table.shape
+    if out.shape != (ids.numel(), d):
+        raise ValueError("embedding: out is [n, d]")
+    _check("gbe_embedding", lib().gbe_embedding(_ptr(table), _ptr(ids), _ptr(out), ids.numel(), d, V,
+                                                _ptr(bad_id_count), _dt(table, out), _stream(stream)))
+
+
+def gbe_argmax(x, out, stream=None) -> None:
+    _dev(x, out)
+    n = x.shape[-1]
+    rows = math.prod(x.shape[:-1])
+    if out.dtype != torch.int32 or out.numel() != rows:
+        raise ValueError("argmax: out is int32 with one entry per row")
+    _check("gbe_argmax", lib().gbe_argmax(_ptr(x), _ptr(out), rows, n, _dt(x), _stream(stream)))
+
+
+# ---- conveniences that allocate the outputs -------------------------------------------
+
+def rmsnorm(x, w, eps: float = 1e-5, out=None, stream=None):
+    y = torch.empty_like(x) if out is None else out
+    gbe_rmsnorm(x, w, y, eps, stream)
+    return y
+
+
+def add_rmsnorm(x, residual, w, eps: float = 1e-5, stream=None):
+    y, h = torch.empty_like(x), torch.empty_like(x)
+    gbe_add_rmsnorm(x, residual, w, y, h, eps, stream)
+    return y, h
+
+
+def rope(x, pos, inv_freq, r: int, mu: float = 1.0, layout: int = 0, in_place: bool = False, stream=None):
+    y = x if in_place else torch.empty_like(x)
+    gbe_rope(x, y, pos, inv_freq, r, mu, layout, stream)
+    return y
+
+
+def silu_mul(gate, up, stream=None):
+    y = torch.empty_like(gate)
+    gbe_silu_mul(gate, up, y, stream)
+    return y
+
+
+def add(a, b, stream=None):
+    y = torch.empty_like(a)
+    gbe_add(a, b, y, stream)
+    return y
+
+
+def embedding(table, ids, bad_id_count=None, stream=None):
+    out = torch.empty((ids.numel(), table.shape[1]), dtype=table.dtype, device=table.device)
+    gbe_embedding(table, ids, out, bad_id_count, stream)
+    return out
+
+
+def argmax(x, stream=None):
+    out = torch.empty(x.shape[:-1], dtype=torch.int32, device=x.device)
+    gbe_argmax(x, out, stream)
+    return out

@@ -1,0 +1,144 @@
+// common.cuh -- device helpers shared by the sm_103a kernels of this library:
+// storage traits (f32 and bf16 in 16-byte vectors), cache-hinted vector
+// loads and stores, and fixed-order reductions.
+//
+// Every arithmetic step that decides result bits is written with an explicit
+// rounding intrinsic (__fmul_rn, __fadd_rn, __fmaf_rn, __fdiv_rn, __fsqrt_rn)
+// so the compiler cannot contract or reorder it differently between code
+// paths (vector or scalar, aligned or not): a row's bits depend only on its
+// own data and on the shape, never on the batch or on where it sits.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gbe {
+
+constexpr int kF32 = 0;
+constexpr int kBF16 = 1;
+
+// ---- 16-byte vectors ---------------------------------------------------------
+
+struct alignas(16) Vec16 {
+    uint32_t w[4];
+};
+
+// Streamed read: skip L1 (each byte is read once), coherent path so it stays
+// correct when the same kernel writes the location afterwards (y == x).
+__device__ __forceinline__ Vec16 ld_stream(const void* p) {
+    Vec16 v;
+    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
+                 : "l"(p));
+    return v;
+}
+
+// Read-only data reused by many rows (an RMSNorm gain): keep it in L1.
+__device__ __forceinline__ Vec16 ld_reuse(const void* p) {
+    Vec16 v;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_stream(void* p, const Vec16& v) {
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.w[0]), "r"(v.w[1]),
+                 "r"(v.w[2]), "r"(v.w[3])
+                 : "memory");
+}
+
+// ---- storage traits ------------------------------------------------------------
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t b16) { return __uint_as_float(b16 << 16); }
+
+__device__ __forceinline__ uint32_t f32_to_bf16_bits(float f) {
+    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+template <int DT>
+struct Store;
+
+template <>
+struct Store<kF32> {
+    using T = float;
+    static constexpr int V = 4;  // elements per 16-byte vector
+    __device__ __forceinline__ static void unpack(const Vec16& v, float (&f)[V]) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) f[e] = __uint_as_float(v.w[e]);
+    }
+    __device__ __forceinline__ static Vec16 pack(const float (&f)[V]) {
+        Vec16 v;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v.w[e] = __float_as_uint(f[e]);
+        return v;
+    }
+    __device__ __forceinline__ static float load1(const void* base, int64_t i) {
+        return static_cast<const float*>(base)[i];
+    }
+    __device__ __forceinline__ static void store1(void* base, int64_t i, float f) {
+        static_cast<float*>(base)[i] = f;
+    }
+    // storage rounding of an f32 value (identity for f32)
+    __device__ __forceinline__ static float round(float f) { return f; }
+};
+
+template <>
+struct Store<kBF16> {
+    using T = __nv_bfloat16;
+    static constexpr int V = 8;
+    __device__ __forceinline__ static void unpack(const Vec16& v, float (&f)[V]) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            f[2 * e] = __uint_as_float(v.w[e] << 16);
+            f[2 * e + 1] = __uint_as_float(v.w[e] & 0xFFFF0000u);
+        }
+    }
+    __device__ __forceinline__ static Vec16 pack(const float (&f)[V]) {
+        Vec16 v;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            v.w[e] = f32_to_bf16_bits(f[2 * e]) | (f32_to_bf16_bits(f[2 * e + 1]) << 16);
+        return v;
+    }
+    __device__ __forceinline__ static float load1(const void* base, int64_t i) {
+        return bf16_bits_to_f32(static_cast<const uint16_t*>(base)[i]);
+    }
+    __device__ __forceinline__ static void store1(void* base, int64_t i, float f) {
+        static_cast<uint16_t*>(base)[i] = (uint16_t)f32_to_bf16_bits(f);
+    }
+    __device__ __forceinline__ static float round(float f) {
+        return bf16_bits_to_f32(f32_to_bf16_bits(f));
+    }
+};
+
+// ---- fixed-order reductions ----------------------------------------------------
+
+// Butterfly sum over the 32 lanes.  Every lane ends with the same bits: at
+// each step the two partners add the same two operands (addition commutes).
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, m));
+    return v;
+}
+
+// Sum over `nwarps` warps of one row, the warp partials added in warp order.
+// `red` holds at least nwarps floats of shared memory.  All threads of the
+// row's warps must call it; every one returns the same bits.
+__device__ __forceinline__ float row_sum(float v, float* red, int warp, int lane, int nwarps) {
+    v = warp_sum(v);
+    if (nwarps == 1) return v;
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float s = red[0];
+    for (int i = 1; i < nwarps; ++i) s = __fadd_rn(s, red[i]);
+    return s;
+}
+
+inline int ceil_div_i(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
+
+// SM count of the current device, cached per device.
+int sm_count();
+
+}  // namespace gbe

@@ -1,0 +1,29 @@
+// launch.h -- internal launchers behind the C ABI (abi.cu validates every
+// argument before any of these is called; they only pick a kernel variant
+// and launch it on the caller's stream).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gbe {
+
+// res == nullptr: RMSNorm; otherwise the fused residual add + RMSNorm, h = x + res.
+cudaError_t launch_rmsnorm(const void* x, const void* res, const void* w, void* y, void* h, int64_t rows,
+                           int64_t d, float eps, int dtype, bool vec, cudaStream_t st);
+
+cudaError_t launch_rope(const void* x, void* y, const int32_t* pos, int64_t T, int64_t H, int64_t D, int64_t r,
+                        const float* inv_freq, float mu, int layout, int dtype, bool vec, cudaStream_t st);
+
+cudaError_t launch_silu_mul(const void* gate, const void* up, void* y, int64_t n, int dtype, bool vec,
+                            cudaStream_t st);
+
+cudaError_t launch_add(const void* a, const void* b, void* y, int64_t n, int dtype, bool vec, cudaStream_t st);
+
+cudaError_t launch_embedding(const void* table, const int32_t* ids, void* out, int64_t n, int64_t d, int64_t V,
+                             int32_t* bad_id_count, int dtype, bool vec, cudaStream_t st);
+
+cudaError_t launch_argmax(const void* x, int32_t* out, int64_t rows, int64_t n, int dtype, bool vec,
+                          cudaStream_t st);
+
+}  // namespace gbe

@@ -1,0 +1,124 @@
+// pointwise.cu -- SiLU-mul and residual add on sm_103a.
+//
+// SiLU-mul ("Elementwise kernels in C", section 2.3; "Operations", section 4,
+// Silu and SwiGlu): y = g / (1 + e^-g) * u, silu first, then the product.
+// Written as a quotient it saturates: for g -> -inf, e^-g overflows to +inf
+// and the quotient is -0 (no NaN); for g -> +inf the quotient is g.
+// Add ("Operations", section 1; "Elementwise kernels in C", section 2.4):
+// y = a + b, the residual connection.
+//
+// Both read two flat arrays of n elements and write one; y may be either
+// input (exactly, not a partial overlap).  The math is f32; bf16 inputs are
+// widened exactly and the result rounded to nearest-even once.
+//
+// Map: each thread owns U = 4 16-byte vectors spaced one CTA-width apart
+// (so every load instruction of a warp covers 512 contiguous bytes), issues
+// all 2U loads before any use, then computes and stores.  One CTA covers
+// 256 * U vectors; the last CTA also does the n mod V elements past the last
+// whole vector.  Misaligned pointers take a scalar path with the same
+// per-element arithmetic.
+#include "common.cuh"
+#include "launch.h"
+
+namespace gbe {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kU = 4;
+
+enum { kSiluMul = 0, kAdd = 1 };
+
+template <int OP>
+__device__ __forceinline__ float op1(float a, float b) {
+    if (OP == kSiluMul) {
+        const float silu = __fdiv_rn(a, __fadd_rn(1.0f, expf(-a)));
+        return __fmul_rn(silu, b);
+    }
+    return __fadd_rn(a, b);
+}
+
+template <int DT, int OP>
+__global__ void __launch_bounds__(kThreads)
+pointwise_vec(const void* a, const void* b, void* y, int64_t n) {
+    using S = Store<DT>;
+    constexpr int V = S::V;
+    const int64_t nvec = n / V;
+    const int64_t v0 = (int64_t)blockIdx.x * (kThreads * kU) + threadIdx.x;
+    const char* pa = static_cast<const char*>(a);
+    const char* pb = static_cast<const char*>(b);
+    char* py = static_cast<char*>(y);
+    Vec16 ra[kU], rb[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+        const int64_t i = v0 + (int64_t)u * kThreads;
+        if (i < nvec) {
+            ra[u] = ld_stream(pa + i * 16);
+            rb[u] = ld_stream(pb + i * 16);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+        const int64_t i = v0 + (int64_t)u * kThreads;
+        if (i < nvec) {
+            float fa[V], fb[V], fy[V];
+            S::unpack(ra[u], fa);
+            S::unpack(rb[u], fb);
+#pragma unroll
+            for (int e = 0; e < V; ++e) fy[e] = op1<OP>(fa[e], fb[e]);
+            st_stream(py + i * 16, S::pack(fy));
+        }
+    }
+    if (blockIdx.x == gridDim.x - 1) {
+        const int64_t tail0 = nvec * V;
+        const int64_t i = tail0 + threadIdx.x;
+        if (i < n) S::store1(y, i, op1<OP>(S::load1(a, i), S::load1(b, i)));
+    }
+}
+
+template <int DT, int OP>
+__global__ void __launch_bounds__(kThreads)
+pointwise_scalar(const void* a, const void* b, void* y, int64_t n) {
+    using S = Store<DT>;
+    const int64_t i0 = (int64_t)blockIdx.x * (kThreads * kU) + threadIdx.x;
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+        const int64_t i = i0 + (int64_t)u * kThreads;
+        if (i < n) S::store1(y, i, op1<OP>(S::load1(a, i), S::load1(b, i)));
+    }
+}
+
+template <int OP>
+cudaError_t launch_pw(const void* a, const void* b, void* y, int64_t n, int dtype, bool vec, cudaStream_t st) {
+    const int V = dtype == kF32 ? 4 : 8;
+    const int64_t per_cta = (int64_t)kThreads * kU;
+    if (vec) {
+        const int64_t nvec = n / V;
+        int64_t grid = (nvec + per_cta - 1) / per_cta;
+        if (grid < 1) grid = 1;  // the tail alone (n < V) still needs one CTA
+        if (dtype == kF32)
+            pointwise_vec<kF32, OP><<<(unsigned)grid, kThreads, 0, st>>>(a, b, y, n);
+        else
+            pointwise_vec<kBF16, OP><<<(unsigned)grid, kThreads, 0, st>>>(a, b, y, n);
+    } else {
+        const int64_t grid = (n + per_cta - 1) / per_cta;
+        if (dtype == kF32)
+            pointwise_scalar<kF32, OP><<<(unsigned)grid, kThreads, 0, st>>>(a, b, y, n);
+        else
+            pointwise_scalar<kBF16, OP><<<(unsigned)grid, kThreads, 0, st>>>(a, b, y, n);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_silu_mul(const void* gate, const void* up, void* y, int64_t n, int dtype, bool vec,
+                            cudaStream_t st) {
+    return launch_pw<kSiluMul>(gate, up, y, n, dtype, vec, st);
+}
+
+cudaError_t launch_add(const void* a, const void* b, void* y, int64_t n, int dtype, bool vec, cudaStream_t st) {
+    return launch_pw<kAdd>(a, b, y, n, dtype, vec, st);
+}
+
+}  // namespace gbe

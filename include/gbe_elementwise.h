@@ -1,0 +1,179 @@
+/*
+ * gbe_elementwise.h -- C ABI of the GB300 (sm_103a) elementwise and
+ * row-wise transformer ops: RMSNorm, fused residual add + RMSNorm, RoPE,
+ * SiLU-mul, embedding gather, residual add and greedy argmax.
+ *
+ * Sources of the definitions (cited per entry point below):
+ *   "Operations" -- the op math spec of the glia runtime (sections 1 to 10);
+ *   "Elementwise kernels in C: RMSNorm, RoPE, SiLU-mul, embedding, add,
+ *   argmax" -- course module L9.6 (sections 2 to 5).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Pointers.  Every data pointer is a DEVICE pointer (or host memory the
+ * device can address, e.g. pinned and mapped) of the CUDA device that is
+ * current when the call is made.  The caller allocates and owns every
+ * buffer; the library never allocates, frees or synchronises.  Each pointer
+ * must be aligned to its element size (4 bytes for f32, int32; 2 for bf16).
+ * 16-byte aligned pointers (and row widths that keep rows 16-byte aligned)
+ * take the vectorised path; others take a scalar path with the same
+ * per-element arithmetic and the same results.
+ *
+ * Stream.  Work is enqueued on `stream` (NULL = the legacy default stream)
+ * and the call returns without waiting.  Results are valid once the stream
+ * has reached the call.
+ *
+ * Storage types.  `dtype` is GBE_F32 or GBE_BF16; all float tensors of one
+ * call share it (except RoPE's inv_freq, always f32).  The math is f32 in
+ * both cases; bf16 values are widened exactly and each result is rounded to
+ * nearest-even once.
+ *
+ * Aliasing.  Only the exact aliases listed per entry point are allowed (an
+ * output equal to a named input, same pointer and same extent).  Any other
+ * overlap between an output and any other buffer is GBE_ERR_ALIAS.
+ *
+ * Errors.  Every argument is checked on the host before anything is
+ * launched; a nonzero status means nothing was enqueued, except
+ * GBE_ERR_CUDA, which reports a launch error from the CUDA runtime.  Memory
+ * checks: a pointer that is not device-addressable memory of the current
+ * device, or whose extent runs past the end of its allocation, is
+ * GBE_ERR_POINTER (so a wrong shape is refused instead of reading past a
+ * buffer).  Empty work (rows, n or T equal to 0) returns GBE_OK without a
+ * launch, except argmax over rows of length 0, which is GBE_ERR_EMPTY.
+ * Calls are thread-safe; calls that write the same buffer on different
+ * streams race, as any two kernels would.
+ */
+#ifndef GBE_ELEMENTWISE_H
+#define GBE_ELEMENTWISE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gbe_dtype { GBE_F32 = 0, GBE_BF16 = 1 } gbe_dtype;
+
+typedef enum gbe_status {
+    GBE_OK = 0,
+    GBE_ERR_NULL = 1,    /* a pointer is NULL while its extent is not empty */
+    GBE_ERR_SHAPE = 2,   /* a size is negative or out of range (d <= 0, D <= 0, counts past int32) */
+    GBE_ERR_DTYPE = 3,   /* dtype is not GBE_F32 or GBE_BF16 */
+    GBE_ERR_LAYOUT = 4,  /* RoPE layout is not 0 or 1 */
+    GBE_ERR_EPS = 5,     /* eps is negative, NaN or infinite */
+    GBE_ERR_ROTARY = 6,  /* RoPE width r is odd, negative or larger than D; mu not finite */
+    GBE_ERR_EMPTY = 7,   /* argmax over rows of length 0 */
+    GBE_ERR_ALIAS = 8,   /* an output overlaps a buffer other than its permitted exact alias */
+    GBE_ERR_ALIGN = 9,   /* a pointer is not aligned to its element size */
+    GBE_ERR_POINTER = 10, /* not device memory of the current device, or the extent exceeds its allocation */
+    GBE_ERR_CUDA = 11    /* the CUDA runtime reported an error at launch */
+} gbe_status;
+
+/* The stream type; the same type as cudaStream_t, so either may be passed. */
+typedef struct CUstream_st *gbe_stream;
+
+/* Static description of a status code (never NULL). */
+const char *gbe_status_string(int status);
+
+/* Version of this ABI as major * 10000 + minor * 100 + patch. */
+int gbe_version(void);
+
+/* The cudaError_t value behind the last GBE_ERR_CUDA returned on the calling
+ * thread (0 when there has been none). */
+int gbe_last_cuda_error(void);
+
+/*
+ * gbe_rmsnorm -- RMSNorm with eps inside the root, over each row.
+ *   "Elementwise kernels in C", section 2.1; "Operations", section 2 (RmsNorm).
+ *   y[r, i] = x[r, i] * (1 / sqrt(sum_j x[r, j]^2 / d + eps)) * w[i]
+ * x, y : [rows, d] row-major, contiguous; w : [d].  dtype for all three.
+ * eps  : finite and >= 0 (0 is allowed; a zero row then gives NaN, as the
+ *        definition does; with eps > 0 a zero row gives zeros).
+ * Alias: y == x allowed (a row's sum is complete before its first write).
+ * Each row's output bits depend only on that row, w, d, eps and dtype: the
+ * same row gives the same bits in a batch of any size and at any offset.
+ */
+int gbe_rmsnorm(const void *x, const void *w, void *y, int64_t rows, int64_t d, float eps, int dtype,
+                gbe_stream stream);
+
+/*
+ * gbe_add_rmsnorm -- fused residual add + RMSNorm, returning both.
+ *   "Operations", section 10 (FusedSkipNorm); the add is "Operations",
+ *   section 1 and "Elementwise kernels in C", section 2.4.
+ *   h = x + residual (rounded to dtype), y = rmsnorm(h, w, eps)
+ * The norm reads the stored (rounded) h, so the result equals gbe_add
+ * followed by gbe_rmsnorm bit for bit.
+ * x, residual, y, h : [rows, d]; w : [d].
+ * Alias: h == residual and/or y == x allowed.
+ */
+int gbe_add_rmsnorm(const void *x, const void *residual, const void *w, void *y, void *h, int64_t rows,
+                    int64_t d, float eps, int dtype, gbe_stream stream);
+
+/*
+ * gbe_rope -- rotary position embedding.
+ *   "Elementwise kernels in C", section 2.2 and 4; "Operations", section 3 (Rope).
+ *   For token t and pair i < r/2: theta = float(pos[t]) * inv_freq[i],
+ *   a' = mu * (a cos(theta) - b sin(theta)), b' = mu * (a sin(theta) + b cos(theta)),
+ *   with (a, b) = (x[t, h, i], x[t, h, i + r/2]) for layout 0 ("half", HF
+ *   Llama) or (x[t, h, 2i], x[t, h, 2i + 1]) for layout 1 ("interleaved").
+ *   Entries r .. D-1 of each head pass through unchanged.
+ * x, y     : [T, H, D] contiguous, dtype.  pos : int32[T], 0 <= pos < 2^24
+ *            (not checked: device data).  inv_freq : f32[r/2], device.
+ * r        : rotated width, even, 0 <= r <= D.  mu : attention scaling
+ *            (1 unless YaRN), finite.  layout : 0 or 1.
+ * Alias: y == x allowed (both members of a pair are read before either is
+ * written); in place the entries r .. D-1 are not touched.
+ */
+int gbe_rope(const void *x, void *y, const int32_t *pos, int64_t T, int64_t H, int64_t D, int64_t r,
+             const float *inv_freq, float mu, int layout, int dtype, gbe_stream stream);
+
+/*
+ * gbe_silu_mul -- the elementwise core of SwiGLU.
+ *   "Elementwise kernels in C", section 2.3; "Operations", section 4 (Silu, SwiGlu).
+ *   y[i] = gate[i] / (1 + exp(-gate[i])) * up[i]
+ * Saturates without NaN: a gate of -1e4 gives -0 (times up), +100 gives gate * up.
+ * gate, up, y : n elements, flat.  Alias: y == gate or y == up allowed.
+ */
+int gbe_silu_mul(const void *gate, const void *up, void *y, int64_t n, int dtype, gbe_stream stream);
+
+/*
+ * gbe_add -- residual add.
+ *   "Operations", section 1 (Add); "Elementwise kernels in C", section 2.4.
+ *   y[i] = a[i] + b[i]
+ * a, b, y : n elements, flat.  Alias: y == a or y == b allowed.
+ */
+int gbe_add(const void *a, const void *b, void *y, int64_t n, int dtype, gbe_stream stream);
+
+/*
+ * gbe_embedding -- embedding-row gather.
+ *   "Elementwise kernels in C", section 2.4; "Operations", section 3 (TokenEmbed).
+ *   out[t, :] = table[ids[t], :], the source row starting at element ids[t] * d.
+ * table : [V, d]; ids : int32[n], device; out : [n, d].
+ * bad_id_count : NULL, or a device int32 counter.  An id outside [0, V) is
+ *   never read: its output row is written as zeros and, when the counter is
+ *   given, the counter is incremented once for that row (the caller zeroes
+ *   it beforehand and reads it after the stream reaches the call).  The
+ *   pages leave the id check to the caller; the guard keeps a bad id from
+ *   reading outside the table.
+ * Alias: out must not overlap table, ids or the counter.
+ */
+int gbe_embedding(const void *table, const int32_t *ids, void *out, int64_t n, int64_t d, int64_t V,
+                  int32_t *bad_id_count, int dtype, gbe_stream stream);
+
+/*
+ * gbe_argmax -- greedy argmax of each row.
+ *   "Elementwise kernels in C", section 2.4 and 4; "Operations", section 1
+ *   (Argmax) and section 8 (Sample, Greedy).
+ *   out[r] = the lowest index of the largest value of row r, NaN entries
+ *   skipped; -1 when the row has no number.  -0 equals +0; +inf is a
+ *   number; a row of -inf gives 0.
+ * x : [rows, n], dtype; out : int32[rows].  n must be >= 1 when rows > 0
+ * (rows of length 0 are rejected with GBE_ERR_EMPTY) and n < 2^31.
+ */
+int gbe_argmax(const void *x, int32_t *out, int64_t rows, int64_t n, int dtype, gbe_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBE_ELEMENTWISE_H */

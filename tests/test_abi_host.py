@@ -1,0 +1,99 @@
+"""The C ABI on the host, no GPU needed: the library loads, exports every
+function include/*.h declares, and rejects invalid arguments before any CUDA
+call (only checks that return before touching the device are exercised)."""
+import ctypes
+import glob
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    import elementwise_row_rmsnorm_gb300 as gbe
+    gbe.build()
+    return gbe.lib()
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(gbe_\w+)\s*\(", text, flags=re.M))
+    return sorted(names)
+
+
+def test_header_declares_the_ops():
+    names = declared_functions()
+    for op in ("gbe_rmsnorm", "gbe_add_rmsnorm", "gbe_rope", "gbe_silu_mul", "gbe_add", "gbe_embedding",
+               "gbe_argmax", "gbe_status_string", "gbe_version", "gbe_last_cuda_error"):
+        assert op in names
+
+
+def test_library_exports_every_declared_function(L):
+    import elementwise_row_rmsnorm_gb300.binding as b
+    out = subprocess.run(["nm", "-D", "--defined-only", b.LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\bT\s+(gbe_\w+)$", out, flags=re.M))
+    for name in declared_functions():
+        assert name in exported, name
+        assert getattr(L, name) is not None
+
+
+def test_status_strings_and_version(L):
+    import elementwise_row_rmsnorm_gb300 as gbe
+    assert L.gbe_version() == 10000
+    for st in range(12):
+        assert gbe.status_string(st) and gbe.status_string(st) != "unknown status"
+    assert gbe.status_string(99) == "unknown status"
+
+
+NULL = None
+S = None  # default stream handle; never reached by these calls
+
+
+def test_rejects_bad_sizes_and_scalars(L):
+    assert L.gbe_rmsnorm(NULL, NULL, NULL, 4, 0, 1e-5, 0, S) == 2          # d <= 0
+    assert L.gbe_rmsnorm(NULL, NULL, NULL, -1, 8, 1e-5, 0, S) == 2         # rows < 0
+    assert L.gbe_rmsnorm(NULL, NULL, NULL, 4, 8, 1e-5, 7, S) == 3          # dtype
+    assert L.gbe_rmsnorm(NULL, NULL, NULL, 4, 8, -1.0, 0, S) == 5          # eps < 0
+    assert L.gbe_rmsnorm(NULL, NULL, NULL, 4, 8, float("nan"), 1, S) == 5  # eps NaN
+    assert L.gbe_rmsnorm(NULL, NULL, NULL, 4, 8, float("inf"), 1, S) == 5
+    assert L.gbe_rmsnorm(NULL, NULL, NULL, 0, 8, 1e-5, 0, S) == 0          # empty: no-op
+    assert L.gbe_add_rmsnorm(NULL, NULL, NULL, NULL, NULL, 2, 8, -3.0, 0, S) == 5
+    assert L.gbe_add_rmsnorm(NULL, NULL, NULL, NULL, NULL, 0, 8, 1e-5, 0, S) == 0
+    # rope: layout, width, scaling, shapes
+    assert L.gbe_rope(NULL, NULL, NULL, 4, 2, 16, 8, NULL, 1.0, 2, 0, S) == 4
+    assert L.gbe_rope(NULL, NULL, NULL, 4, 2, 16, 7, NULL, 1.0, 0, 0, S) == 6   # odd r
+    assert L.gbe_rope(NULL, NULL, NULL, 4, 2, 16, 18, NULL, 1.0, 0, 0, S) == 6  # r > D
+    assert L.gbe_rope(NULL, NULL, NULL, 4, 2, 16, -2, NULL, 1.0, 0, 0, S) == 6
+    assert L.gbe_rope(NULL, NULL, NULL, 4, 2, 16, 8, NULL, float("inf"), 0, 0, S) == 6
+    assert L.gbe_rope(NULL, NULL, NULL, 4, 2, 0, 0, NULL, 1.0, 0, 0, S) == 2
+    assert L.gbe_rope(NULL, NULL, NULL, -4, 2, 16, 8, NULL, 1.0, 0, 0, S) == 2
+    assert L.gbe_rope(NULL, NULL, NULL, 0, 2, 16, 8, NULL, 1.0, 0, 0, S) == 0
+    assert L.gbe_rope(NULL, NULL, NULL, 4, 0, 16, 8, NULL, 1.0, 0, 1, S) == 0
+    # pointwise
+    assert L.gbe_silu_mul(NULL, NULL, NULL, -1, 0, S) == 2
+    assert L.gbe_silu_mul(NULL, NULL, NULL, 0, 1, S) == 0
+    assert L.gbe_add(NULL, NULL, NULL, 5, 2, S) == 3
+    assert L.gbe_add(NULL, NULL, NULL, 0, 0, S) == 0
+    # embedding
+    assert L.gbe_embedding(NULL, NULL, NULL, 3, 0, 10, NULL, 0, S) == 2
+    assert L.gbe_embedding(NULL, NULL, NULL, 3, 4, -1, NULL, 0, S) == 2
+    assert L.gbe_embedding(NULL, NULL, NULL, 0, 4, 10, NULL, 1, S) == 0
+    # argmax: rows of length 0 are rejected, no rows is a no-op
+    assert L.gbe_argmax(NULL, NULL, 3, 0, 0, S) == 7
+    assert L.gbe_argmax(NULL, NULL, 0, 0, 0, S) == 0
+    assert L.gbe_argmax(NULL, NULL, 3, 1 << 31, 0, S) == 2
+    assert L.gbe_argmax(NULL, NULL, 3, 10, 5, S) == 3
+
+
+def test_rejects_size_overflow(L):
+    big = 1 << 62
+    assert L.gbe_silu_mul(NULL, NULL, NULL, big, 0, S) == 2
+    assert L.gbe_rmsnorm(NULL, NULL, NULL, 1 << 31, 1 << 31, 1e-5, 0, S) == 2
+    assert L.gbe_rope(NULL, NULL, NULL, 1 << 31, 1 << 20, 1 << 20, 2, NULL, 1.0, 0, 0, S) == 2
