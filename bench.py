@@ -100,7 +100,9 @@ def op_bytes(op: str, arrays: dict, params: dict) -> tuple[int, int]:
 # ---- clocks sampled during the timed region -------------------------------------
 
 class Clocks:
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi sampling every 50 ms in the background; only the samples
+    whose timestamps fall inside the timed region are kept."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -108,6 +110,7 @@ class Clocks:
         self.dev = device_index
         self.proc = None
         self.path = None
+        self.window = None
 
     def start(self):
         try:
@@ -115,13 +118,18 @@ class Clocks:
             os.close(fd)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                 "-lms", "50"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(1.0)  # let the sampler start before the timed region
         except Exception:
             self.proc = None
+
+    def mark(self, t_begin: float, t_end: float):
+        self.window = (t_begin, t_end)
 
     def stop(self):
         if self.proc is None:
             return None
+        import datetime
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -130,31 +138,45 @@ class Clocks:
         rows = []
         with open(self.path) as f:
             for line in f:
-                parts = [s.strip() for s in line.split(",")]
-                if len(parts) >= 9:
-                    rows.append(parts)
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                except ValueError:
+                    continue
+                rows.append((ts, parts))
         os.unlink(self.path)
-        if not rows:
-            return None
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        if self.window:
+            inside = [r for t, r in rows if self.window[0] - 0.05 <= t <= self.window[1] + 0.05]
+        else:
+            inside = [r for _, r in rows]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(r[2]) for r in inside if num(r[2]) is not None]
+        mx = [num(r[3]) for r in inside if num(r[3]) is not None]
+        pw = [num(r[4]) for r in inside if num(r[4]) is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
-        loaded = [s for s in sm if mx and s >= 0.5 * max(mx)] or sm
-        return {"sm_mhz": statistics.median(loaded) if loaded else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+        reasons = sorted({names[i] for r in inside for i in range(4) if r[6 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None, "reasons": reasons, "samples": len(inside)}
 
 
 # ---- our arm: the CUDA library ------------------------------------------------------
 
-def build_inputs(rank_seed_offset: int = 0):
+def build_inputs(tokens: int = 8192):
+    """The step's inputs; `tokens` < 8192 takes the first rows of every op (a
+    smaller case of the same kernels, for profiling)."""
     from synth import workloads as W
     cases = W.cases(W.PREFILL)
-    data = {}
-    for op, case in STEP:
-        arrays, params = cases[case]()
-        data[op] = (arrays, params)
-    return data
+    rows = None if tokens >= 8192 else (0, tokens)
+    return {op: cases[case](rows=rows) for op, case in STEP}
 
 
 def run_ours(args):
@@ -172,7 +194,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     gbe.lib()
 
-    data = build_inputs()
+    data = build_inputs(args.tokens)
 
     def to_dev(a):
         a = np.ascontiguousarray(a)
@@ -185,17 +207,17 @@ def run_ours(args):
     for op, (arrays, params) in data.items():
         ins = {k: to_dev(v) for k, v in arrays.items()}
         bufs[op] = ins
-    out = {
-        "embedding": torch.empty((8192, 4096), dtype=torch.bfloat16, device=dev),
-        "add_rmsnorm": (torch.empty((8192, 4096), dtype=torch.bfloat16, device=dev),
-                        torch.empty((8192, 4096), dtype=torch.bfloat16, device=dev)),
-        "silu_mul": torch.empty_like(bufs["silu_mul"]["gate"]),
-        "add": torch.empty_like(bufs["add"]["a"]),
-        "rmsnorm": torch.empty_like(bufs["rmsnorm"]["x"]),
-        "argmax": torch.empty((8192,), dtype=torch.int32, device=dev),
-    }
-    for op in ("rope_q_half", "rope_k_half", "rope_q_interleaved", "rope_k_interleaved"):
-        out[op] = torch.empty_like(bufs[op]["x"])
+    out = {}
+    for op in bufs:
+        b = bufs[op]
+        if op == "embedding":
+            out[op] = torch.empty((b["ids"].numel(), b["table"].shape[1]), dtype=b["table"].dtype, device=dev)
+        elif op == "add_rmsnorm":
+            out[op] = (torch.empty_like(b["x"]), torch.empty_like(b["x"]))
+        elif op == "argmax":
+            out[op] = torch.empty((b["x"].shape[0],), dtype=torch.int32, device=dev)
+        else:
+            out[op] = torch.empty_like(b.get("x", b.get("gate", b.get("a"))))
 
     def call(op, b=None, o=None):
         b = bufs[op] if b is None else b
@@ -236,6 +258,7 @@ def run_ours(args):
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     barrier()
+    host_t0 = time.time()
     t0.record(stream)
     for _ in range(args.steps):
         for op, _c in STEP:
@@ -247,6 +270,7 @@ def run_ours(args):
             ev[op].append((a, b))
     t1.record(stream)
     barrier()
+    clocks.mark(host_t0, time.time())
     clk = clocks.stop()
     elapsed_ms = t0.elapsed_time(t1)
     if world > 1:
@@ -281,7 +305,8 @@ def run_ours(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(elapsed_ms / args.steps, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded splitmix64; Llama-3-8B shapes)",
-            "config": {"workload": WORKLOAD, "storage": "bf16", "tokens": 8192, "hidden": 4096,
+            "config": {"workload": WORKLOAD if args.tokens >= 8192 else f"{WORKLOAD} (first {args.tokens} tokens)",
+                       "storage": "bf16", "tokens": min(args.tokens, 8192), "hidden": 4096,
                        "ffn": 14336, "heads_q": 32, "heads_kv": 8, "head_dim": 128, "vocab": 128256,
                        "bytes_per_step": step_bytes,
                        "l2": "inputs larger than L2 (each step moves ~3.9 GB through distinct buffers)",
@@ -487,13 +512,23 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--ops", default="",
+                    help="comma list: run only these ops of the step (for profiling one kernel)")
+    ap.add_argument("--tokens", type=int, default=8192,
+                    help="take the first T tokens of every op (a smaller case, for profiling)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
+    if args.ops:
+        keep = set(args.ops.split(","))
+        unknown = keep - {op for op, _ in STEP}
+        if unknown:
+            ap.error(f"unknown ops {sorted(unknown)}")
+        STEP[:] = [(op, c) for op, c in STEP if op in keep]
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

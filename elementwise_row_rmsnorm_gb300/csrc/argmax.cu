@@ -14,13 +14,16 @@
 // Map: CL CTAs per row (CL in {1, 2, 4, 8}, a thread-block cluster when
 // CL > 1).  The row is cut into CL contiguous segments of 16-byte vectors;
 // within a segment thread t reads vectors t, t + 256, ... in increasing order
-// (4 loads in flight before any compare), so a strict > keeps the first
-// index within a thread.  Threads combine by a warp butterfly and then warp
-// by warp; the CTAs of a cluster combine through distributed shared memory
-// on rank 0 after a cluster barrier (a hardware barrier over co-scheduled
-// CTAs, no spin loop), and a second barrier keeps every CTA's shared memory
-// alive until rank 0 has read it.  CL grows only while rows * CL stays below
-// eight CTAs per SM, so few long rows (decode) still fill the GPU.
+// (8 loads in flight before any compare), so a strict > keeps the first
+// index within a thread.  Per vector, the largest number is found first
+// (fmaxf, which skips NaN) and only a vector whose maximum beats the thread's
+// best is searched for the first position of that maximum.  Threads combine
+// by a warp butterfly and then warp by warp; the CTAs of a cluster combine
+// through distributed shared memory on rank 0 after a cluster barrier (a
+// hardware barrier over co-scheduled CTAs, no spin loop), and a second
+// barrier keeps every CTA's shared memory alive until rank 0 has read it.
+// CL grows only while rows * CL stays below eight CTAs per SM, so few long
+// rows (decode) still fill the GPU.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -44,7 +47,7 @@ int sm_count() {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kBatch = 4;
+constexpr int kBatch = 8;
 
 // (bv, bi) <- better of (bv, bi) and (v, i); bi < 0 means "no number yet".
 __device__ __forceinline__ void take_better(float& bv, int& bi, float v, int i) {
@@ -90,8 +93,20 @@ __device__ __forceinline__ void argmax_body(const void* x, int32_t* out, int64_t
                 if (j < s1) {
                     float f[V];
                     S::unpack(r[u], f);
+                    // the vector's largest number (fmaxf skips NaN; NaN only if all are NaN) ...
+                    float m = f[0];
 #pragma unroll
-                    for (int e = 0; e < V; ++e) scan(bv, bi, f[e], (int)(j * V + e));
+                    for (int e = 1; e < V; ++e) m = fmaxf(m, f[e]);
+                    // ... wins over the thread's best only if strictly greater (earlier
+                    // vectors have lower indices), then its first position is taken
+                    if (m > bv || (bi < 0 && m == m)) {
+                        int e0 = V - 1;
+#pragma unroll
+                        for (int e = V - 1; e >= 0; --e)
+                            if (f[e] == m) e0 = e;
+                        bv = m;
+                        bi = (int)(j * V + e0);
+                    }
                 }
             }
         }

@@ -10,7 +10,8 @@
 //
 // Map: one row per TPR threads (several one-warp rows per CTA when d is
 // small); a row is cut into 16-byte chunks, chunk c goes to thread c mod TPR
-// as its (c div TPR)-th slot, all slot loads are issued before the stores.
+// as its (c div TPR)-th slot (at most 8 slots), and all slot loads are
+// issued before the stores.
 #include "common.cuh"
 #include "launch.h"
 
@@ -39,16 +40,20 @@ embedding_rows(const void* table, const int32_t* ids, void* out, int64_t n, int6
     const char* src = static_cast<const char*>(table) + id * nbytes;
     if (VEC) {
         const int64_t nchunks = d / VE;
-        Vec16 r[K];
+        if (K > 0) {
+            Vec16 r[K > 0 ? K : 1];
 #pragma unroll
-        for (int k = 0; k < K; ++k) {
-            const int64_t c = (int64_t)k * tpr + t;
-            if (c < nchunks) r[k] = ld_stream(src + c * 16);
-        }
+            for (int k = 0; k < K; ++k) {
+                const int64_t c = (int64_t)k * tpr + t;
+                if (c < nchunks) r[k] = ld_stream(src + c * 16);
+            }
 #pragma unroll
-        for (int k = 0; k < K; ++k) {
-            const int64_t c = (int64_t)k * tpr + t;
-            if (c < nchunks) st_stream(dst + c * 16, r[k]);
+            for (int k = 0; k < K; ++k) {
+                const int64_t c = (int64_t)k * tpr + t;
+                if (c < nchunks) st_stream(dst + c * 16, r[k]);
+            }
+        } else {  // very wide rows: stream chunk by chunk
+            for (int64_t c = t; c < nchunks; c += tpr) st_stream(dst + c * 16, ld_stream(src + c * 16));
         }
     } else {
         if (ES == 4) {
@@ -68,16 +73,22 @@ cudaError_t launch_es(const void* table, const int32_t* ids, void* out, int64_t 
                       int32_t* bad, bool vec, cudaStream_t st) {
     constexpr int VE = 16 / ES;
     const int64_t nchunks = (d + VE - 1) / VE;
-    int64_t tpr = ((nchunks + 3) / 4 + 31) / 32 * 32;
+    // enough threads per row that each owns at most 8 chunks (all 8 loads in flight)
+    int64_t tpr = ((nchunks + 7) / 8 + 31) / 32 * 32;
     if (tpr < 32) tpr = 32;
-    if (tpr > 1024) tpr = 1024;
+    const bool wide = tpr > 1024;
+    if (wide) tpr = 1024;
     const int64_t slots = (nchunks + tpr - 1) / tpr;
     const int rpc = tpr == 32 ? 4 : 1;
     const int64_t grid = (n + rpc - 1) / rpc;
     const dim3 block((unsigned)(tpr * rpc));
     const int ti = (int)tpr;
-    if (!vec || slots > 8) {
-        embedding_rows<ES, 1, false, 1024><<<(unsigned)grid, block, 0, st>>>(table, ids, out, n, d, V, bad, ti);
+    if (!vec) {
+        embedding_rows<ES, 0, false, 1024><<<(unsigned)grid, block, 0, st>>>(table, ids, out, n, d, V, bad, ti);
+        return cudaGetLastError();
+    }
+    if (wide) {
+        embedding_rows<ES, 0, true, 1024><<<(unsigned)grid, block, 0, st>>>(table, ids, out, n, d, V, bad, ti);
         return cudaGetLastError();
     }
 #define GBE_EMB_CASE(KK, MT)                                                                                  \
@@ -89,8 +100,8 @@ cudaError_t launch_es(const void* table, const int32_t* ids, void* out, int64_t 
         GBE_EMB_CASE(1, 256)
         GBE_EMB_CASE(2, 256)
         GBE_EMB_CASE(4, 256)
+        GBE_EMB_CASE(8, 256)
     } else {
-        GBE_EMB_CASE(4, 1024)
         GBE_EMB_CASE(8, 1024)
     }
 #undef GBE_EMB_CASE

@@ -12,8 +12,9 @@
 //
 // Work map.  A row is cut into chunks of one 16-byte vector (4 f32 or 8
 // bf16).  Chunk c belongs to thread (c mod TPR) of the row's TPR threads, as
-// that thread's (c div TPR)-th slot.  TPR and the slot count depend only on
-// (d, storage type).  A thread sums the squares of its chunks in slot order
+// that thread's (c div TPR)-th slot; TPR is the smallest multiple of 32 that
+// leaves each thread at most 8 slots (rows of more than 4096 chunks use 1024
+// threads).  TPR and the slot count depend only on (d, storage type).  A thread sums the squares of its chunks in slot order
 // and element order (fused multiply-add), the row's threads are combined by
 // a butterfly within each warp and then warp by warp in warp order.  So the
 // summation tree of a row is fixed by (d, type): the row's output bits do
@@ -21,10 +22,12 @@
 // aligned (vector) and unaligned (scalar) paths use the same map and the
 // same operation order, so they agree bit for bit too.
 //
-// The whole row stays in registers between the sum and the write (one HBM
-// read of x, one write of y), the 16-byte loads of all slots are issued
-// before any is used, and the row's sum is complete before the first write,
-// so y may be x (and h may be residual).
+// Aligned rows (every pointer 16-byte aligned, d a multiple of the vector)
+// stay in registers as packed vectors between the sum and the write (one HBM
+// read of x, one write of y), with the 16-byte loads of all slots issued
+// before any is used.  Other rows take a two-pass kernel with the same map.
+// The row's sum is complete before the first write, so y may be x (and h
+// may be residual).
 #include "common.cuh"
 #include "launch.h"
 
@@ -32,21 +35,18 @@ namespace gbe {
 
 namespace {
 
-constexpr int kMaxSlots = 4;  // more slots of 1024 threads would spill: such rows take the two-pass kernel
+constexpr int kMaxSlots = 8;
 
-template <int DT, bool VEC>
-__device__ __forceinline__ void load_chunk(const void* p, int64_t e0, int d_left, float (&f)[Store<DT>::V],
-                                           Vec16& raw) {
-    using S = Store<DT>;
-    if (VEC) {
-        raw = ld_stream(static_cast<const char*>(p) + e0 * (int64_t)sizeof(typename S::T));
-    } else {
-#pragma unroll
-        for (int e = 0; e < S::V; ++e) f[e] = e < d_left ? S::load1(p, e0 + e) : 0.0f;
-    }
+// Threads per row for a row of `nchunks` 16-byte chunks: enough that each
+// owns at most kMaxSlots chunks.  A function of (d, dtype) only.
+inline int64_t threads_per_row(int64_t nchunks) {
+    int64_t tpr = ((nchunks + kMaxSlots - 1) / kMaxSlots + 31) / 32 * 32;
+    return tpr < 32 ? 32 : tpr;
 }
 
-template <int DT, int K, bool VEC, bool ADD, int MAXT>
+// Aligned rows: the row's chunks stay in registers as packed 16-byte vectors
+// (4 f32 or 8 bf16 each) from the load to the write.
+template <int DT, int K, bool ADD, int MAXT>
 __global__ void __launch_bounds__(MAXT)
 rmsnorm_rows(const void* x, const void* res, const void* w, void* y, void* h, int64_t rows, int d, float eps,
              int tpr) {
@@ -58,53 +58,46 @@ rmsnorm_rows(const void* x, const void* res, const void* w, void* y, void* h, in
     const int t = threadIdx.x - sub * tpr;
     const int64_t row = (int64_t)blockIdx.x * rpc + sub;
     if (row >= rows) return;  // only when several one-warp rows share a CTA: no CTA barrier follows
-    const int nchunks = (d + V - 1) / V;
-    const int64_t base = row * (int64_t)d;
+    const int nchunks = d / V;
+    const int64_t boff = row * (int64_t)d * ES;
     __shared__ float red[32];
 
-    float v[K][V];
-    Vec16 rx[K], rr[K];
+    Vec16 rx[K];
+    Vec16 rr[ADD ? K : 1];
     // 1) every load of the row's slots in flight before any use
 #pragma unroll
     for (int k = 0; k < K; ++k) {
         const int c = k * tpr + t;
         if (c < nchunks) {
-            load_chunk<DT, VEC>(x, base + (int64_t)c * V, d - c * V, v[k], rx[k]);
-            if (ADD) {
-                float vr[V];
-                load_chunk<DT, VEC>(res, base + (int64_t)c * V, d - c * V, vr, rr[k]);
-                if (!VEC) {
-#pragma unroll
-                    for (int e = 0; e < V; ++e) v[k][e] = S::round(__fadd_rn(v[k][e], vr[e]));
-                }
-            }
+            rx[k] = ld_stream(static_cast<const char*>(x) + boff + (int64_t)c * 16);
+            if (ADD) rr[k] = ld_stream(static_cast<const char*>(res) + boff + (int64_t)c * 16);
         }
     }
-    // 2) widen (vector path), form h = x + residual in the storage type, square-sum
+    // 2) h = x + residual rounded to the storage type (stored, and kept as the
+    //    row), then the sum of squares in slot order and element order
     float s = 0.0f;
 #pragma unroll
     for (int k = 0; k < K; ++k) {
         const int c = k * tpr + t;
         if (c < nchunks) {
-            if (VEC) {
-                S::unpack(rx[k], v[k]);
-                if (ADD) {
-                    float vr[V];
-                    S::unpack(rr[k], vr);
+            float f[V];
+            S::unpack(rx[k], f);
+            if (ADD) {
+                float g[V];
+                S::unpack(rr[k], g);
 #pragma unroll
-                    for (int e = 0; e < V; ++e) v[k][e] = S::round(__fadd_rn(v[k][e], vr[e]));
-                    st_stream(static_cast<char*>(h) + (base + (int64_t)c * V) * ES, S::pack(v[k]));
-                }
-            } else if (ADD) {
-                for (int e = 0; e < V && c * V + e < d; ++e) S::store1(h, base + (int64_t)c * V + e, v[k][e]);
+                for (int e = 0; e < V; ++e) f[e] = __fadd_rn(f[e], g[e]);
+                rx[k] = S::pack(f);
+                st_stream(static_cast<char*>(h) + boff + (int64_t)c * 16, rx[k]);
+                S::unpack(rx[k], f);
             }
 #pragma unroll
-            for (int e = 0; e < V; ++e) s = __fmaf_rn(v[k][e], v[k][e], s);
+            for (int e = 0; e < V; ++e) s = __fmaf_rn(f[e], f[e], s);
         }
     }
     // 3) the row's sum, fixed order
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    float total = rpc > 1 ? warp_sum(s) : row_sum(s, red, warp, lane, tpr >> 5);
+    const float total = rpc > 1 ? warp_sum(s) : row_sum(s, red, warp, lane, tpr >> 5);
     const float ms = __fdiv_rn(total, (float)d);
     const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
     // 4) y = x * inv * w
@@ -112,31 +105,25 @@ rmsnorm_rows(const void* x, const void* res, const void* w, void* y, void* h, in
     for (int k = 0; k < K; ++k) {
         const int c = k * tpr + t;
         if (c < nchunks) {
-            float wv[V];
-            if (VEC) {
-                S::unpack(ld_reuse(static_cast<const char*>(w) + (int64_t)c * V * ES), wv);
-            } else {
+            float f[V], wv[V];
+            S::unpack(rx[k], f);
+            S::unpack(ld_reuse(static_cast<const char*>(w) + (int64_t)c * 16), wv);
 #pragma unroll
-                for (int e = 0; e < V; ++e) wv[e] = c * V + e < d ? S::load1(w, (int64_t)c * V + e) : 0.0f;
-            }
-            float o[V];
-#pragma unroll
-            for (int e = 0; e < V; ++e) o[e] = __fmul_rn(__fmul_rn(v[k][e], inv), wv[e]);
-            if (VEC) {
-                st_stream(static_cast<char*>(y) + (base + (int64_t)c * V) * ES, S::pack(o));
-            } else {
-                for (int e = 0; e < V && c * V + e < d; ++e) S::store1(y, base + (int64_t)c * V + e, o[e]);
-            }
+            for (int e = 0; e < V; ++e) f[e] = __fmul_rn(__fmul_rn(f[e], inv), wv[e]);
+            st_stream(static_cast<char*>(y) + boff + (int64_t)c * 16, S::pack(f));
         }
     }
 }
 
-// Rows wider than the register map holds (more than 4 slots of 1024
-// threads: over 16384 f32 or 32768 bf16 entries): the same chunk map and sum order, with x (or h) read twice.
+// Unaligned rows (and rows wider than kMaxSlots chunks of 512 threads): the
+// same chunk map, the same per-thread order and the same reduction tree as
+// rmsnorm_rows would use for this d, element by element, with x (or the
+// stored h) read a second time for the write.  One row per CTA of `tpr`
+// threads.
 template <int DT, bool ADD>
 __global__ void __launch_bounds__(1024)
-rmsnorm_wide_rows(const void* x, const void* res, const void* w, void* y, void* h, int64_t rows, int d,
-                  float eps) {
+rmsnorm_two_pass(const void* x, const void* res, const void* w, void* y, void* h, int64_t rows, int d,
+                 float eps) {
     using S = Store<DT>;
     constexpr int V = S::V;
     const int tpr = blockDim.x;
@@ -148,12 +135,12 @@ rmsnorm_wide_rows(const void* x, const void* res, const void* w, void* y, void* 
     const void* src = ADD ? h : x;
     float s = 0.0f;
     for (int c = t; c < nchunks; c += tpr) {
-        for (int e = 0; e < V; ++e) {
-            const int64_t i = (int64_t)c * V + e;
-            float a = e + c * V < d ? S::load1(x, base + i) : 0.0f;
-            if (ADD && e + c * V < d) {
-                a = S::round(__fadd_rn(a, S::load1(res, base + i)));
-                S::store1(h, base + i, a);
+        for (int e = 0; e < V && c * V + e < d; ++e) {
+            const int64_t i = base + (int64_t)c * V + e;
+            float a = S::load1(x, i);
+            if (ADD) {
+                a = S::round(__fadd_rn(a, S::load1(res, i)));
+                S::store1(h, i, a);
             }
             s = __fmaf_rn(a, a, s);
         }
@@ -163,8 +150,8 @@ rmsnorm_wide_rows(const void* x, const void* res, const void* w, void* y, void* 
     const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
     for (int c = t; c < nchunks; c += tpr) {
         for (int e = 0; e < V && c * V + e < d; ++e) {
-            const int64_t i = (int64_t)c * V + e;
-            S::store1(y, base + i, __fmul_rn(__fmul_rn(S::load1(src, base + i), inv), S::load1(w, i)));
+            const int64_t j = (int64_t)c * V + e;
+            S::store1(y, base + j, __fmul_rn(__fmul_rn(S::load1(src, base + j), inv), S::load1(w, j)));
         }
     }
 }
@@ -174,32 +161,30 @@ cudaError_t launch_dt(const void* x, const void* res, const void* w, void* y, vo
                       float eps, bool vec, cudaStream_t st) {
     constexpr int V = Store<DT>::V;
     const int64_t nchunks = (d + V - 1) / V;
-    int64_t tpr = ((nchunks + 3) / 4 + 31) / 32 * 32;
-    if (tpr < 32) tpr = 32;
-    if (tpr > 1024) tpr = 1024;
-    const int64_t slots = (nchunks + tpr - 1) / tpr;
-    if (slots > kMaxSlots) {
-        rmsnorm_wide_rows<DT, ADD><<<(unsigned)rows, 1024, 0, st>>>(x, res, w, y, h, rows, (int)d, eps);
+    int64_t tpr = threads_per_row(nchunks);
+    const bool wide = tpr > 512;
+    if (wide) tpr = 1024;
+    const int di = (int)d, ti = (int)tpr;
+    if (wide || !vec) {
+        rmsnorm_two_pass<DT, ADD><<<(unsigned)rows, (unsigned)tpr, 0, st>>>(x, res, w, y, h, rows, di, eps);
         return cudaGetLastError();
     }
+    const int64_t slots = (nchunks + tpr - 1) / tpr;
     const int rpc = tpr == 32 ? 4 : 1;
     const int64_t grid = (rows + rpc - 1) / rpc;
     const dim3 block((unsigned)(tpr * rpc));
-    const int di = (int)d, ti = (int)tpr;
-#define GBE_RMS_CASE(KK, MT)                                                                          \
-    if (slots <= KK) {                                                                                \
-        if (vec)                                                                                      \
-            rmsnorm_rows<DT, KK, true, ADD, MT><<<(unsigned)grid, block, 0, st>>>(x, res, w, y, h, rows, di, eps, ti);  \
-        else                                                                                          \
-            rmsnorm_rows<DT, KK, false, ADD, MT><<<(unsigned)grid, block, 0, st>>>(x, res, w, y, h, rows, di, eps, ti); \
-        return cudaGetLastError();                                                                    \
+#define GBE_RMS_CASE(KK, MT)                                                                                   \
+    if (slots <= KK) {                                                                                         \
+        rmsnorm_rows<DT, KK, ADD, MT><<<(unsigned)grid, block, 0, st>>>(x, res, w, y, h, rows, di, eps, ti); \
+        return cudaGetLastError();                                                                             \
     }
     if (tpr * rpc <= 256) {
         GBE_RMS_CASE(1, 256)
         GBE_RMS_CASE(2, 256)
         GBE_RMS_CASE(4, 256)
+        GBE_RMS_CASE(8, 256)
     } else {
-        GBE_RMS_CASE(4, 1024)
+        GBE_RMS_CASE(8, 512)
     }
 #undef GBE_RMS_CASE
     return cudaErrorInvalidValue;

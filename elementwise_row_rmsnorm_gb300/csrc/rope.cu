@@ -17,8 +17,10 @@
 //
 // Both members of a pair are loaded (all loads of a thread's batch, in fact)
 // before either is stored, and no two threads touch the same entry, so the
-// call may run in place (y == x).  Out of place, entries r .. D-1 are copied;
-// in place they are not touched at all.
+// call may run in place (y == x).  Out of place, entries r .. D-1 are
+// copied; in place they are not touched at all.  The first batch's loads are
+// issued before the tile's angles are formed, so the sincos work overlaps the
+// memory latency.
 //
 // The rotation is written with explicit rounding intrinsics, in the order of
 // the definition: mu * ((a * c) - (b * s)) and mu * ((a * s) + (b * c)).
@@ -38,7 +40,7 @@ __device__ __forceinline__ void rotate(float a, float b, float2 cs, float mu, fl
 }
 
 template <int DT, int LAYOUT, bool VEC>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 4)
 rope_tokens(const void* x, void* y, const int32_t* pos, int64_t T, int H, int D, int r, const float* inv_freq,
             float mu, int tt, int copy_tail) {
     using S = Store<DT>;
@@ -48,28 +50,29 @@ rope_tokens(const void* x, void* y, const int32_t* pos, int64_t T, int H, int D,
     const int half = r >> 1;
     const int64_t t0 = (int64_t)blockIdx.x * tt;
     const int ntok = (int)min((int64_t)tt, T - t0);
-
-    // 1) cos / sin of every (token, pair) of the tile, once
-    for (int j = threadIdx.x; j < ntok * half; j += blockDim.x) {
-        const int tk = j / half, i = j - tk * half;
-        const float th = __fmul_rn((float)pos[t0 + tk], inv_freq[i]);
-        float s, c;
-        sincosf(th, &s, &c);
-        cs[j] = make_float2(c, s);
-    }
-    __syncthreads();
-
     const char* px = static_cast<const char*>(x);
     char* py = static_cast<char*>(y);
+
+    // cos / sin of every (token, pair) of the tile, once
+    auto angles = [&]() {
+        for (int j = threadIdx.x; j < ntok * half; j += blockDim.x) {
+            const int tk = j / half, i = j - tk * half;
+            const float th = __fmul_rn((float)pos[t0 + tk], inv_freq[i]);
+            float s, c;
+            sincosf(th, &s, &c);
+            cs[j] = make_float2(c, s);
+        }
+    };
+
     if (VEC) {
-        // 2) rotated part: an item is one 16-byte vector (layout 1) or one pair
-        //    of vectors r/2 apart (layout 0) of one head of one token
+        // an item is one 16-byte vector (layout 1) or one pair of vectors r/2
+        // apart (layout 0) of one head of one token
         const int G = LAYOUT == 0 ? half / V : r / V;
         const int items = ntok * H * G;
-        for (int b0 = threadIdx.x; b0 < items; b0 += kBatch * kThreads) {
-            Vec16 va[kBatch], vb[kBatch];
-            int64_t off[kBatch];
-            int ci[kBatch];
+        Vec16 va[kBatch], vb[kBatch];
+        int64_t off[kBatch];
+        int ci[kBatch];
+        auto load_batch = [&](int b0) {
 #pragma unroll
             for (int u = 0; u < kBatch; ++u) {
                 const int it = b0 + u * kThreads;
@@ -83,6 +86,8 @@ rope_tokens(const void* x, void* y, const int32_t* pos, int64_t T, int H, int D,
                     if (LAYOUT == 0) vb[u] = ld_stream(px + off[u] + (int64_t)half * ES);
                 }
             }
+        };
+        auto rotate_batch = [&](int b0) {
 #pragma unroll
             for (int u = 0; u < kBatch; ++u) {
                 const int it = b0 + u * kThreads;
@@ -112,8 +117,20 @@ rope_tokens(const void* x, void* y, const int32_t* pos, int64_t T, int H, int D,
                     }
                 }
             }
+        };
+        // the first batch's loads go out before the angles are formed, so
+        // the sincos work overlaps the memory latency
+        int b0 = threadIdx.x;
+        load_batch(b0);
+        angles();
+        __syncthreads();
+        for (;;) {
+            rotate_batch(b0);
+            b0 += kBatch * kThreads;
+            if (b0 - (int)threadIdx.x >= items) break;
+            load_batch(b0);
         }
-        // 3) pass-through tail, out of place only
+        // pass-through tail, out of place only
         if (copy_tail) {
             const int GT = (D - r) / V;
             const int titems = ntok * H * GT;
@@ -125,6 +142,8 @@ rope_tokens(const void* x, void* y, const int32_t* pos, int64_t T, int H, int D,
             }
         }
     } else {
+        angles();
+        __syncthreads();
         const int items = ntok * H * half;
         for (int it = threadIdx.x; it < items; it += kThreads) {
             const int i = it % half;

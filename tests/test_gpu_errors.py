@@ -27,16 +27,29 @@ def test_host_pointer_is_refused():
     assert torch.all(y == 7.0)
 
 
+def _allocation_end(ptr: int) -> int:
+    """End address of the driver allocation that holds `ptr` (torch's caching
+    allocator hands out pieces of larger segments)."""
+    cu = ctypes.CDLL("libcuda.so.1")
+    base, size = ctypes.c_uint64(0), ctypes.c_size_t(0)
+    assert cu.cuMemGetAddressRange_v2(ctypes.byref(base), ctypes.byref(size), ctypes.c_uint64(ptr)) == 0
+    return base.value + size.value
+
+
 def test_extent_past_allocation_is_refused():
     L = gbe.lib()
-    n = 16 << 20  # 64 MB of f32: its own allocation
-    a = torch.ones(n, device="cuda")
-    b = torch.ones(n, device="cuda")
-    y = torch.full((n,), 7.0, device="cuda")
-    st = L.gbe_add(a.data_ptr(), b.data_ptr(), y.data_ptr(), 4 * n, 0, _stream())
-    assert st == 10
+    torch.cuda.empty_cache()  # so x starts a fresh segment of its own
+    x = torch.ones(1 << 20, device="cuda")
+    out = torch.full((1,), 7, dtype=torch.int32, device="cuda")
+    n_fit = (_allocation_end(x.data_ptr()) - x.data_ptr()) // 4
+    # one row reaching exactly to the end of the allocation is accepted ...
+    assert L.gbe_argmax(x.data_ptr(), out.data_ptr(), 1, n_fit, 0, _stream()) == 0
     torch.cuda.synchronize()
-    assert torch.all(y == 7.0)
+    out.fill_(7)
+    # ... one element more is refused and nothing runs
+    assert L.gbe_argmax(x.data_ptr(), out.data_ptr(), 1, n_fit + 1, 0, _stream()) == 10
+    torch.cuda.synchronize()
+    assert int(out.item()) == 7
 
 
 def test_partial_overlap_is_refused():
