@@ -9,18 +9,17 @@
 // The angle is the f32 product float(p_t) * omega_i (the correctly rounded
 // product, equal to the double product rounded to f32 for p_t < 2^24), and
 // its cosine and sine come from CUDA's accurate sincosf (never the __sinf
-// approximation: at positions near 2^20 the angles reach 10^6 rad).  Each
-// CTA owns a tile of tokens: it first forms the angles and their cos/sin for
-// every (token, pair) of the tile into shared memory, once, then every head
-// of those tokens reuses them -- the loop order the pages give (token, pair,
-// head) with the angle hoisted out of the head loop.
+// approximation: at positions near 2^20 the angles reach 10^6 rad).  The
+// pages' loop order is token, pair, head with one angle per (token, pair);
+// here a thread owns a group of pairs of one token and forms their angles
+// once, in registers, for a chunk of up to four heads (so an angle is formed
+// once per token for every four heads), with no shared memory and no
+// barrier.
 //
-// Both members of a pair are loaded (all loads of a thread's batch, in fact)
-// before either is stored, and no two threads touch the same entry, so the
-// call may run in place (y == x).  Out of place, entries r .. D-1 are
-// copied; in place they are not touched at all.  The first batch's loads are
-// issued before the tile's angles are formed, so the sincos work overlaps the
-// memory latency.
+// Both members of a pair are loaded (all loads of a thread, in fact) before
+// either is stored, and no two threads touch the same entry, so the call may
+// run in place (y == x).  Out of place, entries r .. D-1 are copied; in
+// place they are not touched at all.
 //
 // The rotation is written with explicit rounding intrinsics, in the order of
 // the definition: mu * ((a * c) - (b * s)) and mu * ((a * s) + (b * c)).
@@ -32,144 +31,138 @@ namespace gbe {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kBatch = 4;  // items a thread loads before it stores any
+constexpr int kHeadsPerThread = 4;  // heads a thread rotates with one set of angles
 
-__device__ __forceinline__ void rotate(float a, float b, float2 cs, float mu, float& a2, float& b2) {
-    a2 = __fmul_rn(mu, __fsub_rn(__fmul_rn(a, cs.x), __fmul_rn(b, cs.y)));
-    b2 = __fmul_rn(mu, __fadd_rn(__fmul_rn(a, cs.y), __fmul_rn(b, cs.x)));
+__device__ __forceinline__ void rotate(float a, float b, float c, float s, float mu, float& a2, float& b2) {
+    a2 = __fmul_rn(mu, __fsub_rn(__fmul_rn(a, c), __fmul_rn(b, s)));
+    b2 = __fmul_rn(mu, __fadd_rn(__fmul_rn(a, s), __fmul_rn(b, c)));
 }
 
-template <int DT, int LAYOUT, bool VEC>
-__global__ void __launch_bounds__(kThreads, 4)
-rope_tokens(const void* x, void* y, const int32_t* pos, int64_t T, int H, int D, int r, const float* inv_freq,
-            float mu, int tt, int copy_tail) {
+// Aligned path.  A thread owns one group of P consecutive pairs (one 16-byte
+// vector of each pair member) of one token, for a chunk of up to 4 heads:
+// it issues the loads of all its heads first, forms the P angles and their
+// cos / sin in registers while those loads are in flight, then rotates and
+// stores every head.  Threads of one token and head chunk cover consecutive
+// 16-byte vectors, so each warp-wide access is contiguous.
+template <int DT, int LAYOUT>
+__global__ void __launch_bounds__(kThreads)
+rope_vec(const void* x, void* y, const int32_t* pos, int64_t T, int H, int D, int r, const float* inv_freq,
+         float mu, int copy_tail) {
     using S = Store<DT>;
     constexpr int V = S::V;
+    constexpr int P = LAYOUT == 0 ? V : V / 2;  // pairs per 16-byte item
     constexpr int64_t ES = sizeof(typename S::T);
-    extern __shared__ float2 cs[];  // [tt][r/2] of (cos, sin)
+    constexpr int HC = kHeadsPerThread;
     const int half = r >> 1;
-    const int64_t t0 = (int64_t)blockIdx.x * tt;
-    const int ntok = (int)min((int64_t)tt, T - t0);
+    const int G = LAYOUT == 0 ? half / V : r / V;  // items per head
+    const int NC = (H + HC - 1) / HC;              // head chunks per token
+    const int64_t gt = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int g = (int)(gt % G);
+    const int64_t rest = gt / G;
+    const int hc = (int)(rest % NC);
+    const int64_t t = rest / NC;
+    if (t >= T) return;
+    const int h0 = hc * HC;
+    const int nh = min(HC, H - h0);
     const char* px = static_cast<const char*>(x);
     char* py = static_cast<char*>(y);
+    const int64_t row0 = (t * H + h0) * (int64_t)D;  // element offset of (t, h0, 0)
+    const int64_t ia = (int64_t)g * V;                // first entry of the item in a head
+    const int64_t hb = (int64_t)half * ES;            // byte distance to the b member (layout 0)
 
-    // cos / sin of every (token, pair) of the tile, once
-    auto angles = [&]() {
-        for (int j = threadIdx.x; j < ntok * half; j += blockDim.x) {
-            const int tk = j / half, i = j - tk * half;
-            const float th = __fmul_rn((float)pos[t0 + tk], inv_freq[i]);
-            float s, c;
-            sincosf(th, &s, &c);
-            cs[j] = make_float2(c, s);
+    Vec16 va[HC], vb[HC];
+#pragma unroll
+    for (int j = 0; j < HC; ++j) {
+        if (j < nh) {
+            const char* p = px + (row0 + (int64_t)j * D + ia) * ES;
+            va[j] = ld_stream(p);
+            if (LAYOUT == 0) vb[j] = ld_stream(p + hb);
         }
-    };
+    }
+    // the angles of this thread's pairs, once for all its heads
+    float c[P], sn[P];
+    const float pf = (float)pos[t];
+    const int i0 = g * P;
+#pragma unroll
+    for (int e = 0; e < P; ++e) sincosf(__fmul_rn(pf, __ldg(inv_freq + i0 + e)), &sn[e], &c[e]);
 
-    if (VEC) {
-        // an item is one 16-byte vector (layout 1) or one pair of vectors r/2
-        // apart (layout 0) of one head of one token
-        const int G = LAYOUT == 0 ? half / V : r / V;
-        const int items = ntok * H * G;
-        Vec16 va[kBatch], vb[kBatch];
-        int64_t off[kBatch];
-        int ci[kBatch];
-        auto load_batch = [&](int b0) {
 #pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-                const int it = b0 + u * kThreads;
-                if (it < items) {
-                    const int g = it % G;
-                    const int th_ = it / G;  // token-in-tile * H + head
-                    const int tk = th_ / H;
-                    off[u] = ((t0 * H + th_) * (int64_t)D + (int64_t)g * V) * ES;
-                    ci[u] = tk * half + (LAYOUT == 0 ? g * V : g * (V / 2));
-                    va[u] = ld_stream(px + off[u]);
-                    if (LAYOUT == 0) vb[u] = ld_stream(px + off[u] + (int64_t)half * ES);
+    for (int j = 0; j < HC; ++j) {
+        if (j < nh) {
+            char* q = py + (row0 + (int64_t)j * D + ia) * ES;
+            float fa[V];
+            S::unpack(va[j], fa);
+            if (LAYOUT == 0) {
+                float fb[V];
+                S::unpack(vb[j], fb);
+#pragma unroll
+                for (int e = 0; e < V; ++e) {
+                    float a2, b2;
+                    rotate(fa[e], fb[e], c[e], sn[e], mu, a2, b2);
+                    fa[e] = a2;
+                    fb[e] = b2;
                 }
-            }
-        };
-        auto rotate_batch = [&](int b0) {
+                st_stream(q, S::pack(fa));
+                st_stream(q + hb, S::pack(fb));
+            } else {
 #pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-                const int it = b0 + u * kThreads;
-                if (it < items) {
-                    float fa[V], fb[V];
-                    S::unpack(va[u], fa);
-                    if (LAYOUT == 0) {
-                        S::unpack(vb[u], fb);
-#pragma unroll
-                        for (int e = 0; e < V; ++e) {
-                            float a2, b2;
-                            rotate(fa[e], fb[e], cs[ci[u] + e], mu, a2, b2);
-                            fa[e] = a2;
-                            fb[e] = b2;
-                        }
-                        st_stream(py + off[u], S::pack(fa));
-                        st_stream(py + off[u] + (int64_t)half * ES, S::pack(fb));
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < V / 2; ++e) {
-                            float a2, b2;
-                            rotate(fa[2 * e], fa[2 * e + 1], cs[ci[u] + e], mu, a2, b2);
-                            fa[2 * e] = a2;
-                            fa[2 * e + 1] = b2;
-                        }
-                        st_stream(py + off[u], S::pack(fa));
-                    }
+                for (int e = 0; e < P; ++e) {
+                    float a2, b2;
+                    rotate(fa[2 * e], fa[2 * e + 1], c[e], sn[e], mu, a2, b2);
+                    fa[2 * e] = a2;
+                    fa[2 * e + 1] = b2;
                 }
+                st_stream(q, S::pack(fa));
             }
-        };
-        // the first batch's loads go out before the angles are formed, so
-        // the sincos work overlaps the memory latency
-        int b0 = threadIdx.x;
-        load_batch(b0);
-        angles();
-        __syncthreads();
-        for (;;) {
-            rotate_batch(b0);
-            b0 += kBatch * kThreads;
-            if (b0 - (int)threadIdx.x >= items) break;
-            load_batch(b0);
         }
-        // pass-through tail, out of place only
-        if (copy_tail) {
-            const int GT = (D - r) / V;
-            const int titems = ntok * H * GT;
-            for (int it = threadIdx.x; it < titems; it += kThreads) {
-                const int g = it % GT;
-                const int th_ = it / GT;
-                const int64_t o = ((t0 * H + th_) * (int64_t)D + r + (int64_t)g * V) * ES;
+    }
+    // pass-through entries, out of place only: the G threads of this token and
+    // head chunk share the (D - r) / V tail vectors of each head
+    if (copy_tail) {
+        const int GT = (D - r) / V;
+        for (int j = 0; j < nh; ++j)
+            for (int k = g; k < GT; k += G) {
+                const int64_t o = (row0 + (int64_t)j * D + r + (int64_t)k * V) * ES;
                 st_stream(py + o, ld_stream(px + o));
             }
+    }
+}
+
+// Unaligned path (or widths that do not split into 16-byte vectors): a
+// thread owns one pair of one token, forms its angle once and rotates that
+// pair in every head; the tail is copied entry by entry.
+template <int DT, int LAYOUT>
+__global__ void __launch_bounds__(kThreads)
+rope_scalar(const void* x, void* y, const int32_t* pos, int64_t T, int H, int D, int r, const float* inv_freq,
+            float mu, int copy_tail) {
+    using S = Store<DT>;
+    const int half = r >> 1;
+    const int per_tok = half + (copy_tail ? D - r : 0);
+    const int64_t gt = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int64_t t = gt / per_tok;
+    const int k = (int)(gt - t * per_tok);
+    if (t >= T) return;
+    if (k < half) {
+        float c, sn;
+        sincosf(__fmul_rn((float)pos[t], __ldg(inv_freq + k)), &sn, &c);
+        const int ia = LAYOUT == 0 ? k : 2 * k;
+        const int ib = LAYOUT == 0 ? k + half : 2 * k + 1;
+        for (int h = 0; h < H; ++h) {
+            const int64_t row = (t * H + h) * (int64_t)D;
+            const float a = S::load1(x, row + ia), b = S::load1(x, row + ib);
+            float a2, b2;
+            rotate(a, b, c, sn, mu, a2, b2);
+            S::store1(y, row + ia, a2);
+            S::store1(y, row + ib, b2);
         }
     } else {
-        angles();
-        __syncthreads();
-        const int items = ntok * H * half;
-        for (int it = threadIdx.x; it < items; it += kThreads) {
-            const int i = it % half;
-            const int th_ = it / half;
-            const int tk = th_ / H;
-            const int64_t row = (t0 * H + th_) * (int64_t)D;
-            const int64_t ia = row + (LAYOUT == 0 ? i : 2 * i);
-            const int64_t ib = row + (LAYOUT == 0 ? i + half : 2 * i + 1);
-            const float a = S::load1(x, ia), b = S::load1(x, ib);
-            float a2, b2;
-            rotate(a, b, cs[tk * half + i], mu, a2, b2);
-            S::store1(y, ia, a2);
-            S::store1(y, ib, b2);
-        }
-        if (copy_tail) {
-            const int w = D - r;
-            const int titems = ntok * H * w;
-            for (int it = threadIdx.x; it < titems; it += kThreads) {
-                const int j = it % w;
-                const int th_ = it / w;
-                const int64_t o = (t0 * H + th_) * (int64_t)D + r + j;
-                if (ES == 4)
-                    static_cast<uint32_t*>(y)[o] = static_cast<const uint32_t*>(x)[o];
-                else
-                    static_cast<uint16_t*>(y)[o] = static_cast<const uint16_t*>(x)[o];
-            }
+        const int j = r + (k - half);
+        for (int h = 0; h < H; ++h) {
+            const int64_t o = (t * H + h) * (int64_t)D + j;
+            if (sizeof(typename S::T) == 4)
+                static_cast<uint32_t*>(y)[o] = static_cast<const uint32_t*>(x)[o];
+            else
+                static_cast<uint16_t*>(y)[o] = static_cast<const uint16_t*>(x)[o];
         }
     }
 }
@@ -180,26 +173,26 @@ cudaError_t launch_dt(const void* x, void* y, const int32_t* pos, int64_t T, int
     constexpr int V = Store<DT>::V;
     const int64_t half = r / 2;
     const bool copy_tail = x != y && r < D;
-    vec = vec && D % V == 0 && (layout == 0 ? half % V == 0 : r % V == 0);
-    // items per token: vector items of the rotation (or scalar pairs), plus the tail copy
-    int64_t per_tok = vec ? H * (layout == 0 ? half / V : r / V) : H * half;
-    if (copy_tail) per_tok += vec ? H * ((D - r) / V) : H * (D - r);
-    if (per_tok < 1) per_tok = 1;
-    int64_t tt = (kBatch * kThreads) / per_tok;
-    if (tt < 1) tt = 1;
-    if (tt > 64) tt = 64;
-    if (half > 0 && tt > 4096 / half) tt = 4096 / half > 0 ? 4096 / half : 1;  // cos/sin tile <= 32 KB
-    const int64_t grid = (T + tt - 1) / tt;
-    const size_t smem = (size_t)tt * (size_t)half * sizeof(float2);
-    const int Hi = (int)H, Di = (int)D, ri = (int)r, tti = (int)tt, ct = copy_tail ? 1 : 0;
-#define GBE_ROPE(L, VV)                                                                                        \
-    rope_tokens<DT, L, VV><<<(unsigned)grid, kThreads, smem, st>>>(x, y, pos, T, Hi, Di, ri, inv_freq, mu, tti, ct)
-    if (layout == 0) {
-        if (vec) GBE_ROPE(0, true); else GBE_ROPE(0, false);
+    vec = vec && r > 0 && D % V == 0 && (layout == 0 ? half % V == 0 : r % V == 0);
+    const int Hi = (int)H, Di = (int)D, ri = (int)r, ct = copy_tail ? 1 : 0;
+    if (vec) {
+        const int64_t G = layout == 0 ? half / V : r / V;
+        const int64_t NC = (H + kHeadsPerThread - 1) / kHeadsPerThread;
+        const int64_t threads = T * NC * G;
+        const int64_t grid = (threads + kThreads - 1) / kThreads;
+        if (layout == 0)
+            rope_vec<DT, 0><<<(unsigned)grid, kThreads, 0, st>>>(x, y, pos, T, Hi, Di, ri, inv_freq, mu, ct);
+        else
+            rope_vec<DT, 1><<<(unsigned)grid, kThreads, 0, st>>>(x, y, pos, T, Hi, Di, ri, inv_freq, mu, ct);
     } else {
-        if (vec) GBE_ROPE(1, true); else GBE_ROPE(1, false);
+        const int64_t per_tok = half + (copy_tail ? D - r : 0);
+        if (per_tok == 0) return cudaSuccess;
+        const int64_t grid = (T * per_tok + kThreads - 1) / kThreads;
+        if (layout == 0)
+            rope_scalar<DT, 0><<<(unsigned)grid, kThreads, 0, st>>>(x, y, pos, T, Hi, Di, ri, inv_freq, mu, ct);
+        else
+            rope_scalar<DT, 1><<<(unsigned)grid, kThreads, 0, st>>>(x, y, pos, T, Hi, Di, ri, inv_freq, mu, ct);
     }
-#undef GBE_ROPE
     return cudaGetLastError();
 }
 
