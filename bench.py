@@ -40,23 +40,21 @@ WORKLOAD = "llama3-8b-prefill-T8192-bf16"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
-# op name -> (workload case, C entry point) in step order
+# op name -> the workload cases it runs on, in step order
 STEP = [
-    ("embedding", "embedding"),
-    ("add_rmsnorm", "add_rmsnorm"),
-    ("rope_q_half", "rope_q"),
-    ("rope_k_half", "rope_k"),
-    ("rope_q_interleaved", "rope_q_interleaved"),
-    ("rope_k_interleaved", "rope_k_interleaved"),
-    ("silu_mul", "silu_mul"),
-    ("add", "add"),
-    ("rmsnorm", "rmsnorm"),
-    ("argmax", "argmax"),
+    ("embedding", ("embedding",)),
+    ("add_rmsnorm", ("add_rmsnorm",)),
+    ("rope_qk_half", ("rope_q", "rope_k")),
+    ("rope_qk_interleaved", ("rope_q_interleaved", "rope_k_interleaved")),
+    ("silu_mul", ("silu_mul",)),
+    ("add", ("add",)),
+    ("rmsnorm", ("rmsnorm",)),
+    ("argmax", ("argmax",)),
 ]
 KERNEL_OF = {  # op -> the kernel it launches (names as ncu lists them)
-    "embedding": "embedding_rows", "add_rmsnorm": "rmsnorm_rows", "rope_q_half": "rope_tokens",
-    "rope_k_half": "rope_tokens", "rope_q_interleaved": "rope_tokens", "rope_k_interleaved": "rope_tokens",
-    "silu_mul": "pointwise_vec", "add": "pointwise_vec", "rmsnorm": "rmsnorm_rows", "argmax": "argmax_rows1",
+    "embedding": "embedding_rows", "add_rmsnorm": "rmsnorm_rows", "rope_qk_half": "rope_vec",
+    "rope_qk_interleaved": "rope_vec", "silu_mul": "pointwise_vec", "add": "pointwise_vec",
+    "rmsnorm": "rmsnorm_rows", "argmax": "argmax_rows1",
 }
 
 
@@ -82,9 +80,13 @@ def op_bytes(op: str, arrays: dict, params: dict) -> tuple[int, int]:
     if op == "add_rmsnorm":
         return 4 * nb(arrays["x"]) + nb(arrays["w"]), params["rows"]
     if op.startswith("rope"):
-        x = arrays["x"]
-        T, H, D, r = params["T"], params["H"], params["D"], params["r"]
-        moved = x.nbytes if r == D or not params.get("in_place") else T * H * r * x.itemsize
+        T, D, r = params["T"], params["D"], params["r"]
+        moved = 0
+        for key in ("q", "k", "x"):
+            if key in arrays:
+                x = arrays[key]
+                H = x.shape[1]
+                moved += x.nbytes if r == D or not params.get("in_place") else T * H * r * x.itemsize
         return 2 * moved + nb(arrays["pos"]) + 4 * (r // 2), T
     if op in ("silu_mul", "add"):
         k = "gate" if op == "silu_mul" else "a"
@@ -170,13 +172,21 @@ class Clocks:
 
 # ---- our arm: the CUDA library ------------------------------------------------------
 
+def combine(op: str, parts):
+    """Inputs of one step op from its workload cases (q and k for the fused RoPE)."""
+    if op.startswith("rope_qk"):
+        (aq, pq), (ak, _) = parts
+        return {"q": aq["x"], "k": ak["x"], "pos": aq["pos"], "inv_freq": aq["inv_freq"]}, pq
+    return parts[0]
+
+
 def build_inputs(tokens: int = 8192):
     """The step's inputs; `tokens` < 8192 takes the first rows of every op (a
     smaller case of the same kernels, for profiling)."""
     from synth import workloads as W
     cases = W.cases(W.PREFILL)
     rows = None if tokens >= 8192 else (0, tokens)
-    return {op: cases[case](rows=rows) for op, case in STEP}
+    return {op: combine(op, [cases[c](rows=rows) for c in names]) for op, names in STEP}
 
 
 def run_ours(args):
@@ -214,6 +224,8 @@ def run_ours(args):
             out[op] = torch.empty((b["ids"].numel(), b["table"].shape[1]), dtype=b["table"].dtype, device=dev)
         elif op == "add_rmsnorm":
             out[op] = (torch.empty_like(b["x"]), torch.empty_like(b["x"]))
+        elif op.startswith("rope_qk"):
+            out[op] = (torch.empty_like(b["q"]), torch.empty_like(b["k"]))
         elif op == "argmax":
             out[op] = torch.empty((b["x"].shape[0],), dtype=torch.int32, device=dev)
         else:
@@ -227,8 +239,8 @@ def run_ours(args):
             gbe.gbe_embedding(b["table"], b["ids"], o)
         elif op == "add_rmsnorm":
             gbe.gbe_add_rmsnorm(b["x"], b["residual"], b["w"], o[0], o[1], p["eps"])
-        elif op.startswith("rope"):
-            gbe.gbe_rope(b["x"], o, b["pos"], b["inv_freq"], p["r"], p["mu"], p["layout"])
+        elif op.startswith("rope_qk"):
+            gbe.gbe_rope_qk(b["q"], o[0], b["k"], o[1], b["pos"], b["inv_freq"], p["r"], p["mu"], p["layout"])
         elif op == "silu_mul":
             gbe.gbe_silu_mul(b["gate"], b["up"], o)
         elif op == "add":
@@ -248,7 +260,7 @@ def run_ours(args):
 
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
-        for op, _c in STEP:
+        for op, _names in STEP:
             call(op)
     barrier()
 
@@ -261,7 +273,7 @@ def run_ours(args):
     host_t0 = time.time()
     t0.record(stream)
     for _ in range(args.steps):
-        for op, _c in STEP:
+        for op, _names in STEP:
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record(stream)
@@ -430,7 +442,7 @@ def sources_hash() -> str:
 SAMPLE_FRACTION = 4  # the CPU runs the first quarter of each op's rows
 CPU_SECONDS = 10.0   # and repeats that sample for about this long
 
-ROW_KEYS = ("x", "residual", "ids", "gate", "up", "a", "b", "pos")
+ROW_KEYS = ("x", "residual", "ids", "gate", "up", "a", "b", "pos", "q", "k")
 
 
 def slice_rows(arrays: dict, params: dict, rows: int):
@@ -456,11 +468,11 @@ def oracle_sample(data=None, fraction=SAMPLE_FRACTION):
     cases = W.cases(W.PREFILL)
     sample = []
     rows = max(1, 8192 // fraction)
-    for op, case in STEP:
+    for op, names in STEP:
         if data is not None:
             arrays, params = slice_rows(*data[op], rows)
         else:
-            arrays, params = cases[case](rows=(0, rows))
+            arrays, params = combine(op, [cases[c](rows=(0, rows)) for c in names])
         bts, _ = op_bytes(op, arrays, params)
         f32 = {k: (o.bf16_widen(v) if v.dtype == np.uint16 else np.ascontiguousarray(v))
                for k, v in arrays.items()}
@@ -476,8 +488,9 @@ def oracle_step(sample):
             o.embedding(a["table"], a["ids"])
         elif op == "add_rmsnorm":
             o.add_rmsnorm(a["x"], a["residual"], a["w"], p["eps"], h_bf16=True)
-        elif op.startswith("rope"):
-            o.rope(a["x"], a["pos"], a["inv_freq"], p["r"], p["mu"], p["layout"])
+        elif op.startswith("rope_qk"):
+            o.rope(a["q"], a["pos"], a["inv_freq"], p["r"], p["mu"], p["layout"])
+            o.rope(a["k"], a["pos"], a["inv_freq"], p["r"], p["mu"], p["layout"])
         elif op == "silu_mul":
             o.silu_mul(a["gate"], a["up"])
         elif op == "add":

@@ -56,6 +56,9 @@ def lib() -> ctypes.CDLL:
                 "gbe_rmsnorm": [vp, vp, vp, i64, i64, f32, i32, vp],
                 "gbe_add_rmsnorm": [vp, vp, vp, vp, vp, i64, i64, f32, i32, vp],
                 "gbe_rope": [vp, vp, vp, i64, i64, i64, i64, vp, f32, i32, i32, vp],
+                "gbe_rope_qk": [vp, vp, i64, i64, vp, vp, i64, i64, vp, i64, i64, i64, vp, vp, i64, f32, i32,
+                                i32, vp],
+                "gbe_rope_cos_sin": [vp, i64, i64, vp, vp],
                 "gbe_silu_mul": [vp, vp, vp, i64, i32, vp],
                 "gbe_add": [vp, vp, vp, i64, i32, vp],
                 "gbe_embedding": [vp, vp, vp, i64, i64, i64, vp, i32, vp],
@@ -144,6 +147,58 @@ def gbe_rope(x, y, pos, inv_freq, r: int, mu: float = 1.0, layout: int = 0, stre
                                       _dt(x, y), _stream(stream)))
 
 
+def _rows_view(t: torch.Tensor, D: int):
+    """(T, H, token stride) of a [T, H, D] view whose heads and entries are
+    contiguous but whose tokens may be strided (a slice of a QKV buffer)."""
+    if t.dim() != 3 or t.shape[2] != D or t.stride(2) != 1 or (t.shape[1] > 1 and t.stride(1) != D):
+        raise ValueError("rope_qk: operands are [T, H, D] views with contiguous heads")
+    return t.shape[0], t.shape[1], t.stride(0) if t.shape[0] > 1 else t.shape[1] * D
+
+
+def gbe_rope_qk(q, q_out, k, k_out, pos, inv_freq, r: int, mu: float = 1.0, layout: int = 0,
+                cos_sin=None, stream=None) -> None:
+    """q, k (and their outputs, which may be the same views): [T, H, D] views
+    of one storage type whose token stride may exceed H * D."""
+    ts = [t for t in (q, q_out, k, k_out, pos, inv_freq) if t is not None]
+    for t in ts:
+        if not t.is_cuda:
+            raise ValueError("tensors must be on the CUDA device")
+    D = (q if q is not None else k).shape[2]
+    T = (q if q is not None else k).shape[0]
+    sides = []
+    for x, y in ((q, q_out), (k, k_out)):
+        if x is None:
+            sides.append((None, None, 0, 0))
+            continue
+        Tx, H, sx = _rows_view(x, D)
+        _, _, sy = _rows_view(y, D)
+        if Tx != T or y.shape != x.shape or sx != sy:
+            raise ValueError("rope_qk: an output has its input's shape and token stride")
+        sides.append((x.data_ptr(), y.data_ptr(), sx, H))
+    if pos.dtype != torch.int32 or pos.numel() != T or not pos.is_contiguous():
+        raise ValueError("rope_qk: pos is int32[T]")
+    if inv_freq.dtype != torch.float32 or inv_freq.numel() < r // 2:
+        raise ValueError("rope_qk: inv_freq is float32[r/2]")
+    cache_len = 0
+    if cos_sin is not None:
+        if cos_sin.dtype != torch.float32 or not cos_sin.is_contiguous() or (r and cos_sin.numel() % r):
+            raise ValueError("rope_qk: cos_sin is float32[cache_len, r/2, 2]")
+        cache_len = cos_sin.numel() // r if r else 0
+    floats = [t for t in (q, q_out, k, k_out) if t is not None]
+    (qx, qy, qs, hq), (kx, ky, ks, hk) = sides
+    _check("gbe_rope_qk", lib().gbe_rope_qk(qx, qy, qs, hq, kx, ky, ks, hk, _ptr(pos), T, D, r, _ptr(inv_freq),
+                                            _ptr(cos_sin), cache_len, mu, layout, _dt(*floats), _stream(stream)))
+
+
+def gbe_rope_cos_sin(cos_sin, inv_freq, r: int, stream=None) -> None:
+    _dev(cos_sin, inv_freq)
+    if cos_sin.dtype != torch.float32 or (r and cos_sin.numel() % r) or inv_freq.dtype != torch.float32:
+        raise ValueError("rope_cos_sin: cos_sin is float32[cache_len, r/2, 2], inv_freq float32[r/2]")
+    cache_len = cos_sin.numel() // r if r else 0
+    _check("gbe_rope_cos_sin", lib().gbe_rope_cos_sin(_ptr(cos_sin), cache_len, r, _ptr(inv_freq),
+                                                      _stream(stream)))
+
+
 def gbe_silu_mul(gate, up, y, stream=None) -> None:
     _dev(gate, up, y)
     if not (gate.shape == up.shape == y.shape):
@@ -201,6 +256,12 @@ def rope(x, pos, inv_freq, r: int, mu: float = 1.0, layout: int = 0, in_place: b
     y = x if in_place else torch.empty_like(x)
     gbe_rope(x, y, pos, inv_freq, r, mu, layout, stream)
     return y
+
+
+def rope_cos_sin(inv_freq, r: int, cache_len: int, stream=None):
+    t = torch.empty((cache_len, r // 2, 2), dtype=torch.float32, device=inv_freq.device)
+    gbe_rope_cos_sin(t, inv_freq, r, stream)
+    return t
 
 
 def silu_mul(gate, up, stream=None):

@@ -91,6 +91,36 @@ bool overlaps(const Buf& a, const Buf& b) {
 
 bool same(const Buf& a, const Buf& b) { return a.p == b.p && a.bytes == b.bytes; }
 
+// A strided 2-D region: `rows` rows of `width` bytes, `stride` bytes apart
+// (width <= stride).  Used for q and k slices of one fused QKV buffer, whose
+// rows interleave without sharing a byte.
+struct Rows {
+    const void* p;
+    int64_t rows, stride, width;
+    Buf extent() const {
+        return {p, rows > 0 && width > 0 ? (uint64_t)((rows - 1) * stride + width) : 0u, 1};
+    }
+};
+
+bool rows_overlap(const Rows& a, const Rows& b) {
+    if (!overlaps(a.extent(), b.extent())) return false;
+    if (a.stride != b.stride || a.stride <= 0) return true;  // cannot tell: treat as overlapping
+    const int64_t s = a.stride;
+    const int64_t delta = (int64_t)(reinterpret_cast<intptr_t>(b.p) - reinterpret_cast<intptr_t>(a.p));
+    // rows t of a and u = t + m of b meet iff -b.width < delta + m * s < a.width
+    auto fdiv = [](int64_t n, int64_t d) { return n >= 0 ? n / d : -((-n + d - 1) / d); };
+    for (int64_t m = fdiv(-b.width - delta, s); m * s < a.width - delta + s; ++m) {
+        const int64_t off = delta + m * s;
+        if (!(off > -b.width && off < a.width)) continue;
+        if (m > -a.rows && m < b.rows) return true;  // some t in [0, a.rows) has t + m in [0, b.rows)
+    }
+    return false;
+}
+
+bool rows_same(const Rows& a, const Rows& b) {
+    return a.p == b.p && a.rows == b.rows && a.stride == b.stride && a.width == b.width;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // bytes = count * esize without overflow; false when it would overflow
@@ -206,27 +236,111 @@ int gbe_add_rmsnorm(const void* x, const void* residual, const void* w, void* y,
     return finish(gbe::launch_rmsnorm(x, residual, w, y, h, rows, d, eps, dtype, vec, as_stream(stream)));
 }
 
-int gbe_rope(const void* x, void* y, const int32_t* pos, int64_t T, int64_t H, int64_t D, int64_t r,
-             const float* inv_freq, float mu, int layout, int dtype, gbe_stream stream) {
+// Shared checks and launch of gbe_rope and gbe_rope_qk.  Operand k of the
+// call: input xs[k], output ys[k], H[k] heads, token stride strides[k].
+static int rope_common(const void* const xs[2], void* const ys[2], const int64_t H[2], const int64_t strides[2],
+                       const int32_t* pos, int64_t T, int64_t D, int64_t r, const float* inv_freq,
+                       const float* cos_sin, int64_t cache_len, float mu, int layout, int dtype,
+                       gbe_stream stream) {
     const int es = elem_size(dtype);
     if (!es) return GBE_ERR_DTYPE;
     if (layout != 0 && layout != 1) return GBE_ERR_LAYOUT;
-    if (T < 0 || H < 0 || D <= 0 || T > INT32_MAX) return GBE_ERR_SHAPE;
-    int64_t hd, n;
-    if (!mul_ok(H, D, &hd) || hd > INT32_MAX / 2 || !mul_ok(T, hd, &n)) return GBE_ERR_SHAPE;
-    if (r < 0 || r > D || (r & 1) || !std::isfinite(mu)) return GBE_ERR_ROTARY;
-    uint64_t bx, bp, bf;
-    if (!extent(n, es, &bx) || !extent(T, 4, &bp) || !extent(r / 2, 4, &bf)) return GBE_ERR_SHAPE;
-    if (n == 0) return GBE_OK;
-    if (x == y && r == 0) {  // in place with nothing to rotate: still validate the buffer
-        const Buf b[1] = {{y, bx, (uint64_t)es}};
-        return check_all(b, 0, [](int, int) { return false; });
+    if (T < 0 || D <= 0 || T > INT32_MAX || D > INT32_MAX) return GBE_ERR_SHAPE;
+    for (int k = 0; k < 2; ++k) {
+        int64_t hd;
+        if (H[k] < 0 || !mul_ok(H[k], D, &hd) || hd > INT32_MAX / 2) return GBE_ERR_SHAPE;
+        if (H[k] > 0 && (strides[k] < hd || strides[k] > INT64_MAX / (T > 0 ? T : 1) / es)) return GBE_ERR_SHAPE;
     }
-    const Buf bufs[4] = {{y, bx, (uint64_t)es}, {x, bx, (uint64_t)es}, {pos, bp, 4}, {inv_freq, bf, 4}};
-    const int st = check_all(bufs, 1, [](int o, int j) { return o == 0 && j == 1; });
+    if (r < 0 || r > D || (r & 1) || !std::isfinite(mu)) return GBE_ERR_ROTARY;
+    if (cos_sin != nullptr && cache_len < 0) return GBE_ERR_SHAPE;
+    const int64_t half = r / 2;
+    Rows in[2], out[2];
+    bool any = false;
+    for (int k = 0; k < 2; ++k) {
+        const int64_t rows = H[k] > 0 ? T : 0;
+        in[k] = {xs[k], rows, strides[k] * es, H[k] * D * es};
+        out[k] = {ys[k], rows, strides[k] * es, H[k] * D * es};
+        any = any || (rows > 0 && D > 0);
+    }
+    if (!any) return GBE_OK;
+    uint64_t bp, bf, bc = 0;
+    int64_t nc = 0;
+    if (!extent(T, 4, &bp) || !extent(half, 4, &bf)) return GBE_ERR_SHAPE;
+    if (cos_sin != nullptr && (!mul_ok(cache_len, half, &nc) || !extent(nc, 8, &bc))) return GBE_ERR_SHAPE;
+    // 0, 1 = outputs; 2, 3 = inputs; 4 = pos; 5 = inv_freq; 6 = cos/sin table
+    Buf bufs[7] = {out[0].extent(), out[1].extent(), in[0].extent(), in[1].extent(),
+                   {pos, bp, 4}, {inv_freq, bf, 4}, {cos_sin, cos_sin ? bc : 0u, 8}};
+    for (int k = 0; k < 4; ++k) bufs[k].align = (uint64_t)es;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        t_last_cuda_error = (int)cudaGetLastError();
+        return GBE_ERR_CUDA;
+    }
+    for (const Buf& b : bufs) {
+        const int st = check_buf(b, dev);
+        if (st != GBE_OK) return st;
+    }
+    for (int o = 0; o < 2; ++o) {
+        // an output may be exactly its own input; it may share no byte with
+        // the other operand (input or output) nor with the small arrays
+        if (rows_overlap(out[o], in[o]) && !rows_same(out[o], in[o])) return GBE_ERR_ALIAS;
+        if (rows_overlap(out[o], in[1 - o]) || rows_overlap(out[o], out[1 - o])) return GBE_ERR_ALIAS;
+        for (int j = 4; j < 7; ++j)
+            if (overlaps(bufs[o], bufs[j])) return GBE_ERR_ALIAS;
+    }
+    const bool vec = aligned16(xs[0]) && aligned16(ys[0]) && aligned16(xs[1]) && aligned16(ys[1]) &&
+                     (strides[0] * es) % 16 == 0 && (strides[1] * es) % 16 == 0;
+    gbe::RopeArgs a;
+    for (int k = 0; k < 2; ++k) a.side[k] = {xs[k], ys[k], strides[k], H[k] > 0 ? H[k] : 0};
+    a.pos = pos;
+    a.T = T;
+    a.D = D;
+    a.r = r;
+    a.inv_freq = inv_freq;
+    a.cos_sin = cos_sin;
+    a.cache_len = cos_sin ? cache_len : 0;
+    a.mu = mu;
+    a.layout = layout;
+    if (xs[0] == ys[0] && xs[1] == ys[1] && r == 0) return GBE_OK;  // in place, nothing to rotate
+    return finish(gbe::launch_rope(a, dtype, vec, as_stream(stream)));
+}
+
+int gbe_rope(const void* x, void* y, const int32_t* pos, int64_t T, int64_t H, int64_t D, int64_t r,
+             const float* inv_freq, float mu, int layout, int dtype, gbe_stream stream) {
+    const void* xs[2] = {x, nullptr};
+    void* ys[2] = {y, nullptr};
+    int64_t hd = 0;
+    if (H > 0 && D > 0 && !mul_ok(H, D, &hd)) return GBE_ERR_SHAPE;
+    const int64_t Hs[2] = {H, 0};
+    const int64_t strides[2] = {hd, 0};
+    return rope_common(xs, ys, Hs, strides, pos, T, D, r, inv_freq, nullptr, 0, mu, layout, dtype, stream);
+}
+
+int gbe_rope_qk(const void* q, void* q_out, int64_t q_stride, int64_t Hq, const void* k, void* k_out,
+                int64_t k_stride, int64_t Hk, const int32_t* pos, int64_t T, int64_t D, int64_t r,
+                const float* inv_freq, const float* cos_sin, int64_t cache_len, float mu, int layout, int dtype,
+                gbe_stream stream) {
+    const void* xs[2] = {q, k};
+    void* ys[2] = {q_out, k_out};
+    const int64_t Hs[2] = {Hq, Hk};
+    const int64_t strides[2] = {q_stride, k_stride};
+    return rope_common(xs, ys, Hs, strides, pos, T, D, r, inv_freq, cos_sin, cache_len, mu, layout, dtype,
+                       stream);
+}
+
+int gbe_rope_cos_sin(float* cos_sin, int64_t cache_len, int64_t r, const float* inv_freq, gbe_stream stream) {
+    if (cache_len < 0 || cache_len > INT32_MAX || r < 0 || (r & 1) || r > INT32_MAX) {
+        return cache_len < 0 ? GBE_ERR_SHAPE : GBE_ERR_ROTARY;
+    }
+    const int64_t half = r / 2;
+    int64_t n;
+    uint64_t bc, bf;
+    if (!mul_ok(cache_len, half, &n) || !extent(n, 8, &bc) || !extent(half, 4, &bf)) return GBE_ERR_SHAPE;
+    if (n == 0) return GBE_OK;
+    const Buf bufs[2] = {{cos_sin, bc, 8}, {inv_freq, bf, 4}};
+    const int st = check_all(bufs, 1, [](int, int) { return false; });
     if (st != GBE_OK) return st;
-    const bool vec = aligned16(x) && aligned16(y);
-    return finish(gbe::launch_rope(x, y, pos, T, H, D, r, inv_freq, mu, layout, dtype, vec, as_stream(stream)));
+    return finish(gbe::launch_rope_cos_sin(cos_sin, cache_len, r, inv_freq, as_stream(stream)));
 }
 
 static int pointwise(const void* a, const void* b, void* y, int64_t n, int dtype, gbe_stream stream, bool silu) {

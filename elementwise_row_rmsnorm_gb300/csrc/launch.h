@@ -12,8 +12,28 @@ namespace gbe {
 cudaError_t launch_rmsnorm(const void* x, const void* res, const void* w, void* y, void* h, int64_t rows,
                            int64_t d, float eps, int dtype, bool vec, cudaStream_t st);
 
-cudaError_t launch_rope(const void* x, void* y, const int32_t* pos, int64_t T, int64_t H, int64_t D, int64_t r,
-                        const float* inv_freq, float mu, int layout, int dtype, bool vec, cudaStream_t st);
+// RoPE over one or two [T, H, D] operands (q and k) that share positions and
+// frequencies; each operand has a token stride (elements) used for its input
+// and its output.  cos_sin: NULL, or a [cache_len, r/2] table of (cos, sin).
+struct RopeArgs {
+    struct Side {
+        const void* x;
+        void* y;
+        int64_t stride;
+        int64_t H;
+    } side[2];
+    const int32_t* pos;
+    int64_t T, D, r;
+    const float* inv_freq;
+    const float* cos_sin;
+    int64_t cache_len;
+    float mu;
+    int layout;
+};
+
+cudaError_t launch_rope(const RopeArgs& a, int dtype, bool vec, cudaStream_t st);
+
+cudaError_t launch_rope_cos_sin(float* cos_sin, int64_t len, int64_t r, const float* inv_freq, cudaStream_t st);
 
 cudaError_t launch_silu_mul(const void* gate, const void* up, void* y, int64_t n, int dtype, bool vec,
                             cudaStream_t st);

@@ -21,6 +21,14 @@
 // run in place (y == x).  Out of place, entries r .. D-1 are copied; in
 // place they are not touched at all.
 //
+// One launch may serve two operands that share positions and frequencies
+// (q and k), each with its own token stride, so q and k can be slices of a
+// fused QKV buffer.  Optionally the cos / sin come from a table indexed by
+// position ("Operations", section 3, Cos/sin cache; "Elementwise kernels in
+// C", Going further), built by rope_cos_sin_table with the very same
+// arithmetic, so the cached and the formed results agree bit for bit; a
+// position outside the table is formed instead of read.
+//
 // The rotation is written with explicit rounding intrinsics, in the order of
 // the definition: mu * ((a * c) - (b * s)) and mu * ((a * s) + (b * c)).
 #include "common.cuh"
@@ -33,63 +41,91 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kHeadsPerThread = 4;  // heads a thread rotates with one set of angles
 
+// One [T, H, D] operand of a launch: input and output bases, their token
+// strides (in elements), and the number of threads this operand takes.
+struct Operand {
+    const char* x;
+    char* y;
+    int64_t xs, ys;
+    int H;
+    int NC;           // head chunks of kHeadsPerThread (vector path)
+    int copy_tail;    // out of place with r < D: entries r .. D-1 are copied
+    int64_t threads;  // threads of the launch that serve this operand
+};
+
 __device__ __forceinline__ void rotate(float a, float b, float c, float s, float mu, float& a2, float& b2) {
     a2 = __fmul_rn(mu, __fsub_rn(__fmul_rn(a, c), __fmul_rn(b, s)));
     b2 = __fmul_rn(mu, __fadd_rn(__fmul_rn(a, s), __fmul_rn(b, c)));
 }
 
+// cos / sin of the angle of pair i at position p: from the table when one is
+// given and p lies inside it (it holds exactly these values), else formed.
+template <bool CACHE>
+__device__ __forceinline__ void angle(int32_t p, int i, const float* inv_freq, const float2* cache,
+                                      int64_t cache_len, int half, float& c, float& s) {
+    if (CACHE && p >= 0 && p < cache_len) {
+        const float2 v = __ldg(cache + (int64_t)p * half + i);
+        c = v.x;
+        s = v.y;
+    } else {
+        sincosf(__fmul_rn((float)p, __ldg(inv_freq + i)), &s, &c);
+    }
+}
+
 // Aligned path.  A thread owns one group of P consecutive pairs (one 16-byte
 // vector of each pair member) of one token, for a chunk of up to 4 heads:
-// it issues the loads of all its heads first, forms the P angles and their
-// cos / sin in registers while those loads are in flight, then rotates and
-// stores every head.  Threads of one token and head chunk cover consecutive
-// 16-byte vectors, so each warp-wide access is contiguous.
-template <int DT, int LAYOUT>
+// it issues the loads of all its heads first, gets the P angles' cos / sin
+// into registers while those loads are in flight, then rotates and stores
+// every head.  Threads of one token and head chunk cover consecutive 16-byte
+// vectors, so each warp-wide access is contiguous.  The launch's threads
+// serve operand A first, then operand B.
+template <int DT, int LAYOUT, bool CACHE>
 __global__ void __launch_bounds__(kThreads)
-rope_vec(const void* x, void* y, const int32_t* pos, int64_t T, int H, int D, int r, const float* inv_freq,
-         float mu, int copy_tail) {
+rope_vec(Operand A, Operand B, const int32_t* pos, int64_t T, int D, int r, const float* inv_freq,
+         const float2* cache, int64_t cache_len, float mu) {
     using S = Store<DT>;
     constexpr int V = S::V;
     constexpr int P = LAYOUT == 0 ? V : V / 2;  // pairs per 16-byte item
     constexpr int64_t ES = sizeof(typename S::T);
     constexpr int HC = kHeadsPerThread;
+    int64_t gt = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const bool second = gt >= A.threads;
+    const Operand R = second ? B : A;
+    if (second) gt -= A.threads;
+    if (gt >= R.threads) return;
     const int half = r >> 1;
     const int G = LAYOUT == 0 ? half / V : r / V;  // items per head
-    const int NC = (H + HC - 1) / HC;              // head chunks per token
-    const int64_t gt = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     const int g = (int)(gt % G);
     const int64_t rest = gt / G;
-    const int hc = (int)(rest % NC);
-    const int64_t t = rest / NC;
-    if (t >= T) return;
+    const int hc = (int)(rest % R.NC);
+    const int64_t t = rest / R.NC;
     const int h0 = hc * HC;
-    const int nh = min(HC, H - h0);
-    const char* px = static_cast<const char*>(x);
-    char* py = static_cast<char*>(y);
-    const int64_t row0 = (t * H + h0) * (int64_t)D;  // element offset of (t, h0, 0)
-    const int64_t ia = (int64_t)g * V;                // first entry of the item in a head
-    const int64_t hb = (int64_t)half * ES;            // byte distance to the b member (layout 0)
+    const int nh = min(HC, R.H - h0);
+    const char* xr = R.x + (t * R.xs + (int64_t)h0 * D) * ES;  // (t, h0, 0)
+    char* yr = R.y + (t * R.ys + (int64_t)h0 * D) * ES;
+    const int64_t ia = (int64_t)g * V * ES;       // byte offset of the item in a head
+    const int64_t hb = (int64_t)half * ES;        // byte distance to the b member (layout 0)
+    const int64_t hd = (int64_t)D * ES;           // byte distance between heads
 
     Vec16 va[HC], vb[HC];
 #pragma unroll
     for (int j = 0; j < HC; ++j) {
         if (j < nh) {
-            const char* p = px + (row0 + (int64_t)j * D + ia) * ES;
-            va[j] = ld_stream(p);
-            if (LAYOUT == 0) vb[j] = ld_stream(p + hb);
+            va[j] = ld_stream(xr + j * hd + ia);
+            if (LAYOUT == 0) vb[j] = ld_stream(xr + j * hd + ia + hb);
         }
     }
-    // the angles of this thread's pairs, once for all its heads
+    // this thread's pairs, once for all its heads
     float c[P], sn[P];
-    const float pf = (float)pos[t];
+    const int32_t p = pos[t];
     const int i0 = g * P;
 #pragma unroll
-    for (int e = 0; e < P; ++e) sincosf(__fmul_rn(pf, __ldg(inv_freq + i0 + e)), &sn[e], &c[e]);
+    for (int e = 0; e < P; ++e) angle<CACHE>(p, i0 + e, inv_freq, cache, cache_len, half, c[e], sn[e]);
 
 #pragma unroll
     for (int j = 0; j < HC; ++j) {
         if (j < nh) {
-            char* q = py + (row0 + (int64_t)j * D + ia) * ES;
+            char* q = yr + j * hd + ia;
             float fa[V];
             S::unpack(va[j], fa);
             if (LAYOUT == 0) {
@@ -118,90 +154,135 @@ rope_vec(const void* x, void* y, const int32_t* pos, int64_t T, int H, int D, in
     }
     // pass-through entries, out of place only: the G threads of this token and
     // head chunk share the (D - r) / V tail vectors of each head
-    if (copy_tail) {
+    if (R.copy_tail) {
         const int GT = (D - r) / V;
         for (int j = 0; j < nh; ++j)
             for (int k = g; k < GT; k += G) {
-                const int64_t o = (row0 + (int64_t)j * D + r + (int64_t)k * V) * ES;
-                st_stream(py + o, ld_stream(px + o));
+                const int64_t o = j * hd + ((int64_t)r + (int64_t)k * V) * ES;
+                st_stream(yr + o, ld_stream(xr + o));
             }
     }
 }
 
 // Unaligned path (or widths that do not split into 16-byte vectors): a
-// thread owns one pair of one token, forms its angle once and rotates that
-// pair in every head; the tail is copied entry by entry.
-template <int DT, int LAYOUT>
+// thread owns one pair of one token, gets its angle once and rotates that
+// pair in every head; tail threads copy one entry per head.
+template <int DT, int LAYOUT, bool CACHE>
 __global__ void __launch_bounds__(kThreads)
-rope_scalar(const void* x, void* y, const int32_t* pos, int64_t T, int H, int D, int r, const float* inv_freq,
-            float mu, int copy_tail) {
+rope_scalar(Operand A, Operand B, const int32_t* pos, int64_t T, int D, int r, const float* inv_freq,
+            const float2* cache, int64_t cache_len, float mu) {
     using S = Store<DT>;
+    constexpr int64_t ES = sizeof(typename S::T);
+    int64_t gt = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const bool second = gt >= A.threads;
+    const Operand R = second ? B : A;
+    if (second) gt -= A.threads;
+    if (gt >= R.threads) return;
     const int half = r >> 1;
-    const int per_tok = half + (copy_tail ? D - r : 0);
-    const int64_t gt = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int per_tok = half + (R.copy_tail ? D - r : 0);
     const int64_t t = gt / per_tok;
     const int k = (int)(gt - t * per_tok);
-    if (t >= T) return;
     if (k < half) {
         float c, sn;
-        sincosf(__fmul_rn((float)pos[t], __ldg(inv_freq + k)), &sn, &c);
+        angle<CACHE>(pos[t], k, inv_freq, cache, cache_len, half, c, sn);
         const int ia = LAYOUT == 0 ? k : 2 * k;
         const int ib = LAYOUT == 0 ? k + half : 2 * k + 1;
-        for (int h = 0; h < H; ++h) {
-            const int64_t row = (t * H + h) * (int64_t)D;
-            const float a = S::load1(x, row + ia), b = S::load1(x, row + ib);
+        for (int h = 0; h < R.H; ++h) {
+            const int64_t xo = t * R.xs + (int64_t)h * D, yo = t * R.ys + (int64_t)h * D;
+            const float a = S::load1(R.x, xo + ia), b = S::load1(R.x, xo + ib);
             float a2, b2;
             rotate(a, b, c, sn, mu, a2, b2);
-            S::store1(y, row + ia, a2);
-            S::store1(y, row + ib, b2);
+            S::store1(R.y, yo + ia, a2);
+            S::store1(R.y, yo + ib, b2);
         }
     } else {
         const int j = r + (k - half);
-        for (int h = 0; h < H; ++h) {
-            const int64_t o = (t * H + h) * (int64_t)D + j;
-            if (sizeof(typename S::T) == 4)
-                static_cast<uint32_t*>(y)[o] = static_cast<const uint32_t*>(x)[o];
+        for (int h = 0; h < R.H; ++h) {
+            const int64_t xo = t * R.xs + (int64_t)h * D + j, yo = t * R.ys + (int64_t)h * D + j;
+            if (ES == 4)
+                reinterpret_cast<uint32_t*>(R.y)[yo] = reinterpret_cast<const uint32_t*>(R.x)[xo];
             else
-                static_cast<uint16_t*>(y)[o] = static_cast<const uint16_t*>(x)[o];
+                reinterpret_cast<uint16_t*>(R.y)[yo] = reinterpret_cast<const uint16_t*>(R.x)[xo];
         }
     }
 }
 
+// The cos / sin table: entry (p, i) = (cos, sin) of float(p) * omega_i, formed
+// exactly as the RoPE kernels form it.
+__global__ void __launch_bounds__(kThreads)
+rope_cos_sin_table(float2* cache, int64_t len, int half, const float* inv_freq) {
+    const int64_t gt = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int64_t p = gt / half;
+    if (p >= len) return;
+    const int i = (int)(gt - p * half);
+    float c, s;
+    sincosf(__fmul_rn((float)p, __ldg(inv_freq + i)), &s, &c);
+    cache[gt] = make_float2(c, s);
+}
+
 template <int DT>
-cudaError_t launch_dt(const void* x, void* y, const int32_t* pos, int64_t T, int64_t H, int64_t D, int64_t r,
-                      const float* inv_freq, float mu, int layout, bool vec, cudaStream_t st) {
+cudaError_t launch_dt(const RopeArgs& a, bool vec, cudaStream_t st) {
     constexpr int V = Store<DT>::V;
-    const int64_t half = r / 2;
-    const bool copy_tail = x != y && r < D;
-    vec = vec && r > 0 && D % V == 0 && (layout == 0 ? half % V == 0 : r % V == 0);
-    const int Hi = (int)H, Di = (int)D, ri = (int)r, ct = copy_tail ? 1 : 0;
-    if (vec) {
-        const int64_t G = layout == 0 ? half / V : r / V;
-        const int64_t NC = (H + kHeadsPerThread - 1) / kHeadsPerThread;
-        const int64_t threads = T * NC * G;
-        const int64_t grid = (threads + kThreads - 1) / kThreads;
-        if (layout == 0)
-            rope_vec<DT, 0><<<(unsigned)grid, kThreads, 0, st>>>(x, y, pos, T, Hi, Di, ri, inv_freq, mu, ct);
-        else
-            rope_vec<DT, 1><<<(unsigned)grid, kThreads, 0, st>>>(x, y, pos, T, Hi, Di, ri, inv_freq, mu, ct);
-    } else {
-        const int64_t per_tok = half + (copy_tail ? D - r : 0);
-        if (per_tok == 0) return cudaSuccess;
-        const int64_t grid = (T * per_tok + kThreads - 1) / kThreads;
-        if (layout == 0)
-            rope_scalar<DT, 0><<<(unsigned)grid, kThreads, 0, st>>>(x, y, pos, T, Hi, Di, ri, inv_freq, mu, ct);
-        else
-            rope_scalar<DT, 1><<<(unsigned)grid, kThreads, 0, st>>>(x, y, pos, T, Hi, Di, ri, inv_freq, mu, ct);
+    const int64_t half = a.r / 2;
+    const bool cached = a.cos_sin != nullptr;
+    const float2* cache = reinterpret_cast<const float2*>(a.cos_sin);
+    vec = vec && a.r > 0 && a.D % V == 0 && (a.layout == 0 ? half % V == 0 : a.r % V == 0);
+    Operand op[2];
+    for (int k = 0; k < 2; ++k) {
+        const RopeArgs::Side& sd = a.side[k];
+        op[k].x = static_cast<const char*>(sd.x);
+        op[k].y = static_cast<char*>(sd.y);
+        op[k].xs = sd.stride;
+        op[k].ys = sd.stride;
+        op[k].H = (int)sd.H;
+        op[k].copy_tail = (sd.x != sd.y && a.r < a.D) ? 1 : 0;
+        op[k].NC = (int)((sd.H + kHeadsPerThread - 1) / kHeadsPerThread);
+        if (sd.H == 0 || a.T == 0) {
+            op[k].threads = 0;
+        } else if (vec) {
+            const int64_t G = a.layout == 0 ? half / V : a.r / V;
+            op[k].threads = a.T * op[k].NC * G;
+        } else {
+            op[k].threads = a.T * (half + (op[k].copy_tail ? a.D - a.r : 0));
+        }
     }
+    const int64_t threads = op[0].threads + op[1].threads;
+    if (threads == 0) return cudaSuccess;
+    const unsigned grid = (unsigned)((threads + kThreads - 1) / kThreads);
+    const int Di = (int)a.D, ri = (int)a.r;
+#define GBE_ROPE(KERNEL, L, C)                                                                               \
+    KERNEL<DT, L, C><<<grid, kThreads, 0, st>>>(op[0], op[1], a.pos, a.T, Di, ri, a.inv_freq, cache,         \
+                                                 a.cache_len, a.mu)
+    if (vec) {
+        if (a.layout == 0) {
+            if (cached) GBE_ROPE(rope_vec, 0, true); else GBE_ROPE(rope_vec, 0, false);
+        } else {
+            if (cached) GBE_ROPE(rope_vec, 1, true); else GBE_ROPE(rope_vec, 1, false);
+        }
+    } else {
+        if (a.layout == 0) {
+            if (cached) GBE_ROPE(rope_scalar, 0, true); else GBE_ROPE(rope_scalar, 0, false);
+        } else {
+            if (cached) GBE_ROPE(rope_scalar, 1, true); else GBE_ROPE(rope_scalar, 1, false);
+        }
+    }
+#undef GBE_ROPE
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_rope(const void* x, void* y, const int32_t* pos, int64_t T, int64_t H, int64_t D, int64_t r,
-                        const float* inv_freq, float mu, int layout, int dtype, bool vec, cudaStream_t st) {
-    if (dtype == kF32) return launch_dt<kF32>(x, y, pos, T, H, D, r, inv_freq, mu, layout, vec, st);
-    return launch_dt<kBF16>(x, y, pos, T, H, D, r, inv_freq, mu, layout, vec, st);
+cudaError_t launch_rope(const RopeArgs& a, int dtype, bool vec, cudaStream_t st) {
+    return dtype == kF32 ? launch_dt<kF32>(a, vec, st) : launch_dt<kBF16>(a, vec, st);
+}
+
+cudaError_t launch_rope_cos_sin(float* cos_sin, int64_t len, int64_t r, const float* inv_freq, cudaStream_t st) {
+    const int64_t half = r / 2;
+    const int64_t n = len * half;
+    if (n == 0) return cudaSuccess;
+    rope_cos_sin_table<<<(unsigned)((n + kThreads - 1) / kThreads), kThreads, 0, st>>>(
+        reinterpret_cast<float2*>(cos_sin), len, (int)half, inv_freq);
+    return cudaGetLastError();
 }
 
 }  // namespace gbe

@@ -128,6 +128,44 @@ int gbe_rope(const void *x, void *y, const int32_t *pos, int64_t T, int64_t H, i
              const float *inv_freq, float mu, int layout, int dtype, gbe_stream stream);
 
 /*
+ * gbe_rope_qk -- RoPE of q and k in one launch, from strided slices, with an
+ * optional cos/sin table.
+ *   The rotation of gbe_rope ("Elementwise kernels in C", section 2.2;
+ *   "Operations", section 3), applied to two operands that share positions
+ *   and frequencies (one angle serves every head of q and of k).  The cos /
+ *   sin table is the precomputed cos[pos, i] / sin[pos, i] of "Operations",
+ *   section 3 (Cos/sin cache), here an accelerator: the results are the same
+ *   bits with or without it.
+ * q     : [T, Hq, D] with token stride q_stride (elements, >= Hq * D), so q
+ *         may be a column slice of a fused QKV buffer; q_out has the same
+ *         shape and stride (q_out == q: in place).  Hq = 0: no q.
+ * k     : likewise with Hk, k_stride, k_out.
+ * pos, inv_freq, r, mu, layout, dtype : as for gbe_rope.
+ * cos_sin : NULL (angles are formed), or a device table of cache_len * r/2
+ *         (cos, sin) f32 pairs, entry p * (r/2) + i for position p and pair
+ *         i, as gbe_rope_cos_sin writes it for the same r and inv_freq; a
+ *         position outside [0, cache_len) is formed instead of read.  8-byte
+ *         aligned.
+ * Alias: q_out == q and k_out == k allowed; q and k may interleave in one
+ * buffer (their rows sharing no byte), which the checks resolve row by row.
+ */
+int gbe_rope_qk(const void *q, void *q_out, int64_t q_stride, int64_t Hq, const void *k, void *k_out,
+                int64_t k_stride, int64_t Hk, const int32_t *pos, int64_t T, int64_t D, int64_t r,
+                const float *inv_freq, const float *cos_sin, int64_t cache_len, float mu, int layout, int dtype,
+                gbe_stream stream);
+
+/*
+ * gbe_rope_cos_sin -- build the cos/sin table for gbe_rope_qk.
+ *   "Operations", section 3 (Cos/sin cache): for every position
+ *   0 <= p < cache_len and pair i < r/2, entry p * (r/2) + i is
+ *   (cos(theta), sin(theta)) with theta = float(p) * inv_freq[i], formed with
+ *   the same arithmetic as the RoPE kernels.
+ * cos_sin : device, f32[cache_len * r/2 * 2], 8-byte aligned, written.
+ * inv_freq : device f32[r/2].  r even, >= 0.  cache_len in [0, 2^31).
+ */
+int gbe_rope_cos_sin(float *cos_sin, int64_t cache_len, int64_t r, const float *inv_freq, gbe_stream stream);
+
+/*
  * gbe_silu_mul -- the elementwise core of SwiGLU.
  *   "Elementwise kernels in C", section 2.3; "Operations", section 4 (Silu, SwiGlu).
  *   y[i] = gate[i] / (1 + exp(-gate[i])) * up[i]

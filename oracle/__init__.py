@@ -68,6 +68,7 @@ class Oracle:
             "orc_add": [vp, vp, vp, i64],
             "orc_add_rmsnorm": [vp, vp, vp, vp, vp, i64, i64, f32, i32],
             "orc_rope": [vp, vp, vp, i64, i64, i64, i64, vp, f32, i32],
+            "orc_rope_cos_sin": [vp, i64, i64, vp],
             "orc_silu_mul": [vp, vp, vp, i64],
             "orc_embedding": [vp, vp, vp, i64, i64, i64],
             "orc_argmax": [vp, i64],
@@ -144,6 +145,15 @@ class Oracle:
         self._check(self.lib.orc_rope(_ptr(x), _ptr(y), _ptr(pos), T, H, D, r, _ptr(om), mu,
                                       layout), "rope")
         return y
+
+    def rope_cos_sin(self, inv_freq, r: int, length: int) -> np.ndarray:
+        """The [length, r/2, 2] table of (cos, sin) per position and pair."""
+        om = _f32(inv_freq)
+        if om.size < r // 2:
+            raise OracleError("rope_cos_sin: inv_freq needs r/2 entries")
+        out = np.empty((length, r // 2, 2), dtype=np.float32)
+        self._check(self.lib.orc_rope_cos_sin(_ptr(out), length, r, _ptr(om)), "rope_cos_sin")
+        return out
 
     def silu_mul(self, gate, up) -> np.ndarray:
         g, u = _f32(gate), _f32(up)

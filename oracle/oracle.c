@@ -188,6 +188,23 @@ int orc_rope(const float *x, float *y, const int32_t *pos, int64_t T, int64_t H,
     return ORC_OK;
 }
 
+/* ---- Cos/sin table -----------------------------------------------------------
+ * [Ops] 3 (Cos/sin cache): cos[pos, i] and sin[pos, i] precomputed for every
+ * position below max_seq.  Entry p * (r/2) + i holds (cos, sin) of the same
+ * f32 angle orc_rope forms, evaluated the same way, so a table-driven
+ * rotation equals the formed one.                                           */
+int orc_rope_cos_sin(float *cos_sin, int64_t len, int64_t r, const float *inv_freq) {
+    if (len < 0 || r < 0 || (r & 1)) return ORC_ERR_ARG;
+    const int64_t half = r / 2;
+    for (int64_t p = 0; p < len; ++p)
+        for (int64_t i = 0; i < half; ++i) {
+            float theta = (float)((double)p * (double)inv_freq[i]);
+            cos_sin[2 * (p * half + i)] = (float)cos((double)theta);
+            cos_sin[2 * (p * half + i) + 1] = (float)sin((double)theta);
+        }
+    return ORC_OK;
+}
+
 /* ---- SiLU-mul ----------------------------------------------------------------
  * [L9.6] 2.3 and [Ops] 4 (Silu): y = g / (1 + e^-g) * u, silu first, then the
  * product with u.  Written this way it saturates: for g -> -inf, e^-g

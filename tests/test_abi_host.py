@@ -29,8 +29,9 @@ def declared_functions():
 
 def test_header_declares_the_ops():
     names = declared_functions()
-    for op in ("gbe_rmsnorm", "gbe_add_rmsnorm", "gbe_rope", "gbe_silu_mul", "gbe_add", "gbe_embedding",
-               "gbe_argmax", "gbe_status_string", "gbe_version", "gbe_last_cuda_error"):
+    for op in ("gbe_rmsnorm", "gbe_add_rmsnorm", "gbe_rope", "gbe_rope_qk", "gbe_rope_cos_sin", "gbe_silu_mul",
+               "gbe_add", "gbe_embedding", "gbe_argmax", "gbe_status_string", "gbe_version",
+               "gbe_last_cuda_error"):
         assert op in names
 
 
@@ -90,6 +91,25 @@ def test_rejects_bad_sizes_and_scalars(L):
     assert L.gbe_argmax(NULL, NULL, 0, 0, 0, S) == 0
     assert L.gbe_argmax(NULL, NULL, 3, 1 << 31, 0, S) == 2
     assert L.gbe_argmax(NULL, NULL, 3, 10, 5, S) == 3
+
+
+def test_rope_qk_and_table_reject_bad_arguments(L):
+    def call(T=4, D=32, r=32, layout=0, mu=1.0, dtype=0, qs=64, ks=32, hq=2, hk=1, cache=None, clen=0):
+        return L.gbe_rope_qk(NULL, NULL, qs, hq, NULL, NULL, ks, hk, NULL, T, D, r, NULL, cache, clen, mu,
+                             layout, dtype, S)
+    assert call(layout=3) == 4
+    assert call(dtype=9) == 3
+    assert call(r=31) == 6 and call(r=34) == 6 and call(mu=float("nan")) == 6
+    assert call(D=0) == 2 and call(T=-1) == 2 and call(hq=-1) == 2
+    assert call(qs=63) == 2            # token stride shorter than Hq * D
+    assert call(ks=31) == 2
+    assert call(cache=1, clen=-1) == 2
+    assert call(T=0) == 0              # nothing to do
+    assert call(hq=0, hk=0) == 0
+    assert L.gbe_rope_cos_sin(NULL, -1, 8, NULL, S) == 2
+    assert L.gbe_rope_cos_sin(NULL, 10, 7, NULL, S) == 6
+    assert L.gbe_rope_cos_sin(NULL, 0, 8, NULL, S) == 0
+    assert L.gbe_rope_cos_sin(NULL, 10, 0, NULL, S) == 0
 
 
 def test_rejects_size_overflow(L):
