@@ -59,6 +59,8 @@ def lib() -> ctypes.CDLL:
                 "gbe_rope_qk": [vp, vp, i64, i64, vp, vp, i64, i64, vp, i64, i64, i64, vp, vp, i64, f32, i32,
                                 i32, vp],
                 "gbe_rope_cos_sin": [vp, i64, i64, vp, vp],
+                "gbe_qk_norm_rope": [vp, vp, i64, i64, vp, vp, vp, i64, i64, vp, f32, vp, i64, i64, i64, vp, vp,
+                                     i64, f32, i32, i32, vp],
                 "gbe_silu_mul": [vp, vp, vp, i64, i32, vp],
                 "gbe_add": [vp, vp, vp, i64, i32, vp],
                 "gbe_embedding": [vp, vp, vp, i64, i64, i64, vp, i32, vp],
@@ -188,6 +190,43 @@ def gbe_rope_qk(q, q_out, k, k_out, pos, inv_freq, r: int, mu: float = 1.0, layo
     (qx, qy, qs, hq), (kx, ky, ks, hk) = sides
     _check("gbe_rope_qk", lib().gbe_rope_qk(qx, qy, qs, hq, kx, ky, ks, hk, _ptr(pos), T, D, r, _ptr(inv_freq),
                                             _ptr(cos_sin), cache_len, mu, layout, _dt(*floats), _stream(stream)))
+
+
+def gbe_qk_norm_rope(q, q_out, gq, k, k_out, gk, eps: float, pos, inv_freq, r: int, mu: float = 1.0,
+                     layout: int = 0, cos_sin=None, stream=None) -> None:
+    """QK-norm (per-head RMSNorm with gains gq / gk of head_dim entries), then
+    RoPE; q, k and outputs as for gbe_rope_qk."""
+    for t in (q, q_out, k, k_out, gq, gk, pos, inv_freq, cos_sin):
+        if t is not None and not t.is_cuda:
+            raise ValueError("tensors must be on the CUDA device")
+    ref = q if q is not None else k
+    T, D = ref.shape[0], ref.shape[2]
+    sides = []
+    for x, y, g in ((q, q_out, gq), (k, k_out, gk)):
+        if x is None:
+            sides.append((None, None, None, 0, 0))
+            continue
+        Tx, H, sx = _rows_view(x, D)
+        _, _, sy = _rows_view(y, D)
+        if Tx != T or y.shape != x.shape or sx != sy:
+            raise ValueError("qk_norm_rope: an output has its input's shape and token stride")
+        if g is None or g.numel() != D or not g.is_contiguous() or g.dtype != x.dtype:
+            raise ValueError("qk_norm_rope: each gain has head_dim entries of the operand's dtype")
+        sides.append((x.data_ptr(), y.data_ptr(), g.data_ptr(), sx, H))
+    if pos.dtype != torch.int32 or pos.numel() != T or not pos.is_contiguous():
+        raise ValueError("qk_norm_rope: pos is int32[T]")
+    if inv_freq.dtype != torch.float32 or inv_freq.numel() < r // 2:
+        raise ValueError("qk_norm_rope: inv_freq is float32[r/2]")
+    cache_len = 0
+    if cos_sin is not None:
+        if cos_sin.dtype != torch.float32 or not cos_sin.is_contiguous() or (r and cos_sin.numel() % r):
+            raise ValueError("qk_norm_rope: cos_sin is float32[cache_len, r/2, 2]")
+        cache_len = cos_sin.numel() // r if r else 0
+    floats = [t for t in (q, q_out, k, k_out, gq, gk) if t is not None]
+    (qx, qy, qg, qs, hq), (kx, ky, kg, ks, hk) = sides
+    _check("gbe_qk_norm_rope", lib().gbe_qk_norm_rope(qx, qy, qs, hq, qg, kx, ky, ks, hk, kg, eps, _ptr(pos), T, D,
+                                                      r, _ptr(inv_freq), _ptr(cos_sin), cache_len, mu, layout,
+                                                      _dt(*floats), _stream(stream)))
 
 
 def gbe_rope_cos_sin(cos_sin, inv_freq, r: int, stream=None) -> None:

@@ -328,6 +328,76 @@ int gbe_rope_qk(const void* q, void* q_out, int64_t q_stride, int64_t Hq, const 
                        stream);
 }
 
+int gbe_qk_norm_rope(const void* q, void* q_out, int64_t q_stride, int64_t Hq, const void* gq, const void* k,
+                     void* k_out, int64_t k_stride, int64_t Hk, const void* gk, float eps, const int32_t* pos,
+                     int64_t T, int64_t D, int64_t r, const float* inv_freq, const float* cos_sin,
+                     int64_t cache_len, float mu, int layout, int dtype, gbe_stream stream) {
+    const int es = elem_size(dtype);
+    if (!es) return GBE_ERR_DTYPE;
+    if (layout != 0 && layout != 1) return GBE_ERR_LAYOUT;
+    if (T < 0 || D <= 0 || T > INT32_MAX || D > 32 * (16 / es)) return GBE_ERR_SHAPE;  // head_dim <= 32 chunks
+    if (!std::isfinite(eps) || eps < 0.0f) return GBE_ERR_EPS;
+    const int64_t Hs[2] = {Hq, Hk}, strides[2] = {q_stride, k_stride};
+    for (int j = 0; j < 2; ++j) {
+        int64_t hd;
+        if (Hs[j] < 0 || !mul_ok(Hs[j], D, &hd) || hd > INT32_MAX / 2) return GBE_ERR_SHAPE;
+        if (Hs[j] > 0 && (strides[j] < hd || strides[j] > INT64_MAX / (T > 0 ? T : 1) / es)) return GBE_ERR_SHAPE;
+    }
+    if (r < 0 || r > D || (r & 1) || !std::isfinite(mu)) return GBE_ERR_ROTARY;
+    if (cos_sin != nullptr && cache_len < 0) return GBE_ERR_SHAPE;
+    if ((Hq == 0 && Hk == 0) || T == 0) return GBE_OK;
+    const int64_t half = r / 2;
+    const void* xs[2] = {q, k};
+    void* ys[2] = {q_out, k_out};
+    const void* gs[2] = {gq, gk};
+    Rows in[2], out[2];
+    for (int j = 0; j < 2; ++j) {
+        const int64_t rows = Hs[j] > 0 ? T : 0;
+        in[j] = {xs[j], rows, strides[j] * es, Hs[j] * D * es};
+        out[j] = {ys[j], rows, strides[j] * es, Hs[j] * D * es};
+    }
+    uint64_t bp, bf, bg, bc = 0;
+    int64_t nc = 0;
+    if (!extent(T, 4, &bp) || !extent(half, 4, &bf) || !extent(D, es, &bg)) return GBE_ERR_SHAPE;
+    if (cos_sin != nullptr && (!mul_ok(cache_len, half, &nc) || !extent(nc, 8, &bc))) return GBE_ERR_SHAPE;
+    // 0, 1 outputs; 2, 3 inputs; 4, 5 gains; 6 pos; 7 inv_freq; 8 table
+    Buf bufs[9] = {out[0].extent(), out[1].extent(), in[0].extent(), in[1].extent(),
+                   {gq, Hq > 0 ? bg : 0u, (uint64_t)es}, {gk, Hk > 0 ? bg : 0u, (uint64_t)es},
+                   {pos, bp, 4}, {inv_freq, half > 0 ? bf : 0u, 4}, {cos_sin, cos_sin ? bc : 0u, 8}};
+    for (int j = 0; j < 4; ++j) bufs[j].align = (uint64_t)es;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        t_last_cuda_error = (int)cudaGetLastError();
+        return GBE_ERR_CUDA;
+    }
+    for (const Buf& b : bufs) {
+        const int st = check_buf(b, dev);
+        if (st != GBE_OK) return st;
+    }
+    for (int o = 0; o < 2; ++o) {
+        if (rows_overlap(out[o], in[o]) && !rows_same(out[o], in[o])) return GBE_ERR_ALIAS;
+        if (rows_overlap(out[o], in[1 - o]) || rows_overlap(out[o], out[1 - o])) return GBE_ERR_ALIAS;
+        for (int j = 4; j < 9; ++j)
+            if (overlaps(bufs[o], bufs[j])) return GBE_ERR_ALIAS;
+    }
+    const bool vec = aligned16(q) && aligned16(q_out) && aligned16(k) && aligned16(k_out) &&
+                     (Hq == 0 || aligned16(gq)) && (Hk == 0 || aligned16(gk)) && (q_stride * es) % 16 == 0 &&
+                     (k_stride * es) % 16 == 0;
+    gbe::QkNormRopeArgs a;
+    for (int j = 0; j < 2; ++j) a.side[j] = {xs[j], ys[j], gs[j], strides[j], Hs[j]};
+    a.eps = eps;
+    a.pos = pos;
+    a.T = T;
+    a.D = D;
+    a.r = r;
+    a.inv_freq = inv_freq;
+    a.cos_sin = cos_sin;
+    a.cache_len = cos_sin ? cache_len : 0;
+    a.mu = mu;
+    a.layout = layout;
+    return finish(gbe::launch_qk_norm_rope(a, dtype, vec, as_stream(stream)));
+}
+
 int gbe_rope_cos_sin(float* cos_sin, int64_t cache_len, int64_t r, const float* inv_freq, gbe_stream stream) {
     if (cache_len < 0 || cache_len > INT32_MAX || r < 0 || (r & 1) || r > INT32_MAX) {
         return cache_len < 0 ? GBE_ERR_SHAPE : GBE_ERR_ROTARY;

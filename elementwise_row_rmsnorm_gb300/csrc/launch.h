@@ -35,6 +35,27 @@ cudaError_t launch_rope(const RopeArgs& a, int dtype, bool vec, cudaStream_t st)
 
 cudaError_t launch_rope_cos_sin(float* cos_sin, int64_t len, int64_t r, const float* inv_freq, cudaStream_t st);
 
+// QK-norm (per-head RMSNorm with a [D] gain per operand) followed by RoPE.
+struct QkNormRopeArgs {
+    struct Side {
+        const void* x;
+        void* y;
+        const void* g;
+        int64_t stride;
+        int64_t H;
+    } side[2];
+    float eps;
+    const int32_t* pos;
+    int64_t T, D, r;
+    const float* inv_freq;
+    const float* cos_sin;
+    int64_t cache_len;
+    float mu;
+    int layout;
+};
+
+cudaError_t launch_qk_norm_rope(const QkNormRopeArgs& a, int dtype, bool vec, cudaStream_t st);
+
 cudaError_t launch_silu_mul(const void* gate, const void* up, void* y, int64_t n, int dtype, bool vec,
                             cudaStream_t st);
 

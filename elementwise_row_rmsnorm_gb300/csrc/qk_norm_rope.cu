@@ -1,0 +1,226 @@
+// qk_norm_rope.cu -- QK-norm followed by RoPE, in one pass, on sm_103a.
+//
+// Definition ("Operations", section 5, QK-norm): before RoPE, every head of
+// q and of k is RMS-normalised on its own -- the mean of squares runs over
+// head_dim, not over heads x head_dim -- with a gain of [head_dim] (g_q for
+// q, g_k for k); then q and k are rotated as gbe_rope defines
+// ("Elementwise kernels in C", section 2.2; "Operations", section 3).
+//
+// The fused pass equals the unfused composition bit for bit: gbe_rmsnorm
+// over the T*H head rows (d = head_dim), the result stored in the storage
+// type, then gbe_rope / gbe_rope_qk on the stored values.  To get there:
+//  * a head row is reduced with the very tree gbe_rmsnorm uses for d =
+//    head_dim: lane c of a row sums chunk c (one 16-byte vector, in element
+//    order, fused multiply-add) and the lanes are combined by a butterfly.
+//    gbe_rmsnorm puts such rows on one warp whose lanes past the last chunk
+//    hold zero; a butterfly over the W = next power of two >= chunks lanes
+//    adds exactly the same values (the wider steps only add +0), so several
+//    rows can share a warp;
+//  * the normalised value is rounded to the storage type before the
+//    rotation reads it, as a stored intermediate would be;
+//  * the angles are float(p) * omega_i and CUDA's sincosf (or the same values
+//    from the cos/sin table), as in rope.cu.
+//
+// Map: one warp per token.  It forms the angles of its lanes' entries once
+// and reuses them for every head of q and of k.  Per pass, 32 / W head rows
+// are loaded (up to four passes' loads in flight before any use),
+// normalised, staged in shared memory (so a lane can read the partner of
+// each of its entries), rotated and stored.  Head width is limited to 32
+// chunks (head_dim <= 128 f32 / 256 bf16).
+#include "common.cuh"
+#include "launch.h"
+
+namespace gbe {
+
+namespace {
+
+constexpr int kWarps = 4;   // warps (tokens) per CTA
+constexpr int kPasses = 4;  // head-row passes whose loads are in flight together
+constexpr int kMaxRow = 256;  // floats of one warp's staging: 32 chunks of <= 8 entries
+
+struct QkSide {
+    const char* x;
+    char* y;
+    const char* g;
+    int64_t xs, ys;  // token strides in elements
+    int H;
+};
+
+template <int DT, bool VEC>
+__device__ __forceinline__ void load_chunk(const char* row, int c, int D, float (&f)[Store<DT>::V]) {
+    using S = Store<DT>;
+    constexpr int V = S::V;
+    if (VEC) {
+        S::unpack(ld_stream(row + (int64_t)c * 16), f);
+    } else {
+#pragma unroll
+        for (int e = 0; e < V; ++e) f[e] = c * V + e < D ? S::load1(row, (int64_t)c * V + e) : 0.0f;
+    }
+}
+
+template <int DT, int LAYOUT, bool VEC, bool CACHE>
+__global__ void __launch_bounds__(kWarps * 32)
+qk_norm_rope_kernel(QkSide A, QkSide B, float eps, const int32_t* pos, int64_t T, int D, int r,
+                    const float* inv_freq, const float2* cache, int64_t cache_len, float mu, int W) {
+    using S = Store<DT>;
+    constexpr int V = S::V;
+    constexpr int64_t ES = sizeof(typename S::T);
+    __shared__ float stage[kWarps][kMaxRow];
+    const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t t = (int64_t)blockIdx.x * kWarps + wib;
+    if (t >= T) return;  // whole warps leave together: no CTA barrier follows
+    const int nchunks = (D + V - 1) / V;
+    const int R = 32 / W;        // head rows per pass
+    const int sub = lane / W;    // row of this lane within a pass
+    const int c = lane - sub * W;  // chunk of this lane
+    const bool has = c < nchunks;
+    const int half = r >> 1;
+    float* row_buf = &stage[wib][sub * (nchunks * V)];
+
+    // the angle of every entry this lane writes (pair of entry j)
+    float ca[V], sa[V];
+    const int32_t p = pos[t];
+#pragma unroll
+    for (int e = 0; e < V; ++e) {
+        const int j = c * V + e;
+        ca[e] = 1.0f;
+        sa[e] = 0.0f;
+        if (has && j < r) {
+            const int i = LAYOUT == 0 ? (j < half ? j : j - half) : (j >> 1);
+            if (CACHE && p >= 0 && p < cache_len) {
+                const float2 v = __ldg(cache + (int64_t)p * half + i);
+                ca[e] = v.x;
+                sa[e] = v.y;
+            } else {
+                sincosf(__fmul_rn((float)p, __ldg(inv_freq + i)), &sa[e], &ca[e]);
+            }
+        }
+    }
+
+    for (int side = 0; side < 2; ++side) {
+        const QkSide Q = side == 0 ? A : B;
+        if (Q.H == 0) continue;
+        // this lane's gain chunk, the same for every head
+        float gv[V];
+        if (has) {
+            if (VEC)
+                S::unpack(ld_reuse(Q.g + (int64_t)c * 16), gv);
+            else
+#pragma unroll
+                for (int e = 0; e < V; ++e) gv[e] = c * V + e < D ? S::load1(Q.g, (int64_t)c * V + e) : 0.0f;
+        }
+        const char* xt = Q.x + t * Q.xs * ES;
+        char* yt = Q.y + t * Q.ys * ES;
+        for (int h0 = 0; h0 < Q.H; h0 += R * kPasses) {
+            float f[kPasses][V];
+#pragma unroll
+            for (int k = 0; k < kPasses; ++k) {
+                const int h = h0 + k * R + sub;
+                if (has && h < Q.H) load_chunk<DT, VEC>(xt + (int64_t)h * D * ES, c, D, f[k]);
+            }
+#pragma unroll
+            for (int k = 0; k < kPasses; ++k) {
+                if (h0 + k * R >= Q.H) break;  // uniform across the warp
+                const int h = h0 + k * R + sub;
+                const bool live = has && h < Q.H;
+                // 1) the row's mean of squares: lane sum, then a width-W butterfly
+                float s = 0.0f;
+                if (live) {
+#pragma unroll
+                    for (int e = 0; e < V; ++e) s = __fmaf_rn(f[k][e], f[k][e], s);
+                }
+                for (int m = W >> 1; m >= 1; m >>= 1) s = __fadd_rn(s, __shfl_xor_sync(0xFFFFFFFFu, s, m));
+                const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(s, (float)D), eps)));
+                // 2) normalised, stored in the storage type, staged for the partners
+                float n[V];
+                if (live) {
+#pragma unroll
+                    for (int e = 0; e < V; ++e) {
+                        n[e] = S::round(__fmul_rn(__fmul_rn(f[k][e], inv), gv[e]));
+                        if (c * V + e < D) row_buf[c * V + e] = n[e];
+                    }
+                }
+                __syncwarp();
+                // 3) rotate: every entry from itself and its partner
+                if (live) {
+                    float o[V];
+#pragma unroll
+                    for (int e = 0; e < V; ++e) {
+                        const int j = c * V + e;
+                        o[e] = n[e];
+                        if (j < r) {
+                            float a, b;
+                            bool first;
+                            if (LAYOUT == 0) {
+                                first = j < half;
+                                a = first ? n[e] : row_buf[j - half];
+                                b = first ? row_buf[j + half] : n[e];
+                            } else {
+                                first = (j & 1) == 0;
+                                a = first ? n[e] : row_buf[j - 1];
+                                b = first ? row_buf[j + 1] : n[e];
+                            }
+                            o[e] = first ? __fmul_rn(mu, __fsub_rn(__fmul_rn(a, ca[e]), __fmul_rn(b, sa[e])))
+                                         : __fmul_rn(mu, __fadd_rn(__fmul_rn(a, sa[e]), __fmul_rn(b, ca[e])));
+                        }
+                    }
+                    char* yr = yt + (int64_t)h * D * ES;
+                    if (VEC) {
+                        st_stream(yr + (int64_t)c * 16, S::pack(o));
+                    } else {
+                        for (int e = 0; e < V && c * V + e < D; ++e) S::store1(yr, (int64_t)c * V + e, o[e]);
+                    }
+                }
+                __syncwarp();  // the staging row is rewritten by the next pass
+            }
+        }
+    }
+}
+
+template <int DT>
+cudaError_t launch_dt(const QkNormRopeArgs& a, bool vec, cudaStream_t st) {
+    constexpr int V = Store<DT>::V;
+    const int64_t nchunks = (a.D + V - 1) / V;
+    int W = 1;
+    while (W < nchunks) W <<= 1;
+    vec = vec && a.D % V == 0;
+    QkSide sd[2];
+    for (int k = 0; k < 2; ++k) {
+        sd[k].x = static_cast<const char*>(a.side[k].x);
+        sd[k].y = static_cast<char*>(a.side[k].y);
+        sd[k].g = static_cast<const char*>(a.side[k].g);
+        sd[k].xs = a.side[k].stride;
+        sd[k].ys = a.side[k].stride;
+        sd[k].H = (int)a.side[k].H;
+    }
+    const unsigned grid = (unsigned)((a.T + kWarps - 1) / kWarps);
+    const float2* cache = reinterpret_cast<const float2*>(a.cos_sin);
+    const bool cached = cache != nullptr;
+    const int Di = (int)a.D, ri = (int)a.r;
+#define GBE_QKN(L, VV, C)                                                                                  \
+    qk_norm_rope_kernel<DT, L, VV, C><<<grid, kWarps * 32, 0, st>>>(sd[0], sd[1], a.eps, a.pos, a.T, Di, ri, \
+                                                                     a.inv_freq, cache, a.cache_len, a.mu, W)
+#define GBE_QKN_L(L)                                                  \
+    if (vec) {                                                        \
+        if (cached) GBE_QKN(L, true, true); else GBE_QKN(L, true, false);   \
+    } else {                                                          \
+        if (cached) GBE_QKN(L, false, true); else GBE_QKN(L, false, false); \
+    }
+    if (a.layout == 0) {
+        GBE_QKN_L(0)
+    } else {
+        GBE_QKN_L(1)
+    }
+#undef GBE_QKN_L
+#undef GBE_QKN
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_qk_norm_rope(const QkNormRopeArgs& a, int dtype, bool vec, cudaStream_t st) {
+    if (a.T == 0) return cudaSuccess;
+    return dtype == kF32 ? launch_dt<kF32>(a, vec, st) : launch_dt<kBF16>(a, vec, st);
+}
+
+}  // namespace gbe

@@ -155,6 +155,26 @@ int gbe_rope_qk(const void *q, void *q_out, int64_t q_stride, int64_t Hq, const 
                 gbe_stream stream);
 
 /*
+ * gbe_qk_norm_rope -- QK-norm, then RoPE, of q and k in one pass.
+ *   "Operations", section 5 (QK-norm): each head of q and of k is
+ *   RMS-normalised over head_dim alone (not over heads x head_dim) with the
+ *   gain gq[D] (q) or gk[D] (k) and eps inside the root; then both are
+ *   rotated as gbe_rope defines.
+ * The result equals gbe_rmsnorm over the T*H head rows, stored in dtype,
+ * followed by gbe_rope_qk, bit for bit.
+ * q, q_out, q_stride, Hq, k, k_out, k_stride, Hk, pos, T, D, r, inv_freq,
+ * cos_sin, cache_len, mu, layout, dtype : as for gbe_rope_qk.
+ * gq, gk : device gains of D entries in dtype (ignored when Hq / Hk is 0).
+ * eps    : finite and >= 0.
+ * D      : at most 32 16-byte chunks (128 f32 or 256 bf16), else GBE_ERR_SHAPE.
+ * Alias: q_out == q and k_out == k allowed.
+ */
+int gbe_qk_norm_rope(const void *q, void *q_out, int64_t q_stride, int64_t Hq, const void *gq, const void *k,
+                     void *k_out, int64_t k_stride, int64_t Hk, const void *gk, float eps, const int32_t *pos,
+                     int64_t T, int64_t D, int64_t r, const float *inv_freq, const float *cos_sin,
+                     int64_t cache_len, float mu, int layout, int dtype, gbe_stream stream);
+
+/*
  * gbe_rope_cos_sin -- build the cos/sin table for gbe_rope_qk.
  *   "Operations", section 3 (Cos/sin cache): for every position
  *   0 <= p < cache_len and pair i < r/2, entry p * (r/2) + i is

@@ -69,6 +69,7 @@ class Oracle:
             "orc_add_rmsnorm": [vp, vp, vp, vp, vp, i64, i64, f32, i32],
             "orc_rope": [vp, vp, vp, i64, i64, i64, i64, vp, f32, i32],
             "orc_rope_cos_sin": [vp, i64, i64, vp],
+            "orc_qk_norm_rope": [vp, vp, vp, vp, i64, i64, i64, f32, i64, vp, f32, i32, i32],
             "orc_silu_mul": [vp, vp, vp, i64],
             "orc_embedding": [vp, vp, vp, i64, i64, i64],
             "orc_argmax": [vp, i64],
@@ -154,6 +155,21 @@ class Oracle:
         out = np.empty((length, r // 2, 2), dtype=np.float32)
         self._check(self.lib.orc_rope_cos_sin(_ptr(out), length, r, _ptr(om)), "rope_cos_sin")
         return out
+
+    def qk_norm_rope(self, x, g, eps: float, pos, inv_freq, r: int, mu: float, layout: int,
+                     n_bf16: bool = False) -> np.ndarray:
+        """RMSNorm of every head row of x [T, H, D] with gain g [D], the result
+        stored (rounded to bf16 when n_bf16), then RoPE."""
+        x, g = _f32(x), _f32(g)
+        T, H, D = x.shape
+        pos = np.ascontiguousarray(pos, dtype=np.int32)
+        om = _f32(inv_freq)
+        if g.size != D or pos.size != T or om.size < r // 2:
+            raise OracleError("qk_norm_rope: g has D entries, pos T, inv_freq r/2")
+        y = np.empty_like(x)
+        self._check(self.lib.orc_qk_norm_rope(_ptr(x), _ptr(g), _ptr(y), _ptr(pos), T, H, D, eps, r,
+                                              _ptr(om), mu, layout, int(n_bf16)), "qk_norm_rope")
+        return y
 
     def silu_mul(self, gate, up) -> np.ndarray:
         g, u = _f32(gate), _f32(up)

@@ -10,8 +10,8 @@
  *
  * What it follows.  The two pages define every op in f32:
  *   [Ops]  "Operations" (glia runtime spec): section 1 (Argmax, Add),
- *          section 2 (RmsNorm), section 3 (Rope, TokenEmbed), section 4
- *          (Silu), section 10 (FusedSkipNorm).  Its CPU reference computes
+ *          section 2 (RmsNorm), section 3 (Rope, Cos/sin cache, TokenEmbed),
+ *          section 4 (Silu), section 5 (QK-norm), section 10 (FusedSkipNorm).  Its CPU reference computes
  *          everything in f32.
  *   [L9.6] "Elementwise kernels in C: RMSNorm, RoPE, SiLU-mul, embedding,
  *          add, argmax": section 2 (principles and the symbol table),
@@ -24,7 +24,9 @@
  * the function's comment.
  *
  * Planted mistakes.  Building with -DORACLE_MUTANT=k (1..15) swaps in the
- * k-th wrong variant of the pitfalls table of [L9.6] section 5 (s01..s15).
+ * k-th wrong variant of the pitfalls table of [L9.6] section 5 (s01..s15);
+ * k = 16 is the pitfall [Ops] section 5 warns about for QK-norm (the norm
+ * taken over num_heads * head_dim instead of per head).
  * The tests build those variants on the CPU to show that their pins reject
  * each one.  A normal build (ORACLE_MUTANT undefined) contains none of them.
  */
@@ -203,6 +205,50 @@ int orc_rope_cos_sin(float *cos_sin, int64_t len, int64_t r, const float *inv_fr
             cos_sin[2 * (p * half + i) + 1] = (float)sin((double)theta);
         }
     return ORC_OK;
+}
+
+#if ORACLE_MUTANT == 16
+/* s16 only: one RMSNorm over all H * D entries of a token, the [D] gain tiled per head. */
+static int orc_rmsnorm_gain_tiled(const float *x, const float *g, float *y, int64_t T, int64_t H,
+                                  int64_t D, float eps) {
+    for (int64_t t = 0; t < T; ++t) {
+        const float *xt = x + t * H * D;
+        float ss = 0.0f;
+        for (int64_t i = 0; i < H * D; ++i) ss = ss + xt[i] * xt[i];
+        float inv = 1.0f / sqrtf(ss / (float)(H * D) + eps);
+        for (int64_t i = 0; i < H * D; ++i) y[t * H * D + i] = (xt[i] * inv) * g[i % D];
+    }
+    return ORC_OK;
+}
+#else
+#define orc_rmsnorm_gain_tiled(x, g, y, T, H, D, eps) ORC_ERR_ARG
+#endif
+
+/* ---- QK-norm, then RoPE -------------------------------------------------------
+ * [Ops] 5 (QK-norm): before RoPE, q and k are RMS-normalised per head -- the
+ * mean of squares runs over head_dim only, each head with the gain g[D] --
+ * and then rotated by [Ops] 3 / [L9.6] 2.2.  The composition is written out:
+ * orc_rmsnorm over the T*H rows of D entries, the result stored in the
+ * storage type (rounded to bf16 when n_bf16 != 0, as the unfused composition
+ * stores it), then orc_rope on the stored values.  x is [T, H, D]
+ * contiguous; y may be x.                                                    */
+int orc_qk_norm_rope(const float *x, const float *g, float *y, const int32_t *pos, int64_t T,
+                     int64_t H, int64_t D, float eps, int64_t r, const float *inv_freq, float mu,
+                     int layout, int n_bf16) {
+    if (T < 0 || H < 0 || D <= 0) return ORC_ERR_ARG;
+    int st;
+    if (MUT(16)) /* s16: the norm taken over the whole token (H * D), not per head */
+        st = orc_rmsnorm_gain_tiled(x, g, y, T, H, D, eps);
+    else
+        st = orc_rmsnorm(x, g, y, T * H, D, eps);
+    if (st != ORC_OK) return st;
+    if (n_bf16) {
+        for (int64_t i = 0; i < T * H * D; ++i) {
+            uint16_t b = orc_round_one(y[i]);
+            orc_bf16_widen(&b, &y[i], 1);
+        }
+    }
+    return orc_rope(y, y, pos, T, H, D, r, inv_freq, mu, layout);
 }
 
 /* ---- SiLU-mul ----------------------------------------------------------------

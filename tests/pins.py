@@ -254,6 +254,34 @@ def pin_rope_cos_sin_table(o):
         assert _same_bits(y[t, :, 16:], (a * sn + b * c).astype(np.float32))
 
 
+def pin_qk_norm_rope_per_head(o):
+    """QK-norm normalises each head over head_dim alone ("Operations", section 5),
+    then rotates: against float64 torch rms_norm over the last dim of [T, H, D]
+    followed by float64 rotations; heads are independent of one another."""
+    T, H, D, r = 3, 4, 16, 12
+    x = _rand(T, H, D, scale=2.0)
+    x[:, 2] *= 50.0  # one loud head must not change its neighbours
+    g = RNG.uniform(0.5, 1.5, D).astype(np.float32)
+    pos = np.array([0, 5, 300], np.int32)
+    om = RNG.uniform(1e-3, 1.0, r // 2).astype(np.float32)
+    for layout in (0, 1):
+        y = o.qk_norm_rope(x, g, 1e-5, pos, om, r, 1.0, layout)
+        n = torch.nn.functional.rms_norm(torch.from_numpy(x).double(), (D,), torch.from_numpy(g).double(),
+                                         1e-5).numpy()
+        ref = _brute_rope(n, pos, om, r, 1.0, layout)
+        assert np.allclose(y, ref, rtol=0, atol=4e-6 * np.abs(n).max()), layout
+        quiet = x.copy()
+        quiet[:, 2] /= 50.0
+        y2 = o.qk_norm_rope(quiet, g, 1e-5, pos, om, r, 1.0, layout)
+        for h in (0, 1, 3):
+            assert _same_bits(y2[:, h], y[:, h]), "other heads must not depend on head 2"
+    # with eps = 0, a power-of-two scale of one head leaves its output unchanged
+    y0 = o.qk_norm_rope(x, g, 0.0, pos, om, r, 1.0, 0)
+    xs = x.copy()
+    xs[:, 1] *= np.float32(8.0)
+    assert _same_bits(o.qk_norm_rope(xs, g, 0.0, pos, om, r, 1.0, 0), y0)
+
+
 # ---- SiLU-mul ------------------------------------------------------------------
 
 def pin_silu_mul_saturates_without_nan(o):
@@ -370,4 +398,5 @@ KILLS = {
     13: "argmax_ties_nan_and_empty",
     14: "argmax_ties_nan_and_empty",
     15: "rmsnorm_rows_are_independent_and_in_place",
+    16: "qk_norm_rope_per_head",
 }

@@ -112,6 +112,19 @@ def test_rope_qk_and_table_reject_bad_arguments(L):
     assert L.gbe_rope_cos_sin(NULL, 10, 0, NULL, S) == 0
 
 
+def test_qk_norm_rope_rejects_bad_arguments(L):
+    def call(T=4, D=128, r=128, layout=0, eps=1e-6, mu=1.0, dtype=1, qs=1024, hq=8, ks=256, hk=2):
+        return L.gbe_qk_norm_rope(NULL, NULL, qs, hq, NULL, NULL, NULL, ks, hk, NULL, eps, NULL, T, D, r, NULL,
+                                  NULL, 0, mu, layout, dtype, S)
+    assert call(layout=2) == 4 and call(dtype=5) == 3
+    assert call(eps=-1.0) == 5 and call(eps=float("inf")) == 5
+    assert call(D=264) == 2                 # bf16 head rows of more than 32 chunks
+    assert call(D=256, dtype=0, qs=2048, ks=512, r=256) == 2   # f32: 64 chunks
+    assert call(r=130) == 6 and call(r=7) == 6
+    assert call(qs=1000) == 2
+    assert call(T=0) == 0 and call(hq=0, hk=0) == 0
+
+
 def test_rejects_size_overflow(L):
     big = 1 << 62
     assert L.gbe_silu_mul(NULL, NULL, NULL, big, 0, S) == 2
