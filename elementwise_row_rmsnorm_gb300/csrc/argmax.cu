@@ -70,6 +70,7 @@ __device__ __forceinline__ void argmax_body(const void* x, int32_t* out, int64_t
     using S = Store<DT>;
     constexpr int V = S::V;
     constexpr int64_t ES = sizeof(typename S::T);
+    pdl_begin();
     const int64_t row = blockIdx.x / CL;
     const int rank = (int)(blockIdx.x % CL);
     const char* base = static_cast<const char*>(x) + row * n * ES;
@@ -183,14 +184,13 @@ cudaError_t launch_cl(const void* x, int32_t* out, int64_t rows, int64_t n, cuda
     const int64_t target = 8LL * sm_count();
     int cl = 1;
     while (cl < 8 && rows * cl < target && n / (cl * 2) >= 2048) cl *= 2;
-    const unsigned grid = (unsigned)(rows * cl);
+    const dim3 grid((unsigned)(rows * cl));
     switch (cl) {
-        case 1: argmax_rows1<DT, VEC><<<grid, kThreads, 0, st>>>(x, out, rows, n); break;
-        case 2: argmax_rows2<DT, VEC><<<grid, kThreads, 0, st>>>(x, out, rows, n); break;
-        case 4: argmax_rows4<DT, VEC><<<grid, kThreads, 0, st>>>(x, out, rows, n); break;
-        default: argmax_rows8<DT, VEC><<<grid, kThreads, 0, st>>>(x, out, rows, n); break;
+        case 1: return launch(argmax_rows1<DT, VEC>, grid, dim3(kThreads), 0, st, x, out, rows, n);
+        case 2: return launch(argmax_rows2<DT, VEC>, grid, dim3(kThreads), 0, st, x, out, rows, n);
+        case 4: return launch(argmax_rows4<DT, VEC>, grid, dim3(kThreads), 0, st, x, out, rows, n);
+        default: return launch(argmax_rows8<DT, VEC>, grid, dim3(kThreads), 0, st, x, out, rows, n);
     }
-    return cudaGetLastError();
 }
 
 }  // namespace

@@ -13,6 +13,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace gbe {
 
 constexpr int kF32 = 0;
@@ -47,6 +49,39 @@ __device__ __forceinline__ void st_stream(void* p, const Vec16& v) {
     asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.w[0]), "r"(v.w[1]),
                  "r"(v.w[2]), "r"(v.w[3])
                  : "memory");
+}
+
+// ---- programmatic dependent launch ---------------------------------------------
+//
+// Every kernel of this library is launched with programmatic stream
+// serialization and opens with pdl_begin(): it first lets the next kernel on
+// the stream be launched (that kernel's CTAs are placed on the SMs as this
+// kernel's last wave drains), then waits in hardware until the kernel before
+// it on the stream has completed and its writes are visible.  A chain of
+// dependent ops therefore stays correct, and the launch gap between them is
+// hidden.  griddepcontrol.wait is a no-op for a kernel launched without the
+// attribute, and it is a hardware wait on the previous grid, not a spin loop.
+__device__ __forceinline__ void pdl_begin() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                          Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+    if (e != cudaSuccess) cudaGetLastError();  // clear it; the caller reports e
+    return e;
 }
 
 // ---- storage traits ------------------------------------------------------------

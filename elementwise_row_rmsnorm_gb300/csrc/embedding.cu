@@ -24,6 +24,7 @@ __global__ void __launch_bounds__(MAXT)
 embedding_rows(const void* table, const int32_t* ids, void* out, int64_t n, int64_t d, int64_t V, int32_t* bad,
                int tpr) {
     constexpr int VE = 16 / ES;  // elements per 16-byte chunk
+    pdl_begin();
     const int rpc = blockDim.x / tpr;
     const int sub = threadIdx.x / tpr;
     const int t = threadIdx.x - sub * tpr;
@@ -83,19 +84,12 @@ cudaError_t launch_es(const void* table, const int32_t* ids, void* out, int64_t 
     const int64_t grid = (n + rpc - 1) / rpc;
     const dim3 block((unsigned)(tpr * rpc));
     const int ti = (int)tpr;
-    if (!vec) {
-        embedding_rows<ES, 0, false, 1024><<<(unsigned)grid, block, 0, st>>>(table, ids, out, n, d, V, bad, ti);
-        return cudaGetLastError();
-    }
-    if (wide) {
-        embedding_rows<ES, 0, true, 1024><<<(unsigned)grid, block, 0, st>>>(table, ids, out, n, d, V, bad, ti);
-        return cudaGetLastError();
-    }
-#define GBE_EMB_CASE(KK, MT)                                                                                  \
-    if (slots <= KK) {                                                                                        \
-        embedding_rows<ES, KK, true, MT><<<(unsigned)grid, block, 0, st>>>(table, ids, out, n, d, V, bad, ti); \
-        return cudaGetLastError();                                                                            \
-    }
+    const dim3 g((unsigned)grid);
+    if (!vec) return launch(embedding_rows<ES, 0, false, 1024>, g, block, 0, st, table, ids, out, n, d, V, bad, ti);
+    if (wide) return launch(embedding_rows<ES, 0, true, 1024>, g, block, 0, st, table, ids, out, n, d, V, bad, ti);
+#define GBE_EMB_CASE(KK, MT)                                                                                 \
+    if (slots <= KK)                                                                                         \
+        return launch(embedding_rows<ES, KK, true, MT>, g, block, 0, st, table, ids, out, n, d, V, bad, ti);
     if (tpr * rpc <= 256) {
         GBE_EMB_CASE(1, 256)
         GBE_EMB_CASE(2, 256)

@@ -43,6 +43,7 @@ __global__ void __launch_bounds__(kThreads)
 pointwise_vec(const void* a, const void* b, void* y, int64_t n) {
     using S = Store<DT>;
     constexpr int V = S::V;
+    pdl_begin();
     const int64_t nvec = n / V;
     const int64_t v0 = (int64_t)blockIdx.x * (kThreads * kU) + threadIdx.x;
     const char* pa = static_cast<const char*>(a);
@@ -80,6 +81,7 @@ template <int DT, int OP>
 __global__ void __launch_bounds__(kThreads)
 pointwise_scalar(const void* a, const void* b, void* y, int64_t n) {
     using S = Store<DT>;
+    pdl_begin();
     const int64_t i0 = (int64_t)blockIdx.x * (kThreads * kU) + threadIdx.x;
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
@@ -96,18 +98,12 @@ cudaError_t launch_pw(const void* a, const void* b, void* y, int64_t n, int dtyp
         const int64_t nvec = n / V;
         int64_t grid = (nvec + per_cta - 1) / per_cta;
         if (grid < 1) grid = 1;  // the tail alone (n < V) still needs one CTA
-        if (dtype == kF32)
-            pointwise_vec<kF32, OP><<<(unsigned)grid, kThreads, 0, st>>>(a, b, y, n);
-        else
-            pointwise_vec<kBF16, OP><<<(unsigned)grid, kThreads, 0, st>>>(a, b, y, n);
-    } else {
-        const int64_t grid = (n + per_cta - 1) / per_cta;
-        if (dtype == kF32)
-            pointwise_scalar<kF32, OP><<<(unsigned)grid, kThreads, 0, st>>>(a, b, y, n);
-        else
-            pointwise_scalar<kBF16, OP><<<(unsigned)grid, kThreads, 0, st>>>(a, b, y, n);
+        if (dtype == kF32) return launch(pointwise_vec<kF32, OP>, dim3((unsigned)grid), dim3(kThreads), 0, st, a, b, y, n);
+        return launch(pointwise_vec<kBF16, OP>, dim3((unsigned)grid), dim3(kThreads), 0, st, a, b, y, n);
     }
-    return cudaGetLastError();
+    const int64_t grid = (n + per_cta - 1) / per_cta;
+    if (dtype == kF32) return launch(pointwise_scalar<kF32, OP>, dim3((unsigned)grid), dim3(kThreads), 0, st, a, b, y, n);
+    return launch(pointwise_scalar<kBF16, OP>, dim3((unsigned)grid), dim3(kThreads), 0, st, a, b, y, n);
 }
 
 }  // namespace

@@ -66,6 +66,7 @@ qk_norm_rope_kernel(QkSide A, QkSide B, float eps, const int32_t* pos, int64_t T
     constexpr int V = S::V;
     constexpr int64_t ES = sizeof(typename S::T);
     __shared__ float stage[kWarps][kMaxRow];
+    pdl_begin();
     const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t t = (int64_t)blockIdx.x * kWarps + wib;
     if (t >= T) return;  // whole warps leave together: no CTA barrier follows
@@ -197,9 +198,9 @@ cudaError_t launch_dt(const QkNormRopeArgs& a, bool vec, cudaStream_t st) {
     const float2* cache = reinterpret_cast<const float2*>(a.cos_sin);
     const bool cached = cache != nullptr;
     const int Di = (int)a.D, ri = (int)a.r;
-#define GBE_QKN(L, VV, C)                                                                                  \
-    qk_norm_rope_kernel<DT, L, VV, C><<<grid, kWarps * 32, 0, st>>>(sd[0], sd[1], a.eps, a.pos, a.T, Di, ri, \
-                                                                     a.inv_freq, cache, a.cache_len, a.mu, W)
+#define GBE_QKN(L, VV, C)                                                                                 \
+    return launch(qk_norm_rope_kernel<DT, L, VV, C>, dim3(grid), dim3(kWarps * 32), 0, st, sd[0], sd[1], a.eps, \
+                  a.pos, a.T, Di, ri, a.inv_freq, cache, a.cache_len, a.mu, W)
 #define GBE_QKN_L(L)                                                  \
     if (vec) {                                                        \
         if (cached) GBE_QKN(L, true, true); else GBE_QKN(L, true, false);   \
@@ -213,7 +214,6 @@ cudaError_t launch_dt(const QkNormRopeArgs& a, bool vec, cudaStream_t st) {
     }
 #undef GBE_QKN_L
 #undef GBE_QKN
-    return cudaGetLastError();
 }
 
 }  // namespace

@@ -13,10 +13,11 @@
 // Work map.  A row is cut into chunks of one 16-byte vector (4 f32 or 8
 // bf16).  Chunk c belongs to thread (c mod TPR) of the row's TPR threads, as
 // that thread's (c div TPR)-th slot; TPR is the smallest multiple of 32 that
-// leaves each thread at most 8 slots (rows of more than 4096 chunks use 1024
-// threads).  TPR and the slot count depend only on (d, storage type).  A thread sums the squares of its chunks in slot order
-// and element order (fused multiply-add), the row's threads are combined by
-// a butterfly within each warp and then warp by warp in warp order.  So the
+// leaves each thread at most 4 slots (rows of more than 4096 chunks use 1024
+// threads and more slots).  TPR and the slot count depend only on (d,
+// storage type).  A thread sums the squares of its chunks in slot order and
+// element order (fused multiply-add), the row's threads are combined by a
+// butterfly within each warp and then warp by warp in warp order.  So the
 // summation tree of a row is fixed by (d, type): the row's output bits do
 // not depend on how many rows the call holds or where the row sits.  The
 // aligned (vector) and unaligned (scalar) paths use the same map and the
@@ -25,9 +26,10 @@
 // Aligned rows (every pointer 16-byte aligned, d a multiple of the vector)
 // stay in registers as packed vectors between the sum and the write (one HBM
 // read of x, one write of y), with the 16-byte loads of all slots issued
-// before any is used.  Other rows take a two-pass kernel with the same map.
-// The row's sum is complete before the first write, so y may be x (and h
-// may be residual).
+// before any is used.  Other rows, and rows wider than 4096 chunks, take a
+// two-pass kernel with the same map.  The row's sum is complete before the
+// first write, so y may be x (and h may be residual).  Launches overlap the
+// previous kernel's tail (programmatic dependent launch, see common.cuh).
 #include "common.cuh"
 #include "launch.h"
 
@@ -35,7 +37,7 @@ namespace gbe {
 
 namespace {
 
-constexpr int kMaxSlots = 8;
+constexpr int kMaxSlots = 4;
 
 // Threads per row for a row of `nchunks` 16-byte chunks: enough that each
 // owns at most kMaxSlots chunks.  A function of (d, dtype) only.
@@ -53,6 +55,7 @@ rmsnorm_rows(const void* x, const void* res, const void* w, void* y, void* h, in
     using S = Store<DT>;
     constexpr int V = S::V;
     constexpr int64_t ES = sizeof(typename S::T);
+    pdl_begin();
     const int rpc = blockDim.x / tpr;
     const int sub = threadIdx.x / tpr;
     const int t = threadIdx.x - sub * tpr;
@@ -115,7 +118,7 @@ rmsnorm_rows(const void* x, const void* res, const void* w, void* y, void* h, in
     }
 }
 
-// Unaligned rows (and rows wider than kMaxSlots chunks of 512 threads): the
+// Unaligned rows (and rows wider than kMaxSlots chunks of 1024 threads): the
 // same chunk map, the same per-thread order and the same reduction tree as
 // rmsnorm_rows would use for this d, element by element, with x (or the
 // stored h) read a second time for the write.  One row per CTA of `tpr`
@@ -126,6 +129,7 @@ rmsnorm_two_pass(const void* x, const void* res, const void* w, void* y, void* h
                  float eps) {
     using S = Store<DT>;
     constexpr int V = S::V;
+    pdl_begin();
     const int tpr = blockDim.x;
     const int t = threadIdx.x;
     const int64_t row = blockIdx.x;
@@ -162,29 +166,27 @@ cudaError_t launch_dt(const void* x, const void* res, const void* w, void* y, vo
     constexpr int V = Store<DT>::V;
     const int64_t nchunks = (d + V - 1) / V;
     int64_t tpr = threads_per_row(nchunks);
-    const bool wide = tpr > 512;
+    const bool wide = tpr > 1024;
     if (wide) tpr = 1024;
     const int di = (int)d, ti = (int)tpr;
     if (wide || !vec) {
-        rmsnorm_two_pass<DT, ADD><<<(unsigned)rows, (unsigned)tpr, 0, st>>>(x, res, w, y, h, rows, di, eps);
-        return cudaGetLastError();
+        return launch(rmsnorm_two_pass<DT, ADD>, dim3((unsigned)rows), dim3((unsigned)tpr), 0, st, x, res, w, y, h,
+                      rows, di, eps);
     }
     const int64_t slots = (nchunks + tpr - 1) / tpr;
     const int rpc = tpr == 32 ? 4 : 1;
     const int64_t grid = (rows + rpc - 1) / rpc;
     const dim3 block((unsigned)(tpr * rpc));
-#define GBE_RMS_CASE(KK, MT)                                                                                   \
-    if (slots <= KK) {                                                                                         \
-        rmsnorm_rows<DT, KK, ADD, MT><<<(unsigned)grid, block, 0, st>>>(x, res, w, y, h, rows, di, eps, ti); \
-        return cudaGetLastError();                                                                             \
-    }
+#define GBE_RMS_CASE(KK, MT)                                                                                  \
+    if (slots <= KK)                                                                                          \
+        return launch(rmsnorm_rows<DT, KK, ADD, MT>, dim3((unsigned)grid), block, 0, st, x, res, w, y, h, rows, di, \
+                      eps, ti);
     if (tpr * rpc <= 256) {
         GBE_RMS_CASE(1, 256)
         GBE_RMS_CASE(2, 256)
         GBE_RMS_CASE(4, 256)
-        GBE_RMS_CASE(8, 256)
     } else {
-        GBE_RMS_CASE(8, 512)
+        GBE_RMS_CASE(4, 1024)
     }
 #undef GBE_RMS_CASE
     return cudaErrorInvalidValue;

@@ -88,6 +88,7 @@ rope_vec(Operand A, Operand B, const int32_t* pos, int64_t T, int D, int r, cons
     constexpr int P = LAYOUT == 0 ? V : V / 2;  // pairs per 16-byte item
     constexpr int64_t ES = sizeof(typename S::T);
     constexpr int HC = kHeadsPerThread;
+    pdl_begin();
     int64_t gt = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     const bool second = gt >= A.threads;
     const Operand R = second ? B : A;
@@ -173,6 +174,7 @@ rope_scalar(Operand A, Operand B, const int32_t* pos, int64_t T, int D, int r, c
             const float2* cache, int64_t cache_len, float mu) {
     using S = Store<DT>;
     constexpr int64_t ES = sizeof(typename S::T);
+    pdl_begin();
     int64_t gt = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     const bool second = gt >= A.threads;
     const Operand R = second ? B : A;
@@ -211,6 +213,7 @@ rope_scalar(Operand A, Operand B, const int32_t* pos, int64_t T, int D, int r, c
 // exactly as the RoPE kernels form it.
 __global__ void __launch_bounds__(kThreads)
 rope_cos_sin_table(float2* cache, int64_t len, int half, const float* inv_freq) {
+    pdl_begin();
     const int64_t gt = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     const int64_t p = gt / half;
     if (p >= len) return;
@@ -250,9 +253,9 @@ cudaError_t launch_dt(const RopeArgs& a, bool vec, cudaStream_t st) {
     if (threads == 0) return cudaSuccess;
     const unsigned grid = (unsigned)((threads + kThreads - 1) / kThreads);
     const int Di = (int)a.D, ri = (int)a.r;
-#define GBE_ROPE(KERNEL, L, C)                                                                               \
-    KERNEL<DT, L, C><<<grid, kThreads, 0, st>>>(op[0], op[1], a.pos, a.T, Di, ri, a.inv_freq, cache,         \
-                                                 a.cache_len, a.mu)
+#define GBE_ROPE(KERNEL, L, C)                                                                              \
+    return launch(KERNEL<DT, L, C>, dim3(grid), dim3(kThreads), 0, st, op[0], op[1], a.pos, a.T, Di, ri,    \
+                  a.inv_freq, cache, a.cache_len, a.mu)
     if (vec) {
         if (a.layout == 0) {
             if (cached) GBE_ROPE(rope_vec, 0, true); else GBE_ROPE(rope_vec, 0, false);
@@ -267,7 +270,6 @@ cudaError_t launch_dt(const RopeArgs& a, bool vec, cudaStream_t st) {
         }
     }
 #undef GBE_ROPE
-    return cudaGetLastError();
 }
 
 }  // namespace
@@ -280,9 +282,8 @@ cudaError_t launch_rope_cos_sin(float* cos_sin, int64_t len, int64_t r, const fl
     const int64_t half = r / 2;
     const int64_t n = len * half;
     if (n == 0) return cudaSuccess;
-    rope_cos_sin_table<<<(unsigned)((n + kThreads - 1) / kThreads), kThreads, 0, st>>>(
-        reinterpret_cast<float2*>(cos_sin), len, (int)half, inv_freq);
-    return cudaGetLastError();
+    return launch(rope_cos_sin_table, dim3((unsigned)((n + kThreads - 1) / kThreads)), dim3(kThreads), 0, st,
+                  reinterpret_cast<float2*>(cos_sin), len, (int)half, inv_freq);
 }
 
 }  // namespace gbe
