@@ -206,49 +206,12 @@ def run_ours(args):
 
     data = build_inputs(args.tokens)
 
-    def to_dev(a):
-        a = np.ascontiguousarray(a)
-        if a.dtype == np.uint16:
-            return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
-        return torch.from_numpy(a).to(dev)
-
     # device buffers: inputs (a separate copy per op), outputs
-    bufs = {}
-    for op, (arrays, params) in data.items():
-        ins = {k: to_dev(v) for k, v in arrays.items()}
-        bufs[op] = ins
-    out = {}
-    for op in bufs:
-        b = bufs[op]
-        if op == "embedding":
-            out[op] = torch.empty((b["ids"].numel(), b["table"].shape[1]), dtype=b["table"].dtype, device=dev)
-        elif op == "add_rmsnorm":
-            out[op] = (torch.empty_like(b["x"]), torch.empty_like(b["x"]))
-        elif op.startswith("rope_qk"):
-            out[op] = (torch.empty_like(b["q"]), torch.empty_like(b["k"]))
-        elif op == "argmax":
-            out[op] = torch.empty((b["x"].shape[0],), dtype=torch.int32, device=dev)
-        else:
-            out[op] = torch.empty_like(b.get("x", b.get("gate", b.get("a"))))
+    bufs = {op: {k: to_device(torch, dev, v) for k, v in arrays.items()} for op, (arrays, params) in data.items()}
+    out = {op: make_outputs(torch, dev, op, b) for op, b in bufs.items()}
 
-    def call(op, b=None, o=None):
-        b = bufs[op] if b is None else b
-        o = out[op] if o is None else o
-        p = data[op][1]
-        if op == "embedding":
-            gbe.gbe_embedding(b["table"], b["ids"], o)
-        elif op == "add_rmsnorm":
-            gbe.gbe_add_rmsnorm(b["x"], b["residual"], b["w"], o[0], o[1], p["eps"])
-        elif op.startswith("rope_qk"):
-            gbe.gbe_rope_qk(b["q"], o[0], b["k"], o[1], b["pos"], b["inv_freq"], p["r"], p["mu"], p["layout"])
-        elif op == "silu_mul":
-            gbe.gbe_silu_mul(b["gate"], b["up"], o)
-        elif op == "add":
-            gbe.gbe_add(b["a"], b["b"], o)
-        elif op == "rmsnorm":
-            gbe.gbe_rmsnorm(b["x"], b["w"], o, p["eps"])
-        elif op == "argmax":
-            gbe.gbe_argmax(b["x"], o)
+    def call(op):
+        run_op(gbe, op, data[op][1], bufs[op], out[op])
 
     nbytes = {op: op_bytes(op, *data[op]) for op in data}
     step_bytes = sum(b for b, _ in nbytes.values())
@@ -353,6 +316,94 @@ def run_ours(args):
     return result
 
 
+def run_isolated(args):
+    """Each op alone, launched back to back over rotating copies of its inputs
+    and outputs (together more than four times the L2), timed with one CUDA
+    event pair around the loop: the op's sustained rate when it streams."""
+    import torch
+
+    import elementwise_row_rmsnorm_gb300 as gbe
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    gbe.lib()
+    data = build_inputs(args.tokens)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    res = {}
+    for op, _names in STEP:
+        arrays, params = data[op]
+        nb, rows = op_bytes(op, arrays, params)
+        sets = int(min(12, max(2, -(-4 * l2 // nb) + 1)))
+        base = {k: to_device(torch, dev, v) for k, v in arrays.items()}
+        shared = ("table", "w", "inv_freq", "pos", "ids")
+        rings = []
+        for _ in range(sets):
+            b = {k: (v if k in shared else v.clone()) for k, v in base.items()}
+            rings.append((b, make_outputs(torch, dev, op, b)))
+        p = params
+
+        def go(b, o):
+            run_op(gbe, op, p, b, o)
+        for i in range(3 * sets):
+            go(*rings[i % sets])
+        torch.cuda.synchronize()
+        n = max(50, 4 * sets)
+        a = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for i in range(n):
+            go(*rings[i % sets])
+        e.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(e) / n
+        res[op] = {"bytes": nb, "us": round(ms * 1e3, 2), "gbs": round(nb / ms / 1e6, 1), "copies": sets}
+        del rings, base
+        torch.cuda.empty_cache()
+    peak, kind = peaks()
+    for v in res.values():
+        v["frac_of_peak"] = round(v["gbs"] / peak, 4)
+        v["frac_of_8tbs"] = round(v["gbs"] / NOMINAL_HBM_GBS, 4)
+    line = {"mode": "isolated", "workload": WORKLOAD if args.tokens >= 8192 else f"{WORKLOAD} (first {args.tokens} tokens)",
+            "unit": "GB/s", "peak": peak, "peak_source": kind, "per_op": res}
+    print(json.dumps(line), flush=True)
+    return line
+
+
+def to_device(torch, dev, a):
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+    return torch.from_numpy(a).to(dev)
+
+
+def make_outputs(torch, dev, op, b):
+    if op == "embedding":
+        return torch.empty((b["ids"].numel(), b["table"].shape[1]), dtype=b["table"].dtype, device=dev)
+    if op == "add_rmsnorm":
+        return (torch.empty_like(b["x"]), torch.empty_like(b["x"]))
+    if op.startswith("rope_qk"):
+        return (torch.empty_like(b["q"]), torch.empty_like(b["k"]))
+    if op == "argmax":
+        return torch.empty((b["x"].shape[0],), dtype=torch.int32, device=dev)
+    return torch.empty_like(b["x"] if "x" in b else (b["gate"] if "gate" in b else b["a"]))
+
+
+def run_op(gbe, op, p, b, o):
+    if op == "embedding":
+        gbe.gbe_embedding(b["table"], b["ids"], o)
+    elif op == "add_rmsnorm":
+        gbe.gbe_add_rmsnorm(b["x"], b["residual"], b["w"], o[0], o[1], p["eps"])
+    elif op.startswith("rope_qk"):
+        gbe.gbe_rope_qk(b["q"], o[0], b["k"], o[1], b["pos"], b["inv_freq"], p["r"], p["mu"], p["layout"])
+    elif op == "silu_mul":
+        gbe.gbe_silu_mul(b["gate"], b["up"], o)
+    elif op == "add":
+        gbe.gbe_add(b["a"], b["b"], o)
+    elif op == "rmsnorm":
+        gbe.gbe_rmsnorm(b["x"], b["w"], o, p["eps"])
+    elif op == "argmax":
+        gbe.gbe_argmax(b["x"], o)
+
+
 def run_e2e(args, gbe, torch, dev, data, bufs, out, call, nbytes, step_bytes):
     """The step from pinned host buffers: every op's per-step inputs copied
     host->device and every result copied back, inside the timed region
@@ -413,17 +464,48 @@ def run_e2e(args, gbe, torch, dev, data, bufs, out, call, nbytes, step_bytes):
     steps = max(1, min(args.steps, 10))
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
-    a.record(s_in)
+    a.record(comp)
+    s_in.wait_stream(comp)
+    s_out.wait_stream(comp)
     for _ in range(steps):
         one()
     comp.wait_stream(s_out)
     comp.wait_stream(s_in)
     b.record(comp)
     torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / steps
-    return {"value": round(step_bytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(ms, 3),
-            "steps": steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "overlap": "copy-in, kernels and copy-out on three streams"}
+    ms_copy = a.elapsed_time(b) / steps
+
+    # the same step with no copies at all: the kernels read each op's inputs
+    # from the pinned host buffers and write its results to pinned host
+    # buffers, through the C ABI (pinned host memory is mapped at the same
+    # address on the device, and NVLink-C2C carries the traffic)
+    host_bufs = {op: dict(bufs[op]) for op in bufs}
+    for op in host_bufs:
+        for k, h in host_in[op]:
+            host_bufs[op][k] = h
+    host_outs = {op: (tuple(h for _, h in host_out[op]) if isinstance(out[op], tuple) else host_out[op][0][1])
+                 for op in out}
+
+    def one_zero_copy():
+        for op in ops:
+            run_op(gbe, op, data[op][1], host_bufs[op], host_outs[op])
+
+    one_zero_copy()
+    torch.cuda.synchronize()
+    a.record(comp)
+    for _ in range(steps):
+        one_zero_copy()
+    b.record(comp)
+    torch.cuda.synchronize()
+    ms_zero = a.elapsed_time(b) / steps
+    copy_leg = {"value": round(step_bytes / (ms_copy * 1e-3) / 1e9, 1), "ms_per_step": round(ms_copy, 3),
+                "method": "cudaMemcpyAsync in and out on their own streams, overlapped with the kernels"}
+    zero_leg = {"value": round(step_bytes / (ms_zero * 1e-3) / 1e9, 1), "ms_per_step": round(ms_zero, 3),
+                "method": "kernels read inputs from and write results to pinned host memory (zero-copy)"}
+    best, other = (zero_leg, copy_leg) if ms_zero < ms_copy else (copy_leg, zero_leg)
+    return {"value": best["value"], "unit": "GB/s", "ms_per_step": best["ms_per_step"], "steps": steps,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "method": best["method"],
+            "alternative": other}
 
 
 def dram_traffic(op: str):
@@ -574,6 +656,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--isolated", action="store_true",
+                    help="time each op alone, back to back over rotating buffers, and print that instead")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
     if args.ops:
@@ -584,6 +668,8 @@ def main(argv=None):
         STEP[:] = [(op, c) for op, c in STEP if op in keep]
     if args.impl == "reference":
         return run_reference(args)
+    if args.isolated:
+        return run_isolated(args)
     return run_ours(args)
 
 

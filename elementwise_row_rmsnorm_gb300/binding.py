@@ -1,7 +1,8 @@
 """Python binding of the C ABI (include/gbe_elementwise.h).
 
 Argument marshalling only: each ``gbe_*`` function takes torch tensors that
-already live on the current CUDA device, checks that their shapes and dtypes
+live on the current CUDA device (or in pinned host memory, which the kernels
+then read and write in place over the host link), checks that their shapes and dtypes
 agree with one another, and passes their pointers, sizes and the current
 stream to the C entry point of the same name.  Every step of every op runs
 in the CUDA library; there is no other code path.  If the library is not
@@ -103,10 +104,16 @@ def _dt(*ts) -> int:
     return _DTYPES[dt]
 
 
+def _on_device(t) -> bool:
+    """CUDA tensors, and pinned host tensors (mapped at the same address on the
+    device, so kernels read and write them in place: zero-copy)."""
+    return t.is_cuda or t.is_pinned()
+
+
 def _dev(*ts):
     for t in ts:
-        if not t.is_cuda:
-            raise ValueError("tensors must be on the CUDA device")
+        if not _on_device(t):
+            raise ValueError("tensors must be on the CUDA device or in pinned host memory")
         if not t.is_contiguous():
             raise ValueError("tensors must be contiguous")
 
@@ -163,8 +170,8 @@ def gbe_rope_qk(q, q_out, k, k_out, pos, inv_freq, r: int, mu: float = 1.0, layo
     of one storage type whose token stride may exceed H * D."""
     ts = [t for t in (q, q_out, k, k_out, pos, inv_freq) if t is not None]
     for t in ts:
-        if not t.is_cuda:
-            raise ValueError("tensors must be on the CUDA device")
+        if not _on_device(t):
+            raise ValueError("tensors must be on the CUDA device or in pinned host memory")
     D = (q if q is not None else k).shape[2]
     T = (q if q is not None else k).shape[0]
     sides = []
@@ -197,8 +204,8 @@ def gbe_qk_norm_rope(q, q_out, gq, k, k_out, gk, eps: float, pos, inv_freq, r: i
     """QK-norm (per-head RMSNorm with gains gq / gk of head_dim entries), then
     RoPE; q, k and outputs as for gbe_rope_qk."""
     for t in (q, q_out, k, k_out, gq, gk, pos, inv_freq, cos_sin):
-        if t is not None and not t.is_cuda:
-            raise ValueError("tensors must be on the CUDA device")
+        if t is not None and not _on_device(t):
+            raise ValueError("tensors must be on the CUDA device or in pinned host memory")
     ref = q if q is not None else k
     T, D = ref.shape[0], ref.shape[2]
     sides = []
