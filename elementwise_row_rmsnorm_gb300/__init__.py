@@ -8,8 +8,8 @@ kernel each, in ``lib/libgbe_elementwise.so`` (declared in
 :mod:`elementwise_row_rmsnorm_gb300.binding`.
 """
 from .binding import (GBE_BF16, GBE_F32, GbeError, LibraryMissing, add, add_rmsnorm, argmax, embedding,
-                      gbe_add, gbe_add_rmsnorm, gbe_argmax, gbe_embedding, gbe_qk_norm_rope, gbe_rmsnorm, gbe_rope,
-                      gbe_rope_cos_sin, gbe_rope_qk, gbe_silu_mul, lib, rmsnorm, rope, rope_cos_sin, silu_mul,
+                      gbe_add, gbe_add_rmsnorm, gbe_argmax, gbe_embedding, gbe_layernorm, gbe_qk_norm_rope, gbe_rmsnorm, gbe_rope,
+                      gbe_rope_cos_sin, gbe_rope_qk, gbe_silu_mul, layernorm, lib, rmsnorm, rope, rope_cos_sin, silu_mul,
                       status_string)
 
 
@@ -21,7 +21,7 @@ def build(force: bool = False) -> str:
 
 __all__ = [
     "GBE_BF16", "GBE_F32", "GbeError", "LibraryMissing", "add", "add_rmsnorm", "argmax", "build",
-    "embedding", "gbe_add", "gbe_add_rmsnorm", "gbe_argmax", "gbe_embedding", "gbe_qk_norm_rope", "gbe_rmsnorm", "gbe_rope",
-    "gbe_rope_cos_sin", "gbe_rope_qk", "gbe_silu_mul", "lib", "rmsnorm", "rope", "rope_cos_sin", "silu_mul",
+    "embedding", "gbe_add", "gbe_add_rmsnorm", "gbe_argmax", "gbe_embedding", "gbe_layernorm", "gbe_qk_norm_rope", "gbe_rmsnorm", "gbe_rope",
+    "gbe_rope_cos_sin", "gbe_rope_qk", "gbe_silu_mul", "layernorm", "lib", "rmsnorm", "rope", "rope_cos_sin", "silu_mul",
     "status_string",
 ]

@@ -56,6 +56,7 @@ def lib() -> ctypes.CDLL:
             sigs = {
                 "gbe_rmsnorm": [vp, vp, vp, i64, i64, f32, i32, vp],
                 "gbe_add_rmsnorm": [vp, vp, vp, vp, vp, i64, i64, f32, i32, vp],
+                "gbe_layernorm": [vp, vp, vp, vp, i64, i64, f32, i32, vp],
                 "gbe_rope": [vp, vp, vp, i64, i64, i64, i64, vp, f32, i32, i32, vp],
                 "gbe_rope_qk": [vp, vp, i64, i64, vp, vp, i64, i64, vp, i64, i64, i64, vp, vp, i64, f32, i32,
                                 i32, vp],
@@ -131,6 +132,17 @@ def gbe_rmsnorm(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor, eps: float, s
         raise ValueError("rmsnorm: y must match x and w must have x.shape[-1] entries")
     _check("gbe_rmsnorm", lib().gbe_rmsnorm(_ptr(x), _ptr(w), _ptr(y), x.numel() // d if d else 0, d,
                                             eps, _dt(x, w, y), _stream(stream)))
+
+
+def gbe_layernorm(x, g, b, y, eps: float, stream=None) -> None:
+    """b may be None (no bias)."""
+    _dev(*[t for t in (x, g, b, y) if t is not None])
+    d = x.shape[-1]
+    if y.shape != x.shape or g.numel() != d or (b is not None and b.numel() != d):
+        raise ValueError("layernorm: y matches x; g and b have x.shape[-1] entries")
+    floats = [t for t in (x, g, b, y) if t is not None]
+    _check("gbe_layernorm", lib().gbe_layernorm(_ptr(x), _ptr(g), _ptr(b), _ptr(y), x.numel() // d if d else 0, d,
+                                                eps, _dt(*floats), _stream(stream)))
 
 
 def gbe_add_rmsnorm(x, residual, w, y, h, eps: float, stream=None) -> None:
@@ -289,6 +301,12 @@ def gbe_argmax(x, out, stream=None) -> None:
 def rmsnorm(x, w, eps: float = 1e-5, out=None, stream=None):
     y = torch.empty_like(x) if out is None else out
     gbe_rmsnorm(x, w, y, eps, stream)
+    return y
+
+
+def layernorm(x, g, b=None, eps: float = 1e-5, stream=None):
+    y = torch.empty_like(x)
+    gbe_layernorm(x, g, b, y, eps, stream)
     return y
 
 

@@ -213,6 +213,24 @@ int gbe_rmsnorm(const void* x, const void* w, void* y, int64_t rows, int64_t d, 
     return finish(gbe::launch_rmsnorm(x, nullptr, w, y, nullptr, rows, d, eps, dtype, vec, as_stream(stream)));
 }
 
+int gbe_layernorm(const void* x, const void* g, const void* b, void* y, int64_t rows, int64_t d, float eps,
+                  int dtype, gbe_stream stream) {
+    const int es = elem_size(dtype);
+    if (!es) return GBE_ERR_DTYPE;
+    if (rows < 0 || d <= 0 || d > INT32_MAX || rows > INT32_MAX) return GBE_ERR_SHAPE;
+    if (!std::isfinite(eps) || eps < 0.0f) return GBE_ERR_EPS;
+    int64_t n;
+    uint64_t bx, bw;
+    if (!mul_ok(rows, d, &n) || !extent(n, es, &bx) || !extent(d, es, &bw)) return GBE_ERR_SHAPE;
+    if (rows == 0) return GBE_OK;
+    const Buf bufs[4] = {{y, bx, (uint64_t)es}, {x, bx, (uint64_t)es}, {g, bw, (uint64_t)es},
+                         {b, b ? bw : 0u, (uint64_t)es}};
+    const int st = check_all(bufs, 1, [](int o, int j) { return o == 0 && j == 1; });
+    if (st != GBE_OK) return st;
+    const bool vec = aligned16(x) && aligned16(y) && aligned16(g) && aligned16(b) && (d * es) % 16 == 0;
+    return finish(gbe::launch_layernorm(x, g, b, y, rows, d, eps, dtype, vec, as_stream(stream)));
+}
+
 int gbe_add_rmsnorm(const void* x, const void* residual, const void* w, void* y, void* h, int64_t rows,
                     int64_t d, float eps, int dtype, gbe_stream stream) {
     const int es = elem_size(dtype);

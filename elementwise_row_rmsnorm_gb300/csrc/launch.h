@@ -12,6 +12,10 @@ namespace gbe {
 cudaError_t launch_rmsnorm(const void* x, const void* res, const void* w, void* y, void* h, int64_t rows,
                            int64_t d, float eps, int dtype, bool vec, cudaStream_t st);
 
+// LayerNorm of each row with gain g and optional bias b (nullptr: none).
+cudaError_t launch_layernorm(const void* x, const void* g, const void* b, void* y, int64_t rows, int64_t d,
+                             float eps, int dtype, bool vec, cudaStream_t st);
+
 // RoPE over one or two [T, H, D] operands (q and k) that share positions and
 // frequencies; each operand has a token stride (elements) used for its input
 // and its output.  cos_sin: NULL, or a [cache_len, r/2] table of (cos, sin).

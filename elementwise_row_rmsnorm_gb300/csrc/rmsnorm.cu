@@ -1,4 +1,5 @@
-// rmsnorm.cu -- RMSNorm and fused residual add + RMSNorm on sm_103a.
+// rmsnorm.cu -- RMSNorm, fused residual add + RMSNorm, and LayerNorm on
+// sm_103a.
 //
 // Definition ("Elementwise kernels in C", section 2.1; "Operations",
 // section 2, RmsNorm): y_i = x_i / sqrt(mean_j(x_j^2) + eps) * w_i over each
@@ -160,6 +161,134 @@ rmsnorm_two_pass(const void* x, const void* res, const void* w, void* y, void* h
     }
 }
 
+// LayerNorm ("Operations", section 2): mu = mean(x), var = mean((x - mu)^2),
+// y = ((x - mu) * (1 / sqrt(var + eps))) * g (+ b).  The same chunk map as
+// RMSNorm; the row's two sums (of x, then of (x - mu)^2) each take the same
+// fixed tree, so a row's bits depend only on the row, d and the type.
+template <int DT, int K, int MAXT>
+__global__ void __launch_bounds__(MAXT)
+layernorm_rows(const void* x, const void* g, const void* b, void* y, int64_t rows, int d, float eps, int tpr) {
+    using S = Store<DT>;
+    constexpr int V = S::V;
+    constexpr int64_t ES = sizeof(typename S::T);
+    pdl_begin();
+    const int rpc = blockDim.x / tpr;
+    const int sub = threadIdx.x / tpr;
+    const int t = threadIdx.x - sub * tpr;
+    const int64_t row = (int64_t)blockIdx.x * rpc + sub;
+    if (row >= rows) return;  // only when several one-warp rows share a CTA
+    const int nchunks = d / V;
+    const int64_t boff = row * (int64_t)d * ES;
+    __shared__ float red[2][32];
+    Vec16 rx[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const int c = k * tpr + t;
+        if (c < nchunks) rx[k] = ld_stream(static_cast<const char*>(x) + boff + (int64_t)c * 16);
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float s = 0.0f;
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const int c = k * tpr + t;
+        if (c < nchunks) {
+            float f[V];
+            S::unpack(rx[k], f);
+#pragma unroll
+            for (int e = 0; e < V; ++e) s = __fadd_rn(s, f[e]);
+        }
+    }
+    const float mu = __fdiv_rn(rpc > 1 ? warp_sum(s) : row_sum(s, red[0], warp, lane, tpr >> 5), (float)d);
+    float s2 = 0.0f;
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const int c = k * tpr + t;
+        if (c < nchunks) {
+            float f[V];
+            S::unpack(rx[k], f);
+#pragma unroll
+            for (int e = 0; e < V; ++e) {
+                const float cc = __fsub_rn(f[e], mu);
+                s2 = __fmaf_rn(cc, cc, s2);
+            }
+        }
+    }
+    const float var = __fdiv_rn(rpc > 1 ? warp_sum(s2) : row_sum(s2, red[1], warp, lane, tpr >> 5), (float)d);
+    const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, eps)));
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const int c = k * tpr + t;
+        if (c < nchunks) {
+            float f[V], gv[V], bv[V];
+            S::unpack(rx[k], f);
+            S::unpack(ld_reuse(static_cast<const char*>(g) + (int64_t)c * 16), gv);
+            if (b != nullptr) S::unpack(ld_reuse(static_cast<const char*>(b) + (int64_t)c * 16), bv);
+#pragma unroll
+            for (int e = 0; e < V; ++e) {
+                const float u = __fmul_rn(__fmul_rn(__fsub_rn(f[e], mu), inv), gv[e]);
+                f[e] = b != nullptr ? __fadd_rn(u, bv[e]) : u;
+            }
+            st_stream(static_cast<char*>(y) + boff + (int64_t)c * 16, S::pack(f));
+        }
+    }
+}
+
+// LayerNorm for unaligned or very wide rows: the same map and trees, x read
+// three times (sum, centred sum of squares, write).  One row per CTA.
+template <int DT>
+__global__ void __launch_bounds__(1024)
+layernorm_three_pass(const void* x, const void* g, const void* b, void* y, int64_t rows, int d, float eps) {
+    using S = Store<DT>;
+    constexpr int V = S::V;
+    pdl_begin();
+    const int tpr = blockDim.x;
+    const int t = threadIdx.x;
+    const int64_t base = (int64_t)blockIdx.x * d;
+    const int nchunks = (d + V - 1) / V;
+    __shared__ float red[2][32];
+    float s = 0.0f;
+    for (int c = t; c < nchunks; c += tpr)
+        for (int e = 0; e < V && c * V + e < d; ++e) s = __fadd_rn(s, S::load1(x, base + (int64_t)c * V + e));
+    const float mu = __fdiv_rn(row_sum(s, red[0], t >> 5, t & 31, tpr >> 5), (float)d);
+    float s2 = 0.0f;
+    for (int c = t; c < nchunks; c += tpr)
+        for (int e = 0; e < V && c * V + e < d; ++e) {
+            const float cc = __fsub_rn(S::load1(x, base + (int64_t)c * V + e), mu);
+            s2 = __fmaf_rn(cc, cc, s2);
+        }
+    const float var = __fdiv_rn(row_sum(s2, red[1], t >> 5, t & 31, tpr >> 5), (float)d);
+    const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, eps)));
+    for (int c = t; c < nchunks; c += tpr)
+        for (int e = 0; e < V && c * V + e < d; ++e) {
+            const int64_t j = (int64_t)c * V + e;
+            const float u = __fmul_rn(__fmul_rn(__fsub_rn(S::load1(x, base + j), mu), inv), S::load1(g, j));
+            S::store1(y, base + j, b != nullptr ? __fadd_rn(u, S::load1(b, j)) : u);
+        }
+}
+
+template <int DT>
+cudaError_t launch_ln(const void* x, const void* g, const void* b, void* y, int64_t rows, int64_t d, float eps,
+                      bool vec, cudaStream_t st) {
+    constexpr int V = Store<DT>::V;
+    const int64_t nchunks = (d + V - 1) / V;
+    int64_t tpr = threads_per_row(nchunks);
+    const bool wide = tpr > 1024;
+    if (wide) tpr = 1024;
+    const int di = (int)d, ti = (int)tpr;
+    if (wide || !vec)
+        return launch(layernorm_three_pass<DT>, dim3((unsigned)rows), dim3((unsigned)tpr), 0, st, x, g, b, y, rows,
+                      di, eps);
+    const int64_t slots = (nchunks + tpr - 1) / tpr;
+    const int rpc = tpr == 32 ? 4 : 1;
+    const dim3 grid((unsigned)((rows + rpc - 1) / rpc)), block((unsigned)(tpr * rpc));
+    if (tpr * rpc <= 256) {
+        if (slots <= 1) return launch(layernorm_rows<DT, 1, 256>, grid, block, 0, st, x, g, b, y, rows, di, eps, ti);
+        if (slots <= 2) return launch(layernorm_rows<DT, 2, 256>, grid, block, 0, st, x, g, b, y, rows, di, eps, ti);
+        return launch(layernorm_rows<DT, 4, 256>, grid, block, 0, st, x, g, b, y, rows, di, eps, ti);
+    }
+    return launch(layernorm_rows<DT, 4, 1024>, grid, block, 0, st, x, g, b, y, rows, di, eps, ti);
+}
+
 template <int DT, bool ADD>
 cudaError_t launch_dt(const void* x, const void* res, const void* w, void* y, void* h, int64_t rows, int64_t d,
                       float eps, bool vec, cudaStream_t st) {
@@ -193,6 +322,12 @@ cudaError_t launch_dt(const void* x, const void* res, const void* w, void* y, vo
 }
 
 }  // namespace
+
+cudaError_t launch_layernorm(const void* x, const void* g, const void* b, void* y, int64_t rows, int64_t d,
+                             float eps, int dtype, bool vec, cudaStream_t st) {
+    return dtype == kF32 ? launch_ln<kF32>(x, g, b, y, rows, d, eps, vec, st)
+                         : launch_ln<kBF16>(x, g, b, y, rows, d, eps, vec, st);
+}
 
 cudaError_t launch_rmsnorm(const void* x, const void* res, const void* w, void* y, void* h, int64_t rows, int64_t d,
                            float eps, int dtype, bool vec, cudaStream_t st) {

@@ -110,6 +110,18 @@ int gbe_add_rmsnorm(const void *x, const void *residual, const void *w, void *y,
                     int64_t d, float eps, int dtype, gbe_stream stream);
 
 /*
+ * gbe_layernorm -- LayerNorm over each row.
+ *   "Operations", section 2 (LayerNorm): mu = mean(x), var = mean((x - mu)^2)
+ *   over the row, y = (x - mu) / sqrt(var + eps) * g + b, eps inside the root.
+ * x, y : [rows, d] row-major, contiguous; g : [d]; b : [d] or NULL (no bias).
+ * eps  : finite and >= 0.  Alias: y == x allowed.
+ * Like gbe_rmsnorm, a row's output bits depend only on that row, g, b, d,
+ * eps and dtype.
+ */
+int gbe_layernorm(const void *x, const void *g, const void *b, void *y, int64_t rows, int64_t d, float eps,
+                  int dtype, gbe_stream stream);
+
+/*
  * gbe_rope -- rotary position embedding.
  *   "Elementwise kernels in C", section 2.2 and 4; "Operations", section 3 (Rope).
  *   For token t and pair i < r/2: theta = float(pos[t]) * inv_freq[i],

@@ -66,6 +66,7 @@ class Oracle:
         sig = {
             "orc_rmsnorm": [vp, vp, vp, i64, i64, f32],
             "orc_add": [vp, vp, vp, i64],
+            "orc_layernorm": [vp, vp, vp, vp, i64, i64, f32],
             "orc_add_rmsnorm": [vp, vp, vp, vp, vp, i64, i64, f32, i32],
             "orc_rope": [vp, vp, vp, i64, i64, i64, i64, vp, f32, i32],
             "orc_rope_cos_sin": [vp, i64, i64, vp],
@@ -113,6 +114,18 @@ class Oracle:
             raise OracleError("rmsnorm: w must have d entries")
         y = np.empty_like(x) if out is None else out
         self._check(self.lib.orc_rmsnorm(_ptr(x), _ptr(w), _ptr(y), rows, d, eps), "rmsnorm")
+        return y
+
+    def layernorm(self, x, g, b, eps: float) -> np.ndarray:
+        """LayerNorm of every row of x with gain g and bias b (None: no bias)."""
+        x, g = _f32(x), _f32(g)
+        d = x.shape[-1]
+        bb = None if b is None else _f32(b)
+        if g.size != d or (bb is not None and bb.size != d):
+            raise OracleError("layernorm: g and b have d entries")
+        y = np.empty_like(x)
+        self._check(self.lib.orc_layernorm(_ptr(x), _ptr(g), None if bb is None else _ptr(bb), _ptr(y),
+                                           x.size // d, d, eps), "layernorm")
         return y
 
     def add(self, a, b) -> np.ndarray:

@@ -10,7 +10,7 @@
  *
  * What it follows.  The two pages define every op in f32:
  *   [Ops]  "Operations" (glia runtime spec): section 1 (Argmax, Add),
- *          section 2 (RmsNorm), section 3 (Rope, Cos/sin cache, TokenEmbed),
+ *          section 2 (RmsNorm, LayerNorm), section 3 (Rope, Cos/sin cache, TokenEmbed),
  *          section 4 (Silu), section 5 (QK-norm), section 10 (FusedSkipNorm).  Its CPU reference computes
  *          everything in f32.
  *   [L9.6] "Elementwise kernels in C: RMSNorm, RoPE, SiLU-mul, embedding,
@@ -26,7 +26,8 @@
  * Planted mistakes.  Building with -DORACLE_MUTANT=k (1..15) swaps in the
  * k-th wrong variant of the pitfalls table of [L9.6] section 5 (s01..s15);
  * k = 16 is the pitfall [Ops] section 5 warns about for QK-norm (the norm
- * taken over num_heads * head_dim instead of per head).
+ * taken over num_heads * head_dim instead of per head); k = 17 plants a
+ * LayerNorm whose variance is not centred on the mean ([Ops] section 2).
  * The tests build those variants on the CPU to show that their pins reject
  * each one.  A normal build (ORACLE_MUTANT undefined) contains none of them.
  */
@@ -99,6 +100,40 @@ int orc_rmsnorm(const float *x, const float *w, float *y, int64_t rows, int64_t 
         for (int64_t i = 0; i < d; ++i) {
             float t = xr[i] * inv;
             yr[i] = MUT(3) ? t : t * w[i];             /* s03: gain forgotten */
+        }
+    }
+    return ORC_OK;
+}
+
+/* ---- LayerNorm ---------------------------------------------------------------
+ * [Ops] 2 (LayerNorm): mu = mean(x), var = mean((x - mu)^2) over one row,
+ * y = (x - mu) / sqrt(var + eps) * g + b.  Per row: sum x in f32 in
+ * increasing i and divide by d; then sum (x_i - mu)^2 the same way and
+ * divide by d; then write ((x_i - mu) * inv) * g_i + b_i with
+ * inv = 1 / sqrt(var + eps).  b may be NULL (no bias; the ruDNN page makes
+ * the bias optional).  Reading: the division by the root is taken as a
+ * product with its correctly rounded inverse, as for RMSNorm.  y may be x.  */
+int orc_layernorm(const float *x, const float *g, const float *b, float *y, int64_t rows, int64_t d,
+                  float eps) {
+    if (rows < 0 || d <= 0) return ORC_ERR_ARG;
+    for (int64_t r = 0; r < rows; ++r) {
+        const float *xr = x + r * d;
+        float *yr = y + r * d;
+        float s = 0.0f;
+        for (int64_t i = 0; i < d; ++i) s = s + xr[i];
+        float mu = s / (float)d;
+        float s2 = 0.0f;
+        for (int64_t i = 0; i < d; ++i) {
+            float c = MUT(17) ? xr[i] : xr[i] - mu; /* s17: variance not centred on the mean */
+            float sq = c * c;
+            s2 = s2 + sq;
+        }
+        float var = s2 / (float)d;
+        float inv = 1.0f / sqrtf(var + eps);
+        for (int64_t i = 0; i < d; ++i) {
+            float t = (xr[i] - mu) * inv;
+            float u = t * g[i];
+            yr[i] = b ? u + b[i] : u;
         }
     }
     return ORC_OK;

@@ -99,6 +99,32 @@ def pin_rmsnorm_closed_forms(o):
     assert np.allclose(rms, 1.0, atol=2e-6), rms
 
 
+def pin_layernorm(o):
+    """LayerNorm against float64 torch layer_norm, its closed forms (zero mean
+    and unit variance of (y - b) / g at eps = 0, invariance to a constant
+    shift by a power of two), and a constant row giving exactly b."""
+    for d in (1, 7, 64, 1000, 4096):
+        x = _rand(5, d, scale=3.0) + np.float32(0.75)
+        g = RNG.uniform(0.5, 1.5, d).astype(np.float32)
+        b = _rand(d, scale=0.2)
+        y = o.layernorm(x, g, b, 1e-5).astype(np.float64)
+        ref = torch.nn.functional.layer_norm(torch.from_numpy(x).double(), (d,), torch.from_numpy(g).double(),
+                                             torch.from_numpy(b).double(), 1e-5).numpy()
+        scale = np.abs(ref - b).max(axis=-1, keepdims=True) + np.abs(b).max() + 1e-30
+        assert np.all(np.abs(y - ref) <= 4e-6 * scale), d
+        y0 = o.layernorm(x, g, None, 1e-5).astype(np.float64)
+        assert np.all(np.abs(y0 - (ref - b)) <= 4e-6 * scale), d
+    x = _rand(6, 513)
+    g = RNG.uniform(0.5, 1.5, 513).astype(np.float32)
+    b = _rand(513, scale=0.3)
+    z = (o.layernorm(x, g, b, 0.0).astype(np.float64) - b) / g
+    assert np.allclose(z.mean(axis=1), 0.0, atol=1e-6) and np.allclose((z ** 2).mean(axis=1), 1.0, atol=4e-6)
+    shifted = o.layernorm(x + np.float32(4.0), g, b, 0.0)
+    assert np.allclose(shifted, o.layernorm(x, g, b, 0.0), rtol=0, atol=2e-5)
+    const = np.full((2, 40), 3.25, np.float32)
+    assert _same_bits(o.layernorm(const, g[:40], b[:40], 1e-5), np.broadcast_to(b[:40], (2, 40)))
+
+
 def pin_add_rmsnorm_composition(o):
     d = 300
     x, r = _rand(4, d), _rand(4, d)
@@ -399,4 +425,5 @@ KILLS = {
     14: "argmax_ties_nan_and_empty",
     15: "rmsnorm_rows_are_independent_and_in_place",
     16: "qk_norm_rope_per_head",
+    17: "layernorm",
 }

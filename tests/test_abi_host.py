@@ -30,7 +30,7 @@ def declared_functions():
 def test_header_declares_the_ops():
     names = declared_functions()
     for op in ("gbe_rmsnorm", "gbe_add_rmsnorm", "gbe_rope", "gbe_rope_qk", "gbe_rope_cos_sin", "gbe_silu_mul",
-               "gbe_add", "gbe_embedding", "gbe_argmax", "gbe_status_string", "gbe_version",
+               "gbe_add", "gbe_embedding", "gbe_argmax", "gbe_layernorm", "gbe_status_string", "gbe_version",
                "gbe_last_cuda_error"):
         assert op in names
 
@@ -67,6 +67,10 @@ def test_rejects_bad_sizes_and_scalars(L):
     assert L.gbe_rmsnorm(NULL, NULL, NULL, 0, 8, 1e-5, 0, S) == 0          # empty: no-op
     assert L.gbe_add_rmsnorm(NULL, NULL, NULL, NULL, NULL, 2, 8, -3.0, 0, S) == 5
     assert L.gbe_add_rmsnorm(NULL, NULL, NULL, NULL, NULL, 0, 8, 1e-5, 0, S) == 0
+    assert L.gbe_layernorm(NULL, NULL, NULL, NULL, 4, 0, 1e-5, 0, S) == 2
+    assert L.gbe_layernorm(NULL, NULL, NULL, NULL, 4, 8, float("nan"), 0, S) == 5
+    assert L.gbe_layernorm(NULL, NULL, NULL, NULL, 4, 8, 1e-5, 3, S) == 3
+    assert L.gbe_layernorm(NULL, NULL, NULL, NULL, 0, 8, 1e-5, 1, S) == 0
     # rope: layout, width, scaling, shapes
     assert L.gbe_rope(NULL, NULL, NULL, 4, 2, 16, 8, NULL, 1.0, 2, 0, S) == 4
     assert L.gbe_rope(NULL, NULL, NULL, 4, 2, 16, 7, NULL, 1.0, 0, 0, S) == 6   # odd r
