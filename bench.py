@@ -79,6 +79,14 @@ def op_bytes(op: str, arrays: dict, params: dict) -> tuple[int, int]:
         return 2 * n * d * es + nb(arrays["ids"]), n
     if op == "add_rmsnorm":
         return 4 * nb(arrays["x"]) + nb(arrays["w"]), params["rows"]
+    if op == "qk_norm_rope":
+        return (2 * (nb(arrays["q"]) + nb(arrays["k"])) + nb(arrays["gq"]) + nb(arrays["gk"]) + nb(arrays["pos"])
+                + 4 * (params["r"] // 2)), params["T"]
+    if op == "layernorm":
+        return 2 * nb(arrays["x"]) + nb(arrays["g"]) + nb(arrays["b"]), params["rows"]
+    if op == "rope_qk_half_cached":
+        T, r = params["T"], params["r"]
+        return 2 * (nb(arrays["q"]) + nb(arrays["k"])) + nb(arrays["pos"]) + T * (r // 2) * 8, T
     if op.startswith("rope"):
         T, D, r = params["T"], params["D"], params["r"]
         moved = 0
@@ -178,6 +186,32 @@ def combine(op: str, parts):
         (aq, pq), (ak, _) = parts
         return {"q": aq["x"], "k": ak["x"], "pos": aq["pos"], "inv_freq": aq["inv_freq"]}, pq
     return parts[0]
+
+
+EXTRA = ("qk_norm_rope", "rope_qk_half_cached", "layernorm")
+
+
+def build_extra_inputs(tokens: int = 8192):
+    """Inputs of the ops beyond the step, at the same prefill shapes: QK-norm
+    then RoPE on q [T, 32, 128] and k [T, 8, 128] (gains U(0.5, 1.5)); RoPE of
+    q and k driven by a cos/sin table of 8192 positions; LayerNorm of
+    [T, 4096] with gain and bias."""
+    import synth
+    from synth import workloads as W
+    cases = W.cases(W.PREFILL)
+    rows = None if tokens >= 8192 else (0, tokens)
+    seed = W.SEEDS[W.PREFILL]
+    (aq, pq), (ak, _) = cases["rope_q"](rows=rows), cases["rope_k"](rows=rows)
+    gq = synth.uniform_bf16(seed, "qk_norm.gq", (128,), 0.5, 1.5)
+    gk = synth.uniform_bf16(seed, "qk_norm.gk", (128,), 0.5, 1.5)
+    qk = {"q": aq["x"], "k": ak["x"], "pos": aq["pos"], "inv_freq": aq["inv_freq"]}
+    ax, px = cases["rmsnorm"](rows=rows)
+    lb = synth.normal_bf16(seed, "layernorm.b", (ax["x"].shape[1],), 0.0, 0.2)
+    return {
+        "qk_norm_rope": (dict(qk, gq=gq, gk=gk), dict(pq, eps=1e-6)),
+        "rope_qk_half_cached": (dict(qk), dict(pq, cache_len=8192)),
+        "layernorm": ({"x": ax["x"], "g": ax["w"], "b": lb}, px),
+    }
 
 
 def build_inputs(tokens: int = 8192):
@@ -327,14 +361,18 @@ def run_isolated(args):
     torch.cuda.set_device(dev)
     gbe.lib()
     data = build_inputs(args.tokens)
+    if args.extra:
+        data.update(build_extra_inputs(args.tokens))
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     res = {}
-    for op, _names in STEP:
+    for op in list(data):
         arrays, params = data[op]
         nb, rows = op_bytes(op, arrays, params)
         sets = int(min(12, max(2, -(-4 * l2 // nb) + 1)))
         base = {k: to_device(torch, dev, v) for k, v in arrays.items()}
-        shared = ("table", "w", "inv_freq", "pos", "ids")
+        shared = ("table", "w", "g", "gq", "gk", "inv_freq", "pos", "ids", "cos_sin")
+        if op == "rope_qk_half_cached":
+            base["cos_sin"] = gbe.rope_cos_sin(base["inv_freq"], params["r"], params["cache_len"])
         rings = []
         for _ in range(sets):
             b = {k: (v if k in shared else v.clone()) for k, v in base.items()}
@@ -380,7 +418,7 @@ def make_outputs(torch, dev, op, b):
         return torch.empty((b["ids"].numel(), b["table"].shape[1]), dtype=b["table"].dtype, device=dev)
     if op == "add_rmsnorm":
         return (torch.empty_like(b["x"]), torch.empty_like(b["x"]))
-    if op.startswith("rope_qk"):
+    if op.startswith("rope_qk") or op == "qk_norm_rope":
         return (torch.empty_like(b["q"]), torch.empty_like(b["k"]))
     if op == "argmax":
         return torch.empty((b["x"].shape[0],), dtype=torch.int32, device=dev)
@@ -392,14 +430,22 @@ def run_op(gbe, op, p, b, o):
         gbe.gbe_embedding(b["table"], b["ids"], o)
     elif op == "add_rmsnorm":
         gbe.gbe_add_rmsnorm(b["x"], b["residual"], b["w"], o[0], o[1], p["eps"])
+    elif op == "rope_qk_half_cached":
+        gbe.gbe_rope_qk(b["q"], o[0], b["k"], o[1], b["pos"], b["inv_freq"], p["r"], p["mu"], p["layout"],
+                        cos_sin=b["cos_sin"])
     elif op.startswith("rope_qk"):
         gbe.gbe_rope_qk(b["q"], o[0], b["k"], o[1], b["pos"], b["inv_freq"], p["r"], p["mu"], p["layout"])
+    elif op == "qk_norm_rope":
+        gbe.gbe_qk_norm_rope(b["q"], o[0], b["gq"], b["k"], o[1], b["gk"], p["eps"], b["pos"], b["inv_freq"], p["r"],
+                             p["mu"], p["layout"])
     elif op == "silu_mul":
         gbe.gbe_silu_mul(b["gate"], b["up"], o)
     elif op == "add":
         gbe.gbe_add(b["a"], b["b"], o)
     elif op == "rmsnorm":
         gbe.gbe_rmsnorm(b["x"], b["w"], o, p["eps"])
+    elif op == "layernorm":
+        gbe.gbe_layernorm(b["x"], b["g"], b["b"], o, p["eps"])
     elif op == "argmax":
         gbe.gbe_argmax(b["x"], o)
 
@@ -658,6 +704,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--isolated", action="store_true",
                     help="time each op alone, back to back over rotating buffers, and print that instead")
+    ap.add_argument("--extra", action="store_true",
+                    help="with --isolated: also time the ops beyond the step (QK-norm+RoPE, table-driven RoPE, "
+                         "LayerNorm)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
     if args.ops:
