@@ -21,12 +21,13 @@
 //  * the angles are float(p) * omega_i and CUDA's sincosf (or the same values
 //    from the cos/sin table), as in rope.cu.
 //
-// Map: one warp per token.  It forms the angles of its lanes' entries once
-// and reuses them for every head of q and of k.  Per pass, 32 / W head rows
-// are loaded (up to four passes' loads in flight before any use),
-// normalised, staged in shared memory (so a lane can read the partner of
-// each of its entries), rotated and stored.  Head width is limited to 32
-// chunks (head_dim <= 128 f32 / 256 bf16).
+// Map: a warp owns one chunk of head rows of one token (4 passes of 32 / W
+// rows: 8 rows for bf16 head_dim 128), so the heads of a token spread over
+// several warps.  It issues the loads of all its rows first, forms its
+// lanes' angles while they are in flight, reduces the rows side by side,
+// stages the normalised rows in shared memory (so a lane can read the
+// partner of each of its entries), rotates and stores them.  Head width is
+// limited to 32 chunks (head_dim <= 128 f32 / 256 bf16).
 #include "common.cuh"
 #include "launch.h"
 
@@ -60,24 +61,48 @@ __device__ __forceinline__ void load_chunk(const char* row, int c, int D, float 
 
 template <int DT, int LAYOUT, bool VEC, bool CACHE>
 __global__ void __launch_bounds__(kWarps * 32)
-qk_norm_rope_kernel(QkSide A, QkSide B, float eps, const int32_t* pos, int64_t T, int D, int r,
+qk_norm_rope_kernel(QkSide A, QkSide B, int nca, int ncb, float eps, const int32_t* pos, int64_t T, int D, int r,
                     const float* inv_freq, const float2* cache, int64_t cache_len, float mu, int W) {
     using S = Store<DT>;
     constexpr int V = S::V;
     constexpr int64_t ES = sizeof(typename S::T);
-    __shared__ float stage[kWarps][kMaxRow];
+    __shared__ float stage[kWarps][kPasses][kMaxRow];
     pdl_begin();
     const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t t = (int64_t)blockIdx.x * kWarps + wib;
+    // work item of this warp: (token, operand, chunk of R * kPasses heads)
+    const int64_t item = (int64_t)blockIdx.x * kWarps + wib;
+    const int per_tok = nca + ncb;
+    const int64_t t = item / per_tok;
     if (t >= T) return;  // whole warps leave together: no CTA barrier follows
+    const int ci = (int)(item - t * per_tok);
+    const bool second = ci >= nca;
+    const QkSide Q = second ? B : A;
     const int nchunks = (D + V - 1) / V;
-    const int R = 32 / W;        // head rows per pass
-    const int sub = lane / W;    // row of this lane within a pass
+    const int R = 32 / W;          // head rows per pass
+    const int sub = lane / W;      // row of this lane within a pass
     const int c = lane - sub * W;  // chunk of this lane
     const bool has = c < nchunks;
     const int half = r >> 1;
-    float* row_buf = &stage[wib][sub * (nchunks * V)];
+    const int h0 = (second ? ci - nca : ci) * R * kPasses;
 
+    // loads of every head row of the chunk, before anything else
+    const char* xt = Q.x + t * Q.xs * ES;
+    char* yt = Q.y + t * Q.ys * ES;
+    float f[kPasses][V];
+#pragma unroll
+    for (int k = 0; k < kPasses; ++k) {
+        const int h = h0 + k * R + sub;
+        if (has && h < Q.H) load_chunk<DT, VEC>(xt + (int64_t)h * D * ES, c, D, f[k]);
+    }
+    // this lane's gain chunk
+    float gv[V];
+    if (has) {
+        if (VEC)
+            S::unpack(ld_reuse(Q.g + (int64_t)c * 16), gv);
+        else
+#pragma unroll
+            for (int e = 0; e < V; ++e) gv[e] = c * V + e < D ? S::load1(Q.g, (int64_t)c * V + e) : 0.0f;
+    }
     // the angle of every entry this lane writes (pair of entry j)
     float ca[V], sa[V];
     const int32_t p = pos[t];
@@ -97,83 +122,67 @@ qk_norm_rope_kernel(QkSide A, QkSide B, float eps, const int32_t* pos, int64_t T
             }
         }
     }
-
-    for (int side = 0; side < 2; ++side) {
-        const QkSide Q = side == 0 ? A : B;
-        if (Q.H == 0) continue;
-        // this lane's gain chunk, the same for every head
-        float gv[V];
-        if (has) {
-            if (VEC)
-                S::unpack(ld_reuse(Q.g + (int64_t)c * 16), gv);
-            else
+    // 1) every row's mean of squares: lane sums, then width-W butterflies
+    float s[kPasses];
 #pragma unroll
-                for (int e = 0; e < V; ++e) gv[e] = c * V + e < D ? S::load1(Q.g, (int64_t)c * V + e) : 0.0f;
+    for (int k = 0; k < kPasses; ++k) {
+        s[k] = 0.0f;
+        if (has && h0 + k * R + sub < Q.H) {
+#pragma unroll
+            for (int e = 0; e < V; ++e) s[k] = __fmaf_rn(f[k][e], f[k][e], s[k]);
         }
-        const char* xt = Q.x + t * Q.xs * ES;
-        char* yt = Q.y + t * Q.ys * ES;
-        for (int h0 = 0; h0 < Q.H; h0 += R * kPasses) {
-            float f[kPasses][V];
+    }
+    for (int m = W >> 1; m >= 1; m >>= 1) {
 #pragma unroll
-            for (int k = 0; k < kPasses; ++k) {
-                const int h = h0 + k * R + sub;
-                if (has && h < Q.H) load_chunk<DT, VEC>(xt + (int64_t)h * D * ES, c, D, f[k]);
+        for (int k = 0; k < kPasses; ++k) s[k] = __fadd_rn(s[k], __shfl_xor_sync(0xFFFFFFFFu, s[k], m));
+    }
+    // 2) normalised, stored in the storage type, staged for the partners
+    float* rows = &stage[wib][0][sub * (nchunks * V)];
+#pragma unroll
+    for (int k = 0; k < kPasses; ++k) {
+        const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(s[k], (float)D), eps)));
+        if (has && h0 + k * R + sub < Q.H) {
+#pragma unroll
+            for (int e = 0; e < V; ++e) {
+                f[k][e] = S::round(__fmul_rn(__fmul_rn(f[k][e], inv), gv[e]));
+                if (c * V + e < D) rows[k * kMaxRow + c * V + e] = f[k][e];
             }
+        }
+    }
+    __syncwarp();
+    // 3) rotate every entry from itself and its partner, store
 #pragma unroll
-            for (int k = 0; k < kPasses; ++k) {
-                if (h0 + k * R >= Q.H) break;  // uniform across the warp
-                const int h = h0 + k * R + sub;
-                const bool live = has && h < Q.H;
-                // 1) the row's mean of squares: lane sum, then a width-W butterfly
-                float s = 0.0f;
-                if (live) {
+    for (int k = 0; k < kPasses; ++k) {
+        const int h = h0 + k * R + sub;
+        if (!(has && h < Q.H)) continue;
+        const float* row = rows + k * kMaxRow;
+        float o[V];
 #pragma unroll
-                    for (int e = 0; e < V; ++e) s = __fmaf_rn(f[k][e], f[k][e], s);
+        for (int e = 0; e < V; ++e) {
+            const int j = c * V + e;
+            const float n = f[k][e];
+            o[e] = n;
+            if (j < r) {
+                float a, b;
+                bool first;
+                if (LAYOUT == 0) {
+                    first = j < half;
+                    a = first ? n : row[j - half];
+                    b = first ? row[j + half] : n;
+                } else {
+                    first = (j & 1) == 0;
+                    a = first ? n : row[j - 1];
+                    b = first ? row[j + 1] : n;
                 }
-                for (int m = W >> 1; m >= 1; m >>= 1) s = __fadd_rn(s, __shfl_xor_sync(0xFFFFFFFFu, s, m));
-                const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(s, (float)D), eps)));
-                // 2) normalised, stored in the storage type, staged for the partners
-                float n[V];
-                if (live) {
-#pragma unroll
-                    for (int e = 0; e < V; ++e) {
-                        n[e] = S::round(__fmul_rn(__fmul_rn(f[k][e], inv), gv[e]));
-                        if (c * V + e < D) row_buf[c * V + e] = n[e];
-                    }
-                }
-                __syncwarp();
-                // 3) rotate: every entry from itself and its partner
-                if (live) {
-                    float o[V];
-#pragma unroll
-                    for (int e = 0; e < V; ++e) {
-                        const int j = c * V + e;
-                        o[e] = n[e];
-                        if (j < r) {
-                            float a, b;
-                            bool first;
-                            if (LAYOUT == 0) {
-                                first = j < half;
-                                a = first ? n[e] : row_buf[j - half];
-                                b = first ? row_buf[j + half] : n[e];
-                            } else {
-                                first = (j & 1) == 0;
-                                a = first ? n[e] : row_buf[j - 1];
-                                b = first ? row_buf[j + 1] : n[e];
-                            }
-                            o[e] = first ? __fmul_rn(mu, __fsub_rn(__fmul_rn(a, ca[e]), __fmul_rn(b, sa[e])))
-                                         : __fmul_rn(mu, __fadd_rn(__fmul_rn(a, sa[e]), __fmul_rn(b, ca[e])));
-                        }
-                    }
-                    char* yr = yt + (int64_t)h * D * ES;
-                    if (VEC) {
-                        st_stream(yr + (int64_t)c * 16, S::pack(o));
-                    } else {
-                        for (int e = 0; e < V && c * V + e < D; ++e) S::store1(yr, (int64_t)c * V + e, o[e]);
-                    }
-                }
-                __syncwarp();  // the staging row is rewritten by the next pass
+                o[e] = first ? __fmul_rn(mu, __fsub_rn(__fmul_rn(a, ca[e]), __fmul_rn(b, sa[e])))
+                             : __fmul_rn(mu, __fadd_rn(__fmul_rn(a, sa[e]), __fmul_rn(b, ca[e])));
             }
+        }
+        char* yr = yt + (int64_t)h * D * ES;
+        if (VEC) {
+            st_stream(yr + (int64_t)c * 16, S::pack(o));
+        } else {
+            for (int e = 0; e < V && c * V + e < D; ++e) S::store1(yr, (int64_t)c * V + e, o[e]);
         }
     }
 }
@@ -194,13 +203,17 @@ cudaError_t launch_dt(const QkNormRopeArgs& a, bool vec, cudaStream_t st) {
         sd[k].ys = a.side[k].stride;
         sd[k].H = (int)a.side[k].H;
     }
-    const unsigned grid = (unsigned)((a.T + kWarps - 1) / kWarps);
+    const int rows_per_item = (32 / W) * kPasses;  // head rows one warp handles
+    const int nca = (int)((a.side[0].H + rows_per_item - 1) / rows_per_item);
+    const int ncb = (int)((a.side[1].H + rows_per_item - 1) / rows_per_item);
+    const int64_t items = a.T * (nca + ncb);
+    const unsigned grid = (unsigned)((items + kWarps - 1) / kWarps);
     const float2* cache = reinterpret_cast<const float2*>(a.cos_sin);
     const bool cached = cache != nullptr;
     const int Di = (int)a.D, ri = (int)a.r;
 #define GBE_QKN(L, VV, C)                                                                                 \
-    return launch(qk_norm_rope_kernel<DT, L, VV, C>, dim3(grid), dim3(kWarps * 32), 0, st, sd[0], sd[1], a.eps, \
-                  a.pos, a.T, Di, ri, a.inv_freq, cache, a.cache_len, a.mu, W)
+    return launch(qk_norm_rope_kernel<DT, L, VV, C>, dim3(grid), dim3(kWarps * 32), 0, st, sd[0], sd[1], nca, ncb, \
+                  a.eps, a.pos, a.T, Di, ri, a.inv_freq, cache, a.cache_len, a.mu, W)
 #define GBE_QKN_L(L)                                                  \
     if (vec) {                                                        \
         if (cached) GBE_QKN(L, true, true); else GBE_QKN(L, true, false);   \

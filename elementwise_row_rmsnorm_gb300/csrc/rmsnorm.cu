@@ -49,15 +49,26 @@ inline int64_t threads_per_row(int64_t nchunks) {
 
 // Aligned rows: the row's chunks stay in registers as packed 16-byte vectors
 // (4 f32 or 8 bf16 each) from the load to the write.
-template <int DT, int K, bool ADD, int MAXT>
-__global__ void __launch_bounds__(MAXT)
+// TPR > 0: threads per row fixed at compile time (one row per CTA, or four
+// one-warp rows when TPR is 32); TPR == 0: taken from `tpr_rt` (any multiple
+// of 32 up to 1024, one row per CTA).  Either way the map and tree are those
+// of the header comment.
+template <int TPR>
+struct RowShape {
+    static constexpr int kRpc = TPR == 32 ? 4 : 1;
+    static constexpr int kMaxThreads = TPR == 0 ? 1024 : TPR * kRpc;
+};
+
+template <int DT, int K, bool ADD, int TPR>
+__global__ void __launch_bounds__(RowShape<TPR>::kMaxThreads)
 rmsnorm_rows(const void* x, const void* res, const void* w, void* y, void* h, int64_t rows, int d, float eps,
-             int tpr) {
+             int tpr_rt) {
     using S = Store<DT>;
     constexpr int V = S::V;
     constexpr int64_t ES = sizeof(typename S::T);
+    constexpr int rpc = RowShape<TPR>::kRpc;
+    const int tpr = TPR > 0 ? TPR : tpr_rt;
     pdl_begin();
-    const int rpc = blockDim.x / tpr;
     const int sub = threadIdx.x / tpr;
     const int t = threadIdx.x - sub * tpr;
     const int64_t row = (int64_t)blockIdx.x * rpc + sub;
@@ -101,7 +112,7 @@ rmsnorm_rows(const void* x, const void* res, const void* w, void* y, void* h, in
     }
     // 3) the row's sum, fixed order
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const float total = rpc > 1 ? warp_sum(s) : row_sum(s, red, warp, lane, tpr >> 5);
+    const float total = (TPR == 32) ? warp_sum(s) : row_sum(s, red, warp, lane, tpr >> 5);
     const float ms = __fdiv_rn(total, (float)d);
     const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
     // 4) y = x * inv * w
@@ -165,14 +176,15 @@ rmsnorm_two_pass(const void* x, const void* res, const void* w, void* y, void* h
 // y = ((x - mu) * (1 / sqrt(var + eps))) * g (+ b).  The same chunk map as
 // RMSNorm; the row's two sums (of x, then of (x - mu)^2) each take the same
 // fixed tree, so a row's bits depend only on the row, d and the type.
-template <int DT, int K, int MAXT>
-__global__ void __launch_bounds__(MAXT)
-layernorm_rows(const void* x, const void* g, const void* b, void* y, int64_t rows, int d, float eps, int tpr) {
+template <int DT, int K, int TPR>
+__global__ void __launch_bounds__(RowShape<TPR>::kMaxThreads)
+layernorm_rows(const void* x, const void* g, const void* b, void* y, int64_t rows, int d, float eps, int tpr_rt) {
     using S = Store<DT>;
     constexpr int V = S::V;
     constexpr int64_t ES = sizeof(typename S::T);
+    constexpr int rpc = RowShape<TPR>::kRpc;
+    const int tpr = TPR > 0 ? TPR : tpr_rt;
     pdl_begin();
-    const int rpc = blockDim.x / tpr;
     const int sub = threadIdx.x / tpr;
     const int t = threadIdx.x - sub * tpr;
     const int64_t row = (int64_t)blockIdx.x * rpc + sub;
@@ -198,7 +210,7 @@ layernorm_rows(const void* x, const void* g, const void* b, void* y, int64_t row
             for (int e = 0; e < V; ++e) s = __fadd_rn(s, f[e]);
         }
     }
-    const float mu = __fdiv_rn(rpc > 1 ? warp_sum(s) : row_sum(s, red[0], warp, lane, tpr >> 5), (float)d);
+    const float mu = __fdiv_rn((TPR == 32) ? warp_sum(s) : row_sum(s, red[0], warp, lane, tpr >> 5), (float)d);
     float s2 = 0.0f;
 #pragma unroll
     for (int k = 0; k < K; ++k) {
@@ -213,7 +225,7 @@ layernorm_rows(const void* x, const void* g, const void* b, void* y, int64_t row
             }
         }
     }
-    const float var = __fdiv_rn(rpc > 1 ? warp_sum(s2) : row_sum(s2, red[1], warp, lane, tpr >> 5), (float)d);
+    const float var = __fdiv_rn((TPR == 32) ? warp_sum(s2) : row_sum(s2, red[1], warp, lane, tpr >> 5), (float)d);
     const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, eps)));
 #pragma unroll
     for (int k = 0; k < K; ++k) {
@@ -279,14 +291,22 @@ cudaError_t launch_ln(const void* x, const void* g, const void* b, void* y, int6
         return launch(layernorm_three_pass<DT>, dim3((unsigned)rows), dim3((unsigned)tpr), 0, st, x, g, b, y, rows,
                       di, eps);
     const int64_t slots = (nchunks + tpr - 1) / tpr;
-    const int rpc = tpr == 32 ? 4 : 1;
-    const dim3 grid((unsigned)((rows + rpc - 1) / rpc)), block((unsigned)(tpr * rpc));
-    if (tpr * rpc <= 256) {
-        if (slots <= 1) return launch(layernorm_rows<DT, 1, 256>, grid, block, 0, st, x, g, b, y, rows, di, eps, ti);
-        if (slots <= 2) return launch(layernorm_rows<DT, 2, 256>, grid, block, 0, st, x, g, b, y, rows, di, eps, ti);
-        return launch(layernorm_rows<DT, 4, 256>, grid, block, 0, st, x, g, b, y, rows, di, eps, ti);
+    const dim3 one((unsigned)rows), four((unsigned)((rows + 3) / 4));
+#define GBE_LN(KK, TT, GRID, BLOCK) \
+    return launch(layernorm_rows<DT, KK, TT>, GRID, dim3(BLOCK), 0, st, x, g, b, y, rows, di, eps, ti)
+    switch (tpr) {
+        case 32:
+            if (slots <= 1) GBE_LN(1, 32, four, 128);
+            if (slots <= 2) GBE_LN(2, 32, four, 128);
+            GBE_LN(4, 32, four, 128);
+        case 64: GBE_LN(4, 64, one, 64);
+        case 128: GBE_LN(4, 128, one, 128);
+        case 256: GBE_LN(4, 256, one, 256);
+        case 512: GBE_LN(4, 512, one, 512);
+        case 1024: GBE_LN(4, 1024, one, 1024);
+        default: GBE_LN(4, 0, one, tpr);
     }
-    return launch(layernorm_rows<DT, 4, 1024>, grid, block, 0, st, x, g, b, y, rows, di, eps, ti);
+#undef GBE_LN
 }
 
 template <int DT, bool ADD>
@@ -303,22 +323,22 @@ cudaError_t launch_dt(const void* x, const void* res, const void* w, void* y, vo
                       rows, di, eps);
     }
     const int64_t slots = (nchunks + tpr - 1) / tpr;
-    const int rpc = tpr == 32 ? 4 : 1;
-    const int64_t grid = (rows + rpc - 1) / rpc;
-    const dim3 block((unsigned)(tpr * rpc));
-#define GBE_RMS_CASE(KK, MT)                                                                                  \
-    if (slots <= KK)                                                                                          \
-        return launch(rmsnorm_rows<DT, KK, ADD, MT>, dim3((unsigned)grid), block, 0, st, x, res, w, y, h, rows, di, \
-                      eps, ti);
-    if (tpr * rpc <= 256) {
-        GBE_RMS_CASE(1, 256)
-        GBE_RMS_CASE(2, 256)
-        GBE_RMS_CASE(4, 256)
-    } else {
-        GBE_RMS_CASE(4, 1024)
+    const dim3 one((unsigned)rows), four((unsigned)((rows + 3) / 4));
+#define GBE_RMS(KK, TT, GRID, BLOCK) \
+    return launch(rmsnorm_rows<DT, KK, ADD, TT>, GRID, dim3(BLOCK), 0, st, x, res, w, y, h, rows, di, eps, ti)
+    switch (tpr) {
+        case 32:
+            if (slots <= 1) GBE_RMS(1, 32, four, 128);
+            if (slots <= 2) GBE_RMS(2, 32, four, 128);
+            GBE_RMS(4, 32, four, 128);
+        case 64: GBE_RMS(4, 64, one, 64);
+        case 128: GBE_RMS(4, 128, one, 128);
+        case 256: GBE_RMS(4, 256, one, 256);
+        case 512: GBE_RMS(4, 512, one, 512);
+        case 1024: GBE_RMS(4, 1024, one, 1024);
+        default: GBE_RMS(4, 0, one, tpr);
     }
-#undef GBE_RMS_CASE
-    return cudaErrorInvalidValue;
+#undef GBE_RMS
 }
 
 }  // namespace
