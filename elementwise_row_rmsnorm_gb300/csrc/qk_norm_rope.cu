@@ -36,7 +36,8 @@ namespace gbe {
 namespace {
 
 constexpr int kWarps = 4;   // warps (tokens) per CTA
-constexpr int kPasses = 4;  // head-row passes whose loads are in flight together
+constexpr int kPasses = 4;      // head-row passes whose loads are in flight together
+constexpr int kPassesShfl = 8;  // the same for the shuffle path (no staging rows to hold)
 constexpr int kMaxRow = 256;  // floats of one warp's staging: 32 chunks of <= 8 entries
 
 struct QkSide {
@@ -56,6 +57,124 @@ __device__ __forceinline__ void load_chunk(const char* row, int c, int D, float 
     } else {
 #pragma unroll
         for (int e = 0; e < V; ++e) f[e] = c * V + e < D ? S::load1(row, (int64_t)c * V + e) : 0.0f;
+    }
+}
+
+// Aligned rows whose pair partners lie a whole number of chunks apart (the
+// half layout with r/2 a multiple of the vector, or the interleaved layout
+// with r a multiple of it): no shared memory.  A lane's partner chunk is
+// fetched from the partner lane with four register shuffles (half layout),
+// or sits in the lane's own chunk (interleaved).  Same arithmetic as below.
+template <int DT, int LAYOUT, bool CACHE>
+__global__ void __launch_bounds__(kWarps * 32)
+qk_norm_rope_shfl(QkSide A, QkSide B, int nca, int ncb, float eps, const int32_t* pos, int64_t T, int D, int r,
+                  const float* inv_freq, const float2* cache, int64_t cache_len, float mu, int W) {
+    using S = Store<DT>;
+    constexpr int V = S::V;
+    constexpr int64_t ES = sizeof(typename S::T);
+    constexpr int NP = kPassesShfl;
+    pdl_begin();
+    const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t item = (int64_t)blockIdx.x * kWarps + wib;
+    const int per_tok = nca + ncb;
+    const int64_t t = item / per_tok;
+    if (t >= T) return;  // whole warps leave together
+    const int ci = (int)(item - t * per_tok);
+    const bool second = ci >= nca;
+    const QkSide Q = second ? B : A;
+    const int nchunks = D / V;
+    const int R = 32 / W;
+    const int sub = lane / W;
+    const int c = lane - sub * W;
+    const bool has = c < nchunks;
+    const int half = r >> 1;
+    const int G = half / V;  // chunks between pair members (half layout)
+    const int h0 = (second ? ci - nca : ci) * R * NP;
+    const char* xt = Q.x + t * Q.xs * ES;
+    char* yt = Q.y + t * Q.ys * ES;
+
+    Vec16 raw[NP];
+#pragma unroll
+    for (int k = 0; k < NP; ++k) {
+        const int h = h0 + k * R + sub;
+        raw[k] = Vec16{{0u, 0u, 0u, 0u}};
+        if (has && h < Q.H) raw[k] = ld_stream(xt + ((int64_t)h * D + (int64_t)c * V) * ES);
+    }
+    float gv[V];
+    if (has) S::unpack(ld_reuse(Q.g + (int64_t)c * 16), gv);
+    // the angles of the pairs this lane's entries belong to
+    float ca[V], sa[V];
+    const int32_t p = pos[t];
+#pragma unroll
+    for (int e = 0; e < V; ++e) {
+        const int j = c * V + e;
+        ca[e] = 1.0f;
+        sa[e] = 0.0f;
+        if (has && j < r) {
+            const int i = LAYOUT == 0 ? (j < half ? j : j - half) : (j >> 1);
+            if (CACHE && p >= 0 && p < cache_len) {
+                const float2 v = __ldg(cache + (int64_t)p * half + i);
+                ca[e] = v.x;
+                sa[e] = v.y;
+            } else {
+                sincosf(__fmul_rn((float)p, __ldg(inv_freq + i)), &sa[e], &ca[e]);
+            }
+        }
+    }
+    float s[NP];
+#pragma unroll
+    for (int k = 0; k < NP; ++k) {
+        s[k] = 0.0f;
+        if (has && h0 + k * R + sub < Q.H) {
+            float f[V];
+            S::unpack(raw[k], f);
+#pragma unroll
+            for (int e = 0; e < V; ++e) s[k] = __fmaf_rn(f[e], f[e], s[k]);
+        }
+    }
+    for (int m = W >> 1; m >= 1; m >>= 1) {
+#pragma unroll
+        for (int k = 0; k < NP; ++k) s[k] = __fadd_rn(s[k], __shfl_xor_sync(0xFFFFFFFFu, s[k], m));
+    }
+    const bool rot = has && c * V < r;        // this chunk is rotated
+    const bool first = LAYOUT == 0 ? c < G : true;
+    const int src = LAYOUT == 0 ? (c < G ? lane + G : (c < 2 * G ? lane - G : lane)) : lane;
+#pragma unroll
+    for (int k = 0; k < NP; ++k) {
+        if (h0 + k * R >= Q.H) break;  // uniform across the warp
+        const int h = h0 + k * R + sub;
+        const bool live = has && h < Q.H;
+        const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(s[k], (float)D), eps)));
+        float n[V];
+        S::unpack(raw[k], n);
+#pragma unroll
+        for (int e = 0; e < V; ++e) n[e] = __fmul_rn(__fmul_rn(n[e], inv), gv[e]);
+        const Vec16 nv = S::pack(n);  // the stored (rounded) normalised chunk
+        S::unpack(nv, n);
+        float o[V];
+        if (LAYOUT == 0) {
+            Vec16 pv;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) pv.w[q] = __shfl_sync(0xFFFFFFFFu, nv.w[q], src);
+            float m2[V];
+            S::unpack(pv, m2);
+#pragma unroll
+            for (int e = 0; e < V; ++e) {
+                const float a = first ? n[e] : m2[e];
+                const float b = first ? m2[e] : n[e];
+                o[e] = !rot ? n[e]
+                            : first ? __fmul_rn(mu, __fsub_rn(__fmul_rn(a, ca[e]), __fmul_rn(b, sa[e])))
+                                    : __fmul_rn(mu, __fadd_rn(__fmul_rn(a, sa[e]), __fmul_rn(b, ca[e])));
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < V; e += 2) {
+                const float a = n[e], b = n[e + 1];
+                o[e] = rot ? __fmul_rn(mu, __fsub_rn(__fmul_rn(a, ca[e]), __fmul_rn(b, sa[e]))) : a;
+                o[e + 1] = rot ? __fmul_rn(mu, __fadd_rn(__fmul_rn(a, sa[e + 1]), __fmul_rn(b, ca[e + 1]))) : b;
+            }
+        }
+        if (live) st_stream(yt + ((int64_t)h * D + (int64_t)c * V) * ES, S::pack(o));
     }
 }
 
@@ -203,7 +322,8 @@ cudaError_t launch_dt(const QkNormRopeArgs& a, bool vec, cudaStream_t st) {
         sd[k].ys = a.side[k].stride;
         sd[k].H = (int)a.side[k].H;
     }
-    const int rows_per_item = (32 / W) * kPasses;  // head rows one warp handles
+    const bool shfl = vec && a.r > 0 && (a.layout == 0 ? (a.r / 2) % V == 0 : a.r % V == 0);
+    const int rows_per_item = (32 / W) * (shfl ? kPassesShfl : kPasses);  // head rows one warp handles
     const int nca = (int)((a.side[0].H + rows_per_item - 1) / rows_per_item);
     const int ncb = (int)((a.side[1].H + rows_per_item - 1) / rows_per_item);
     const int64_t items = a.T * (nca + ncb);
@@ -214,6 +334,17 @@ cudaError_t launch_dt(const QkNormRopeArgs& a, bool vec, cudaStream_t st) {
 #define GBE_QKN(L, VV, C)                                                                                 \
     return launch(qk_norm_rope_kernel<DT, L, VV, C>, dim3(grid), dim3(kWarps * 32), 0, st, sd[0], sd[1], nca, ncb, \
                   a.eps, a.pos, a.T, Di, ri, a.inv_freq, cache, a.cache_len, a.mu, W)
+#define GBE_QKN_S(L, C)                                                                                        \
+    return launch(qk_norm_rope_shfl<DT, L, C>, dim3(grid), dim3(kWarps * 32), 0, st, sd[0], sd[1], nca, ncb, a.eps, \
+                  a.pos, a.T, Di, ri, a.inv_freq, cache, a.cache_len, a.mu, W)
+    if (shfl) {
+        if (a.layout == 0) {
+            if (cached) GBE_QKN_S(0, true); else GBE_QKN_S(0, false);
+        } else {
+            if (cached) GBE_QKN_S(1, true); else GBE_QKN_S(1, false);
+        }
+    }
+#undef GBE_QKN_S
 #define GBE_QKN_L(L)                                                  \
     if (vec) {                                                        \
         if (cached) GBE_QKN(L, true, true); else GBE_QKN(L, true, false);   \
