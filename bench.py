@@ -361,8 +361,9 @@ def run_isolated(args):
     torch.cuda.set_device(dev)
     gbe.lib()
     data = build_inputs(args.tokens)
-    if args.extra:
-        data.update(build_extra_inputs(args.tokens))
+    if args.extra or (args.keep and args.keep & set(EXTRA)):
+        extra = build_extra_inputs(args.tokens)
+        data.update({op: v for op, v in extra.items() if not args.keep or op in args.keep})
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     res = {}
     for op in list(data):
@@ -709,12 +710,16 @@ def main(argv=None):
                          "LayerNorm)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
+    keep = None
     if args.ops:
         keep = set(args.ops.split(","))
-        unknown = keep - {op for op, _ in STEP}
+        unknown = keep - {op for op, _ in STEP} - set(EXTRA)
         if unknown:
             ap.error(f"unknown ops {sorted(unknown)}")
+        if keep & set(EXTRA) and not args.isolated:
+            ap.error("the ops beyond the step run with --isolated only")
         STEP[:] = [(op, c) for op, c in STEP if op in keep]
+    args.keep = keep
     if args.impl == "reference":
         return run_reference(args)
     if args.isolated:

@@ -137,8 +137,16 @@ qk_norm_rope_shfl(QkSide A, QkSide B, int nca, int ncb, float eps, const int32_t
         for (int k = 0; k < NP; ++k) s[k] = __fadd_rn(s[k], __shfl_xor_sync(0xFFFFFFFFu, s[k], m));
     }
     const bool rot = has && c * V < r;        // this chunk is rotated
-    const bool first = LAYOUT == 0 ? c < G : true;
     const int src = LAYOUT == 0 ? (c < G ? lane + G : (c < 2 * G ? lane - G : lane)) : lane;
+    // Both members of a pair take one formula, out = mu * (own * cos + partner * sg)
+    // with sg = -sin for the first member and +sin for the second: IEEE gives
+    // a - b == a + (-b) and a + b == b + a exactly, so this is the same
+    // arithmetic as mu * (a cos - b sin) and mu * (a sin + b cos).
+#pragma unroll
+    for (int e = 0; e < V; ++e) {
+        const bool first_e = LAYOUT == 0 ? c < G : (e & 1) == 0;
+        sa[e] = first_e ? -sa[e] : sa[e];
+    }
 #pragma unroll
     for (int k = 0; k < NP; ++k) {
         if (h0 + k * R >= Q.H) break;  // uniform across the warp
@@ -151,29 +159,19 @@ qk_norm_rope_shfl(QkSide A, QkSide B, int nca, int ncb, float eps, const int32_t
         for (int e = 0; e < V; ++e) n[e] = __fmul_rn(__fmul_rn(n[e], inv), gv[e]);
         const Vec16 nv = S::pack(n);  // the stored (rounded) normalised chunk
         S::unpack(nv, n);
-        float o[V];
+        float o[V], m2[V];
         if (LAYOUT == 0) {
             Vec16 pv;
 #pragma unroll
             for (int q = 0; q < 4; ++q) pv.w[q] = __shfl_sync(0xFFFFFFFFu, nv.w[q], src);
-            float m2[V];
             S::unpack(pv, m2);
-#pragma unroll
-            for (int e = 0; e < V; ++e) {
-                const float a = first ? n[e] : m2[e];
-                const float b = first ? m2[e] : n[e];
-                o[e] = !rot ? n[e]
-                            : first ? __fmul_rn(mu, __fsub_rn(__fmul_rn(a, ca[e]), __fmul_rn(b, sa[e])))
-                                    : __fmul_rn(mu, __fadd_rn(__fmul_rn(a, sa[e]), __fmul_rn(b, ca[e])));
-            }
         } else {
 #pragma unroll
-            for (int e = 0; e < V; e += 2) {
-                const float a = n[e], b = n[e + 1];
-                o[e] = rot ? __fmul_rn(mu, __fsub_rn(__fmul_rn(a, ca[e]), __fmul_rn(b, sa[e]))) : a;
-                o[e + 1] = rot ? __fmul_rn(mu, __fadd_rn(__fmul_rn(a, sa[e + 1]), __fmul_rn(b, ca[e + 1]))) : b;
-            }
+            for (int e = 0; e < V; ++e) m2[e] = n[e ^ 1];
         }
+#pragma unroll
+        for (int e = 0; e < V; ++e)
+            o[e] = rot ? __fmul_rn(mu, __fadd_rn(__fmul_rn(n[e], ca[e]), __fmul_rn(m2[e], sa[e]))) : n[e];
         if (live) st_stream(yt + ((int64_t)h * D + (int64_t)c * V) * ES, S::pack(o));
     }
 }
