@@ -61,6 +61,7 @@ def lib() -> ctypes.CDLL:
                 "gbe_rope_qk": [vp, vp, i64, i64, vp, vp, i64, i64, vp, i64, i64, i64, vp, vp, i64, f32, i32,
                                 i32, vp],
                 "gbe_rope_cos_sin": [vp, i64, i64, vp, vp],
+                "gbe_rope_multi": [vp, vp, vp, i64, i64, i64, i64, vp, vp, f32, i32, i32, vp],
                 "gbe_qk_norm_rope": [vp, vp, i64, i64, vp, vp, vp, i64, i64, vp, f32, vp, i64, i64, i64, vp, vp,
                                      i64, f32, i32, i32, vp],
                 "gbe_silu_mul": [vp, vp, vp, i64, i32, vp],
@@ -246,6 +247,24 @@ def gbe_qk_norm_rope(q, q_out, gq, k, k_out, gk, eps: float, pos, inv_freq, r: i
     _check("gbe_qk_norm_rope", lib().gbe_qk_norm_rope(qx, qy, qs, hq, qg, kx, ky, ks, hk, kg, eps, _ptr(pos), T, D,
                                                       r, _ptr(inv_freq), _ptr(cos_sin), cache_len, mu, layout,
                                                       _dt(*floats), _stream(stream)))
+
+
+def gbe_rope_multi(x, y, pos, dims, inv_freq, mu: float = 1.0, layout: int = 0, stream=None) -> None:
+    """x, y: [T, H, D]; pos: int32 [T, A]; dims: A even slice widths (a host
+    sequence); inv_freq: float32, the axes' frequencies concatenated."""
+    _dev(x, y, pos, inv_freq)
+    if x.dim() != 3 or y.shape != x.shape:
+        raise ValueError("rope_multi: x is [T, H, D] and y matches it")
+    T, H, D = x.shape
+    dims_arr = (ctypes.c_int64 * max(1, len(dims)))(*[int(v) for v in dims])
+    A = len(dims)
+    if pos.dtype != torch.int32 or pos.numel() != T * A:
+        raise ValueError("rope_multi: pos is int32[T, A]")
+    if inv_freq.dtype != torch.float32 or inv_freq.numel() < sum(int(v) for v in dims) // 2:
+        raise ValueError("rope_multi: inv_freq holds sum(dims)/2 float32 entries")
+    _check("gbe_rope_multi", lib().gbe_rope_multi(_ptr(x), _ptr(y), _ptr(pos), T, H, D, A,
+                                                  ctypes.cast(dims_arr, ctypes.c_void_p), _ptr(inv_freq), mu, layout,
+                                                  _dt(x, y), _stream(stream)))
 
 
 def gbe_rope_cos_sin(cos_sin, inv_freq, r: int, stream=None) -> None:

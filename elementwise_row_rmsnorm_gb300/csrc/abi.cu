@@ -416,6 +416,36 @@ int gbe_qk_norm_rope(const void* q, void* q_out, int64_t q_stride, int64_t Hq, c
     return finish(gbe::launch_qk_norm_rope(a, dtype, vec, as_stream(stream)));
 }
 
+int gbe_rope_multi(const void* x, void* y, const int32_t* pos, int64_t T, int64_t H, int64_t D, int64_t A,
+                   const int64_t* dims, const float* inv_freq, float mu, int layout, int dtype, gbe_stream stream) {
+    const int es = elem_size(dtype);
+    if (!es) return GBE_ERR_DTYPE;
+    if (layout != 0 && layout != 1) return GBE_ERR_LAYOUT;
+    if (T < 0 || H < 0 || D <= 0 || A < 0 || A > gbe::kMaxAxes || T > INT32_MAX) return GBE_ERR_SHAPE;
+    if (A > 0 && dims == nullptr) return GBE_ERR_NULL;
+    if (!std::isfinite(mu)) return GBE_ERR_ROTARY;
+    gbe::MultiAxis ax;
+    ax.A = (int)A;
+    int64_t total = 0;
+    ax.poff[0] = 0;
+    for (int64_t a = 0; a < A; ++a) {
+        if (dims[a] < 0 || (dims[a] & 1) || dims[a] > D) return GBE_ERR_ROTARY;
+        ax.off[a] = (int)total;
+        total += dims[a];
+        ax.poff[a + 1] = ax.poff[a] + (int)(dims[a] / 2);
+    }
+    if (total > D) return GBE_ERR_ROTARY;
+    int64_t hd, n;
+    if (!mul_ok(H, D, &hd) || hd > INT32_MAX / 2 || !mul_ok(T, hd, &n)) return GBE_ERR_SHAPE;
+    uint64_t bx, bp, bf;
+    if (!extent(n, es, &bx) || !extent(T * A, 4, &bp) || !extent(total / 2, 4, &bf)) return GBE_ERR_SHAPE;
+    if (n == 0 || (x == y && total == 0)) return GBE_OK;
+    const Buf bufs[4] = {{y, bx, (uint64_t)es}, {x, bx, (uint64_t)es}, {pos, bp, 4}, {inv_freq, bf, 4}};
+    const int st = check_all(bufs, 1, [](int o, int j) { return o == 0 && j == 1; });
+    if (st != GBE_OK) return st;
+    return finish(gbe::launch_rope_multi(x, y, pos, T, H, D, ax, inv_freq, mu, layout, dtype, as_stream(stream)));
+}
+
 int gbe_rope_cos_sin(float* cos_sin, int64_t cache_len, int64_t r, const float* inv_freq, gbe_stream stream) {
     if (cache_len < 0 || cache_len > INT32_MAX || r < 0 || (r & 1) || r > INT32_MAX) {
         return cache_len < 0 ? GBE_ERR_SHAPE : GBE_ERR_ROTARY;

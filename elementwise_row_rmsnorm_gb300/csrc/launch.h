@@ -39,6 +39,19 @@ cudaError_t launch_rope(const RopeArgs& a, int dtype, bool vec, cudaStream_t st)
 
 cudaError_t launch_rope_cos_sin(float* cos_sin, int64_t len, int64_t r, const float* inv_freq, cudaStream_t st);
 
+// Multi-axis RoPE: A <= 8 slices; slice a starts at entry off[a] and holds
+// poff[a + 1] - poff[a] pairs; poff[A] is the number of rotated pairs.
+constexpr int kMaxAxes = 8;
+struct MultiAxis {
+    int A;
+    int off[kMaxAxes];
+    int poff[kMaxAxes + 1];
+};
+
+cudaError_t launch_rope_multi(const void* x, void* y, const int32_t* pos, int64_t T, int64_t H, int64_t D,
+                              const MultiAxis& ax, const float* inv_freq, float mu, int layout, int dtype,
+                              cudaStream_t st);
+
 // QK-norm (per-head RMSNorm with a [D] gain per operand) followed by RoPE.
 struct QkNormRopeArgs {
     struct Side {

@@ -209,6 +209,55 @@ rope_scalar(Operand A, Operand B, const int32_t* pos, int64_t T, int D, int r, c
     }
 }
 
+// Multi-axis RoPE ("Operations", section 3): head_dim is cut into per-axis
+// slices; slice a (entries off[a] .. off[a] + 2 half[a] - 1) turns at the
+// token's position for axis a, pos[t * A + a], with its own frequencies
+// (inv_freq[poff[a] + j] for its pair j).  A thread owns one pair of one
+// token: it forms that pair's angle once and rotates the pair in every head.
+// Out of place, tail threads copy the entries past the last slice.
+template <int DT, int LAYOUT>
+__global__ void __launch_bounds__(kThreads)
+rope_multi_kernel(const void* x, void* y, const int32_t* pos, int64_t T, int H, int D, MultiAxis ax,
+                  const float* inv_freq, float mu, int copy_tail) {
+    using S = Store<DT>;
+    constexpr int64_t ES = sizeof(typename S::T);
+    pdl_begin();
+    const int npairs = ax.poff[ax.A];
+    const int rot = 2 * npairs;  // rotated entries, all slices
+    const int per_tok = npairs + (copy_tail ? D - rot : 0);
+    const int64_t gt = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int64_t t = gt / per_tok;
+    if (t >= T) return;
+    const int k = (int)(gt - t * per_tok);
+    if (k < npairs) {
+        int a = 0;
+        while (a + 1 < ax.A && k >= ax.poff[a + 1]) ++a;
+        const int j = k - ax.poff[a];
+        const int half = ax.poff[a + 1] - ax.poff[a];
+        float c, sn;
+        sincosf(__fmul_rn((float)pos[t * ax.A + a], __ldg(inv_freq + k)), &sn, &c);
+        const int ia = ax.off[a] + (LAYOUT == 0 ? j : 2 * j);
+        const int ib = ax.off[a] + (LAYOUT == 0 ? j + half : 2 * j + 1);
+        for (int h = 0; h < H; ++h) {
+            const int64_t row = (t * H + h) * (int64_t)D;
+            const float av = S::load1(x, row + ia), bv = S::load1(x, row + ib);
+            float a2, b2;
+            rotate(av, bv, c, sn, mu, a2, b2);
+            S::store1(y, row + ia, a2);
+            S::store1(y, row + ib, b2);
+        }
+    } else {
+        const int jj = rot + (k - npairs);
+        for (int h = 0; h < H; ++h) {
+            const int64_t o = (t * H + h) * (int64_t)D + jj;
+            if (ES == 4)
+                static_cast<uint32_t*>(y)[o] = static_cast<const uint32_t*>(x)[o];
+            else
+                static_cast<uint16_t*>(y)[o] = static_cast<const uint16_t*>(x)[o];
+        }
+    }
+}
+
 // The cos / sin table: entry (p, i) = (cos, sin) of float(p) * omega_i, formed
 // exactly as the RoPE kernels form it.
 __global__ void __launch_bounds__(kThreads)
@@ -276,6 +325,29 @@ cudaError_t launch_dt(const RopeArgs& a, bool vec, cudaStream_t st) {
 
 cudaError_t launch_rope(const RopeArgs& a, int dtype, bool vec, cudaStream_t st) {
     return dtype == kF32 ? launch_dt<kF32>(a, vec, st) : launch_dt<kBF16>(a, vec, st);
+}
+
+cudaError_t launch_rope_multi(const void* x, void* y, const int32_t* pos, int64_t T, int64_t H, int64_t D,
+                              const MultiAxis& ax, const float* inv_freq, float mu, int layout, int dtype,
+                              cudaStream_t st) {
+    const int npairs = ax.poff[ax.A];
+    const int copy_tail = (x != y && 2 * npairs < D) ? 1 : 0;
+    const int64_t per_tok = npairs + (copy_tail ? D - 2 * npairs : 0);
+    if (per_tok == 0 || T == 0 || H == 0) return cudaSuccess;
+    const dim3 grid((unsigned)((T * per_tok + kThreads - 1) / kThreads));
+    const int Hi = (int)H, Di = (int)D;
+    if (dtype == kF32) {
+        if (layout == 0)
+            return launch(rope_multi_kernel<kF32, 0>, grid, dim3(kThreads), 0, st, x, y, pos, T, Hi, Di, ax, inv_freq,
+                          mu, copy_tail);
+        return launch(rope_multi_kernel<kF32, 1>, grid, dim3(kThreads), 0, st, x, y, pos, T, Hi, Di, ax, inv_freq, mu,
+                      copy_tail);
+    }
+    if (layout == 0)
+        return launch(rope_multi_kernel<kBF16, 0>, grid, dim3(kThreads), 0, st, x, y, pos, T, Hi, Di, ax, inv_freq,
+                      mu, copy_tail);
+    return launch(rope_multi_kernel<kBF16, 1>, grid, dim3(kThreads), 0, st, x, y, pos, T, Hi, Di, ax, inv_freq, mu,
+                  copy_tail);
 }
 
 cudaError_t launch_rope_cos_sin(float* cos_sin, int64_t len, int64_t r, const float* inv_freq, cudaStream_t st) {

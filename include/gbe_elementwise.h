@@ -198,6 +198,23 @@ int gbe_qk_norm_rope(const void *q, void *q_out, int64_t q_stride, int64_t Hq, c
 int gbe_rope_cos_sin(float *cos_sin, int64_t cache_len, int64_t r, const float *inv_freq, gbe_stream stream);
 
 /*
+ * gbe_rope_multi -- multi-axis RoPE (video / image DiT positions).
+ *   "Operations", section 3 (Multi-axis RoPE): a token's position is a
+ *   vector of A axis positions; head_dim is cut into consecutive slices of
+ *   dims[0], ..., dims[A-1] entries (each even, summing to at most D), and
+ *   slice a gets its own RoPE at position pos[t * A + a] with its own
+ *   frequencies.  Within a slice the pairing follows `layout` as in
+ *   gbe_rope; entries past the last slice pass through.
+ * x, y     : [T, H, D] contiguous, dtype.  pos : device int32[T * A].
+ * dims     : HOST array of A int64 (read during the call), 0 <= A <= 8.
+ * inv_freq : device f32, the axes' frequencies concatenated: axis a's
+ *            dims[a] / 2 entries follow those of the earlier axes.
+ * mu, layout : as for gbe_rope.  Alias: y == x allowed.
+ */
+int gbe_rope_multi(const void *x, void *y, const int32_t *pos, int64_t T, int64_t H, int64_t D, int64_t A,
+                   const int64_t *dims, const float *inv_freq, float mu, int layout, int dtype, gbe_stream stream);
+
+/*
  * gbe_silu_mul -- the elementwise core of SwiGLU.
  *   "Elementwise kernels in C", section 2.3; "Operations", section 4 (Silu, SwiGlu).
  *   y[i] = gate[i] / (1 + exp(-gate[i])) * up[i]

@@ -70,6 +70,7 @@ class Oracle:
             "orc_add_rmsnorm": [vp, vp, vp, vp, vp, i64, i64, f32, i32],
             "orc_rope": [vp, vp, vp, i64, i64, i64, i64, vp, f32, i32],
             "orc_rope_cos_sin": [vp, i64, i64, vp],
+            "orc_rope_multi": [vp, vp, vp, i64, i64, i64, i64, vp, vp, f32, i32],
             "orc_qk_norm_rope": [vp, vp, vp, vp, i64, i64, i64, f32, i64, vp, f32, i32, i32],
             "orc_silu_mul": [vp, vp, vp, i64],
             "orc_embedding": [vp, vp, vp, i64, i64, i64],
@@ -158,6 +159,22 @@ class Oracle:
         y = x if in_place else np.empty_like(x)
         self._check(self.lib.orc_rope(_ptr(x), _ptr(y), _ptr(pos), T, H, D, r, _ptr(om), mu,
                                       layout), "rope")
+        return y
+
+    def rope_multi(self, x, pos, dims, inv_freq, mu: float, layout: int) -> np.ndarray:
+        """Multi-axis RoPE: x [T, H, D], pos [T, A], dims [A] (even, summing to at
+        most D), inv_freq the concatenated per-axis frequencies."""
+        x = _f32(x)
+        T, H, D = x.shape
+        dims_a = np.ascontiguousarray(dims, dtype=np.int64)
+        A = dims_a.size
+        pos = np.ascontiguousarray(pos, dtype=np.int32).reshape(T, A)
+        om = _f32(inv_freq)
+        if om.size < int(dims_a.sum()) // 2:
+            raise OracleError("rope_multi: inv_freq needs sum(dims)/2 entries")
+        y = np.empty_like(x)
+        self._check(self.lib.orc_rope_multi(_ptr(x), _ptr(y), _ptr(pos), T, H, D, A, _ptr(dims_a), _ptr(om), mu,
+                                            layout), "rope_multi")
         return y
 
     def rope_cos_sin(self, inv_freq, r: int, length: int) -> np.ndarray:

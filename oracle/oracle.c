@@ -10,7 +10,8 @@
  *
  * What it follows.  The two pages define every op in f32:
  *   [Ops]  "Operations" (glia runtime spec): section 1 (Argmax, Add),
- *          section 2 (RmsNorm, LayerNorm), section 3 (Rope, Cos/sin cache, TokenEmbed),
+ *          section 2 (RmsNorm, LayerNorm), section 3 (Rope, Multi-axis RoPE, Cos/sin cache,
+ *          TokenEmbed),
  *          section 4 (Silu), section 5 (QK-norm), section 10 (FusedSkipNorm).  Its CPU reference computes
  *          everything in f32.
  *   [L9.6] "Elementwise kernels in C: RMSNorm, RoPE, SiLU-mul, embedding,
@@ -221,6 +222,53 @@ int orc_rope(const float *x, float *y, const int32_t *pos, int64_t T, int64_t H,
             for (int64_t h = 0; h < H; ++h)
                 for (int64_t j = r; j < D; ++j) y[(t * H + h) * D + j] = x[(t * H + h) * D + j];
         }
+    }
+    return ORC_OK;
+}
+
+/* ---- Multi-axis RoPE -----------------------------------------------------------
+ * [Ops] 3 (Multi-axis RoPE): a token's position is a vector (e.g. [t, h, w]);
+ * head_dim is cut into consecutive slices of dims[a] entries, one per axis
+ * (each even), and slice a -- entries off_a .. off_a + dims[a] - 1 with off_a
+ * the sum of the earlier dims -- gets its own RoPE at position pos[t, a]:
+ * pair j < dims[a] / 2 turns by pos[t, a] * omega_a[j].  The frequencies of
+ * all axes are concatenated in inv_freq (axis a's start after the earlier
+ * axes' dims / 2).  Pairs within a slice follow `layout` as in orc_rope;
+ * entries past the last slice pass through.  Each slice is exactly orc_rope
+ * applied to that slice alone.                                              */
+int orc_rope_multi(const float *x, float *y, const int32_t *pos, int64_t T, int64_t H, int64_t D,
+                   int64_t A, const int64_t *dims, const float *inv_freq, float mu, int layout) {
+    if (T < 0 || H < 0 || D <= 0 || A < 0 || (layout != 0 && layout != 1)) return ORC_ERR_ARG;
+    int64_t total = 0;
+    for (int64_t a = 0; a < A; ++a) {
+        if (dims[a] < 0 || (dims[a] & 1)) return ORC_ERR_ARG;
+        total += dims[a];
+    }
+    if (total > D) return ORC_ERR_ARG;
+    if (y != x)
+        for (int64_t i = 0; i < T * H * D; ++i) y[i] = x[i];
+    int64_t off = 0, foff = 0;
+    for (int64_t a = 0; a < A; ++a) {
+        const int64_t half = dims[a] / 2;
+        for (int64_t t = 0; t < T; ++t) {
+            for (int64_t j = 0; j < half; ++j) {
+                float theta = (float)((double)pos[t * A + a] * (double)inv_freq[foff + j]);
+                float c = (float)cos((double)theta);
+                float s = (float)sin((double)theta);
+                for (int64_t h = 0; h < H; ++h) {
+                    float *v = y + (t * H + h) * D + off;
+                    int64_t ia = layout == 0 ? j : 2 * j;
+                    int64_t ib = layout == 0 ? j + half : 2 * j + 1;
+                    float av = v[ia], bv = v[ib];
+                    float a2 = mu * (av * c - bv * s);
+                    float b2 = mu * (av * s + bv * c);
+                    v[ia] = a2;
+                    v[ib] = b2;
+                }
+            }
+        }
+        off += dims[a];
+        foff += half;
     }
     return ORC_OK;
 }

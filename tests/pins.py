@@ -227,6 +227,35 @@ def pin_rope_brute_force(o):
             assert np.all(np.abs(y[..., idx] - ref[..., idx]) <= 2e-6 * 1.2 * norm + 1e-30)
 
 
+def pin_rope_multi_axis(o):
+    """Multi-axis RoPE ("Operations", section 3): one axis is plain RoPE; each
+    slice equals RoPE of that slice alone at its axis's position (bit exact);
+    an axis's position moves only its slice; float64 brute force."""
+    T, H, D = 4, 3, 40
+    dims = [12, 10, 10]  # 32 rotated entries, 8 pass through
+    x = _rand(T, H, D)
+    pos = RNG.integers(0, 3000, (T, 3)).astype(np.int32)
+    om = RNG.uniform(1e-3, 1.0, 16).astype(np.float32)
+    for layout in (0, 1):
+        y = o.rope_multi(x, pos, dims, om, 1.1, layout)
+        assert _same_bits(y[..., 32:], x[..., 32:]), "entries past the slices pass through"
+        off = foff = 0
+        for a, d in enumerate(dims):
+            sl = np.ascontiguousarray(x[..., off:off + d])
+            ref = o.rope(sl, pos[:, a], om[foff:foff + d // 2], d, 1.1, layout)
+            assert _same_bits(y[..., off:off + d], ref), (layout, a)
+            brute = _brute_rope(sl, pos[:, a], om[foff:foff + d // 2], d, 1.1, layout)
+            assert np.all(np.abs(y[..., off:off + d] - brute) <= 2e-6 * 1.1 * np.abs(sl).max() * 2)
+            off, foff = off + d, foff + d // 2
+        moved = pos.copy()
+        moved[:, 1] += 17
+        y2 = o.rope_multi(x, moved, dims, om, 1.1, layout)
+        assert _same_bits(y2[..., :12], y[..., :12]) and _same_bits(y2[..., 22:], y[..., 22:])
+        assert not np.array_equal(y2[..., 12:22], y[..., 12:22])
+    om1 = RNG.uniform(1e-3, 1.0, D // 2).astype(np.float32)
+    assert _same_bits(o.rope_multi(x, pos[:, :1], [D], om1, 1.0, 0), o.rope(x, pos[:, 0], om1, D, 1.0, 0))
+
+
 def pin_rope_relative_position(o):
     D, r = 16, 16
     om = (10000.0 ** (-2.0 * np.arange(8) / 16)).astype(np.float32)

@@ -29,7 +29,7 @@ def declared_functions():
 
 def test_header_declares_the_ops():
     names = declared_functions()
-    for op in ("gbe_rmsnorm", "gbe_add_rmsnorm", "gbe_rope", "gbe_rope_qk", "gbe_rope_cos_sin", "gbe_silu_mul",
+    for op in ("gbe_rmsnorm", "gbe_add_rmsnorm", "gbe_rope", "gbe_rope_qk", "gbe_rope_cos_sin", "gbe_rope_multi", "gbe_qk_norm_rope", "gbe_silu_mul",
                "gbe_add", "gbe_embedding", "gbe_argmax", "gbe_layernorm", "gbe_status_string", "gbe_version",
                "gbe_last_cuda_error"):
         assert op in names
