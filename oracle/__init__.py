@@ -76,6 +76,7 @@ class Oracle:
             "orc_embedding": [vp, vp, vp, i64, i64, i64],
             "orc_argmax": [vp, i64],
             "orc_argmax_rows": [vp, vp, i64, i64],
+            "orc_sample_rows": [vp, vp, i64, i64, i32, f32, i64, f32, vp, vp, vp],
             "orc_bf16_widen": [vp, vp, i64],
             "orc_bf16_round": [vp, vp, i64],
             "orc_mutant": [],
@@ -226,6 +227,25 @@ class Oracle:
         if st == -3:
             raise OracleError("argmax: empty row")
         self._check(st, "argmax")
+        return out
+
+    METHODS = {"greedy": 0, "temperature": 1, "top_k": 2, "top_p": 3, "min_p": 4}
+
+    def sample(self, x, method: str, u, temperature: float = 1.0, top_k: int = 1, top_p: float = 1.0,
+               min_p: float = 0.0) -> np.ndarray:
+        """One draw per row of x [rows, n] by the inverse CDF at u[row]."""
+        x = _f32(x)
+        if x.ndim == 1:
+            x = x.reshape(1, -1)
+        rows, n = x.shape
+        u = np.ascontiguousarray(np.broadcast_to(np.asarray(u, np.float32), (rows,)), dtype=np.float32)
+        out = np.empty(rows, dtype=np.int32)
+        idx = np.empty(n, dtype=np.int64)
+        buf = np.empty(n, dtype=np.float32)
+        m = self.METHODS[method]
+        pp = top_p if method == "top_p" else min_p
+        self._check(self.lib.orc_sample_rows(_ptr(x), _ptr(out), rows, n, m, temperature, top_k, pp, _ptr(u),
+                                             _ptr(idx), _ptr(buf)), "sample")
         return out
 
     def argmax_one(self, x) -> int:

@@ -12,7 +12,8 @@
  *   [Ops]  "Operations" (glia runtime spec): section 1 (Argmax, Add),
  *          section 2 (RmsNorm, LayerNorm), section 3 (Rope, Multi-axis RoPE, Cos/sin cache,
  *          TokenEmbed),
- *          section 4 (Silu), section 5 (QK-norm), section 10 (FusedSkipNorm).  Its CPU reference computes
+ *          section 4 (Silu), section 5 (QK-norm), section 8 (Sample),
+ *          section 10 (FusedSkipNorm).  Its CPU reference computes
  *          everything in f32.
  *   [L9.6] "Elementwise kernels in C: RMSNorm, RoPE, SiLU-mul, embedding,
  *          add, argmax": section 2 (principles and the symbol table),
@@ -28,12 +29,15 @@
  * k-th wrong variant of the pitfalls table of [L9.6] section 5 (s01..s15);
  * k = 16 is the pitfall [Ops] section 5 warns about for QK-norm (the norm
  * taken over num_heads * head_dim instead of per head); k = 17 plants a
- * LayerNorm whose variance is not centred on the mean ([Ops] section 2).
+ * LayerNorm whose variance is not centred on the mean ([Ops] section 2);
+ * k = 18 drops the rule that top-p always keeps its first entry ([Ops]
+ * section 8).
  * The tests build those variants on the CPU to show that their pins reject
  * each one.  A normal build (ORACLE_MUTANT undefined) contains none of them.
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #ifndef ORACLE_MUTANT
@@ -393,6 +397,113 @@ int32_t orc_argmax(const float *x, int64_t n) {
     }
     if (MUT(14) && best < 0) return 0; /* s14: 0 for an empty or all-NaN row */
     return best;
+}
+
+/* ---- Sampling ------------------------------------------------------------------
+ * [Ops] 8 (Sample): Greedy is argmax; Temperature(t) draws from
+ * softmax(logits / t); TopK(k, t) from the softmax of the k largest logits
+ * (in descending order); TopP(p, t) from the sorted softmax cut to the
+ * prefix whose running sum stays <= p (the first entry always kept),
+ * renormalised; MinP(p, t) from the softmax cut to entries >= p * its
+ * maximum, renormalised.  Readings: sample_categorical is the inverse CDF
+ * -- with one uniform u in [0, 1) per row, supplied by the caller, the first
+ * entry (in the distribution's order) whose running sum exceeds u times the
+ * sum of all its entries; if rounding leaves none, the last entry with
+ * positive weight.  NaN logits take no part (as in argmax); equal logits sort
+ * by ascending index; a row with no number gives -1.  Every step is f32 in
+ * the order written: z = x / t, m = max z, e = expf(z - m), sums in the
+ * distribution's order, probs = e / sum.                                     */
+
+enum { ORC_GREEDY = 0, ORC_TEMPERATURE = 1, ORC_TOP_K = 2, ORC_TOP_P = 3, ORC_MIN_P = 4 };
+
+/* inverse CDF over q[0 .. L) with uniform u */
+static int64_t orc_categorical(const float *q, int64_t L, float u) {
+    float c = 0.0f;
+    int64_t last = -1;
+    for (int64_t j = 0; j < L; ++j) c = c + q[j];
+    float target = u * c;
+    c = 0.0f;
+    for (int64_t j = 0; j < L; ++j) {
+        c = c + q[j];
+        if (q[j] > 0.0f) {
+            last = j;
+            if (c > target) return j;
+        }
+    }
+    return last;
+}
+
+static const float *orc_sort_base;
+static int orc_desc_cmp(const void *pa, const void *pb) {
+    int64_t a = *(const int64_t *)pa, b = *(const int64_t *)pb;
+    float va = orc_sort_base[a], vb = orc_sort_base[b];
+    if (va > vb) return -1;
+    if (va < vb) return 1;
+    return a < b ? -1 : (a > b ? 1 : 0);
+}
+
+/* one row; idx and buf are scratch of n entries each */
+static int32_t orc_sample_one(const float *x, int64_t n, int method, float t, int64_t k, float p, float u,
+                              int64_t *idx, float *buf) {
+    if (method == ORC_GREEDY) return orc_argmax(x, n);
+    int64_t nv = 0;
+    for (int64_t i = 0; i < n; ++i)
+        if (x[i] == x[i]) idx[nv++] = i;
+    if (nv == 0) return -1;
+    if (method == ORC_TOP_K || method == ORC_TOP_P) {
+        orc_sort_base = x;
+        qsort(idx, (size_t)nv, sizeof(int64_t), orc_desc_cmp);
+    }
+    int64_t L = nv;
+    if (method == ORC_TOP_K && k < L) L = k;
+    /* softmax over the (ordered) candidates */
+    float m = -INFINITY;
+    for (int64_t j = 0; j < L; ++j) {
+        float z = x[idx[j]] / t;
+        buf[j] = z;
+        if (z > m) m = z;
+    }
+    float S = 0.0f;
+    for (int64_t j = 0; j < L; ++j) {
+        buf[j] = expf(buf[j] - m);
+        S = S + buf[j];
+    }
+    for (int64_t j = 0; j < L; ++j) buf[j] = buf[j] / S;
+    if (method == ORC_TOP_P) {
+        float c = 0.0f;
+        int64_t keep = 0;
+        for (int64_t j = 0; j < L; ++j) {
+            c = c + buf[j];
+            if (c <= p) keep = j + 1;
+            else break;
+        }
+        if (keep < 1 && !MUT(18)) keep = 1; /* s18: the first entry not forced into the nucleus */
+        for (int64_t j = keep; j < L; ++j) buf[j] = 0.0f;
+    } else if (method == ORC_MIN_P) {
+        float mx = 0.0f;
+        for (int64_t j = 0; j < L; ++j)
+            if (buf[j] > mx) mx = buf[j];
+        float thr = p * mx;
+        for (int64_t j = 0; j < L; ++j)
+            if (!(buf[j] >= thr)) buf[j] = 0.0f;
+    }
+    if (method == ORC_TOP_P || method == ORC_MIN_P) {
+        float S2 = 0.0f;
+        for (int64_t j = 0; j < L; ++j) S2 = S2 + buf[j];
+        if (S2 > 0.0f)
+            for (int64_t j = 0; j < L; ++j) buf[j] = buf[j] / S2;
+    }
+    int64_t j = orc_categorical(buf, L, u);
+    return j < 0 ? -1 : (int32_t)idx[j];
+}
+
+int orc_sample_rows(const float *x, int32_t *out, int64_t rows, int64_t n, int method, float t, int64_t k,
+                    float p, const float *u, int64_t *idx, float *buf) {
+    if (rows < 0 || n <= 0 || method < 0 || method > 4) return ORC_ERR_ARG;
+    if (method != ORC_GREEDY && !(t > 0.0f)) return ORC_ERR_ARG;
+    for (int64_t r = 0; r < rows; ++r)
+        out[r] = orc_sample_one(x + r * n, n, method, t, k, p, u ? u[r] : 0.0f, idx, buf);
+    return ORC_OK;
 }
 
 int orc_argmax_rows(const float *x, int32_t *out, int64_t rows, int64_t n) {

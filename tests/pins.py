@@ -363,6 +363,85 @@ def pin_silu_library(o):
     assert err.max() <= 1e-6, err.max()
 
 
+# ---- Sampling ("Operations", section 8) --------------------------------------------
+
+def sampling_probs_f64(x, method, t=1.0, k=1, p=1.0):
+    """The distribution each method draws from, in float64, written from the
+    definition independently of the oracle: (probabilities per index, the
+    order the draw walks, the smallest margin of any keep/cut decision)."""
+    x = np.asarray(x, np.float64)
+    valid = ~np.isnan(x)
+    order_sorted = sorted(np.nonzero(valid)[0], key=lambda i: (-x[i], i))
+    probs = np.zeros_like(x)
+    margin = np.inf
+    if method == "temperature" or method == "min_p":
+        z = torch.from_numpy(np.where(valid, x / t, -np.inf))
+        sm = torch.softmax(z, 0).numpy()
+        if method == "min_p":
+            thr = p * sm.max()
+            keep = sm >= thr
+            margin = np.min(np.abs(sm[valid] - thr)) / sm.max()
+            sm = np.where(keep, sm, 0.0)
+            sm = sm / sm.sum()
+        probs = sm
+        order = np.arange(len(x))
+    else:
+        cand = order_sorted[:k] if method == "top_k" else order_sorted
+        z = torch.from_numpy(x[cand] / t)
+        sm = torch.softmax(z, 0).numpy()
+        if method == "top_p":
+            c = np.cumsum(sm)
+            keep = c <= p
+            keep[0] = True
+            margin = np.min(np.abs(c - p))
+            sm = np.where(keep, sm, 0.0)
+            sm = sm / sm.sum()
+        probs[cand] = sm
+        order = np.array(order_sorted)
+    return probs, order, margin
+
+
+def _grid_counts(o, x, method, n_grid, **kw):
+    u = ((np.arange(n_grid) + 0.5) / n_grid).astype(np.float32)
+    rows = np.repeat(np.asarray(x, np.float32).reshape(1, -1), n_grid, axis=0)
+    return np.bincount(o.sample(rows, method, u, **kw), minlength=rows.shape[1])
+
+
+def pin_sampling_draws_in_proportion(o):
+    """Inverse-CDF property: over a fine grid of u, each index is drawn
+    n_grid * p_i times (+-2), p_i from the float64 definition."""
+    for trial in range(6):
+        x = _rand(60, scale=2.0)
+        x[[5, 17]] = x[3]  # exact ties
+        x[11] = np.nan
+        for method, kw in (("temperature", dict(temperature=0.8)), ("top_k", dict(temperature=1.3, top_k=7)),
+                           ("top_p", dict(temperature=0.9, top_p=0.6)), ("min_p", dict(temperature=1.0, min_p=0.2))):
+            pr, order, margin = sampling_probs_f64(x, method, t=kw["temperature"], k=kw.get("top_k", 1),
+                                                   p=kw.get("top_p", kw.get("min_p", 1.0)))
+            if margin < 1e-4:
+                continue  # a keep/cut decision within rounding of its threshold
+            counts = _grid_counts(o, x, method, 4000, **kw)
+            assert np.all(np.abs(counts - 4000 * pr) <= 2.5), (trial, method, np.abs(counts - 4000 * pr).max())
+            assert counts[11] == 0, "NaN is never drawn"
+
+
+def pin_sampling_limits(o):
+    """Greedy is argmax; top-k with k = 1, and top-p with a tiny p (only the
+    first entry is ever kept), give the argmax too; a row of NaN gives -1."""
+    x = _rand(8, 300, scale=3.0)
+    x[2, 7] = x[2, 250] = 50.0  # tie at the maximum: the lower index
+    x[3] = np.nan
+    u = RNG.random(8).astype(np.float32)
+    want = o.argmax(x)
+    assert np.array_equal(o.sample(x, "greedy", u), want)
+    assert np.array_equal(o.sample(x, "top_k", u, temperature=0.7, top_k=1), want)
+    assert np.array_equal(o.sample(x, "top_p", u, temperature=1.0, top_p=1e-9), want)
+    assert o.sample(x[3:4], "temperature", [0.5])[0] == -1
+    # min_p = 0 keeps everything: the same draws as temperature sampling
+    assert np.array_equal(o.sample(x, "min_p", u, temperature=0.9, min_p=0.0),
+                          o.sample(x, "temperature", u, temperature=0.9))
+
+
 # ---- Embedding / add / argmax / bf16 ---------------------------------------------
 
 def pin_embedding_gathers_rows(o):
@@ -455,4 +534,5 @@ KILLS = {
     15: "rmsnorm_rows_are_independent_and_in_place",
     16: "qk_norm_rope_per_head",
     17: "layernorm",
+    18: "sampling_limits",
 }
