@@ -104,6 +104,8 @@ def op_bytes(op: str, arrays: dict, params: dict) -> tuple[int, int]:
         return 2 * nb(arrays["x"]) + nb(arrays["w"]), params["rows"]
     if op == "argmax":
         return nb(arrays["x"]) + 4 * params["rows"], params["rows"]
+    if op.startswith("sample_"):
+        return nb(arrays["x"]) + nb(arrays["u"]) + 4 * params["rows"], params["rows"]
     raise KeyError(op)
 
 
@@ -188,14 +190,20 @@ def combine(op: str, parts):
     return parts[0]
 
 
-EXTRA = ("qk_norm_rope", "rope_qk_half_cached", "layernorm")
+EXTRA = ("qk_norm_rope", "rope_qk_half_cached", "layernorm", "sample_temperature", "sample_top_k", "sample_top_p",
+         "sample_min_p")
+SAMPLING = {"sample_temperature": ("temperature", dict(temperature=0.7)),
+            "sample_top_k": ("top_k", dict(temperature=0.7, top_k=50)),
+            "sample_top_p": ("top_p", dict(temperature=0.7, p=0.9)),
+            "sample_min_p": ("min_p", dict(temperature=0.7, p=0.05))}
 
 
 def build_extra_inputs(tokens: int = 8192):
     """Inputs of the ops beyond the step, at the same prefill shapes: QK-norm
     then RoPE on q [T, 32, 128] and k [T, 8, 128] (gains U(0.5, 1.5)); RoPE of
     q and k driven by a cos/sin table of 8192 positions; LayerNorm of
-    [T, 4096] with gain and bias."""
+    [T, 4096] with gain and bias; one draw per row of the logits
+    [T, 128256] by each sampling method at a uniform u per row."""
     import synth
     from synth import workloads as W
     cases = W.cases(W.PREFILL)
@@ -207,10 +215,14 @@ def build_extra_inputs(tokens: int = 8192):
     qk = {"q": aq["x"], "k": ak["x"], "pos": aq["pos"], "inv_freq": aq["inv_freq"]}
     ax, px = cases["rmsnorm"](rows=rows)
     lb = synth.normal_bf16(seed, "layernorm.b", (ax["x"].shape[1],), 0.0, 0.2)
+    al, pl = cases["argmax"](rows=rows)
+    u = synth.units(seed, "sample.u", al["x"].shape[0]).astype(np.float32)
+    sampling = {op: ({"x": al["x"], "u": u}, dict(pl, method=m, kw=kw)) for op, (m, kw) in SAMPLING.items()}
     return {
         "qk_norm_rope": (dict(qk, gq=gq, gk=gk), dict(pq, eps=1e-6)),
         "rope_qk_half_cached": (dict(qk), dict(pq, cache_len=8192)),
         "layernorm": ({"x": ax["x"], "g": ax["w"], "b": lb}, px),
+        **sampling,
     }
 
 
@@ -371,7 +383,7 @@ def run_isolated(args):
         nb, rows = op_bytes(op, arrays, params)
         sets = int(min(12, max(2, -(-4 * l2 // nb) + 1)))
         base = {k: to_device(torch, dev, v) for k, v in arrays.items()}
-        shared = ("table", "w", "g", "gq", "gk", "inv_freq", "pos", "ids", "cos_sin")
+        shared = ("table", "w", "g", "gq", "gk", "inv_freq", "pos", "ids", "cos_sin", "u")
         if op == "rope_qk_half_cached":
             base["cos_sin"] = gbe.rope_cos_sin(base["inv_freq"], params["r"], params["cache_len"])
         rings = []
@@ -421,7 +433,7 @@ def make_outputs(torch, dev, op, b):
         return (torch.empty_like(b["x"]), torch.empty_like(b["x"]))
     if op.startswith("rope_qk") or op == "qk_norm_rope":
         return (torch.empty_like(b["q"]), torch.empty_like(b["k"]))
-    if op == "argmax":
+    if op == "argmax" or op.startswith("sample_"):
         return torch.empty((b["x"].shape[0],), dtype=torch.int32, device=dev)
     return torch.empty_like(b["x"] if "x" in b else (b["gate"] if "gate" in b else b["a"]))
 
@@ -449,6 +461,8 @@ def run_op(gbe, op, p, b, o):
         gbe.gbe_layernorm(b["x"], b["g"], b["b"], o, p["eps"])
     elif op == "argmax":
         gbe.gbe_argmax(b["x"], o)
+    elif op.startswith("sample_"):
+        gbe.gbe_sample(b["x"], b["u"], o, p["method"], **p["kw"])
 
 
 def run_e2e(args, gbe, torch, dev, data, bufs, out, call, nbytes, step_bytes):

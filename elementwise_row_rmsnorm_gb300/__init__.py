@@ -9,8 +9,8 @@ kernel each, in ``lib/libgbe_elementwise.so`` (declared in
 """
 from .binding import (GBE_BF16, GBE_F32, GbeError, LibraryMissing, add, add_rmsnorm, argmax, embedding,
                       gbe_add, gbe_add_rmsnorm, gbe_argmax, gbe_embedding, gbe_layernorm, gbe_qk_norm_rope, gbe_rmsnorm, gbe_rope,
-                      gbe_rope_cos_sin, gbe_rope_multi, gbe_rope_qk, gbe_silu_mul, layernorm, lib, rmsnorm, rope, rope_cos_sin, silu_mul,
-                      status_string)
+                      gbe_rope_cos_sin, gbe_rope_multi, gbe_rope_qk, gbe_sample, gbe_silu_mul, layernorm, lib, rmsnorm, rope,
+                      rope_cos_sin, sample, silu_mul, status_string)
 
 
 def build(force: bool = False) -> str:
@@ -22,6 +22,6 @@ def build(force: bool = False) -> str:
 __all__ = [
     "GBE_BF16", "GBE_F32", "GbeError", "LibraryMissing", "add", "add_rmsnorm", "argmax", "build",
     "embedding", "gbe_add", "gbe_add_rmsnorm", "gbe_argmax", "gbe_embedding", "gbe_layernorm", "gbe_qk_norm_rope", "gbe_rmsnorm", "gbe_rope",
-    "gbe_rope_cos_sin", "gbe_rope_multi", "gbe_rope_qk", "gbe_silu_mul", "layernorm", "lib", "rmsnorm", "rope", "rope_cos_sin", "silu_mul",
-    "status_string",
+    "gbe_rope_cos_sin", "gbe_rope_multi", "gbe_rope_qk", "gbe_sample", "gbe_silu_mul", "layernorm", "lib", "rmsnorm", "rope",
+    "rope_cos_sin", "sample", "silu_mul", "status_string",
 ]

@@ -68,6 +68,7 @@ def lib() -> ctypes.CDLL:
                 "gbe_add": [vp, vp, vp, i64, i32, vp],
                 "gbe_embedding": [vp, vp, vp, i64, i64, i64, vp, i32, vp],
                 "gbe_argmax": [vp, vp, i64, i64, i32, vp],
+                "gbe_sample": [vp, vp, vp, i64, i64, i32, f32, i64, f32, i32, vp],
                 "gbe_version": [],
                 "gbe_last_cuda_error": [],
                 "gbe_status_string": [i32],
@@ -315,6 +316,29 @@ def gbe_argmax(x, out, stream=None) -> None:
     _check("gbe_argmax", lib().gbe_argmax(_ptr(x), _ptr(out), rows, n, _dt(x), _stream(stream)))
 
 
+SAMPLE_METHODS = {"greedy": 0, "temperature": 1, "top_k": 2, "top_p": 3, "min_p": 4}
+
+
+def gbe_sample(x, u, out, method: str, temperature: float = 1.0, top_k: int = 1, p: float = 1.0,
+               stream=None) -> None:
+    """One draw per row of x [..., n] at the uniforms u (f32, one per row);
+    `p` is top-p's mass or min-p's ratio.  u may be None for greedy."""
+    if method not in SAMPLE_METHODS:
+        raise ValueError(f"sample: method is one of {sorted(SAMPLE_METHODS)}")
+    _dev(x, out)
+    n = x.shape[-1]
+    rows = math.prod(x.shape[:-1])
+    if out.dtype != torch.int32 or out.numel() != rows:
+        raise ValueError("sample: out is int32 with one entry per row")
+    if u is not None:
+        _dev(u)
+        if u.dtype != torch.float32 or u.numel() != rows:
+            raise ValueError("sample: u is float32 with one entry per row")
+    _check("gbe_sample", lib().gbe_sample(_ptr(x), None if u is None else _ptr(u), _ptr(out), rows, n,
+                                          SAMPLE_METHODS[method], temperature, top_k, p, _dt(x),
+                                          _stream(stream)))
+
+
 # ---- conveniences that allocate the outputs -------------------------------------------
 
 def rmsnorm(x, w, eps: float = 1e-5, out=None, stream=None):
@@ -368,4 +392,10 @@ def embedding(table, ids, bad_id_count=None, stream=None):
 def argmax(x, stream=None):
     out = torch.empty(x.shape[:-1], dtype=torch.int32, device=x.device)
     gbe_argmax(x, out, stream)
+    return out
+
+
+def sample(x, u, method: str, temperature: float = 1.0, top_k: int = 1, p: float = 1.0, stream=None):
+    out = torch.empty(x.shape[:-1], dtype=torch.int32, device=x.device)
+    gbe_sample(x, u, out, method, temperature, top_k, p, stream)
     return out

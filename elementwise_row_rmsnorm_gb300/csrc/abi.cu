@@ -188,6 +188,7 @@ const char* gbe_status_string(int status) {
         case GBE_ERR_ALIGN: return "a pointer is not aligned to its element size";
         case GBE_ERR_POINTER: return "a pointer is not memory of the current device, or its extent exceeds its allocation";
         case GBE_ERR_CUDA: return "the CUDA runtime reported an error at launch";
+        case GBE_ERR_SAMPLING: return "a sampling method or parameter is out of range";
         default: return "unknown status";
     }
 }
@@ -520,6 +521,32 @@ int gbe_argmax(const void* x, int32_t* out, int64_t rows, int64_t n, int dtype, 
     if (st != GBE_OK) return st;
     const bool vec = aligned16(x) && (n * es) % 16 == 0;
     return finish(gbe::launch_argmax(x, out, rows, n, dtype, vec, as_stream(stream)));
+}
+
+int gbe_sample(const void* x, const float* u, int32_t* out, int64_t rows, int64_t n, int method,
+               float temperature, int64_t top_k, float p, int dtype, gbe_stream stream) {
+    const int es = elem_size(dtype);
+    if (!es) return GBE_ERR_DTYPE;
+    if (method < GBE_SAMPLE_GREEDY || method > GBE_SAMPLE_MIN_P) return GBE_ERR_SAMPLING;
+    const bool greedy = method == GBE_SAMPLE_GREEDY;
+    if (!greedy && !(temperature > 0.0f)) return GBE_ERR_SAMPLING;
+    if (method == GBE_SAMPLE_TOP_K && top_k < 1) return GBE_ERR_SAMPLING;
+    if ((method == GBE_SAMPLE_TOP_P || method == GBE_SAMPLE_MIN_P) && !(p >= 0.0f && p <= 1.0f))
+        return GBE_ERR_SAMPLING;
+    if (rows < 0 || n < 0 || n > (1LL << 23) || rows > (1LL << 28)) return GBE_ERR_SHAPE;
+    if (rows == 0) return GBE_OK;
+    if (n == 0) return GBE_ERR_EMPTY;
+    int64_t nx;
+    uint64_t bx, bo, bu;
+    if (!mul_ok(rows, n, &nx) || !extent(nx, es, &bx) || !extent(rows, 4, &bo) || !extent(rows, 4, &bu))
+        return GBE_ERR_SHAPE;
+    if (greedy) bu = 0;  // u is not read
+    const Buf bufs[3] = {{out, bo, 4}, {x, bx, (uint64_t)es}, {u, bu, 4}};
+    const int st = check_all(bufs, 1, [](int, int) { return false; });
+    if (st != GBE_OK) return st;
+    const bool vec = aligned16(x) && (n * es) % 16 == 0;
+    return finish(gbe::launch_sample(x, out, rows, n, method, temperature, top_k, p, u, dtype, vec,
+                                     as_stream(stream)));
 }
 
 }  // extern "C"

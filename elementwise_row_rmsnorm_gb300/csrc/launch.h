@@ -84,4 +84,7 @@ cudaError_t launch_embedding(const void* table, const int32_t* ids, void* out, i
 cudaError_t launch_argmax(const void* x, int32_t* out, int64_t rows, int64_t n, int dtype, bool vec,
                           cudaStream_t st);
 
+cudaError_t launch_sample(const void* x, int32_t* out, int64_t rows, int64_t n, int method, float t, int64_t k,
+                          float p, const float* u, int dtype, bool vec, cudaStream_t st);
+
 }  // namespace gbe

@@ -66,7 +66,8 @@ typedef enum gbe_status {
     GBE_ERR_ALIAS = 8,   /* an output overlaps a buffer other than its permitted exact alias */
     GBE_ERR_ALIGN = 9,   /* a pointer is not aligned to its element size */
     GBE_ERR_POINTER = 10, /* not device memory of the current device, or the extent exceeds its allocation */
-    GBE_ERR_CUDA = 11    /* the CUDA runtime reported an error at launch */
+    GBE_ERR_CUDA = 11,   /* the CUDA runtime reported an error at launch */
+    GBE_ERR_SAMPLING = 12 /* a sampling method or parameter is out of range */
 } gbe_status;
 
 /* The stream type; the same type as cudaStream_t, so either may be passed. */
@@ -258,6 +259,49 @@ int gbe_embedding(const void *table, const int32_t *ids, void *out, int64_t n, i
  * (rows of length 0 are rejected with GBE_ERR_EMPTY) and n < 2^31.
  */
 int gbe_argmax(const void *x, int32_t *out, int64_t rows, int64_t n, int dtype, gbe_stream stream);
+
+/* Sampling methods of gbe_sample. */
+typedef enum gbe_sample_method {
+    GBE_SAMPLE_GREEDY = 0,
+    GBE_SAMPLE_TEMPERATURE = 1,
+    GBE_SAMPLE_TOP_K = 2,
+    GBE_SAMPLE_TOP_P = 3,
+    GBE_SAMPLE_MIN_P = 4
+} gbe_sample_method;
+
+/*
+ * gbe_sample -- one draw per row of logits.
+ *   "Operations", section 8 (Sample: Greedy, Temperature, TopK, TopP, MinP
+ *   and the categorical draw behind them).
+ *   GREEDY      : gbe_argmax (u, temperature, top_k and p unused).
+ *   TEMPERATURE : draw from softmax(x / t).
+ *   TOP_K       : draw from the softmax of the top_k largest logits.
+ *   TOP_P       : draw from the descending softmax cut to the longest prefix
+ *                 whose running sum stays <= p (the first entry always kept).
+ *   MIN_P       : draw from the softmax cut to the entries >= p times its
+ *                 largest entry.
+ *   The draw is the inverse CDF at u[r]: the first entry, in the
+ *   distribution's order (index order for TEMPERATURE and MIN_P, descending
+ *   logit with equal logits by ascending index for TOP_K and TOP_P), whose
+ *   running sum exceeds u[r] times the sum of the kept entries.
+ *   Arithmetic: e = expf(x / t - max(x) / t) in f32, each e held as the
+ *   integer rn(e * 2^40); sums and cuts are exact integer arithmetic on those
+ *   weights, so the result is deterministic and independent of the batch.
+ *   It equals an f32 evaluation of the definition except where u[r] falls
+ *   within rounding of a boundary between two entries (or an entry sits
+ *   within rounding of a cut), where either neighbour is a valid draw.
+ *   NaN logits take no part; a row with no number, or whose largest x / t is
+ *   not finite (+inf in the row, or an overflow of x / t), gives -1.
+ * x : [rows, n] row-major, dtype; u : f32[rows], uniforms in [0, 1) (values
+ * outside are clamped: u <= 0 takes the first kept entry, u >= 1 the last);
+ * out : int32[rows], which overlaps nothing else.  n in [1, 2^23]; rows of
+ * length 0 are GBE_ERR_EMPTY.  temperature > 0 (+inf allowed: every logit
+ * equal), top_k >= 1 (larger than n keeps all), p in [0, 1]; otherwise
+ * GBE_ERR_SAMPLING.  u is read only by methods other than GREEDY, and may be
+ * NULL for GREEDY.
+ */
+int gbe_sample(const void *x, const float *u, int32_t *out, int64_t rows, int64_t n, int method,
+               float temperature, int64_t top_k, float p, int dtype, gbe_stream stream);
 
 #ifdef __cplusplus
 }

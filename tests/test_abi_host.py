@@ -30,7 +30,7 @@ def declared_functions():
 def test_header_declares_the_ops():
     names = declared_functions()
     for op in ("gbe_rmsnorm", "gbe_add_rmsnorm", "gbe_rope", "gbe_rope_qk", "gbe_rope_cos_sin", "gbe_rope_multi", "gbe_qk_norm_rope", "gbe_silu_mul",
-               "gbe_add", "gbe_embedding", "gbe_argmax", "gbe_layernorm", "gbe_status_string", "gbe_version",
+               "gbe_add", "gbe_embedding", "gbe_argmax", "gbe_sample", "gbe_layernorm", "gbe_status_string", "gbe_version",
                "gbe_last_cuda_error"):
         assert op in names
 
@@ -48,7 +48,7 @@ def test_library_exports_every_declared_function(L):
 def test_status_strings_and_version(L):
     import elementwise_row_rmsnorm_gb300 as gbe
     assert L.gbe_version() == 10000
-    for st in range(12):
+    for st in range(13):
         assert gbe.status_string(st) and gbe.status_string(st) != "unknown status"
     assert gbe.status_string(99) == "unknown status"
 
@@ -127,6 +127,20 @@ def test_qk_norm_rope_rejects_bad_arguments(L):
     assert call(r=130) == 6 and call(r=7) == 6
     assert call(qs=1000) == 2
     assert call(T=0) == 0 and call(hq=0, hk=0) == 0
+
+
+def test_sample_rejects_bad_arguments(L):
+    def call(rows=4, n=100, method=1, t=1.0, k=5, p=0.5, dtype=1):
+        return L.gbe_sample(NULL, NULL, NULL, rows, n, method, t, k, p, dtype, S)
+    assert call(method=5) == 12 and call(method=-1) == 12
+    assert call(t=0.0) == 12 and call(t=-1.0) == 12 and call(t=float("nan")) == 12
+    assert call(method=2, k=0) == 12 and call(method=2, k=-3) == 12
+    for m in (3, 4):
+        assert call(method=m, p=-0.1) == 12 and call(method=m, p=1.5) == 12 and call(method=m, p=float("nan")) == 12
+    assert call(dtype=4) == 3
+    assert call(n=(1 << 23) + 1) == 2 and call(rows=-1) == 2 and call(n=-1) == 2
+    assert call(n=0) == 7
+    assert call(rows=0) == 0 and call(rows=0, n=0) == 0
 
 
 def test_rejects_size_overflow(L):

@@ -1,0 +1,252 @@
+"""Sampling on the GPU against the oracle, through the C ABI.
+
+The oracle evaluates the definition in f32 (running sums in the
+distribution's order); the kernel sums exact fixed-point weights.  Both are
+the inverse CDF at the same u, so they pick the same entry except where u
+lies within rounding of a boundary between two entries, or an entry sits
+within rounding of a top-p / min-p cut.  The bar:
+  * every row where the two differ is such a case: u lies within DELTA of
+    the boundary between them in the float64 distribution (written from the
+    definition in pins.sampling_probs_f64, independently of both), or the
+    row has a keep/cut decision within DELTA of its threshold, and then the
+    kernel's pick is still an entry the float64 distribution keeps;
+  * such rows are few (MAX_MISS of the rows);
+  * on flat rows of 152k entries, where the oracle's f32 running sums drift
+    across boundaries, every draw is held to the float64 distribution within
+    1e-7 (the kernel's sums are exact);
+  * exact limits: top_k = 1 and top_p = 0 give the argmax; min_p = 0 gives
+    the temperature draw; a row with no number, or with +inf, gives -1.
+DELTA = 1e-5 of the kept mass covers the f32 running sums of rows of up to
+152k entries in the oracle and the f32 rounding of x / t in both."""
+import numpy as np
+import pytest
+import torch
+
+import elementwise_row_rmsnorm_gb300 as gbe
+import oracle
+from gpu_util import to_dev, widen
+from pins import sampling_probs_f64
+from synth import normal, to_bf16, units
+from synth import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+DELTA = 1e-5
+MAX_MISS = 0.05
+
+METHODS = [("temperature", dict(temperature=0.8)), ("top_k", dict(temperature=1.3, top_k=50)),
+           ("top_p", dict(temperature=0.9, p=0.9)), ("min_p", dict(temperature=1.0, p=0.05))]
+
+
+def _oracle(x32, u, method, kw):
+    okw = dict(temperature=kw.get("temperature", 1.0), top_k=kw.get("top_k", 1))
+    if method == "top_p":
+        okw["top_p"] = kw["p"]
+    if method == "min_p":
+        okw["min_p"] = kw["p"]
+    return oracle.get().sample(x32, method, u, **okw)
+
+
+def _interval(x_row, method, kw, idx):
+    """(lo, hi) of entry idx in the float64 CDF, and the row's cut margin."""
+    pr, order, margin = sampling_probs_f64(x_row, method, t=kw.get("temperature", 1.0), k=kw.get("top_k", 1),
+                                           p=kw.get("p", 1.0))
+    c = np.cumsum(pr[order])
+    pos = np.nonzero(order == idx)[0]
+    if idx < 0 or pos.size == 0 or pr[idx] <= 0:
+        return None, margin
+    hi = c[pos[0]]
+    return (hi - pr[idx], hi), margin
+
+
+def _valid_draw(x_row, u, method, kw, idx, delta):
+    """idx is the float64 inverse CDF at u up to delta: u lies within delta of
+    idx's interval; where a keep/cut decision of the row lies within delta of
+    its threshold, idx need only be a number of the row."""
+    g, m = _interval(x_row, method, kw, idx)
+    if m < delta:
+        return 0 <= idx < len(x_row) and not np.isnan(x_row[idx])
+    return g is not None and g[0] - delta <= u <= g[1] + delta
+
+
+def _check(x, u, method, kw, what, max_miss=MAX_MISS):
+    xd = to_dev(x)
+    ud = torch.from_numpy(np.ascontiguousarray(u, np.float32)).cuda()
+    got = gbe.sample(xd, ud, method, **kw).cpu().numpy()
+    x32 = widen(x)
+    want = _oracle(x32, u, method, kw)
+    miss = np.nonzero(got != want)[0]
+    for r in miss:
+        assert _valid_draw(x32[r], float(u[r]), method, kw, int(got[r]), DELTA), (
+            f"{what}: row {r} u={u[r]} drew {got[r]}, oracle {want[r]}: not within rounding of a boundary")
+    assert miss.size <= max(1, max_miss * len(got)), f"{what}: {miss.size} of {len(got)} rows differ"
+    return got
+
+
+def _logits(rows, n, dtype, seed=31, std=4.0, nan_frac=0.0, tag="s"):
+    x = normal(seed, f"t.smp.{tag}.{rows}.{n}", (rows, n), 0.0, std)
+    if nan_frac:
+        v = units(seed, f"t.smp.nan.{tag}.{rows}.{n}", rows * n).reshape(rows, n)
+        x[v < nan_frac] = np.nan
+    return to_bf16(x) if dtype == "bf16" else x
+
+
+def _u(rows, tag, seed=31):
+    return units(seed, f"t.smp.u.{tag}.{rows}", rows).astype(np.float32)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("method,kw", METHODS)
+@pytest.mark.parametrize("rows,n", [(1, 1), (3, 7), (9, 1000), (4, 4097), (16, 32000), (2, 65536 + 3)])
+def test_shapes(dtype, method, kw, rows, n):
+    x = _logits(rows, n, dtype, nan_frac=0.01)
+    u = _u(rows, f"{rows}.{n}")
+    _check(x, u, method, kw, f"{method} {dtype} [{rows},{n}]")
+
+
+@pytest.mark.parametrize("method,kw", METHODS)
+def test_decode_logits(method, kw):
+    """The decode workload's logits: 64 rows of a 128256-entry vocabulary, bf16."""
+    a, _ = W.cases(W.DECODE)["argmax"]()
+    x = a["x"]
+    u = _u(x.shape[0], "decode")
+    _check(x, u, method, kw, f"{method} decode")
+
+
+@pytest.mark.parametrize("method,kw", [("temperature", dict(temperature=1.0)),
+                                       ("top_k", dict(temperature=0.7, top_k=1000)),
+                                       ("top_p", dict(temperature=1.0, p=0.5)),
+                                       ("min_p", dict(temperature=0.6, p=0.001))])
+def test_flat_wide_rows(method, kw):
+    """Flat logits over 152064 entries, f32, with NaN and exact ties: every
+    entry carries mass, so boundaries lie ~1e-5 apart and the oracle's f32
+    running sums drift across several of them.  Here every draw is held to
+    the float64 distribution itself, within 1e-7 of the kept mass."""
+    x = _logits(24, 152064, "f32", std=0.5, nan_frac=0.001, tag="flat")
+    x[:, 100:200] = x[:, 1000:1100]
+    u = _u(24, f"flat.{method}")
+    got = gbe.sample(to_dev(x), torch.from_numpy(u).cuda(), method, **kw).cpu().numpy()
+    for r in range(24):
+        assert _valid_draw(x[r], float(u[r]), method, kw, int(got[r]), 1e-7), (method, r, u[r], got[r])
+
+
+def test_draws_in_proportion():
+    """Inverse CDF on the GPU: over a grid of 4000 u, each index of a short
+    row is drawn 4000 * p_i times (+-2.5), p_i from the float64 definition."""
+    rng = np.random.default_rng(7)
+    for trial in range(4):
+        x = (rng.standard_normal(60) * 2.0).astype(np.float32)
+        x[[5, 17]] = x[3]
+        x[11] = np.nan
+        for method, kw in (("temperature", dict(temperature=0.8)), ("top_k", dict(temperature=1.3, top_k=7)),
+                           ("top_p", dict(temperature=0.9, p=0.6)), ("min_p", dict(temperature=1.0, p=0.2))):
+            pr, _, margin = sampling_probs_f64(x, method, t=kw["temperature"], k=kw.get("top_k", 1),
+                                               p=kw.get("p", 1.0))
+            if margin < 1e-4:
+                continue
+            u = ((np.arange(4000) + 0.5) / 4000).astype(np.float32)
+            rows = torch.from_numpy(np.repeat(x.reshape(1, -1), 4000, axis=0)).cuda()
+            got = gbe.sample(rows, torch.from_numpy(u).cuda(), method, **kw).cpu().numpy()
+            counts = np.bincount(got, minlength=60)
+            assert np.all(np.abs(counts - 4000 * pr) <= 2.5), (trial, method, np.abs(counts - 4000 * pr).max())
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_limits(dtype):
+    x = _logits(40, 5000, dtype, nan_frac=0.02, tag="lim")
+    x32 = widen(x)
+    x32[3] = np.nan
+    x32[4, :] = -np.inf
+    x32[5, 77] = np.inf
+    x32[6, 10] = x32[6, 4000] = 60.0  # tie at the maximum
+    x = to_bf16(x32) if dtype == "bf16" else x32
+    xd = to_dev(x)
+    u = torch.from_numpy(_u(40, "lim")).cuda()
+    want = gbe.argmax(xd).cpu().numpy()
+    g = lambda m, **kw: gbe.sample(xd, u, m, **kw).cpu().numpy()
+    got_k1 = g("top_k", temperature=0.7, top_k=1)
+    got_p0 = g("top_p", temperature=1.0, p=0.0)
+    greedy = gbe.sample(xd, None, "greedy").cpu().numpy()
+    assert np.array_equal(greedy, want)
+    for got in (got_k1, got_p0):
+        assert np.array_equal(np.delete(got, [4, 5]), np.delete(want, [4, 5]))
+        assert got[4] == -1 and got[5] == -1
+    assert got_k1[6] == 10
+    for m, kw in METHODS:
+        got = g(m, **kw)
+        assert got[3] == -1 and got[4] == -1 and got[5] == -1, m
+    assert np.array_equal(g("min_p", temperature=0.9, p=0.0), g("temperature", temperature=0.9))
+    # min_p = 1 keeps only the entries equal to the maximum
+    got = g("min_p", temperature=1.0, p=1.0)
+    assert np.array_equal(np.delete(got, [4, 5, 6]), np.delete(want, [4, 5, 6]))
+    assert got[6] in (10, 4000)
+    # x / t overflowing to +inf leaves no finite maximum
+    big = torch.full((1, 64), 3e38, device="cuda")
+    assert gbe.sample(big, u[:1], "temperature", temperature=0.5).item() == -1
+
+
+def test_u_edges_and_top_k_past_n():
+    x = _logits(8, 3000, "f32", tag="edge")
+    xd = to_dev(x)
+    for uu, pick in ((0.0, "first"), (np.nextafter(np.float32(1), np.float32(0)), "last"), (-3.0, "first"),
+                     (7.0, "last")):
+        u = torch.full((8,), float(uu), device="cuda")
+        got = gbe.sample(xd, u, "top_k", temperature=1.0, top_k=10).cpu().numpy()
+        for r in range(8):
+            order = sorted(range(3000), key=lambda i: (-x[r, i], i))[:10]
+            assert got[r] == (order[0] if pick == "first" else order[-1]), (uu, r)
+    u = torch.from_numpy(_u(8, "edge")).cuda()
+    a = gbe.sample(xd, u, "top_k", temperature=1.0, top_k=3000).cpu().numpy()
+    b = gbe.sample(xd, u, "top_k", temperature=1.0, top_k=1 << 40).cpu().numpy()
+    assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("method,kw", METHODS)
+def test_unaligned_and_batch_invariant(dtype, method, kw):
+    """The scalar path (rows not 16-byte aligned) draws what the vector path
+    does, and a row's draw does not depend on the rows around it."""
+    rows, n = 12, 8192
+    x = _logits(rows, n, dtype, nan_frac=0.01, tag="inv")
+    xd = to_dev(x)
+    u = torch.from_numpy(_u(rows, "inv")).cuda()
+    ref = gbe.sample(xd, u, method, **kw).cpu().numpy()
+    buf = torch.empty(rows * n + 1, dtype=xd.dtype, device="cuda")
+    xs = buf[1:].view(rows, n)
+    xs.copy_(xd)
+    assert np.array_equal(gbe.sample(xs, u, method, **kw).cpu().numpy(), ref)
+    for r0, r1 in ((0, 1), (3, 7), (11, 12)):
+        got = gbe.sample(xd[r0:r1].contiguous(), u[r0:r1].contiguous(), method, **kw).cpu().numpy()
+        assert np.array_equal(got, ref[r0:r1]), (r0, r1)
+
+
+@pytest.mark.parametrize("method,kw", METHODS)
+def test_prefill_logits_sampled_rows(method, kw):
+    """All 8192 rows of the prefill logits [8192, 128256] bf16 in one launch;
+    64 of them checked against the oracle."""
+    a, _ = W.cases(W.PREFILL)["argmax"]()
+    x = a["x"]
+    u = _u(x.shape[0], "prefill")
+    got = gbe.sample(to_dev(x), torch.from_numpy(u).cuda(), method, **kw).cpu().numpy()
+    pick = np.linspace(0, x.shape[0] - 1, 64).astype(np.int64)
+    sub = _check(x[pick], u[pick], method, kw, f"{method} prefill rows")
+    assert np.array_equal(got[pick], sub)
+
+
+def test_refusals_on_device():
+    x = torch.randn(4, 1000, device="cuda")
+    u = torch.rand(4, device="cuda")
+    out = torch.empty(4, dtype=torch.int32, device="cuda")
+    L = gbe.lib()
+    # out inside x: an alias
+    assert L.gbe_sample(x.data_ptr(), u.data_ptr(), x.data_ptr() + 64, 4, 1000, 1, 1.0, 1, 1.0, 0, None) == 8
+    # u in pageable host memory
+    uh = torch.rand(4)
+    assert L.gbe_sample(x.data_ptr(), uh.data_ptr(), out.data_ptr(), 4, 1000, 1, 1.0, 1, 1.0, 0, None) == 10
+    # u NULL: refused except for greedy, which does not read it
+    assert L.gbe_sample(x.data_ptr(), None, out.data_ptr(), 4, 1000, 1, 1.0, 1, 1.0, 0, None) == 1
+    assert L.gbe_sample(x.data_ptr(), None, out.data_ptr(), 4, 1000, 0, 0.0, 0, 9.0, 0, None) == 0
+    torch.cuda.synchronize()
+    assert torch.equal(out, gbe.argmax(x))
+    with pytest.raises(gbe.GbeError):
+        gbe.sample(x, u, "top_k", temperature=1.0, top_k=0)
