@@ -529,7 +529,7 @@ int gbe_sample(const void* x, const float* u, int32_t* out, int64_t rows, int64_
     if (!es) return GBE_ERR_DTYPE;
     if (method < GBE_SAMPLE_GREEDY || method > GBE_SAMPLE_MIN_P) return GBE_ERR_SAMPLING;
     const bool greedy = method == GBE_SAMPLE_GREEDY;
-    if (!greedy && !(temperature > 0.0f)) return GBE_ERR_SAMPLING;
+    if (!greedy && !(temperature > 0.0f && std::isfinite(temperature))) return GBE_ERR_SAMPLING;
     if (method == GBE_SAMPLE_TOP_K && top_k < 1) return GBE_ERR_SAMPLING;
     if ((method == GBE_SAMPLE_TOP_P || method == GBE_SAMPLE_MIN_P) && !(p >= 0.0f && p <= 1.0f))
         return GBE_ERR_SAMPLING;

@@ -11,27 +11,36 @@
 // the sum.  NaN logits take no part; equal logits order by ascending index;
 // a row whose largest logit / t is not finite gives -1.
 //
-// Arithmetic.  For every logit e = expf(x / t - m), m the largest x / t, so
-// 0 <= e <= 1; e is then held as the integer w = rn(e * 2^40), and every sum,
+// Arithmetic.  For every logit e = 2^((x - M) * c) in f32, M the largest
+// logit and c = log2(e) / t (exp2f; e = 1 exactly where x = M), so
+// 0 <= e <= 1 -- the softmax numerator exp(x / t - M / t) up to a few f32
+// roundings.  e is then held as the integer w = rn(e * 2^40), and every sum,
 // histogram and threshold is an integer.  Integer sums do not depend on their
 // order, so a draw is deterministic however the threads are scheduled, and
-// the normalisation by the sum is never divided out: the target of a draw
-// is floor(u * W) for the kept mass W.  (The min-p cut e / S >= p * max(e / S)
-// is taken as the equivalent e >= p, since max(e) = 1.)  Rows are limited to
-// 2^23 entries so that W < 2^63.
+// the normalisation is never divided out: the target of a draw is
+// floor(u * W) for the kept mass W, and the drawn entry is the first whose
+// running mass exceeds it.  (The min-p cut e / S >= p * max(e / S) is taken
+// as the equivalent e >= p, since max(e) = 1.)  Rows are limited to 2^23
+// entries so that W < 2^63.
 //
-// Map: one CTA of 1024 threads per row; thread i owns a contiguous chunk of
-// the row (index order within a thread, threads in order), read with 16-byte
-// loads when the row allows, from L2 after the first pass.
-//  * temperature, min-p (index order): one pass forms the chunk sums, a block
-//    scan finds the chunk holding the target, its thread walks the chunk.
-//  * top-k, top-p (descending order): the position where the descending
-//    running count (top-k's cut) or mass (top-p's cut, and the draw) passes
-//    its target is found digit by digit -- 8-bit digits of an order-keeping
-//    32-bit key of the logit, a 256-bin histogram per digit (the first
-//    digit's built once) -- then inside the group of logits equal to the
-//    found key, in index order.  No sort of the vocabulary and no memory
-//    beyond the inputs and the outputs.
+// Map: one CTA of 512 threads (16 warps) per row.  Warp w owns a contiguous
+// segment of the row, read in coalesced tiles of 32 16-byte vectors (lane l
+// holds tile entries [l V, l V + V)), so index order is warp, tile, lane,
+// element.  The first pass reads HBM; later ones hit L2.
+//  * temperature, min-p (index order): pass 1 the maximum, pass 2 each
+//    warp's kept mass; the warp holding the target walks its segment tile by
+//    tile with warp scans.
+//  * top-k, top-p (descending order): an order-keeping 32-bit key of each
+//    logit is split into 12 / 10 / 10-bit digits.  A 4096-bin histogram of
+//    the first digit (counts, and for top-p masses) locates the bin where the
+//    descending running count or mass passes its target; that bin's entries
+//    -- few, at the head of a peaked distribution -- are gathered into shared
+//    memory as (key, ~index) pairs, sorted descending (equal keys then come
+//    in index order), and walked.  A bin of more than 4096 entries is split by
+//    the next digit, and a group of more than 4096 equal logits is walked in
+//    index order by the warps.  Top-k with k within the gather limit gathers
+//    every bin down to the k-th entry and draws among the first k.
+// No memory beyond the inputs and the outputs.
 #include "common.cuh"
 #include "launch.h"
 
@@ -39,97 +48,202 @@ namespace gbe {
 
 namespace {
 
-constexpr int kT = 1024;
-constexpr int kWarps = kT / 32;
+constexpr int kT = 512;
+constexpr int kW = kT / 32;
+constexpr int kU = 4;                       // tiles in flight per lane
+constexpr int kMaxCand = 4096;              // entries gathered into shared memory
+constexpr int kTopGather = 1024;            // entries top-p gathers from the top of a row first
+constexpr int kBins0 = 4096, kBins1 = 1024;  // 12-bit first digit, 10-bit others
 constexpr float kScale = 1099511627776.0f;  // 2^40
+constexpr unsigned kFull = 0xFFFFFFFFu;
 typedef unsigned long long u64;
 
 enum { kGreedy = 0, kTemperature = 1, kTopK = 2, kTopP = 3, kMinP = 4 };
 
-// Larger logit, larger key (the IEEE order of non-NaN floats, -0 below +0).
+// Larger logit, larger key (the IEEE order of non-NaN floats, -0 below +0),
+// and back.
 __device__ __forceinline__ uint32_t order_key(float v) {
     const uint32_t b = __float_as_uint(v);
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
+__device__ __forceinline__ float key_value(uint32_t key) {
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+// candidate = key above, complemented index below: descending order of the
+// candidates is descending key, then ascending index
+__device__ __forceinline__ u64 cand_of(uint32_t key, int i) { return ((u64)key << 32) | (uint32_t)~(uint32_t)i; }
+__device__ __forceinline__ int cand_index(u64 c) { return (int)~(uint32_t)c; }
 
-struct Smem {
-    u64 mass0[256];  // first-digit histogram of every valid entry, kept for reuse
-    unsigned cnt0[256];
-    u64 mass[256];  // histogram of the current digit
-    unsigned cnt[256];
-    u64 wu[kWarps];
-    float wf[kWarps];
-    int wi[kWarps];
-    u64 bu[2];
-    int bi[2];
+struct Sh {
+    u64 wu[kW];
+    float wf[kW];
+    int wi[kW];
+    u64 ru[4];
+    int ri[4];
+    unsigned ncand;
 };
+
+
+// 2^a, the hardware approximation (relative error near 2^-22; results below
+// 2^-126 flush to 0, far below the 2^-41 resolution of the weights).
+__device__ __forceinline__ float ex2(float a) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(a));
+    return r;
+}
+
+// rn(e * 2^40) for 0 <= e <= 1, exactly: below 2^23 the sum with 2^23 rounds
+// to the nearest integer (ties to even) and leaves it in the low mantissa
+// bits; from 2^23 on, e * 2^40 is an integer and the mantissa, shifted, is it.
+__device__ __forceinline__ bool fixed40_small(float y) { return y < 8388608.0f; }
+__device__ __forceinline__ uint32_t fixed40_lo(float y) {
+    return __float_as_uint(__fadd_rn(y, 8388608.0f)) - 0x4B000000u;
+}
+__device__ __forceinline__ u64 fixed40_hi(float e) {
+    const uint32_t b = __float_as_uint(e);
+    return (u64)((b & 0x7FFFFFu) | 0x800000u) << ((int)(b >> 23) - 127 + 17);
+}
+__device__ __forceinline__ u64 fixed40(float e) {
+    const float y = __fmul_rn(e, kScale);
+    return fixed40_small(y) ? (u64)fixed40_lo(y) : fixed40_hi(e);
+}
+
+// A running sum of fixed40 weights: the common small ones (below 2^23) in a
+// 32-bit word, folded into the 64-bit sum after every kU tiles (at most 32
+// additions, so the word cannot overflow).
+struct MassAcc {
+    u64 big = 0;
+    uint32_t small = 0;
+    __device__ __forceinline__ void add(float e) {
+        const float y = __fmul_rn(e, kScale);
+        if (fixed40_small(y)) small += fixed40_lo(y);
+        else big += fixed40_hi(e);
+    }
+    __device__ __forceinline__ void fold() {
+        big += small;
+        small = 0;
+    }
+    __device__ __forceinline__ u64 total() const { return big + small; }
+};
+
+// The float interval of the keys [lo_key, hi_key] (NaN patterns at either
+// end widen it to an infinity); every non-NaN float whose key lies in the
+// range lies in the interval (-0 and +0 compare equal, so the interval may
+// admit one of them from outside: callers recheck the key).
+__device__ __forceinline__ float key_floor(u64 lo_key) {
+    return lo_key < 0x00800000ull ? -INFINITY : key_value((uint32_t)lo_key);
+}
+__device__ __forceinline__ float key_ceil(u64 hi_key) {
+    return hi_key >= 0xFF800000ull ? INFINITY : key_value((uint32_t)hi_key);
+}
 
 template <int DT, bool VEC>
 struct Row {
+    static constexpr int V = Store<DT>::V;
+    static constexpr int kTile = 32 * V;
     const void* x;
     int64_t base;  // element offset of the row
-    float t, m;    // temperature; the largest x / t
-    int c0, c1;    // this thread's chunk [c0, c1)
+    float t, mx, c;  // temperature; the largest logit; log2(e) / t
+    int s0, s1;      // this warp's segment [s0, s1)
+    int lane;
 
-    __device__ __forceinline__ float e_of(float v) const { return expf(__fsub_rn(__fdiv_rn(v, t), m)); }
-    __device__ __forceinline__ static u64 w_of(float e) { return __float2ull_rn(__fmul_rn(e, kScale)); }
+    __device__ __forceinline__ float e_of(float v) const {
+        const float d = __fsub_rn(v, mx);
+        return d == 0.0f ? 1.0f : ex2(__fmul_rn(d, c));
+    }
+    __device__ __forceinline__ static u64 w_of(float e) { return fixed40(e); }
     // fixed-point weight of a logit that is not NaN
     __device__ __forceinline__ u64 weight(float v) const { return w_of(e_of(v)); }
 
-    // f(i, v) for every entry of the chunk in index order, NaN included
-    template <typename F>
-    __device__ __forceinline__ void each(F f) const {
+    // this lane's V entries of the tile starting at j (NaN past the segment)
+    __device__ __forceinline__ void load(int j, float (&v)[V]) const {
+        const int i = j + lane * V;
         if (VEC) {
-            constexpr int V = Store<DT>::V;
-            const char* p = static_cast<const char*>(x) + (base + c0) * (int64_t)sizeof(typename Store<DT>::T);
-            for (int i = c0; i < c1; i += V, p += 16) {
-                float fv[V];
-                Store<DT>::unpack(ld_reuse(p), fv);
+            if (i < s1) {
+                Store<DT>::unpack(
+                    ld_reuse(static_cast<const char*>(x) + (base + i) * (int64_t)sizeof(typename Store<DT>::T)), v);
+            } else {
 #pragma unroll
-                for (int e = 0; e < V; ++e) f(i + e, fv[e]);
+                for (int e = 0; e < V; ++e) v[e] = __int_as_float(0x7FC00000);
             }
         } else {
-            for (int i = c0; i < c1; ++i) f(i, Store<DT>::load1(x, base + i));
+#pragma unroll
+            for (int e = 0; e < V; ++e) v[e] = i + e < s1 ? Store<DT>::load1(x, base + i + e) : __int_as_float(0x7FC00000);
         }
+    }
+
+    // f(i, v) for every entry of the segment, NaN past its end, then after()
+    // once per kU tiles; every lane of the warp makes every call, so f may
+    // use warp-wide operations
+    template <typename F, typename G>
+    __device__ __forceinline__ void each(F f, G after) const {
+        for (int j0 = s0; j0 < s1; j0 += kTile * kU) {
+            float v[kU][V];
+#pragma unroll
+            for (int q = 0; q < kU; ++q) load(j0 + q * kTile, v[q]);
+#pragma unroll
+            for (int q = 0; q < kU; ++q)
+#pragma unroll
+                for (int e = 0; e < V; ++e) f(j0 + q * kTile + lane * V + e, v[q][e]);
+            after();
+        }
+    }
+    template <typename F>
+    __device__ __forceinline__ void each(F f) const {
+        each(f, [] {});
     }
 };
 
-// ---- block primitives (1024 threads; each opens with a barrier so that the
-//      shared slots of the previous call are free) -------------------------------
+// ---- warp and block primitives ----------------------------------------------------
 
-__device__ __forceinline__ float block_max(float v, Smem& sh) {
-    for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+__device__ __forceinline__ u64 warp_sum_u64(u64 v) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+    return v;
+}
+
+__device__ __forceinline__ u64 warp_incl_scan_u64(u64 v, int lane) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const u64 y = __shfl_up_sync(kFull, v, o);
+        if (lane >= o) v += y;
+    }
+    return v;
+}
+
+// Each block primitive opens with a barrier, so the shared slots of the
+// previous call are free.
+__device__ __forceinline__ float block_max(float v, Sh& sh) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
     __syncthreads();
     if ((threadIdx.x & 31) == 0) sh.wf[threadIdx.x >> 5] = v;
     __syncthreads();
     float r = sh.wf[0];
-    for (int w = 1; w < kWarps; ++w) r = fmaxf(r, sh.wf[w]);
+    for (int w = 1; w < kW; ++w) r = fmaxf(r, sh.wf[w]);
     return r;
 }
 
-__device__ __forceinline__ int block_sum_int(int v, Smem& sh) {
-    for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+__device__ __forceinline__ int block_sum_int(int v, Sh& sh) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
     __syncthreads();
     if ((threadIdx.x & 31) == 0) sh.wi[threadIdx.x >> 5] = v;
     __syncthreads();
     int r = 0;
-    for (int w = 0; w < kWarps; ++w) r += sh.wi[w];
+    for (int w = 0; w < kW; ++w) r += sh.wi[w];
     return r;
 }
 
 // exclusive prefix of v over the threads in order; *total gets the sum
-__device__ __forceinline__ u64 block_exscan(u64 v, Smem& sh, u64* total) {
+__device__ __forceinline__ u64 block_exscan(u64 v, Sh& sh, u64* total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    u64 inc = v;
-    for (int o = 1; o < 32; o <<= 1) {
-        const u64 y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
-        if (lane >= o) inc += y;
-    }
+    const u64 inc = warp_incl_scan_u64(v, lane);
     __syncthreads();
     if (lane == 31) sh.wu[warp] = inc;
     __syncthreads();
     u64 before = 0, all = 0;
-    for (int w = 0; w < kWarps; ++w) {
+    for (int w = 0; w < kW; ++w) {
         if (w < warp) before += sh.wu[w];
         all += sh.wu[w];
     }
@@ -137,99 +251,19 @@ __device__ __forceinline__ u64 block_exscan(u64 v, Smem& sh, u64* total) {
     return before + inc - v;
 }
 
-// ---- descending order ------------------------------------------------------------
-//
-// The entry at which the descending running count (BY_COUNT) or mass first
-// exceeds `target` (target < the total of the valid entries).  Returns its
-// index; *ahead gets the mass of the entries before it in descending order.
-// The first digit's histogram must be in mass0 / cnt0.
-template <int DT, bool VEC, bool BY_COUNT>
-__device__ int find_descending(const Row<DT, VEC>& row, u64 target, Smem& sh, u64* ahead) {
-    uint32_t prefix = 0;
-    u64 base_m = 0, base_c = 0;  // mass and count of the entries above the current bin
-    for (int level = 0; level < 4; ++level) {
-        const int shift = 24 - 8 * level;
-        if (level > 0) {
-            __syncthreads();
-            for (int b = threadIdx.x; b < 256; b += kT) {
-                sh.mass[b] = 0;
-                sh.cnt[b] = 0;
-            }
-            __syncthreads();
-            row.each([&](int, float v) {
-                if (v != v) return;
-                const uint32_t key = order_key(v);
-                if ((key >> (shift + 8)) != prefix) return;
-                const int bin = (key >> shift) & 255;
-                atomicAdd(&sh.cnt[bin], 1u);
-                atomicAdd(&sh.mass[bin], row.weight(v));
-            });
-            __syncthreads();
-        }
-        if (threadIdx.x == 0) {
-            const u64* mm = level == 0 ? sh.mass0 : sh.mass;
-            const unsigned* cc = level == 0 ? sh.cnt0 : sh.cnt;
-            int chosen = 0;
-            for (int b = 255; b >= 0; --b) {
-                const u64 step = BY_COUNT ? (u64)cc[b] : mm[b];
-                const u64 run = BY_COUNT ? base_c : base_m;
-                if (step > 0 && run + step > target) {
-                    chosen = b;
-                    break;
-                }
-                base_m += mm[b];
-                base_c += cc[b];
-            }
-            sh.bu[0] = base_m;
-            sh.bu[1] = base_c;
-            sh.bi[0] = chosen;
-        }
-        __syncthreads();
-        base_m = sh.bu[0];
-        base_c = sh.bu[1];
-        prefix = (prefix << 8) | (uint32_t)sh.bi[0];
-        __syncthreads();
+// exclusive prefix over the warps of a value every lane of a warp holds
+__device__ __forceinline__ u64 warp_exscan(u64 warp_value, Sh& sh, u64* total) {
+    const int warp = threadIdx.x >> 5;
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) sh.wu[warp] = warp_value;
+    __syncthreads();
+    u64 before = 0, all = 0;
+    for (int w = 0; w < kW; ++w) {
+        if (w < warp) before += sh.wu[w];
+        all += sh.wu[w];
     }
-    // The group of entries equal to `prefix`, in index order.  All of them
-    // carry the same weight w (the same logit), so within the group the
-    // position follows from a count: the found entry is the group's j-th,
-    // j = (target - base) / (1 or w), and `ahead` adds the j entries before it.
-    const uint32_t key = prefix;
-    u64 w_key = 0, mine = 0;
-    row.each([&](int, float v) {
-        if (v == v && order_key(v) == key) {
-            ++mine;
-            w_key = row.weight(v);
-        }
-    });
-    u64 dummy;
-    // every thread learns the group's weight (the largest of the per-thread copies)
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) sh.wu[threadIdx.x >> 5] = 0;
-    __syncthreads();
-    if (mine > 0) atomicMax(&sh.wu[threadIdx.x >> 5], w_key);
-    __syncthreads();
-    u64 w = 0;
-    for (int q = 0; q < kWarps; ++q) w = sh.wu[q] > w ? sh.wu[q] : w;
-    const u64 ex = block_exscan(mine, sh, &dummy);  // entries of the group in earlier chunks
-    const u64 j = BY_COUNT ? target - base_c : (target - base_m) / w;
-    __syncthreads();
-    if (threadIdx.x == 0) sh.bi[1] = -1;
-    __syncthreads();
-    if (mine > 0 && ex <= j && j < ex + mine) {
-        u64 seen = ex;
-        int found = -1;
-        row.each([&](int i, float v) {
-            if (found < 0 && v == v && order_key(v) == key) {
-                if (seen == j) found = i;
-                ++seen;
-            }
-        });
-        sh.bi[1] = found;
-    }
-    __syncthreads();
-    *ahead = base_m + j * w;
-    return sh.bi[1];
+    *total = all;
+    return before;
 }
 
 __device__ __forceinline__ u64 scaled(float u, u64 total) {
@@ -237,109 +271,512 @@ __device__ __forceinline__ u64 scaled(float u, u64 total) {
     return t >= total ? total - 1 : t;
 }
 
-template <int DT, bool VEC>
-__device__ __forceinline__ void sample_body(const void* x, int32_t* out, int n, int method, float t, int k, float p,
-                                            const float* u, Smem& sh) {
-    const int64_t r = blockIdx.x;
-    Row<DT, VEC> row;
-    row.x = x;
-    row.base = r * (int64_t)n;
-    row.t = t;
-    row.m = 0.0f;
-    // chunk length: a whole number of 16-byte vectors for either storage type
-    const int chunk = ((n + kT - 1) / kT + 7) & ~7;
-    row.c0 = min(n, (int)threadIdx.x * chunk);
-    row.c1 = min(n, row.c0 + chunk);
+// The warp walks its segment tile by tile and returns the first index whose
+// running measure (meas(v) per entry, 0 for entries that take no part)
+// exceeds target, measured from the segment's start; -1 if none does.
+template <int DT, bool VEC, typename M>
+__device__ int warp_walk(const Row<DT, VEC>& row, u64 target, M meas) {
+    constexpr int V = Row<DT, VEC>::V;
+    u64 run = 0;
+    for (int j = row.s0; j < row.s1; j += Row<DT, VEC>::kTile) {
+        float v[V];
+        row.load(j, v);
+        u64 s = 0;
+#pragma unroll
+        for (int e = 0; e < V; ++e) s += meas(v[e]);
+        const u64 inc = warp_incl_scan_u64(s, row.lane);
+        const u64 tot = __shfl_sync(kFull, inc, 31);
+        if (run + tot > target) {
+            int found = -1;
+            const u64 ex = inc - s;
+            if (run + ex <= target && target < run + inc) {
+                u64 r = run + ex;
+#pragma unroll
+                for (int e = 0; e < V; ++e) {
+                    r += meas(v[e]);
+                    if (found < 0 && r > target) found = j + row.lane * V + e;
+                }
+            }
+            const unsigned who = __ballot_sync(kFull, found >= 0);
+            return __shfl_sync(kFull, found, __ffs(who) - 1);
+        }
+        run += tot;
+    }
+    return -1;
+}
 
-    // pass 0: the largest logit and the count of valid entries
+// ---- index order: temperature and min-p -------------------------------------------
+
+template <int DT, bool VEC>
+__device__ __forceinline__ void setup(Row<DT, VEC>& row, const void* x, int n, float t) {
+    constexpr int kTile = Row<DT, VEC>::kTile;
+    row.x = x;
+    row.base = (int64_t)blockIdx.x * n;
+    row.t = t;
+    row.mx = 0.0f;
+    row.c = __fdiv_rn(1.44269502f, t);  // log2(e) / t
+    row.lane = threadIdx.x & 31;
+    const int per = ((n + kW - 1) / kW + kTile - 1) / kTile * kTile;
+    const int w = threadIdx.x >> 5;
+    row.s0 = min(n, w * per);
+    row.s1 = min(n, row.s0 + per);
+}
+
+// pass 1: the largest logit (and with COUNT the count of numbers); false
+// (and -1 written) when the row has no number or no finite largest x / t
+template <bool COUNT, int DT, bool VEC>
+__device__ __forceinline__ bool first_pass(Row<DT, VEC>& row, int32_t* out, Sh& sh, int* nv_out) {
     float mx = -INFINITY;
     int nv = 0;
     row.each([&](int, float v) {
-        if (v == v) {
-            mx = fmaxf(mx, v);
-            ++nv;
-        }
+        mx = fmaxf(mx, v);  // NaN is ignored
+        if (COUNT && v == v) ++nv;
     });
     mx = block_max(mx, sh);
-    nv = block_sum_int(nv, sh);
-    row.m = __fdiv_rn(mx, t);
-    if (nv == 0 || !isfinite(row.m)) {
-        if (threadIdx.x == 0) out[r] = -1;
-        return;
+    if (COUNT) nv = block_sum_int(nv, sh);
+    row.mx = mx;
+    *nv_out = nv;
+    // a row of NaN leaves mx = -inf, which is not finite either
+    if (!isfinite(__fdiv_rn(mx, row.t))) {
+        if (threadIdx.x == 0) out[blockIdx.x] = -1;
+        return false;
     }
-    const float ur = u[r];
-
-    if (method == kTemperature || method == kMinP) {
-        const bool minp = method == kMinP;
-        u64 mine = 0;
-        row.each([&](int, float v) {
-            if (v != v) return;
-            const float e = row.e_of(v);
-            if (minp && !(e >= p)) return;
-            mine += row.w_of(e);
-        });
-        u64 total;
-        const u64 ex = block_exscan(mine, sh, &total);
-        const u64 target = scaled(ur, total);
-        if (mine > 0 && ex <= target && target < ex + mine) {
-            u64 run = ex;
-            int found = -1;
-            row.each([&](int i, float v) {
-                if (found >= 0 || v != v) return;
-                const float e = row.e_of(v);
-                if (minp && !(e >= p)) return;
-                run += row.w_of(e);
-                if (run > target) found = i;
-            });
-            out[r] = found;
-        }
-        return;
-    }
-
-    // top-k, top-p: the first digit's histogram of every valid entry
-    for (int b = threadIdx.x; b < 256; b += kT) {
-        sh.mass0[b] = 0;
-        sh.cnt0[b] = 0;
-    }
-    __syncthreads();
-    row.each([&](int, float v) {
-        if (v != v) return;
-        const int bin = order_key(v) >> 24;
-        atomicAdd(&sh.cnt0[bin], 1u);
-        atomicAdd(&sh.mass0[bin], row.weight(v));
-    });
-    __syncthreads();
-    u64 all = 0;
-    for (int b = 0; b < 256; ++b) all += sh.mass0[b];
-    u64 kept = all;
-    if (method == kTopK) {
-        if (k < nv) find_descending<DT, VEC, true>(row, (u64)k, sh, &kept);  // first entry past the k-th
-    } else {
-        // keep the prefix whose running mass stays <= p * W; the first entry always
-        const u64 cut = (u64)((double)p * (double)all);
-        if (cut < all) {
-            find_descending<DT, VEC, false>(row, cut, sh, &kept);
-            if (kept == 0) kept = 1;  // a target of 0 lands on the first entry
-        }
-    }
-    u64 unused;
-    const int idx = find_descending<DT, VEC, false>(row, scaled(ur, kept), sh, &unused);
-    if (threadIdx.x == 0) out[r] = idx;
+    return true;
 }
 
 template <int DT, bool VEC>
-__global__ void __launch_bounds__(kT)
-sample_rows(const void* x, int32_t* out, int n, int method, float t, int k, float p, const float* u) {
+__global__ void __launch_bounds__(kT, 2)
+sample_index_order(const void* x, int32_t* out, int n, int minp, float t, float p, const float* u) {
     pdl_begin();
-    __shared__ Smem sh;
-    sample_body<DT, VEC>(x, out, n, method, t, k, p, u, sh);
+    __shared__ Sh sh;
+    Row<DT, VEC> row;
+    setup(row, x, n, t);
+    int nv;
+    if (!first_pass<false>(row, out, sh, &nv)) return;
+    const float pmin = minp ? p : 0.0f;  // e >= 0 holds for every number
+    MassAcc acc;
+    row.each(
+        [&](int, float v) {
+            if (v != v) return;
+            const float e = row.e_of(v);
+            if (e >= pmin) acc.add(e);
+        },
+        [&] { acc.fold(); });
+    u64 total;
+    const u64 wmass = warp_sum_u64(acc.total());
+    const u64 ex = warp_exscan(wmass, sh, &total);
+    const u64 target = scaled(u[blockIdx.x], total);
+    if (wmass > 0 && ex <= target && target < ex + wmass) {
+        auto meas = [&](float v) -> u64 {
+            if (v != v) return 0ull;
+            const float e = row.e_of(v);
+            return e >= pmin ? row.w_of(e) : 0ull;
+        };
+        const int idx = warp_walk(row, target - ex, meas);
+        if (row.lane == 0) out[blockIdx.x] = idx;
+    }
+}
+
+// ---- descending order: top-k and top-p ---------------------------------------------
+
+// A histogram in shared memory: counts, and masses as exact 64-bit sums held
+// in two 32-bit words, so that every update is a native 32-bit shared atomic
+// (the carry out of the low word goes into the high word).
+struct Hist {
+    unsigned* cnt;
+    unsigned* lo;
+    unsigned* hi;
+    int nbins;
+    __device__ __forceinline__ u64 count(int b) const { return cnt[b]; }
+    __device__ __forceinline__ u64 mass(int b) const { return ((u64)hi[b] << 32) + lo[b]; }
+    __device__ __forceinline__ void clear() const {
+        for (int b = threadIdx.x; b < nbins; b += kT) cnt[b] = lo[b] = hi[b] = 0u;
+    }
+    __device__ __forceinline__ void add(int b, bool with_mass, u64 w) const {
+        atomicAdd(&cnt[b], 1u);
+        if (with_mass && w) {
+            const uint32_t wl = (uint32_t)w;
+            const uint32_t old = atomicAdd(&lo[b], wl);
+            const uint32_t up = (uint32_t)(w >> 32) + (old + wl < old ? 1u : 0u);
+            if (up) atomicAdd(&hi[b], up);
+        }
+    }
+};
+
+struct ShBig {
+    Sh s;
+    unsigned cnt0[kBins0], lo0[kBins0], hi0[kBins0];
+    unsigned cnt1[kBins1], lo1[kBins1], hi1[kBins1];
+    u64 cand[kMaxCand];
+    __device__ __forceinline__ Hist h0() { return Hist{cnt0, lo0, hi0, kBins0}; }
+    __device__ __forceinline__ Hist h1() { return Hist{cnt1, lo1, hi1, kBins1}; }
+};
+
+// The bin (scanning from the top bin down) where the running sum of h(b)
+// passes target (target < the sum); *above gets the sum of the bins above it.
+template <typename H>
+__device__ int find_bin(H h, int nbins, u64 target, Sh& sh, u64* above) {
+    const int per = nbins / kT;
+    const int top = nbins - (int)threadIdx.x * per;  // this thread's bins [top - per, top), from the top
+    u64 local = 0;
+    for (int b = top - 1; b >= top - per; --b) local += h(b);
+    u64 total;
+    const u64 ex = block_exscan(local, sh, &total);
+    if (threadIdx.x == 0) {
+        sh.ri[0] = 0;
+        sh.ru[0] = 0;
+    }
+    __syncthreads();
+    if (local > 0 && ex <= target && target < ex + local) {
+        u64 run = ex;
+        for (int b = top - 1; b >= top - per; --b) {
+            const u64 v = h(b);
+            if (v > 0 && run + v > target) {
+                sh.ri[0] = b;
+                sh.ru[0] = run;
+                break;
+            }
+            run += v;
+        }
+    }
+    __syncthreads();
+    *above = sh.ru[0];
+    return sh.ri[0];
+}
+
+// sum of h(b) over the bins above b0 (all bins when b0 = -1)
+template <typename H>
+__device__ u64 sum_above(H h, int nbins, int b0, Sh& sh) {
+    u64 s = 0;
+    for (int b = b0 + 1 + (int)threadIdx.x; b < nbins; b += kT) s += h(b);
+    u64 total;
+    block_exscan(s, sh, &total);
+    return total;
+}
+
+// First-digit histogram of the valid entries whose first digit is >= from
+// (0: all of them), with masses when hist_mass; returns this thread's share
+// of the row's exact total mass when total_mass (every valid entry, in the
+// histogram or not), else 0.
+template <int DT, bool VEC>
+__device__ u64 build_first(const Row<DT, VEC>& row, ShBig& sb, uint32_t from, bool hist_mass, bool total_mass) {
+    const Hist h = sb.h0();
+    const float x_from = key_floor((u64)from << 20);
+    __syncthreads();
+    h.clear();
+    __syncthreads();
+    MassAcc acc;
+    row.each(
+        [&](int, float v) {
+            if (v != v) return;
+            float e = 0.0f;
+            if (hist_mass || total_mass) e = row.e_of(v);
+            if (total_mass) acc.add(e);
+            if (v >= x_from) {
+                const uint32_t d = order_key(v) >> 20;
+                if (d >= from) h.add((int)d, hist_mass, hist_mass ? row.w_of(e) : 0ull);
+            }
+        },
+        [&] { acc.fold(); });
+    __syncthreads();
+    return acc.total();
+}
+
+// Histogram of the 10-bit digit (key >> shift) & 1023 over the entries whose
+// key >> (shift + 10) equals prefix, with masses.
+template <int DT, bool VEC>
+__device__ void build_next(const Row<DT, VEC>& row, ShBig& sb, int shift, uint32_t prefix) {
+    const Hist h = sb.h1();
+    __syncthreads();
+    h.clear();
+    __syncthreads();
+    row.each([&](int, float v) {
+        if (v != v) return;
+        const uint32_t key = order_key(v);
+        if ((key >> (shift + 10)) != prefix) return;
+        h.add((int)((key >> shift) & (kBins1 - 1)), true, row.weight(v));
+    });
+    __syncthreads();
+}
+
+// Gather the entries for which sel(v) holds into cand as (key, ~index) and
+// sort them descending (after() runs once per kU tiles); returns their count
+// (the caller's selection holds at most kMaxCand entries).
+template <int DT, bool VEC, typename F, typename G>
+__device__ int gather_sorted_by(const Row<DT, VEC>& row, ShBig& sb, F sel, G after) {
+    __syncthreads();
+    if (threadIdx.x == 0) sb.s.ncand = 0;
+    __syncthreads();
+    row.each(
+        [&](int i, float v) {
+            if (!sel(v)) return;
+            const unsigned slot = atomicAdd(&sb.s.ncand, 1u);
+            if (slot < (unsigned)kMaxCand) sb.cand[slot] = cand_of(order_key(v), i);
+        },
+        after);
+    __syncthreads();
+    const int nc = (int)min(sb.s.ncand, (unsigned)kMaxCand);
+    int P = 1;
+    while (P < nc) P <<= 1;
+    for (int i = nc + (int)threadIdx.x; i < P; i += kT) sb.cand[i] = 0ull;  // pads sort last
+    __syncthreads();
+    for (int k = 2; k <= P; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int i = threadIdx.x; i < P; i += kT) {
+                const int ij = i ^ j;
+                if (ij > i) {
+                    const u64 a = sb.cand[i], b = sb.cand[ij];
+                    const bool desc = (i & k) == 0;
+                    if (desc ? (a < b) : (a > b)) {
+                        sb.cand[i] = b;
+                        sb.cand[ij] = a;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+    return nc;
+}
+
+// The entries whose key >> shift lies in [lo, hi], gathered and sorted.
+template <int DT, bool VEC>
+__device__ int gather_sorted(const Row<DT, VEC>& row, int shift, uint32_t lo, uint32_t hi, ShBig& sb) {
+    const float x_lo = key_floor((u64)lo << shift), x_hi = key_ceil((((u64)hi + 1) << shift) - 1);
+    return gather_sorted_by(
+        row, sb,
+        [&](float v) {
+            if (!(v >= x_lo && v <= x_hi)) return false;  // NaN fails too
+            const uint32_t d = order_key(v) >> shift;
+            return d >= lo && d <= hi;
+        },
+        [] {});
+}
+
+// In the sorted candidates [0, L): the first position whose running mass
+// exceeds target; *before gets the mass of the positions ahead of it.
+template <int DT, bool VEC>
+__device__ int sorted_pick(const Row<DT, VEC>& row, int L, u64 target, ShBig& sb, u64* before) {
+    constexpr int per = kMaxCand / kT;
+    const int j0 = (int)threadIdx.x * per;
+    u64 local = 0;
+    for (int j = j0; j < min(L, j0 + per); ++j) local += row.weight(key_value((uint32_t)(sb.cand[j] >> 32)));
+    u64 total;
+    const u64 ex = block_exscan(local, sb.s, &total);
+    if (threadIdx.x == 0) {
+        sb.s.ri[1] = -1;
+        sb.s.ru[1] = 0;
+    }
+    __syncthreads();
+    if (local > 0 && ex <= target && target < ex + local) {
+        u64 run = ex;
+        for (int j = j0; j < min(L, j0 + per); ++j) {
+            const u64 w = row.weight(key_value((uint32_t)(sb.cand[j] >> 32)));
+            if (run + w > target) {
+                sb.s.ri[1] = j;
+                sb.s.ru[1] = run;
+                break;
+            }
+            run += w;
+        }
+    }
+    __syncthreads();
+    *before = sb.s.ru[1];
+    return sb.s.ri[1];
+}
+
+// mass of the sorted candidates [0, q)
+template <int DT, bool VEC>
+__device__ u64 sorted_mass(const Row<DT, VEC>& row, int q, ShBig& sb) {
+    u64 s = 0;
+    for (int j = threadIdx.x; j < q; j += kT) s += row.weight(key_value((uint32_t)(sb.cand[j] >> 32)));
+    u64 total;
+    block_exscan(s, sb.s, &total);
+    return total;
+}
+
+// The entry where the descending running count (BY_COUNT) or mass first
+// exceeds target; returns its index, *ahead gets the mass of the entries
+// before it.  The first-digit histogram must hold, with masses, every entry
+// down to the bin where target falls (whole bins: a histogram of the top
+// bins only serves every target below its sum).
+template <int DT, bool VEC, bool BY_COUNT>
+__device__ int desc_search(const Row<DT, VEC>& row, u64 target, ShBig& sb, u64* ahead) {
+    const Hist h0 = sb.h0(), h1 = sb.h1();
+    auto c0 = [&](int b) { return h0.count(b); };
+    auto m0 = [&](int b) { return h0.mass(b); };
+    auto c1 = [&](int b) { return h1.count(b); };
+    auto m1 = [&](int b) { return h1.mass(b); };
+    u64 a_meas;  // count or mass of the entries above the current bin
+    const int b0 = BY_COUNT ? find_bin(c0, kBins0, target, sb.s, &a_meas) : find_bin(m0, kBins0, target, sb.s, &a_meas);
+    u64 a_mass = BY_COUNT ? sum_above(m0, kBins0, b0, sb.s) : a_meas;
+    uint32_t prefix = (uint32_t)b0;
+    int shift = 20;
+    u64 count = h0.count(b0);
+    // split bins too large to gather by the next digits
+    for (int level = 1; level <= 2 && count > (u64)kMaxCand; ++level) {
+        shift -= 10;
+        build_next(row, sb, shift, prefix);
+        u64 a1;
+        const int b1 = BY_COUNT ? find_bin(c1, kBins1, target - a_meas, sb.s, &a1)
+                                : find_bin(m1, kBins1, target - a_meas, sb.s, &a1);
+        a_mass += BY_COUNT ? sum_above(m1, kBins1, b1, sb.s) : a1;
+        a_meas += a1;
+        prefix = (prefix << 10) | (uint32_t)b1;
+        count = h1.count(b1);
+    }
+    if (count <= (u64)kMaxCand) {
+        const int nc = gather_sorted(row, shift, prefix, prefix, sb);
+        int q;
+        u64 before;
+        if (BY_COUNT) {
+            q = (int)(target - a_meas);
+            before = sorted_mass(row, q, sb);
+        } else {
+            q = sorted_pick(row, nc, target - a_meas, sb, &before);
+        }
+        *ahead = a_mass + before;
+        return q >= 0 && q < nc ? cand_index(sb.cand[q]) : -1;
+    }
+    // more than kMaxCand equal logits: they share one weight, so the entry is
+    // the group's j-th in index order
+    const uint32_t key = prefix;
+    const u64 w = row.weight(key_value(key));
+    const u64 j = BY_COUNT ? target - a_meas : (target - a_meas) / w;
+    auto is_key = [&](float v) -> u64 { return v == v && order_key(v) == key ? 1ull : 0ull; };
+    u64 mine = 0;
+    row.each([&](int, float v) { mine += is_key(v); });
+    u64 total;
+    const u64 wc = warp_sum_u64(mine);
+    const u64 ex = warp_exscan(wc, sb.s, &total);
+    if (threadIdx.x == 0) sb.s.ri[2] = -1;
+    __syncthreads();
+    if (wc > 0 && ex <= j && j < ex + wc) {
+        const int idx = warp_walk(row, j - ex, is_key);
+        if (row.lane == 0) sb.s.ri[2] = idx;
+    }
+    __syncthreads();
+    *ahead = a_mass + j * w;
+    return sb.s.ri[2];
+}
+
+template <int DT, bool VEC>
+__global__ void __launch_bounds__(kT, 2)
+sample_descending(const void* x, int32_t* out, int n, int method, float t, int k, float p, const float* u) {
+    pdl_begin();
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    ShBig& sb = *reinterpret_cast<ShBig*>(smem_raw);
+    Row<DT, VEC> row;
+    setup(row, x, n, t);
+    int nv;
+    if (method == kTopK ? !first_pass<true>(row, out, sb.s, &nv) : !first_pass<false>(row, out, sb.s, &nv)) return;
+    const float ur = u[blockIdx.x];
+    // The head of the row: the first-digit bins from that of M - 24 / c down
+    // -- every entry of weight above 2^-24 of the largest (and some below).
+    // The rest of a row of n entries weighs at most n 2^-24 of the largest, so
+    // for the vocabularies in use the head carries the top-p cut of any p up
+    // to 0.99 and the top k of a moderate k; otherwise the whole row is
+    // histogrammed.
+    const uint32_t head = order_key(__fsub_rn(row.mx, __fdiv_rn(24.0f, row.c))) >> 20;
+    auto c0 = [&](int b) { return sb.h0().count(b); };
+    auto m0 = [&](int b) { return sb.h0().mass(b); };
+    if (method == kTopK) {
+        if (k < nv) {
+            build_first(row, sb, head, false, false);
+            const u64 in_head = sum_above(c0, kBins0, -1, sb.s);
+            if (in_head >= (u64)k) {
+                // the bin of the k-th entry; gather it and every bin above
+                u64 above;
+                const int b = find_bin(c0, kBins0, (u64)(k - 1), sb.s, &above);
+                if (above + sb.cnt0[b] <= (u64)kMaxCand) {
+                    gather_sorted(row, 20, (uint32_t)b, (uint32_t)(kBins0 - 1), sb);
+                    const u64 wk = sorted_mass(row, k, sb);
+                    u64 unused;
+                    const int q = sorted_pick(row, k, scaled(ur, wk), sb, &unused);
+                    if (threadIdx.x == 0) out[blockIdx.x] = q >= 0 ? cand_index(sb.cand[q]) : -1;
+                    return;
+                }
+            }
+        }
+        u64 all;
+        block_exscan(build_first(row, sb, 0u, true, true), sb.s, &all);
+        u64 kept = all;
+        if (k < nv) desc_search<DT, VEC, true>(row, (u64)k, sb, &kept);  // the entry past the k-th
+        u64 unused;
+        const int idx = desc_search<DT, VEC, false>(row, scaled(ur, kept), sb, &unused);
+        if (threadIdx.x == 0) out[blockIdx.x] = idx;
+        return;
+    }
+    // top-p: keep the prefix whose running mass stays <= p * W (the first
+    // entry always), then draw from it.  First try the top of the row: the
+    // whole first-digit bins that together hold at most kTopGather entries,
+    // gathered and sorted; when their exact mass passes the cut, the cut and
+    // the draw both fall among them.
+    u64 all;
+    block_exscan(build_first(row, sb, head, false, true), sb.s, &all);
+    const u64 cut = (u64)((double)p * (double)all);
+    const u64 in_head = sum_above(c0, kBins0, -1, sb.s);
+    int b_lo = (int)head;  // gather the bins [b_lo, top]
+    if (in_head > (u64)kTopGather) {
+        u64 above;
+        b_lo = find_bin(c0, kBins0, (u64)kTopGather, sb.s, &above) + 1;  // the bins above the one that overflows
+    }
+    u64 kept = all, unused;
+    int idx = -1;
+    bool ok = false;
+    if (b_lo < kBins0) {
+        const int nc = gather_sorted(row, 20, (uint32_t)b_lo, (uint32_t)(kBins0 - 1), sb);
+        const u64 top_mass = sorted_mass(row, nc, sb);
+        if (cut < all) {
+            if (cut < top_mass) {
+                sorted_pick(row, nc, cut, sb, &kept);
+                if (kept == 0) kept = 1;  // a target of 0 lands on the first entry
+                ok = true;
+            }
+        } else {
+            ok = true;
+        }
+        const u64 target = scaled(ur, kept);
+        if (ok && target < top_mass) {
+            const int q = sorted_pick(row, nc, target, sb, &unused);
+            idx = q >= 0 ? cand_index(sb.cand[q]) : -1;
+        } else {
+            ok = false;
+        }
+    }
+    if (!ok) {  // the exact digit histograms of the whole row
+        build_first(row, sb, 0u, true, false);
+        kept = all;
+        if (cut < all) {
+            desc_search<DT, VEC, false>(row, cut, sb, &kept);
+            if (kept == 0) kept = 1;
+        }
+        idx = desc_search<DT, VEC, false>(row, scaled(ur, kept), sb, &unused);
+    }
+    if (threadIdx.x == 0) out[blockIdx.x] = idx;
+}
+
+template <int DT, bool VEC>
+cudaError_t launch_vec(const void* x, int32_t* out, int64_t rows, int n, int method, float t, int k, float p,
+                       const float* u, cudaStream_t st) {
+    if (method == kTemperature || method == kMinP)
+        return launch(sample_index_order<DT, VEC>, dim3((unsigned)rows), dim3(kT), 0, st, x, out, n,
+                      method == kMinP ? 1 : 0, t, p, u);
+    const size_t smem = sizeof(ShBig);
+    const cudaError_t e =
+        cudaFuncSetAttribute(sample_descending<DT, VEC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return e;
+    }
+    return launch(sample_descending<DT, VEC>, dim3((unsigned)rows), dim3(kT), smem, st, x, out, n, method, t, k, p, u);
 }
 
 template <int DT>
 cudaError_t launch_dt(const void* x, int32_t* out, int64_t rows, int n, int method, float t, int k, float p,
                       const float* u, bool vec, cudaStream_t st) {
-    if (vec) return launch(sample_rows<DT, true>, dim3((unsigned)rows), dim3(kT), 0, st, x, out, n, method, t, k, p, u);
-    return launch(sample_rows<DT, false>, dim3((unsigned)rows), dim3(kT), 0, st, x, out, n, method, t, k, p, u);
+    if (vec) return launch_vec<DT, true>(x, out, rows, n, method, t, k, p, u, st);
+    return launch_vec<DT, false>(x, out, rows, n, method, t, k, p, u, st);
 }
 
 }  // namespace

@@ -284,19 +284,20 @@ typedef enum gbe_sample_method {
  *   distribution's order (index order for TEMPERATURE and MIN_P, descending
  *   logit with equal logits by ascending index for TOP_K and TOP_P), whose
  *   running sum exceeds u[r] times the sum of the kept entries.
- *   Arithmetic: e = expf(x / t - max(x) / t) in f32, each e held as the
- *   integer rn(e * 2^40); sums and cuts are exact integer arithmetic on those
- *   weights, so the result is deterministic and independent of the batch.
- *   It equals an f32 evaluation of the definition except where u[r] falls
- *   within rounding of a boundary between two entries (or an entry sits
- *   within rounding of a cut), where either neighbour is a valid draw.
+ *   Arithmetic: e = exp2f((x - max(x)) * (log2(e) / t)) in f32 (e = 1 at the
+ *   maximum), each e held as the integer rn(e * 2^40); sums and cuts are
+ *   exact integer arithmetic on those weights, so the result is
+ *   deterministic and independent of the batch.  It equals an exact
+ *   evaluation of the definition except where u[r] falls within rounding of
+ *   a boundary between two entries (or an entry sits within rounding of a
+ *   cut), where either neighbour is a valid draw.
  *   NaN logits take no part; a row with no number, or whose largest x / t is
  *   not finite (+inf in the row, or an overflow of x / t), gives -1.
  * x : [rows, n] row-major, dtype; u : f32[rows], uniforms in [0, 1) (values
  * outside are clamped: u <= 0 takes the first kept entry, u >= 1 the last);
  * out : int32[rows], which overlaps nothing else.  n in [1, 2^23]; rows of
- * length 0 are GBE_ERR_EMPTY.  temperature > 0 (+inf allowed: every logit
- * equal), top_k >= 1 (larger than n keeps all), p in [0, 1]; otherwise
+ * length 0 are GBE_ERR_EMPTY.  temperature finite and > 0, top_k >= 1
+ * (larger than n keeps all), p in [0, 1]; otherwise
  * GBE_ERR_SAMPLING.  u is read only by methods other than GREEDY, and may be
  * NULL for GREEDY.
  */

@@ -133,7 +133,7 @@ def test_sample_rejects_bad_arguments(L):
     def call(rows=4, n=100, method=1, t=1.0, k=5, p=0.5, dtype=1):
         return L.gbe_sample(NULL, NULL, NULL, rows, n, method, t, k, p, dtype, S)
     assert call(method=5) == 12 and call(method=-1) == 12
-    assert call(t=0.0) == 12 and call(t=-1.0) == 12 and call(t=float("nan")) == 12
+    assert call(t=0.0) == 12 and call(t=-1.0) == 12 and call(t=float("nan")) == 12 and call(t=float("inf")) == 12
     assert call(method=2, k=0) == 12 and call(method=2, k=-3) == 12
     for m in (3, 4):
         assert call(method=m, p=-0.1) == 12 and call(method=m, p=1.5) == 12 and call(method=m, p=float("nan")) == 12

@@ -13,7 +13,9 @@ within rounding of a top-p / min-p cut.  The bar:
   * such rows are few (MAX_MISS of the rows);
   * on flat rows of 152k entries, where the oracle's f32 running sums drift
     across boundaries, every draw is held to the float64 distribution within
-    1e-7 (the kernel's sums are exact);
+    2e-6 (the kernel's sums are exact; its weights carry a few f32 roundings
+    of the exponent, log2(e) / t among them, which shift the whole CDF by at
+    most |x - max| / t * 1e-7 of the mass);
   * exact limits: top_k = 1 and top_p = 0 give the argmax; min_p = 0 gives
     the temperature draw; a row with no number, or with +inf, gives -1.
 DELTA = 1e-5 of the kept mass covers the f32 running sums of rows of up to
@@ -121,13 +123,13 @@ def test_flat_wide_rows(method, kw):
     """Flat logits over 152064 entries, f32, with NaN and exact ties: every
     entry carries mass, so boundaries lie ~1e-5 apart and the oracle's f32
     running sums drift across several of them.  Here every draw is held to
-    the float64 distribution itself, within 1e-7 of the kept mass."""
+    the float64 distribution itself, within 2e-6 of the kept mass."""
     x = _logits(24, 152064, "f32", std=0.5, nan_frac=0.001, tag="flat")
     x[:, 100:200] = x[:, 1000:1100]
     u = _u(24, f"flat.{method}")
     got = gbe.sample(to_dev(x), torch.from_numpy(u).cuda(), method, **kw).cpu().numpy()
     for r in range(24):
-        assert _valid_draw(x[r], float(u[r]), method, kw, int(got[r]), 1e-7), (method, r, u[r], got[r])
+        assert _valid_draw(x[r], float(u[r]), method, kw, int(got[r]), 2e-6), (method, r, u[r], got[r])
 
 
 def test_draws_in_proportion():
@@ -250,3 +252,46 @@ def test_refusals_on_device():
     assert torch.equal(out, gbe.argmax(x))
     with pytest.raises(gbe.GbeError):
         gbe.sample(x, u, "top_k", temperature=1.0, top_k=0)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_search_paths(dtype):
+    """The less common routes of the descending search: top-k past the
+    gather limit (the full histogram, split by the next digits), top-p with
+    p = 1 and p = 0.999 (the cut past the head of the row), groups of more
+    equal logits than the gather limit (walked in index order), and a row of
+    a few repeated values.  Over tens of thousands of equal probabilities the
+    oracle's f32 running sums drift by more than one entry, so here any row
+    may differ from it, and every draw is held to the float64 distribution
+    (within DELTA of a boundary)."""
+    rows, n = 6, 65536
+    x = _logits(rows, n, dtype, std=1.0, tag="paths")
+    x32 = widen(x)
+    x32[2] = 0.75                                              # one value: a single group of n
+    x32[3] = np.floor(units(31, "paths.rep", n) * 3) / 8.0     # three values, ~n/3 each
+    x32[4, : n // 2] = 0.5                                     # half tied at the top
+    x = to_bf16(x32) if dtype == "bf16" else x32
+    u = _u(rows, "paths")
+    for method, kw in (("top_k", dict(temperature=1.0, top_k=20000)), ("top_k", dict(temperature=0.5, top_k=5000)),
+                       ("top_k", dict(temperature=1.0, top_k=3)), ("top_p", dict(temperature=1.0, p=1.0)),
+                       ("top_p", dict(temperature=0.8, p=0.999)), ("top_p", dict(temperature=1.0, p=0.5)),
+                       ("top_p", dict(temperature=2.0, p=0.2))):
+        _check(x, u, method, kw, f"{method} {kw} {dtype}", max_miss=1.0)
+
+
+def test_equal_logits_exact():
+    """8192 equal logits (a group larger than the gather limit): every
+    method reduces to a uniform draw over a prefix in index order, and with a
+    power-of-two count the oracle's f32 sums are exact, so the draws match
+    exactly."""
+    n = 8192
+    x = np.full((8, n), 1.5, np.float32)
+    u = _u(8, "equal")
+    xd = to_dev(x)
+    ud = torch.from_numpy(u).cuda()
+    for method, kw, m in (("temperature", dict(temperature=1.0), n), ("top_k", dict(temperature=1.0, top_k=4096), 4096),
+                          ("top_p", dict(temperature=1.0, p=0.5), 4096), ("min_p", dict(temperature=1.0, p=0.5), n)):
+        got = gbe.sample(xd, ud, method, **kw).cpu().numpy()
+        want = np.floor(u.astype(np.float64) * m).astype(np.int64)
+        assert np.array_equal(got, want), (method, got, want)
+        assert np.array_equal(got, _oracle(x, u, method, kw)), method
