@@ -28,8 +28,10 @@
 // holds tile entries [l V, l V + V)), so index order is warp, tile, lane,
 // element.  The first pass reads HBM; later ones hit L2.
 //  * temperature, min-p (index order): pass 1 the maximum, pass 2 each
-//    warp's kept mass; the warp holding the target walks its segment tile by
-//    tile with warp scans.
+//    warp's kept mass in units of V consecutive entries (their e summed in
+//    f32, the unit sum held as a fixed-point integer); the warp holding the
+//    target walks its segment tile by tile with warp scans, then the unit's
+//    own partial sums.
 //  * top-k, top-p (descending order): an order-keeping 32-bit key of each
 //    logit is split into 12 / 10 / 10-bit digits.  A 4096-bin histogram of
 //    the first digit (counts, and for top-p masses) locates the bin where the
@@ -344,36 +346,79 @@ __device__ __forceinline__ bool first_pass(Row<DT, VEC>& row, int32_t* out, Sh& 
     return true;
 }
 
-template <int DT, bool VEC>
+// Index order works on units: a lane's V consecutive entries of one tile.
+// A unit's e (0 for NaN and, under min-p, for e < p) are summed in f32 in
+// index order, and the partial sum s_j after its j-th entry is held as
+// fixed40(s_j); the unit's weight is fixed40(s_{V-1}).  Unit weights are
+// exact integers, so the warp and block sums are order-free; inside the unit
+// the drawn entry is the first j with fixed40(s_j) above the residual target
+// -- fixed40 is monotone and s_j never decreases, so the walk that recomputes
+// the same partial sums always finds it.  Entry j thus weighs
+// fixed40(s_j) - fixed40(s_{j-1}), e_j * 2^40 up to one f32 rounding of s_j.
+template <int DT, bool VEC, bool MINP>
+__device__ __forceinline__ float kept_e(const Row<DT, VEC>& row, float v, float p) {
+    const float e = row.e_of(v);          // NaN for NaN
+    return MINP ? (e >= p ? e : 0.0f)     // NaN fails the test
+                : fmaxf(e, 0.0f);         // NaN gives 0
+}
+
+template <int DT, bool VEC, bool MINP>
 __global__ void __launch_bounds__(kT, 2)
-sample_index_order(const void* x, int32_t* out, int n, int minp, float t, float p, const float* u) {
+sample_index_order(const void* x, int32_t* out, int n, float t, float p, const float* u) {
+    constexpr int V = Row<DT, VEC>::V;
+    constexpr int kTile = Row<DT, VEC>::kTile;
     pdl_begin();
     __shared__ Sh sh;
     Row<DT, VEC> row;
     setup(row, x, n, t);
     int nv;
     if (!first_pass<false>(row, out, sh, &nv)) return;
-    const float pmin = minp ? p : 0.0f;  // e >= 0 holds for every number
-    MassAcc acc;
-    row.each(
-        [&](int, float v) {
-            if (v != v) return;
-            const float e = row.e_of(v);
-            if (e >= pmin) acc.add(e);
-        },
-        [&] { acc.fold(); });
+    auto unit = [&](const float (&v)[V]) -> u64 {
+        float s = 0.0f;
+#pragma unroll
+        for (int e = 0; e < V; ++e) s = __fadd_rn(s, kept_e<DT, VEC, MINP>(row, v[e], p));
+        return fixed40(s);
+    };
+    u64 mine = 0;
+    for (int j0 = row.s0; j0 < row.s1; j0 += kTile * kU) {
+        float v[kU][V];
+#pragma unroll
+        for (int q = 0; q < kU; ++q) row.load(j0 + q * kTile, v[q]);
+#pragma unroll
+        for (int q = 0; q < kU; ++q) mine += unit(v[q]);
+    }
     u64 total;
-    const u64 wmass = warp_sum_u64(acc.total());
+    const u64 wmass = warp_sum_u64(mine);
     const u64 ex = warp_exscan(wmass, sh, &total);
     const u64 target = scaled(u[blockIdx.x], total);
-    if (wmass > 0 && ex <= target && target < ex + wmass) {
-        auto meas = [&](float v) -> u64 {
-            if (v != v) return 0ull;
-            const float e = row.e_of(v);
-            return e >= pmin ? row.w_of(e) : 0ull;
-        };
-        const int idx = warp_walk(row, target - ex, meas);
-        if (row.lane == 0) out[blockIdx.x] = idx;
+    if (!(wmass > 0 && ex <= target && target < ex + wmass)) return;
+    // this warp holds the target: walk its tiles
+    const u64 want = target - ex;
+    u64 run = 0;
+    for (int j = row.s0; j < row.s1; j += kTile) {
+        float v[V];
+        row.load(j, v);
+        const u64 w = unit(v);
+        const u64 inc = warp_incl_scan_u64(w, row.lane);
+        const u64 tot = __shfl_sync(kFull, inc, 31);
+        if (run + tot > want) {
+            int found = -1;
+            const u64 before = run + inc - w;
+            if (before <= want && want < run + inc) {
+                const u64 r = want - before;
+                float s = 0.0f;
+#pragma unroll
+                for (int e = 0; e < V; ++e) {
+                    s = __fadd_rn(s, kept_e<DT, VEC, MINP>(row, v[e], p));
+                    if (found < 0 && fixed40(s) > r) found = j + row.lane * V + e;
+                }
+            }
+            const unsigned who = __ballot_sync(kFull, found >= 0);
+            const int idx = __shfl_sync(kFull, found, who ? __ffs(who) - 1 : 0);
+            if (row.lane == 0) out[blockIdx.x] = idx;
+            return;
+        }
+        run += tot;
     }
 }
 
@@ -759,9 +804,10 @@ sample_descending(const void* x, int32_t* out, int n, int method, float t, int k
 template <int DT, bool VEC>
 cudaError_t launch_vec(const void* x, int32_t* out, int64_t rows, int n, int method, float t, int k, float p,
                        const float* u, cudaStream_t st) {
-    if (method == kTemperature || method == kMinP)
-        return launch(sample_index_order<DT, VEC>, dim3((unsigned)rows), dim3(kT), 0, st, x, out, n,
-                      method == kMinP ? 1 : 0, t, p, u);
+    if (method == kTemperature)
+        return launch(sample_index_order<DT, VEC, false>, dim3((unsigned)rows), dim3(kT), 0, st, x, out, n, t, p, u);
+    if (method == kMinP)
+        return launch(sample_index_order<DT, VEC, true>, dim3((unsigned)rows), dim3(kT), 0, st, x, out, n, t, p, u);
     const size_t smem = sizeof(ShBig);
     const cudaError_t e =
         cudaFuncSetAttribute(sample_descending<DT, VEC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

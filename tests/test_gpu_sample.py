@@ -1,7 +1,9 @@
 """Sampling on the GPU against the oracle, through the C ABI.
 
 The oracle evaluates the definition in f32 (running sums in the
-distribution's order); the kernel sums exact fixed-point weights.  Both are
+distribution's order); the kernel sums fixed-point weights exactly (per
+entry for top-k / top-p, per unit of 4 or 8 consecutive entries summed in
+f32 for temperature / min-p).  Both are
 the inverse CDF at the same u, so they pick the same entry except where u
 lies within rounding of a boundary between two entries, or an entry sits
 within rounding of a top-p / min-p cut.  The bar:
