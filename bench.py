@@ -84,6 +84,8 @@ def op_bytes(op: str, arrays: dict, params: dict) -> tuple[int, int]:
                 + 4 * (params["r"] // 2)), params["T"]
     if op == "layernorm":
         return 2 * nb(arrays["x"]) + nb(arrays["g"]) + nb(arrays["b"]), params["rows"]
+    if op == "rope_multi":
+        return 2 * nb(arrays["x"]) + nb(arrays["pos"]) + nb(arrays["inv_freq"]), params["T"]
     if op == "rope_qk_half_cached":
         T, r = params["T"], params["r"]
         return 2 * (nb(arrays["q"]) + nb(arrays["k"])) + nb(arrays["pos"]) + T * (r // 2) * 8, T
@@ -190,8 +192,9 @@ def combine(op: str, parts):
     return parts[0]
 
 
-EXTRA = ("qk_norm_rope", "rope_qk_half_cached", "layernorm", "sample_temperature", "sample_top_k", "sample_top_p",
-         "sample_min_p")
+EXTRA = ("qk_norm_rope", "rope_qk_half_cached", "layernorm", "rope_multi", "sample_temperature", "sample_top_k",
+         "sample_top_p", "sample_min_p")
+MULTI_DIMS = (32, 48, 48)  # multi-axis RoPE: (t, h, w) slices of head_dim 128
 SAMPLING = {"sample_temperature": ("temperature", dict(temperature=0.7)),
             "sample_top_k": ("top_k", dict(temperature=0.7, top_k=50)),
             "sample_top_p": ("top_p", dict(temperature=0.7, p=0.9)),
@@ -202,7 +205,9 @@ def build_extra_inputs(tokens: int = 8192):
     """Inputs of the ops beyond the step, at the same prefill shapes: QK-norm
     then RoPE on q [T, 32, 128] and k [T, 8, 128] (gains U(0.5, 1.5)); RoPE of
     q and k driven by a cos/sin table of 8192 positions; LayerNorm of
-    [T, 4096] with gain and bias; one draw per row of the logits
+    [T, 4096] with gain and bias; multi-axis RoPE of x [T, 24, 128] bf16 in
+    (t, h, w) slices of 32, 48, 48 (positions below 64, 256, 256, base
+    10000 per axis); one draw per row of the logits
     [T, 128256] by each sampling method at a uniform u per row."""
     import synth
     from synth import workloads as W
@@ -215,6 +220,11 @@ def build_extra_inputs(tokens: int = 8192):
     qk = {"q": aq["x"], "k": ak["x"], "pos": aq["pos"], "inv_freq": aq["inv_freq"]}
     ax, px = cases["rmsnorm"](rows=rows)
     lb = synth.normal_bf16(seed, "layernorm.b", (ax["x"].shape[1],), 0.0, 0.2)
+    T = ax["x"].shape[0]
+    xm = synth.normal_bf16(seed, "rope_multi.x", (T, 24, 128), 0.0, 1.0)
+    pm = np.stack([synth.randint(seed, f"rope_multi.pos{a}", (T,), 0, hi)
+                   for a, hi in enumerate((64, 256, 256))], axis=1).astype(np.int32)
+    fm = np.concatenate([(10000.0 ** (-2.0 * np.arange(d // 2) / d)).astype(np.float32) for d in MULTI_DIMS])
     al, pl = cases["argmax"](rows=rows)
     u = synth.units(seed, "sample.u", al["x"].shape[0]).astype(np.float32)
     sampling = {op: ({"x": al["x"], "u": u}, dict(pl, method=m, kw=kw)) for op, (m, kw) in SAMPLING.items()}
@@ -222,6 +232,7 @@ def build_extra_inputs(tokens: int = 8192):
         "qk_norm_rope": (dict(qk, gq=gq, gk=gk), dict(pq, eps=1e-6)),
         "rope_qk_half_cached": (dict(qk), dict(pq, cache_len=8192)),
         "layernorm": ({"x": ax["x"], "g": ax["w"], "b": lb}, px),
+        "rope_multi": ({"x": xm, "pos": pm, "inv_freq": fm}, {"T": T, "dims": MULTI_DIMS, "mu": 1.0, "layout": 0}),
         **sampling,
     }
 
@@ -459,6 +470,8 @@ def run_op(gbe, op, p, b, o):
         gbe.gbe_rmsnorm(b["x"], b["w"], o, p["eps"])
     elif op == "layernorm":
         gbe.gbe_layernorm(b["x"], b["g"], b["b"], o, p["eps"])
+    elif op == "rope_multi":
+        gbe.gbe_rope_multi(b["x"], o, b["pos"], p["dims"], b["inv_freq"], p["mu"], p["layout"])
     elif op == "argmax":
         gbe.gbe_argmax(b["x"], o)
     elif op.startswith("sample_"):
@@ -575,7 +588,9 @@ def dram_traffic(op: str):
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
-    want = sources_hash()
+    if op not in SOURCE_OF:
+        return None
+    want = sources_hash(op)
     for line in open(path):
         parts = line.split()
         if len(parts) == 3 and not line.startswith("#") and parts[0] == op and parts[2] == want:
@@ -583,11 +598,20 @@ def dram_traffic(op: str):
     return None
 
 
-def sources_hash() -> str:
+SOURCE_OF = {  # op -> the source file of its kernel and launcher
+    "embedding": "embedding.cu", "add_rmsnorm": "rmsnorm.cu", "rope_qk_half": "rope.cu",
+    "rope_qk_interleaved": "rope.cu", "silu_mul": "pointwise.cu", "add": "pointwise.cu",
+    "rmsnorm": "rmsnorm.cu", "argmax": "argmax.cu",
+}
+
+
+def sources_hash(op: str) -> str:
+    """Hash of the sources that decide an op's kernel: its own file and the
+    shared device helpers."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "elementwise_row_rmsnorm_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in ("common.cuh", SOURCE_OF[op]):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
