@@ -217,7 +217,8 @@ rope_scalar(Operand A, Operand B, const int32_t* pos, int64_t T, int D, int r, c
 // Out of place, tail threads copy the entries past the last slice.
 template <int DT, int LAYOUT>
 __global__ void __launch_bounds__(kThreads)
-rope_multi_kernel(const void* x, void* y, const int32_t* pos, int64_t T, int H, int D, MultiAxis ax,
+rope_multi_kernel(const void* x, void* y, const int32_t* pos, int64_t T, int H, int D,
+                  const __grid_constant__ MultiAxis ax,
                   const float* inv_freq, float mu, int copy_tail) {
     using S = Store<DT>;
     constexpr int64_t ES = sizeof(typename S::T);
@@ -255,6 +256,104 @@ rope_multi_kernel(const void* x, void* y, const int32_t* pos, int64_t T, int H, 
             else
                 static_cast<uint16_t*>(y)[o] = static_cast<const uint16_t*>(x)[o];
         }
+    }
+}
+
+// Multi-axis, aligned path (every slice offset and width, and D, split into
+// 16-byte vectors).  rope_vec's map with items drawn from all slices: a
+// thread owns one item (P pairs of one slice) of one token for a chunk of up
+// to four heads, loads all of them first, forms the P angles from its
+// slice's position and frequencies while they are in flight, then rotates
+// and stores.  Item g belongs to the slice whose item range holds it.
+template <int DT, int LAYOUT>
+__global__ void __launch_bounds__(kThreads)
+rope_multi_vec(const char* x, char* y, const int32_t* pos, int64_t T, int H, int D,
+               const __grid_constant__ MultiAxis ax,
+               const float* inv_freq, float mu, int copy_tail, int G, int NC) {
+    using S = Store<DT>;
+    constexpr int V = S::V;
+    constexpr int P = LAYOUT == 0 ? V : V / 2;  // pairs per 16-byte item
+    constexpr int64_t ES = sizeof(typename S::T);
+    constexpr int HC = kHeadsPerThread;
+    pdl_begin();
+    const int64_t gt = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int g = (int)(gt % G);
+    const int64_t rest = gt / G;
+    const int hc = (int)(rest % NC);
+    const int64_t t = rest / NC;
+    if (t >= T) return;
+    // the slice of item g and the item's first pair within it
+    int a = 0, first = 0;
+    for (;;) {
+        const int items = (ax.poff[a + 1] - ax.poff[a]) / P;
+        if (g < first + items || a + 1 == ax.A) break;
+        first += items;
+        ++a;
+    }
+    const int half = ax.poff[a + 1] - ax.poff[a];
+    const int i0 = (g - first) * P;  // first pair of the item within its slice
+    const int h0 = hc * HC;
+    const int nh = min(HC, H - h0);
+    const int64_t hd = (int64_t)D * ES;
+    const char* xr = x + (t * H + h0) * hd;
+    char* yr = y + (t * H + h0) * hd;
+    const int64_t ia = ((int64_t)ax.off[a] + (LAYOUT == 0 ? i0 : 2 * i0)) * ES;
+    const int64_t hb = (int64_t)half * ES;
+
+    Vec16 va[HC], vb[HC];
+#pragma unroll
+    for (int j = 0; j < HC; ++j) {
+        if (j < nh) {
+            va[j] = ld_stream(xr + j * hd + ia);
+            if (LAYOUT == 0) vb[j] = ld_stream(xr + j * hd + ia + hb);
+        }
+    }
+    float c[P], sn[P];
+    const float p = (float)pos[t * ax.A + a];
+    const int k0 = ax.poff[a] + i0;
+#pragma unroll
+    for (int e = 0; e < P; ++e) sincosf(__fmul_rn(p, __ldg(inv_freq + k0 + e)), &sn[e], &c[e]);
+
+#pragma unroll
+    for (int j = 0; j < HC; ++j) {
+        if (j < nh) {
+            char* q = yr + j * hd + ia;
+            float fa[V];
+            S::unpack(va[j], fa);
+            if (LAYOUT == 0) {
+                float fb[V];
+                S::unpack(vb[j], fb);
+#pragma unroll
+                for (int e = 0; e < V; ++e) {
+                    float a2, b2;
+                    rotate(fa[e], fb[e], c[e], sn[e], mu, a2, b2);
+                    fa[e] = a2;
+                    fb[e] = b2;
+                }
+                st_stream(q, S::pack(fa));
+                st_stream(q + hb, S::pack(fb));
+            } else {
+#pragma unroll
+                for (int e = 0; e < P; ++e) {
+                    float a2, b2;
+                    rotate(fa[2 * e], fa[2 * e + 1], c[e], sn[e], mu, a2, b2);
+                    fa[2 * e] = a2;
+                    fa[2 * e + 1] = b2;
+                }
+                st_stream(q, S::pack(fa));
+            }
+        }
+    }
+    // entries past the last slice, out of place only: the G threads of this
+    // token and head chunk share the tail vectors of each head
+    if (copy_tail) {
+        const int rot = 2 * ax.poff[ax.A];
+        const int GT = (D - rot) / V;
+        for (int j = 0; j < nh; ++j)
+            for (int k = g; k < GT; k += G) {
+                const int64_t o = j * hd + ((int64_t)rot + (int64_t)k * V) * ES;
+                st_stream(yr + o, ld_stream(xr + o));
+            }
     }
 }
 
@@ -334,8 +433,34 @@ cudaError_t launch_rope_multi(const void* x, void* y, const int32_t* pos, int64_
     const int copy_tail = (x != y && 2 * npairs < D) ? 1 : 0;
     const int64_t per_tok = npairs + (copy_tail ? D - 2 * npairs : 0);
     if (per_tok == 0 || T == 0 || H == 0) return cudaSuccess;
-    const dim3 grid((unsigned)((T * per_tok + kThreads - 1) / kThreads));
     const int Hi = (int)H, Di = (int)D;
+    // the aligned path: both pointers 16-byte aligned, D and every slice's
+    // offset and item width in whole 16-byte vectors
+    const int V = dtype == kF32 ? 4 : 8;
+    bool vec = npairs > 0 && ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0 &&
+               D % V == 0;
+    int G = 0;
+    for (int a = 0; a < ax.A && vec; ++a) {
+        const int half = ax.poff[a + 1] - ax.poff[a];
+        const int P = layout == 0 ? V : V / 2;
+        vec = ax.off[a] % V == 0 && half % P == 0;
+        G += half / P;
+    }
+    if (vec) {
+        const int NC = (Hi + kHeadsPerThread - 1) / kHeadsPerThread;
+        const dim3 grid((unsigned)((T * NC * G + kThreads - 1) / kThreads));
+        const char* xc = static_cast<const char*>(x);
+        char* yc = static_cast<char*>(y);
+#define GBE_MULTI(D_, L_)                                                                                        \
+    return launch(rope_multi_vec<D_, L_>, grid, dim3(kThreads), 0, st, xc, yc, pos, T, Hi, Di, ax, inv_freq, mu, \
+                  copy_tail, G, NC)
+        if (dtype == kF32) {
+            if (layout == 0) GBE_MULTI(kF32, 0); else GBE_MULTI(kF32, 1);
+        }
+        if (layout == 0) GBE_MULTI(kBF16, 0); else GBE_MULTI(kBF16, 1);
+#undef GBE_MULTI
+    }
+    const dim3 grid((unsigned)((T * per_tok + kThreads - 1) / kThreads));
     if (dtype == kF32) {
         if (layout == 0)
             return launch(rope_multi_kernel<kF32, 0>, grid, dim3(kThreads), 0, st, x, y, pos, T, Hi, Di, ax, inv_freq,
