@@ -237,6 +237,23 @@ def build_extra_inputs(tokens: int = 8192):
     }
 
 
+def build_workload_inputs(workload: str):
+    """Per-op inputs of the other workloads, for --isolated: the f32 RoPE
+    variants (each operand rotated in place), the wide f32 argmax and
+    RMSNorm, and the decode step's ops (T = 64, launch-latency bound)."""
+    from synth import workloads as W
+    cases = W.cases(workload)
+    if workload == W.ROPE_VARIANTS:
+        return {"rope_q_inplace": cases["rope_q"](), "rope_k_inplace": cases["rope_k"]()}
+    if workload == W.WIDE:
+        return {"argmax": cases["argmax"](), "rmsnorm": cases["rmsnorm"]()}
+    if workload == W.DECODE:
+        rope = combine("rope_qk_half", [cases["rope_q"](), cases["rope_k"]()])
+        return {"add_rmsnorm": cases["add_rmsnorm"](), "rope_qk_half": rope, "silu_mul": cases["silu_mul"](),
+                "argmax": cases["argmax"]()}
+    raise KeyError(workload)
+
+
 def build_inputs(tokens: int = 8192):
     """The step's inputs; `tokens` < 8192 takes the first rows of every op (a
     smaller case of the same kernels, for profiling)."""
@@ -383,10 +400,16 @@ def run_isolated(args):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
     gbe.lib()
-    data = build_inputs(args.tokens)
-    if args.extra or (args.keep and args.keep & set(EXTRA)):
-        extra = build_extra_inputs(args.tokens)
-        data.update({op: v for op, v in extra.items() if not args.keep or op in args.keep})
+    workload = args.workload or WORKLOAD
+    if workload != WORKLOAD:
+        data = build_workload_inputs(workload)
+    else:
+        data = build_inputs(args.tokens)
+        if args.extra or (args.keep and args.keep & set(EXTRA)):
+            extra = build_extra_inputs(args.tokens)
+            data.update({op: v for op, v in extra.items() if not args.keep or op in args.keep})
+    if args.keep:
+        data = {op: v for op, v in data.items() if op in args.keep}
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     res = {}
     for op in list(data):
@@ -424,7 +447,8 @@ def run_isolated(args):
     for v in res.values():
         v["frac_of_peak"] = round(v["gbs"] / peak, 4)
         v["frac_of_8tbs"] = round(v["gbs"] / NOMINAL_HBM_GBS, 4)
-    line = {"mode": "isolated", "workload": WORKLOAD if args.tokens >= 8192 else f"{WORKLOAD} (first {args.tokens} tokens)",
+    name = workload if workload != WORKLOAD or args.tokens >= 8192 else f"{WORKLOAD} (first {args.tokens} tokens)"
+    line = {"mode": "isolated", "workload": name,
             "unit": "GB/s", "peak": peak, "peak_source": kind, "per_op": res}
     print(json.dumps(line), flush=True)
     return line
@@ -444,6 +468,8 @@ def make_outputs(torch, dev, op, b):
         return (torch.empty_like(b["x"]), torch.empty_like(b["x"]))
     if op.startswith("rope_qk") or op == "qk_norm_rope":
         return (torch.empty_like(b["q"]), torch.empty_like(b["k"]))
+    if op.endswith("_inplace"):
+        return b["x"]
     if op == "argmax" or op.startswith("sample_"):
         return torch.empty((b["x"].shape[0],), dtype=torch.int32, device=dev)
     return torch.empty_like(b["x"] if "x" in b else (b["gate"] if "gate" in b else b["a"]))
@@ -470,6 +496,8 @@ def run_op(gbe, op, p, b, o):
         gbe.gbe_rmsnorm(b["x"], b["w"], o, p["eps"])
     elif op == "layernorm":
         gbe.gbe_layernorm(b["x"], b["g"], b["b"], o, p["eps"])
+    elif op.startswith("rope") and op.endswith("_inplace"):
+        gbe.gbe_rope(b["x"], b["x"], b["pos"], b["inv_freq"], p["r"], p["mu"], p["layout"])
     elif op == "rope_multi":
         gbe.gbe_rope_multi(b["x"], o, b["pos"], p["dims"], b["inv_freq"], p["mu"], p["layout"])
     elif op == "argmax":
@@ -743,15 +771,18 @@ def main(argv=None):
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--isolated", action="store_true",
                     help="time each op alone, back to back over rotating buffers, and print that instead")
+    ap.add_argument("--workload", default="",
+                    help="with --isolated: another workload's ops (rope-variants-T4096-f32, wide-argmax-rmsnorm-f32, "
+                         "llama3-8b-decode-T64-bf16)")
     ap.add_argument("--extra", action="store_true",
                     help="with --isolated: also time the ops beyond the step (QK-norm+RoPE, table-driven RoPE, "
-                         "LayerNorm)")
+                         "LayerNorm, multi-axis RoPE, sampling)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
     keep = None
     if args.ops:
         keep = set(args.ops.split(","))
-        unknown = keep - {op for op, _ in STEP} - set(EXTRA)
+        unknown = keep - {op for op, _ in STEP} - set(EXTRA) - {"rope_q_inplace", "rope_k_inplace"}
         if unknown:
             ap.error(f"unknown ops {sorted(unknown)}")
         if keep & set(EXTRA) and not args.isolated:

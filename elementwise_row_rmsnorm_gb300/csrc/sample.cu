@@ -705,6 +705,44 @@ __device__ int desc_search(const Row<DT, VEC>& row, u64 target, ShBig& sb, u64* 
     return sb.s.ri[2];
 }
 
+// Top-p's second pass: the count histogram of the head (the first-digit
+// bins from `from` up), and this thread's share of the row's total mass,
+// summed as the index-order kernel sums it (f32 unit sums, each held in
+// fixed point).  That total only sets the cut p * W, so it need not equal
+// the sum of the per-entry weights the walks use; the exact fallback takes
+// its own total from its histogram.
+template <int DT, bool VEC>
+__device__ u64 head_counts_and_mass(const Row<DT, VEC>& row, ShBig& sb, uint32_t from) {
+    constexpr int V = Row<DT, VEC>::V;
+    constexpr int kTile = Row<DT, VEC>::kTile;
+    const Hist h = sb.h0();
+    const float x_from = key_floor((u64)from << 20);
+    __syncthreads();
+    h.clear();
+    __syncthreads();
+    u64 tot = 0;
+    for (int j0 = row.s0; j0 < row.s1; j0 += kTile * kU) {
+        float v[kU][V];
+#pragma unroll
+        for (int q = 0; q < kU; ++q) row.load(j0 + q * kTile, v[q]);
+#pragma unroll
+        for (int q = 0; q < kU; ++q) {
+            float s = 0.0f;
+#pragma unroll
+            for (int e = 0; e < V; ++e) {
+                s = __fadd_rn(s, fmaxf(row.e_of(v[q][e]), 0.0f));  // NaN gives 0
+                if (v[q][e] >= x_from) {
+                    const uint32_t d = order_key(v[q][e]) >> 20;
+                    if (d >= from) atomicAdd(&h.cnt[d], 1u);
+                }
+            }
+            tot += fixed40(s);
+        }
+    }
+    __syncthreads();
+    return tot;
+}
+
 template <int DT, bool VEC>
 __global__ void __launch_bounds__(kT, 2)
 sample_descending(const void* x, int32_t* out, int n, int method, float t, int k, float p, const float* u) {
@@ -758,7 +796,7 @@ sample_descending(const void* x, int32_t* out, int n, int method, float t, int k
     // gathered and sorted; when their exact mass passes the cut, the cut and
     // the draw both fall among them.
     u64 all;
-    block_exscan(build_first(row, sb, head, false, true), sb.s, &all);
+    block_exscan(head_counts_and_mass(row, sb, head), sb.s, &all);
     const u64 cut = (u64)((double)p * (double)all);
     const u64 in_head = sum_above(c0, kBins0, -1, sb.s);
     int b_lo = (int)head;  // gather the bins [b_lo, top]
@@ -789,11 +827,13 @@ sample_descending(const void* x, int32_t* out, int n, int method, float t, int k
             ok = false;
         }
     }
-    if (!ok) {  // the exact digit histograms of the whole row
+    if (!ok) {  // the exact digit histograms of the whole row, with its own total
         build_first(row, sb, 0u, true, false);
-        kept = all;
-        if (cut < all) {
-            desc_search<DT, VEC, false>(row, cut, sb, &kept);
+        const u64 exact = sum_above(m0, kBins0, -1, sb.s);
+        const u64 cut_x = (u64)((double)p * (double)exact);
+        kept = exact;
+        if (cut_x < exact) {
+            desc_search<DT, VEC, false>(row, cut_x, sb, &kept);
             if (kept == 0) kept = 1;
         }
         idx = desc_search<DT, VEC, false>(row, scaled(ur, kept), sb, &unused);
