@@ -434,12 +434,32 @@ def run_isolated(args):
         n = max(50, 4 * sets)
         a = torch.cuda.Event(enable_timing=True)
         e = torch.cuda.Event(enable_timing=True)
-        a.record()
-        for i in range(n):
-            go(*rings[i % sets])
-        e.record()
-        torch.cuda.synchronize()
-        ms = a.elapsed_time(e) / n
+        if args.graph:
+            # the n launches captured once into a CUDA graph, timed over replays
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=side):
+                for i in range(n):
+                    go(*rings[i % sets])
+            for _ in range(3):
+                graph.replay()
+            torch.cuda.synchronize()
+            reps = 10
+            a.record()
+            for _ in range(reps):
+                graph.replay()
+            e.record()
+            torch.cuda.synchronize()
+            ms = a.elapsed_time(e) / (n * reps)
+            del graph
+        else:
+            a.record()
+            for i in range(n):
+                go(*rings[i % sets])
+            e.record()
+            torch.cuda.synchronize()
+            ms = a.elapsed_time(e) / n
         res[op] = {"bytes": nb, "us": round(ms * 1e3, 2), "gbs": round(nb / ms / 1e6, 1), "copies": sets}
         del rings, base
         torch.cuda.empty_cache()
@@ -448,7 +468,7 @@ def run_isolated(args):
         v["frac_of_peak"] = round(v["gbs"] / peak, 4)
         v["frac_of_8tbs"] = round(v["gbs"] / NOMINAL_HBM_GBS, 4)
     name = workload if workload != WORKLOAD or args.tokens >= 8192 else f"{WORKLOAD} (first {args.tokens} tokens)"
-    line = {"mode": "isolated", "workload": name,
+    line = {"mode": "isolated" + (" (CUDA graph)" if args.graph else ""), "workload": name,
             "unit": "GB/s", "peak": peak, "peak_source": kind, "per_op": res}
     print(json.dumps(line), flush=True)
     return line
@@ -771,6 +791,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--isolated", action="store_true",
                     help="time each op alone, back to back over rotating buffers, and print that instead")
+    ap.add_argument("--graph", action="store_true",
+                    help="with --isolated: capture each op's launches in a CUDA graph and time its replays")
     ap.add_argument("--workload", default="",
                     help="with --isolated: another workload's ops (rope-variants-T4096-f32, wide-argmax-rmsnorm-f32, "
                          "llama3-8b-decode-T64-bf16)")

@@ -45,6 +45,8 @@ class GbeError(RuntimeError):
 def lib() -> ctypes.CDLL:
     """The loaded C library (raises LibraryMissing when it is not built)."""
     global _lib
+    if _lib is not None:
+        return _lib
     with _lock:
         if _lib is None:
             if not os.path.exists(LIB_PATH):
@@ -91,8 +93,17 @@ def _check(op: str, st: int):
         raise GbeError(op, st, status_string(st), L.gbe_last_cuda_error() if st == 11 else 0)
 
 
+# The current stream's handle without building a torch Stream object per
+# call (the private accessors torch's own extensions use; the public path
+# where they are absent).
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+_cur_device = getattr(torch._C, "_cuda_getDevice", None)
+
+
 def _stream(stream) -> int:
     if stream is None:
+        if _raw_stream is not None and _cur_device is not None:
+            return _raw_stream(_cur_device())
         stream = torch.cuda.current_stream()
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 

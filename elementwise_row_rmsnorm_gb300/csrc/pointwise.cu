@@ -11,12 +11,14 @@
 // input (exactly, not a partial overlap).  The math is f32; bf16 inputs are
 // widened exactly and the result rounded to nearest-even once.
 //
-// Map: each thread owns U = 4 16-byte vectors spaced one CTA-width apart
-// (so every load instruction of a warp covers 512 contiguous bytes), issues
-// all 2U loads before any use, then computes and stores.  One CTA covers
+// Map: each thread owns U 16-byte vectors spaced one CTA-width apart (so
+// every load instruction of a warp covers 512 contiguous bytes), issues all
+// 2U loads before any use, then computes and stores.  One CTA covers
 // 256 * U vectors; the last CTA also does the n mod V elements past the last
-// whole vector.  Misaligned pointers take a scalar path with the same
-// per-element arithmetic.
+// whole vector.  U = 4 when that still gives at least two CTAs per SM, else
+// U = 1 (small, decode-size arrays: more threads, each with less to do, so
+// the launch fills the GPU).  Misaligned pointers take a scalar path with
+// the same per-element arithmetic.
 #include "common.cuh"
 #include "launch.h"
 
@@ -25,7 +27,7 @@ namespace gbe {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kU = 4;
+constexpr int kU = 4;  // vectors per thread on large arrays
 
 enum { kSiluMul = 0, kAdd = 1 };
 
@@ -38,20 +40,20 @@ __device__ __forceinline__ float op1(float a, float b) {
     return __fadd_rn(a, b);
 }
 
-template <int DT, int OP>
+template <int DT, int OP, int U>
 __global__ void __launch_bounds__(kThreads)
 pointwise_vec(const void* a, const void* b, void* y, int64_t n) {
     using S = Store<DT>;
     constexpr int V = S::V;
     pdl_begin();
     const int64_t nvec = n / V;
-    const int64_t v0 = (int64_t)blockIdx.x * (kThreads * kU) + threadIdx.x;
+    const int64_t v0 = (int64_t)blockIdx.x * (kThreads * U) + threadIdx.x;
     const char* pa = static_cast<const char*>(a);
     const char* pb = static_cast<const char*>(b);
     char* py = static_cast<char*>(y);
-    Vec16 ra[kU], rb[kU];
+    Vec16 ra[U], rb[U];
 #pragma unroll
-    for (int u = 0; u < kU; ++u) {
+    for (int u = 0; u < U; ++u) {
         const int64_t i = v0 + (int64_t)u * kThreads;
         if (i < nvec) {
             ra[u] = ld_stream(pa + i * 16);
@@ -59,7 +61,7 @@ pointwise_vec(const void* a, const void* b, void* y, int64_t n) {
         }
     }
 #pragma unroll
-    for (int u = 0; u < kU; ++u) {
+    for (int u = 0; u < U; ++u) {
         const int64_t i = v0 + (int64_t)u * kThreads;
         if (i < nvec) {
             float fa[V], fb[V], fy[V];
@@ -97,9 +99,16 @@ cudaError_t launch_pw(const void* a, const void* b, void* y, int64_t n, int dtyp
     if (vec) {
         const int64_t nvec = n / V;
         int64_t grid = (nvec + per_cta - 1) / per_cta;
-        if (grid < 1) grid = 1;  // the tail alone (n < V) still needs one CTA
-        if (dtype == kF32) return launch(pointwise_vec<kF32, OP>, dim3((unsigned)grid), dim3(kThreads), 0, st, a, b, y, n);
-        return launch(pointwise_vec<kBF16, OP>, dim3((unsigned)grid), dim3(kThreads), 0, st, a, b, y, n);
+        if (grid < 2 * (int64_t)sm_count()) {  // too few CTAs to fill the GPU: one vector per thread
+            grid = (nvec + kThreads - 1) / kThreads;
+            if (grid < 1) grid = 1;  // the tail alone (n < V) still needs one CTA
+            if (dtype == kF32)
+                return launch(pointwise_vec<kF32, OP, 1>, dim3((unsigned)grid), dim3(kThreads), 0, st, a, b, y, n);
+            return launch(pointwise_vec<kBF16, OP, 1>, dim3((unsigned)grid), dim3(kThreads), 0, st, a, b, y, n);
+        }
+        if (dtype == kF32)
+            return launch(pointwise_vec<kF32, OP, kU>, dim3((unsigned)grid), dim3(kThreads), 0, st, a, b, y, n);
+        return launch(pointwise_vec<kBF16, OP, kU>, dim3((unsigned)grid), dim3(kThreads), 0, st, a, b, y, n);
     }
     const int64_t grid = (n + per_cta - 1) / per_cta;
     if (dtype == kF32) return launch(pointwise_scalar<kF32, OP>, dim3((unsigned)grid), dim3(kThreads), 0, st, a, b, y, n);

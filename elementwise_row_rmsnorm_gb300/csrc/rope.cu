@@ -73,13 +73,15 @@ __device__ __forceinline__ void angle(int32_t p, int i, const float* inv_freq, c
 }
 
 // Aligned path.  A thread owns one group of P consecutive pairs (one 16-byte
-// vector of each pair member) of one token, for a chunk of up to 4 heads:
+// vector of each pair member) of one token, for a chunk of up to HC heads
+// (4, or 1 when the launch would otherwise hold too few threads to fill the
+// GPU, as at decode sizes):
 // it issues the loads of all its heads first, gets the P angles' cos / sin
 // into registers while those loads are in flight, then rotates and stores
 // every head.  Threads of one token and head chunk cover consecutive 16-byte
 // vectors, so each warp-wide access is contiguous.  The launch's threads
 // serve operand A first, then operand B.
-template <int DT, int LAYOUT, bool CACHE>
+template <int DT, int LAYOUT, bool CACHE, int HC>
 __global__ void __launch_bounds__(kThreads)
 rope_vec(Operand A, Operand B, const int32_t* pos, int64_t T, int D, int r, const float* inv_freq,
          const float2* cache, int64_t cache_len, float mu) {
@@ -87,7 +89,6 @@ rope_vec(Operand A, Operand B, const int32_t* pos, int64_t T, int D, int r, cons
     constexpr int V = S::V;
     constexpr int P = LAYOUT == 0 ? V : V / 2;  // pairs per 16-byte item
     constexpr int64_t ES = sizeof(typename S::T);
-    constexpr int HC = kHeadsPerThread;
     pdl_begin();
     int64_t gt = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     const bool second = gt >= A.threads;
@@ -397,6 +398,15 @@ cudaError_t launch_dt(const RopeArgs& a, bool vec, cudaStream_t st) {
             op[k].threads = a.T * (half + (op[k].copy_tail ? a.D - a.r : 0));
         }
     }
+    // few threads (decode sizes): one head per thread instead of four
+    const bool one_head = vec && op[0].threads + op[1].threads < (int64_t)sm_count() * 256;
+    if (one_head) {
+        const int64_t G = a.layout == 0 ? half / V : a.r / V;
+        for (int k = 0; k < 2; ++k) {
+            op[k].NC = op[k].H;
+            op[k].threads = op[k].threads ? a.T * op[k].NC * G : 0;
+        }
+    }
     const int64_t threads = op[0].threads + op[1].threads;
     if (threads == 0) return cudaSuccess;
     const unsigned grid = (unsigned)((threads + kThreads - 1) / kThreads);
@@ -404,11 +414,20 @@ cudaError_t launch_dt(const RopeArgs& a, bool vec, cudaStream_t st) {
 #define GBE_ROPE(KERNEL, L, C)                                                                              \
     return launch(KERNEL<DT, L, C>, dim3(grid), dim3(kThreads), 0, st, op[0], op[1], a.pos, a.T, Di, ri,    \
                   a.inv_freq, cache, a.cache_len, a.mu)
-    if (vec) {
+#define GBE_ROPE_VEC(L, C, HC)                                                                              \
+    return launch(rope_vec<DT, L, C, HC>, dim3(grid), dim3(kThreads), 0, st, op[0], op[1], a.pos, a.T, Di,  \
+                  ri, a.inv_freq, cache, a.cache_len, a.mu)
+    if (vec && one_head) {
         if (a.layout == 0) {
-            if (cached) GBE_ROPE(rope_vec, 0, true); else GBE_ROPE(rope_vec, 0, false);
+            if (cached) GBE_ROPE_VEC(0, true, 1); else GBE_ROPE_VEC(0, false, 1);
         } else {
-            if (cached) GBE_ROPE(rope_vec, 1, true); else GBE_ROPE(rope_vec, 1, false);
+            if (cached) GBE_ROPE_VEC(1, true, 1); else GBE_ROPE_VEC(1, false, 1);
+        }
+    } else if (vec) {
+        if (a.layout == 0) {
+            if (cached) GBE_ROPE_VEC(0, true, kHeadsPerThread); else GBE_ROPE_VEC(0, false, kHeadsPerThread);
+        } else {
+            if (cached) GBE_ROPE_VEC(1, true, kHeadsPerThread); else GBE_ROPE_VEC(1, false, kHeadsPerThread);
         }
     } else {
         if (a.layout == 0) {
@@ -418,6 +437,7 @@ cudaError_t launch_dt(const RopeArgs& a, bool vec, cudaStream_t st) {
         }
     }
 #undef GBE_ROPE
+#undef GBE_ROPE_VEC
 }
 
 }  // namespace
