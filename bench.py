@@ -263,6 +263,23 @@ def build_inputs(tokens: int = 8192):
     return {op: combine(op, [cases[c](rows=rows) for c in names]) for op, names in STEP}
 
 
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The largest of the ranks' values (each rank passes its own): the
+    job's elapsed time is that of its slowest replica."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_gbs(step_bytes: int, steps: int, world: int, elapsed_ms: float) -> float:
+    """Whole-job throughput: every replica moves step_bytes per step."""
+    return step_bytes * steps * world / (elapsed_ms * 1e-3) / 1e9
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -317,11 +334,7 @@ def run_ours(args):
     barrier()
     clocks.mark(host_t0, time.time())
     clk = clocks.stop()
-    elapsed_ms = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+    elapsed_ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
     # timed region 2: the same steps with an event pair around every launch
     # (an event between two launches stops them overlapping, so these per-op
     # times include each launch's full ramp)
@@ -355,7 +368,7 @@ def run_ours(args):
     # dominant kernel: the op with the largest share of the step's time
     dom = max(per_op, key=lambda o: per_op[o]["ms"])
     traffic = dram_traffic(dom)
-    value = step_bytes * args.steps * world / (elapsed_ms * 1e-3) / 1e9
+    value = aggregate_gbs(step_bytes, args.steps, world, elapsed_ms)
 
     result = None
     if rank == 0:

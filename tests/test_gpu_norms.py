@@ -40,7 +40,7 @@ def test_rmsnorm_shapes(dtype, d):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("d", [64, 4096])
+@pytest.mark.parametrize("d", [64, 4096, 12000, 16384, 30000])
 def test_rmsnorm_unaligned_path_same_bits(dtype, d):
     """An element-offset view takes the scalar path; its bits equal the vector path's."""
     x, w = _inputs(9, d, dtype)
@@ -102,7 +102,7 @@ def test_add_rmsnorm_workload_full(workload):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("d", [5, 64, 1000, 4096, 20000])
+@pytest.mark.parametrize("d", [5, 64, 1000, 4096, 12000, 16384, 20000, 30000])
 def test_add_rmsnorm_shapes_and_aliases(dtype, d):
     x, w = _inputs(13, d, dtype, seed=3)
     r, _ = _inputs(13, d, dtype, seed=4)
@@ -158,3 +158,23 @@ def test_batch_invariance_prefill_bf16():
         gbe.gbe_add_rmsnorm(xd[:b], rd[:b], wd, yo[:b], ho[:b], p["eps"])
         assert torch.equal(yo[:b].view(torch.int16), yf[:b].view(torch.int16)), b
         assert torch.equal(ho[:b].view(torch.int16), hf[:b].view(torch.int16)), b
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_add_rmsnorm_wide_rows_unaligned_same_bits(dtype):
+    """Fused add+RMSNorm on rows of 1024 threads (d = 16384 f32 / 30000
+    bf16): the scalar path gives the vector path's y and h bits."""
+    d = 16384 if dtype == "f32" else 30000
+    x, w = _inputs(5, d, dtype, seed=7)
+    r, _ = _inputs(5, d, dtype, seed=8)
+    xd, rd, wd = to_dev(x), to_dev(r), to_dev(w)
+    y, h = gbe.add_rmsnorm(xd, rd, wd, 1e-5)
+
+    def shifted(t):
+        buf = torch.empty(t.numel() + 1, dtype=t.dtype, device="cuda")[1:].view(t.shape)
+        buf.copy_(t)
+        return buf
+    xs, rs = shifted(xd), shifted(rd)
+    ys, hs = shifted(torch.zeros_like(xd)), shifted(torch.zeros_like(xd))
+    gbe.gbe_add_rmsnorm(xs, rs, wd, ys, hs, 1e-5)
+    assert np.array_equal(bits(ys), bits(y)) and np.array_equal(bits(hs), bits(h))
