@@ -102,23 +102,50 @@ qk_norm_rope_shfl(QkSide A, QkSide B, int nca, int ncb, float eps, const int32_t
     }
     float gv[V];
     if (has) S::unpack(ld_reuse(Q.g + (int64_t)c * 16), gv);
-    // the angles of the pairs this lane's entries belong to
-    float ca[V], sa[V];
+    // The angles of the pairs this lane's entries belong to, each formed once
+    // per lane pair, with the same instructions in every lane (no divergent
+    // branch): interleaved, the two members of a pair sit in one lane (even
+    // entries form the angle, odd ones copy it); half layout, a first-member
+    // lane and its partner lane hold the same pairs, so each forms half of
+    // them and they swap the other half by shuffle.
+    const int src = LAYOUT == 0 ? (c < G ? lane + G : (c < 2 * G ? lane - G : lane)) : lane;
+    constexpr int HV = V / 2;
     const int32_t p = pos[t];
+    float tc[HV], ts[HV];
+    const bool low = LAYOUT == 0 ? c < G : true;
 #pragma unroll
-    for (int e = 0; e < V; ++e) {
+    for (int k = 0; k < HV; ++k) {
+        const int e = LAYOUT == 0 ? k + (low ? 0 : HV) : 2 * k;  // the entry whose angle this lane forms
         const int j = c * V + e;
-        ca[e] = 1.0f;
-        sa[e] = 0.0f;
+        tc[k] = 1.0f;
+        ts[k] = 0.0f;
         if (has && j < r) {
             const int i = LAYOUT == 0 ? (j < half ? j : j - half) : (j >> 1);
             if (CACHE && p >= 0 && p < cache_len) {
                 const float2 v = __ldg(cache + (int64_t)p * half + i);
-                ca[e] = v.x;
-                sa[e] = v.y;
+                tc[k] = v.x;
+                ts[k] = v.y;
             } else {
-                sincosf(__fmul_rn((float)p, __ldg(inv_freq + i)), &sa[e], &ca[e]);
+                sincosf(__fmul_rn((float)p, __ldg(inv_freq + i)), &ts[k], &tc[k]);
             }
+        }
+    }
+    float ca[V], sa[V];
+    if (LAYOUT == 1) {
+#pragma unroll
+        for (int k = 0; k < HV; ++k) {
+            ca[2 * k] = ca[2 * k + 1] = tc[k];
+            sa[2 * k] = sa[2 * k + 1] = ts[k];
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < HV; ++k) {
+            const float pc = __shfl_sync(0xFFFFFFFFu, tc[k], src);  // the partner's entry k (low) or k + HV
+            const float ps = __shfl_sync(0xFFFFFFFFu, ts[k], src);
+            ca[k] = low ? tc[k] : pc;
+            sa[k] = low ? ts[k] : ps;
+            ca[k + HV] = low ? pc : tc[k];
+            sa[k + HV] = low ? ps : ts[k];
         }
     }
     float s[NP];
@@ -137,7 +164,6 @@ qk_norm_rope_shfl(QkSide A, QkSide B, int nca, int ncb, float eps, const int32_t
         for (int k = 0; k < NP; ++k) s[k] = __fadd_rn(s[k], __shfl_xor_sync(0xFFFFFFFFu, s[k], m));
     }
     const bool rot = has && c * V < r;        // this chunk is rotated
-    const int src = LAYOUT == 0 ? (c < G ? lane + G : (c < 2 * G ? lane - G : lane)) : lane;
     // Both members of a pair take one formula, out = mu * (own * cos + partner * sg)
     // with sg = -sin for the first member and +sin for the second: IEEE gives
     // a - b == a + (-b) and a + b == b + a exactly, so this is the same
