@@ -32,16 +32,21 @@
 //    f32, the unit sum held as a fixed-point integer); the warp holding the
 //    target walks its segment tile by tile with warp scans, then the unit's
 //    own partial sums.
-//  * top-k, top-p (descending order): an order-keeping 32-bit key of each
-//    logit is split into 12 / 10 / 10-bit digits.  A 4096-bin histogram of
-//    the first digit (counts, and for top-p masses) locates the bin where the
-//    descending running count or mass passes its target; that bin's entries
-//    -- few, at the head of a peaked distribution -- are gathered into shared
-//    memory as (key, ~index) pairs, sorted descending (equal keys then come
-//    in index order), and walked.  A bin of more than 4096 entries is split by
-//    the next digit, and a group of more than 4096 equal logits is walked in
-//    index order by the warps.  Top-k with k within the gather limit gathers
-//    every bin down to the k-th entry and draws among the first k.
+//  * top-k, top-p (descending order): pass 1 also leaves each thread's own
+//    maximum; a floor that enough entries reach (from those maxima, sorted
+//    per warp) selects the few entries at the top of the row, which pass 2
+//    gathers into shared memory as (key, ~index) pairs -- for top-p while
+//    it sums the row's mass -- and a bitonic sort orders descending, equal
+//    logits by index (key: an order-keeping 32-bit image of the logit).
+//    Top-k draws among the first k; top-p walks the sorted prefix for the
+//    cut and the draw when the prefix's mass passes the cut.  Otherwise
+//    (large k, flat or heavily tied rows) an exact radix search: the key's
+//    12 / 10 / 10-bit digits, a histogram per digit (counts, and masses as
+//    exact 64-bit sums in two 32-bit words) locates the bin where the
+//    descending running count or mass passes its target; that bin's
+//    entries are gathered, sorted and walked; a bin of more than 4096
+//    entries is split by the next digit, and a group of more than 4096
+//    equal logits is walked in index order by the warps.
 // No memory beyond the inputs and the outputs.
 #include "common.cuh"
 #include "launch.h"
@@ -54,7 +59,7 @@ constexpr int kT = 512;
 constexpr int kW = kT / 32;
 constexpr int kU = 4;                       // tiles in flight per lane
 constexpr int kMaxCand = 4096;              // entries gathered into shared memory
-constexpr int kTopGather = 1024;            // entries top-p gathers from the top of a row first
+constexpr int kTopLanes = 64;               // top-p first gathers entries >= a floor this many reach
 constexpr int kBins0 = 4096, kBins1 = 1024;  // 12-bit first digit, 10-bit others
 constexpr float kScale = 1099511627776.0f;  // 2^40
 constexpr unsigned kFull = 0xFFFFFFFFu;
@@ -327,13 +332,15 @@ __device__ __forceinline__ void setup(Row<DT, VEC>& row, const void* x, int n, f
 // pass 1: the largest logit (and with COUNT the count of numbers); false
 // (and -1 written) when the row has no number or no finite largest x / t
 template <bool COUNT, int DT, bool VEC>
-__device__ __forceinline__ bool first_pass(Row<DT, VEC>& row, int32_t* out, Sh& sh, int* nv_out) {
+__device__ __forceinline__ bool first_pass(Row<DT, VEC>& row, int32_t* out, Sh& sh, int* nv_out,
+                                           float* thread_max = nullptr) {
     float mx = -INFINITY;
     int nv = 0;
     row.each([&](int, float v) {
         mx = fmaxf(mx, v);  // NaN is ignored
         if (COUNT && v == v) ++nv;
     });
+    if (thread_max) thread_max[threadIdx.x] = mx;  // this thread's own maximum (-inf if it has no number)
     mx = block_max(mx, sh);
     if (COUNT) nv = block_sum_int(nv, sh);
     row.mx = mx;
@@ -453,6 +460,7 @@ struct ShBig {
     unsigned cnt0[kBins0], lo0[kBins0], hi0[kBins0];
     unsigned cnt1[kBins1], lo1[kBins1], hi1[kBins1];
     u64 cand[kMaxCand];
+    float lmax[kT];  // the threads' own maxima of the first pass
     __device__ __forceinline__ Hist h0() { return Hist{cnt0, lo0, hi0, kBins0}; }
     __device__ __forceinline__ Hist h1() { return Hist{cnt1, lo1, hi1, kBins1}; }
 };
@@ -544,6 +552,35 @@ __device__ void build_next(const Row<DT, VEC>& row, ShBig& sb, int shift, uint32
     __syncthreads();
 }
 
+__device__ int sort_cand(ShBig& sb);
+
+// A floor that at least kW * m entries of the row reach (1 <= m <= 32): each
+// warp sorts its 32 threads' own maxima (a bitonic network over lanes, no
+// barrier) and offers its m-th largest; the floor is the least of the
+// warps' offers, so every warp has m threads whose maximum -- an entry of
+// the row -- reaches it.  -inf when some warp has fewer than m threads with
+// a number: then every number reaches it.
+__device__ float maxima_floor(float mine, int m, Sh& sh) {
+    const int lane = threadIdx.x & 31;
+    float v = mine;
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const float o = __shfl_xor_sync(kFull, v, stride);
+            const bool keep_max = ((lane & stride) == 0) == ((lane & size) == 0 || size == 32);
+            v = keep_max ? fmaxf(v, o) : fminf(v, o);
+        }
+    }
+    const float offer = __shfl_sync(kFull, v, m - 1);  // lanes now hold the maxima in descending order
+    __syncthreads();
+    if (lane == 0) sh.wf[threadIdx.x >> 5] = offer;
+    __syncthreads();
+    float f = sh.wf[0];
+    for (int w = 1; w < kW; ++w) f = fminf(f, sh.wf[w]);
+    return f;
+}
+
 // Gather the entries for which sel(v) holds into cand as (key, ~index) and
 // sort them descending (after() runs once per kU tiles); returns their count
 // (the caller's selection holds at most kMaxCand entries).
@@ -559,6 +596,12 @@ __device__ int gather_sorted_by(const Row<DT, VEC>& row, ShBig& sb, F sel, G aft
             if (slot < (unsigned)kMaxCand) sb.cand[slot] = cand_of(order_key(v), i);
         },
         after);
+    return sort_cand(sb);
+}
+
+// Sort the gathered candidates descending (bitonic, in shared memory);
+// returns their count (at most kMaxCand).
+__device__ int sort_cand(ShBig& sb) {
     __syncthreads();
     const int nc = (int)min(sb.s.ncand, (unsigned)kMaxCand);
     int P = 1;
@@ -705,20 +748,16 @@ __device__ int desc_search(const Row<DT, VEC>& row, u64 target, ShBig& sb, u64* 
     return sb.s.ri[2];
 }
 
-// Top-p's second pass: the count histogram of the head (the first-digit
-// bins from `from` up), and this thread's share of the row's total mass,
-// summed as the index-order kernel sums it (f32 unit sums, each held in
-// fixed point).  That total only sets the cut p * W, so it need not equal
-// the sum of the per-entry weights the walks use; the exact fallback takes
-// its own total from its histogram.
+// Top-p's second pass: this thread's share of the row's total mass (f32
+// unit sums, each held in fixed point, as the index-order kernel sums it),
+// and every entry >= T gathered as a candidate (unsorted; ncand counts them
+// all, even past kMaxCand).
 template <int DT, bool VEC>
-__device__ u64 head_counts_and_mass(const Row<DT, VEC>& row, ShBig& sb, uint32_t from) {
+__device__ u64 mass_and_gather(const Row<DT, VEC>& row, ShBig& sb, float T) {
     constexpr int V = Row<DT, VEC>::V;
     constexpr int kTile = Row<DT, VEC>::kTile;
-    const Hist h = sb.h0();
-    const float x_from = key_floor((u64)from << 20);
     __syncthreads();
-    h.clear();
+    if (threadIdx.x == 0) sb.s.ncand = 0;
     __syncthreads();
     u64 tot = 0;
     for (int j0 = row.s0; j0 < row.s1; j0 += kTile * kU) {
@@ -731,15 +770,15 @@ __device__ u64 head_counts_and_mass(const Row<DT, VEC>& row, ShBig& sb, uint32_t
 #pragma unroll
             for (int e = 0; e < V; ++e) {
                 s = __fadd_rn(s, fmaxf(row.e_of(v[q][e]), 0.0f));  // NaN gives 0
-                if (v[q][e] >= x_from) {
-                    const uint32_t d = order_key(v[q][e]) >> 20;
-                    if (d >= from) atomicAdd(&h.cnt[d], 1u);
+                if (v[q][e] >= T) {
+                    const unsigned slot = atomicAdd(&sb.s.ncand, 1u);
+                    if (slot < (unsigned)kMaxCand)
+                        sb.cand[slot] = cand_of(order_key(v[q][e]), j0 + q * kTile + row.lane * V + e);
                 }
             }
             tot += fixed40(s);
         }
     }
-    __syncthreads();
     return tot;
 }
 
@@ -752,7 +791,7 @@ sample_descending(const void* x, int32_t* out, int n, int method, float t, int k
     Row<DT, VEC> row;
     setup(row, x, n, t);
     int nv;
-    if (method == kTopK ? !first_pass<true>(row, out, sb.s, &nv) : !first_pass<false>(row, out, sb.s, &nv)) return;
+    if (!first_pass<false>(row, out, sb.s, &nv, sb.lmax)) return;
     const float ur = u[blockIdx.x];
     // The head of the row: the first-digit bins from that of M - 24 / c down
     // -- every entry of weight above 2^-24 of the largest (and some below).
@@ -764,7 +803,22 @@ sample_descending(const void* x, int32_t* out, int n, int method, float t, int k
     auto c0 = [&](int b) { return sb.h0().count(b); };
     auto m0 = [&](int b) { return sb.h0().mass(b); };
     if (method == kTopK) {
-        if (k < nv) {
+        if (k <= kT) {
+            // the entries >= a floor that k entries reach hold the top k (or
+            // every number, when the floor is -inf)
+            const float T = maxima_floor(sb.lmax[threadIdx.x], (k + kW - 1) / kW, sb.s);
+            const int nc = gather_sorted_by(row, sb, [&](float v) { return v >= T; }, [] {});
+            if (sb.s.ncand <= (unsigned)kMaxCand) {
+                const int L = min(k, nc);
+                const u64 wk = sorted_mass(row, L, sb);
+                u64 unused;
+                const int q = sorted_pick(row, L, scaled(ur, wk), sb, &unused);
+                if (threadIdx.x == 0) out[blockIdx.x] = q >= 0 ? cand_index(sb.cand[q]) : -1;
+                return;
+            }
+        }
+        // more candidates than the gather holds: count the head's bins first
+        {
             build_first(row, sb, head, false, false);
             const u64 in_head = sum_above(c0, kBins0, -1, sb.s);
             if (in_head >= (u64)k) {
@@ -783,6 +837,7 @@ sample_descending(const void* x, int32_t* out, int n, int method, float t, int k
         }
         u64 all;
         block_exscan(build_first(row, sb, 0u, true, true), sb.s, &all);
+        nv = (int)sum_above(c0, kBins0, -1, sb.s);  // the count of numbers
         u64 kept = all;
         if (k < nv) desc_search<DT, VEC, true>(row, (u64)k, sb, &kept);  // the entry past the k-th
         u64 unused;
@@ -792,23 +847,20 @@ sample_descending(const void* x, int32_t* out, int n, int method, float t, int k
     }
     // top-p: keep the prefix whose running mass stays <= p * W (the first
     // entry always), then draw from it.  First try the top of the row: the
-    // whole first-digit bins that together hold at most kTopGather entries,
-    // gathered and sorted; when their exact mass passes the cut, the cut and
-    // the draw both fall among them.
+    // entries >= a floor that at least kTopLanes entries reach (from the
+    // threads' own maxima), gathered in the same pass that sums the row's
+    // mass, and sorted; when their exact mass passes the cut, the cut and the
+    // draw both fall among them.
+    const float T = maxima_floor(sb.lmax[threadIdx.x], kTopLanes / kW, sb.s);
     u64 all;
-    block_exscan(head_counts_and_mass(row, sb, head), sb.s, &all);
+    block_exscan(mass_and_gather(row, sb, T), sb.s, &all);
+    const bool fits = sb.s.ncand <= (unsigned)kMaxCand;  // final: block_exscan's barriers follow every atomic
+    const int nc = sort_cand(sb);
     const u64 cut = (u64)((double)p * (double)all);
-    const u64 in_head = sum_above(c0, kBins0, -1, sb.s);
-    int b_lo = (int)head;  // gather the bins [b_lo, top]
-    if (in_head > (u64)kTopGather) {
-        u64 above;
-        b_lo = find_bin(c0, kBins0, (u64)kTopGather, sb.s, &above) + 1;  // the bins above the one that overflows
-    }
     u64 kept = all, unused;
     int idx = -1;
     bool ok = false;
-    if (b_lo < kBins0) {
-        const int nc = gather_sorted(row, 20, (uint32_t)b_lo, (uint32_t)(kBins0 - 1), sb);
+    if (fits) {
         const u64 top_mass = sorted_mass(row, nc, sb);
         if (cut < all) {
             if (cut < top_mass) {
