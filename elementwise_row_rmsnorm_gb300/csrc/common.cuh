@@ -45,8 +45,26 @@ __device__ __forceinline__ Vec16 ld_reuse(const void* p) {
     return v;
 }
 
+// Read once and written once, with evict-first priority in L2 (.cs): the
+// elementwise ops' whole arrays, which nothing in the same launch reads again.
+__device__ __forceinline__ Vec16 ld_once(const void* p) {
+    Vec16 v;
+    asm volatile("ld.global.cs.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_once(void* p, const Vec16& v) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]),
+                 "r"(v.w[3])
+                 : "memory");
+}
+
+// Output stores: written once by this launch, evict-first in L2 (.cs), so
+// a large output does not push out what the next launch is about to read.
 __device__ __forceinline__ void st_stream(void* p, const Vec16& v) {
-    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.w[0]), "r"(v.w[1]),
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.w[0]), "r"(v.w[1]),
                  "r"(v.w[2]), "r"(v.w[3])
                  : "memory");
 }
