@@ -24,6 +24,7 @@
 // barrier keeps every CTA's shared memory alive until rank 0 has read it.
 // CL grows only while rows * CL stays below eight CTAs per SM, so few long
 // rows (decode) still fill the GPU.
+#include <atomic>
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -34,13 +35,22 @@ namespace cg = cooperative_groups;
 namespace gbe {
 
 int sm_count() {
-    static int cached[64] = {0};
+    static std::atomic<int> cached[64];  // zero-initialised (static storage)
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
-    if (dev < 64 && cached[dev] > 0) return cached[dev];
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+        cudaGetLastError();
+        return 152;
+    }
+    if (dev < 64) {
+        const int c = cached[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
     int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-    if (dev < 64) cached[dev] = n;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        n = 152;
+    }
+    if (dev < 64) cached[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 

@@ -48,6 +48,8 @@
 //    entries is split by the next digit, and a group of more than 4096
 //    equal logits is walked in index order by the warps.
 // No memory beyond the inputs and the outputs.
+#include <atomic>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -901,11 +903,19 @@ cudaError_t launch_vec(const void* x, int32_t* out, int64_t rows, int n, int met
     if (method == kMinP)
         return launch(sample_index_order<DT, VEC, true>, dim3((unsigned)rows), dim3(kT), 0, st, x, out, n, t, p, u);
     const size_t smem = sizeof(ShBig);
-    const cudaError_t e =
-        cudaFuncSetAttribute(sample_descending<DT, VEC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        return e;
+    // the shared-memory opt-in, once per device for this kernel
+    static std::atomic<uint64_t> opted{0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaGetLastError();
+    const uint64_t bit = dev >= 0 && dev < 64 ? 1ull << dev : 0ull;
+    if (!(opted.load(std::memory_order_acquire) & bit) || bit == 0) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(sample_descending<DT, VEC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return e;
+        }
+        opted.fetch_or(bit, std::memory_order_release);
     }
     return launch(sample_descending<DT, VEC>, dim3((unsigned)rows), dim3(kT), smem, st, x, out, n, method, t, k, p, u);
 }

@@ -285,9 +285,11 @@ typedef enum gbe_sample_method {
  *   logit with equal logits by ascending index for TOP_K and TOP_P), whose
  *   running sum exceeds u[r] times the sum of the kept entries.
  *   Arithmetic: e = exp2f((x - max(x)) * (log2(e) / t)) in f32 (e = 1 at the
- *   maximum), each e held as the integer rn(e * 2^40); sums and cuts are
- *   exact integer arithmetic on those weights, so the result is
- *   deterministic and independent of the batch.  It equals an exact
+ *   maximum), held as the integer rn(e * 2^40) -- per entry for TOP_K and
+ *   TOP_P, per f32 sum of 4 (f32) or 8 (bf16) consecutive entries for
+ *   TEMPERATURE and MIN_P; sums and cuts are exact integer arithmetic on
+ *   those weights, so the result is deterministic and independent of the
+ *   batch.  It equals an exact
  *   evaluation of the definition except where u[r] falls within rounding of
  *   a boundary between two entries (or an entry sits within rounding of a
  *   cut), where either neighbour is a valid draw.
