@@ -721,41 +721,55 @@ def oracle_sample(data=None, fraction=SAMPLE_FRACTION):
     return sample
 
 
-def oracle_step(sample):
+def oracle_step(sample, times=None):
+    """One pass of the oracle over the sample; with `times`, each op's
+    elapsed seconds are added to times[op]."""
     import oracle
     o = oracle.get()
     for op, a, p, _b, _r in sample:
-        if op == "embedding":
-            o.embedding(a["table"], a["ids"])
-        elif op == "add_rmsnorm":
-            o.add_rmsnorm(a["x"], a["residual"], a["w"], p["eps"], h_bf16=True)
-        elif op.startswith("rope_qk"):
-            o.rope(a["q"], a["pos"], a["inv_freq"], p["r"], p["mu"], p["layout"])
-            o.rope(a["k"], a["pos"], a["inv_freq"], p["r"], p["mu"], p["layout"])
-        elif op == "silu_mul":
-            o.silu_mul(a["gate"], a["up"])
-        elif op == "add":
-            o.add(a["a"], a["b"])
-        elif op == "rmsnorm":
-            o.rmsnorm(a["x"], a["w"], p["eps"])
-        elif op == "argmax":
-            o.argmax(a["x"])
+        t0 = time.perf_counter()
+        oracle_op(o, op, a, p)
+        if times is not None:
+            times[op] = times.get(op, 0.0) + time.perf_counter() - t0
+
+
+def oracle_op(o, op, a, p):
+    if op == "embedding":
+        o.embedding(a["table"], a["ids"])
+    elif op == "add_rmsnorm":
+        o.add_rmsnorm(a["x"], a["residual"], a["w"], p["eps"], h_bf16=True)
+    elif op.startswith("rope_qk"):
+        o.rope(a["q"], a["pos"], a["inv_freq"], p["r"], p["mu"], p["layout"])
+        o.rope(a["k"], a["pos"], a["inv_freq"], p["r"], p["mu"], p["layout"])
+    elif op == "silu_mul":
+        o.silu_mul(a["gate"], a["up"])
+    elif op == "add":
+        o.add(a["a"], a["b"])
+    elif op == "rmsnorm":
+        o.rmsnorm(a["x"], a["w"], p["eps"])
+    elif op == "argmax":
+        o.argmax(a["x"])
 
 
 def cpu_baseline(data=None):
     """The oracle, as it stands, on the host: one thread, the sample repeated
     for about CPU_SECONDS."""
+    import platform
     sample = oracle_sample(data)
     bts = sum(s[3] for s in sample)
+    times = {}
     reps, t = 0, time.perf_counter()
     while True:
-        oracle_step(sample)
+        oracle_step(sample, times)
         reps += 1
         dt = time.perf_counter() - t
         if dt >= CPU_SECONDS:
             break
+    per_op = {op: {"gbs": round(b * reps / times[op] / 1e9, 3), "rows_per_s": round(r * reps / times[op], 1)}
+              for op, _a, _p, b, r in sample}
     return {"value": round(bts * reps / dt / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "seconds": round(dt, 2), "repeats": reps,
+            "seconds": round(dt, 2), "repeats": reps, "per_op": per_op,
+            "host": {"machine": platform.machine(), "cpus": os.cpu_count()},
             "sample": f"first 1/{SAMPLE_FRACTION} of the rows of every op of the step "
                       f"({bts / 1e6:.0f} MB algorithmic), single-threaded C in f32, repeated for "
                       f"{dt:.1f} s"}
