@@ -12,7 +12,7 @@
 // a row whose largest logit / t is not finite gives -1.
 //
 // Arithmetic.  For every logit e = 2^((x - M) * c) in f32, M the largest
-// logit and c = log2(e) / t (exp2f; e = 1 exactly where x = M), so
+// logit and c = log2(e) / t (ex2.approx; e = 1 exactly where x = M), so
 // 0 <= e <= 1 -- the softmax numerator exp(x / t - M / t) up to a few f32
 // roundings.  e is then held as the integer w = rn(e * 2^40), and every sum,
 // histogram and threshold is an integer.  Integer sums do not depend on their
@@ -156,10 +156,9 @@ struct Row {
     int s0, s1;      // this warp's segment [s0, s1)
     int lane;
 
-    __device__ __forceinline__ float e_of(float v) const {
-        const float d = __fsub_rn(v, mx);
-        return d == 0.0f ? 1.0f : ex2(__fmul_rn(d, c));
-    }
+    // c is finite (clamped at setup), so x = M gives 0 * c = 0 and
+    // ex2.approx(0) = 1 exactly; NaN stays NaN for the callers to drop
+    __device__ __forceinline__ float e_of(float v) const { return ex2(__fmul_rn(__fsub_rn(v, mx), c)); }
     __device__ __forceinline__ static u64 w_of(float e) { return fixed40(e); }
     // fixed-point weight of a logit that is not NaN
     __device__ __forceinline__ u64 weight(float v) const { return w_of(e_of(v)); }
@@ -323,7 +322,7 @@ __device__ __forceinline__ void setup(Row<DT, VEC>& row, const void* x, int n, f
     row.base = (int64_t)blockIdx.x * n;
     row.t = t;
     row.mx = 0.0f;
-    row.c = __fdiv_rn(1.44269502f, t);  // log2(e) / t
+    row.c = fminf(__fdiv_rn(1.44269502f, t), 3.4028234663852886e38f);  // log2(e) / t, finite
     row.lane = threadIdx.x & 31;
     const int per = ((n + kW - 1) / kW + kTile - 1) / kTile * kTile;
     const int w = threadIdx.x >> 5;
@@ -338,10 +337,37 @@ __device__ __forceinline__ bool first_pass(Row<DT, VEC>& row, int32_t* out, Sh& 
                                            float* thread_max = nullptr) {
     float mx = -INFINITY;
     int nv = 0;
-    row.each([&](int, float v) {
-        mx = fmaxf(mx, v);  // NaN is ignored
-        if (COUNT && v == v) ++nv;
-    });
+    if (DT == kBF16 && VEC && !COUNT) {
+        // bf16: the maximum on packed pairs (__hmax2 skips NaN like fmaxf;
+        // a pair of NaN stays NaN, and the -inf start keeps the running value
+        // a number), two entries per instruction, no unpacking
+        constexpr int kTile = Row<DT, VEC>::kTile;
+        __nv_bfloat162 acc = __floats2bfloat162_rn(-INFINITY, -INFINITY);
+        for (int j0 = row.s0; j0 < row.s1; j0 += kTile * kU) {
+            Vec16 q[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int i = j0 + u * kTile + row.lane * Row<DT, VEC>::V;
+                if (i < row.s1) {
+                    q[u] = ld_reuse(static_cast<const char*>(row.x) + (row.base + i) * (int64_t)2);
+                } else {
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) q[u].w[w] = 0x7FC07FC0u;  // NaN pairs
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kU; ++u)
+#pragma unroll
+                for (int w = 0; w < 4; ++w) acc = __hmax2(acc, *reinterpret_cast<const __nv_bfloat162*>(&q[u].w[w]));
+        }
+        const float2 f = __bfloat1622float2(acc);
+        mx = fmaxf(f.x, f.y);
+    } else {
+        row.each([&](int, float v) {
+            mx = fmaxf(mx, v);  // NaN is ignored
+            if (COUNT && v == v) ++nv;
+        });
+    }
     if (thread_max) thread_max[threadIdx.x] = mx;  // this thread's own maximum (-inf if it has no number)
     mx = block_max(mx, sh);
     if (COUNT) nv = block_sum_int(nv, sh);
