@@ -776,6 +776,43 @@ __device__ int desc_search(const Row<DT, VEC>& row, u64 target, ShBig& sb, u64* 
     return sb.s.ri[2];
 }
 
+// Append the entries i0 + e of the row whose bits e are set in `in` (rare:
+// kept out of the per-entry path, so that the common case is one compare
+// and one OR per entry; each such entry is read again from cache).
+template <int DT, bool VEC>
+__device__ __forceinline__ void gather_bits(const Row<DT, VEC>& row, ShBig& sb, unsigned in, int i0) {
+    while (in) {
+        const int e = __ffs(in) - 1;
+        in &= in - 1u;
+        const float v = Store<DT>::load1(row.x, row.base + i0 + e);
+        const unsigned slot = atomicAdd(&sb.s.ncand, 1u);
+        if (slot < (unsigned)kMaxCand) sb.cand[slot] = cand_of(order_key(v), i0 + e);
+    }
+}
+
+// The entries >= T of the row, gathered as candidates (unsorted; ncand
+// counts them all, even past kMaxCand).
+template <int DT, bool VEC>
+__device__ void gather_ge(const Row<DT, VEC>& row, ShBig& sb, float T) {
+    constexpr int V = Row<DT, VEC>::V;
+    constexpr int kTile = Row<DT, VEC>::kTile;
+    __syncthreads();
+    if (threadIdx.x == 0) sb.s.ncand = 0;
+    __syncthreads();
+    for (int j0 = row.s0; j0 < row.s1; j0 += kTile * kU) {
+        float v[kU][V];
+#pragma unroll
+        for (int q = 0; q < kU; ++q) row.load(j0 + q * kTile, v[q]);
+#pragma unroll
+        for (int q = 0; q < kU; ++q) {
+            unsigned in = 0;
+#pragma unroll
+            for (int e = 0; e < V; ++e) in |= (v[q][e] >= T ? 1u : 0u) << e;
+            if (in) gather_bits(row, sb, in, j0 + q * kTile + row.lane * V);
+        }
+    }
+}
+
 // Top-p's second pass: this thread's share of the row's total mass (f32
 // unit sums, each held in fixed point, as the index-order kernel sums it),
 // and every entry >= T gathered as a candidate (unsorted; ncand counts them
@@ -795,16 +832,14 @@ __device__ u64 mass_and_gather(const Row<DT, VEC>& row, ShBig& sb, float T) {
 #pragma unroll
         for (int q = 0; q < kU; ++q) {
             float s = 0.0f;
+            unsigned in = 0;  // the entries >= T, one bit each
 #pragma unroll
             for (int e = 0; e < V; ++e) {
                 s = __fadd_rn(s, fmaxf(row.e_of(v[q][e]), 0.0f));  // NaN gives 0
-                if (v[q][e] >= T) {
-                    const unsigned slot = atomicAdd(&sb.s.ncand, 1u);
-                    if (slot < (unsigned)kMaxCand)
-                        sb.cand[slot] = cand_of(order_key(v[q][e]), j0 + q * kTile + row.lane * V + e);
-                }
+                in |= (v[q][e] >= T ? 1u : 0u) << e;
             }
             tot += fixed40(s);
+            if (in) gather_bits(row, sb, in, j0 + q * kTile + row.lane * V);
         }
     }
     return tot;
@@ -835,7 +870,8 @@ sample_descending(const void* x, int32_t* out, int n, int method, float t, int k
             // the entries >= a floor that k entries reach hold the top k (or
             // every number, when the floor is -inf)
             const float T = maxima_floor(sb.lmax[threadIdx.x], (k + kW - 1) / kW, sb.s);
-            const int nc = gather_sorted_by(row, sb, [&](float v) { return v >= T; }, [] {});
+            gather_ge(row, sb, T);
+            const int nc = sort_cand(sb);
             if (sb.s.ncand <= (unsigned)kMaxCand) {
                 const int L = min(k, nc);
                 const u64 wk = sorted_mass(row, L, sb);
