@@ -493,6 +493,105 @@ struct ShBig {
     __device__ __forceinline__ Hist h1() { return Hist{cnt1, lo1, hi1, kBins1}; }
 };
 
+// ---- one warp over at most 256 candidates ----------------------------------------
+//
+// The common case of top-k and top-p gathers a few hundred candidates at
+// most.  One warp then sorts them in registers (8 per lane, entry
+// i = 8 lane + slot) with a bitonic network -- strides below 8 inside a
+// lane, larger ones by shuffles -- and finds the cut and the draw with warp
+// scans: no block barrier, where the block-wide sort and walks take several
+// dozen.
+constexpr int kWarpCand = 256;
+
+struct WarpSorted {
+    u64 c[8];    // the sorted candidates of this lane (0: past the end)
+    u64 cum[8];  // running mass through each (inclusive), in sorted order
+};
+
+template <int DT, bool VEC>
+__device__ __forceinline__ void warp_sort_weigh(const Row<DT, VEC>& row, const u64* cand, int nc, int lane,
+                                                WarpSorted& ws) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int i = lane * 8 + k;
+        ws.c[k] = i < nc ? cand[i] : 0ull;  // pads sort last
+    }
+#pragma unroll
+    for (int ls = 1; ls <= 8; ++ls) {  // blocks of 2^ls entries
+#pragma unroll
+        for (int lt = ls - 1; lt >= 0; --lt) {  // compare entries 2^lt apart
+            const int size = 1 << ls, stride = 1 << lt;
+            if (lt >= 3) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const u64 o = __shfl_xor_sync(kFull, ws.c[k], stride >> 3);
+                    const int i = lane * 8 + k;
+                    const bool keep_max = ((i & stride) == 0) == ((i & size) == 0);
+                    ws.c[k] = keep_max ? (ws.c[k] > o ? ws.c[k] : o) : (ws.c[k] < o ? ws.c[k] : o);
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    if ((k & stride) == 0) {
+                        const int k2 = k | stride;
+                        const bool desc = ((lane * 8 + k) & size) == 0;
+                        const u64 a = ws.c[k], b = ws.c[k2];
+                        const bool swap = desc ? a < b : a > b;
+                        ws.c[k] = swap ? b : a;
+                        ws.c[k2] = swap ? a : b;
+                    }
+                }
+            }
+        }
+    }
+    u64 run = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        run += ws.c[k] ? row.weight(key_value((uint32_t)(ws.c[k] >> 32))) : 0ull;
+        ws.cum[k] = run;
+    }
+    const u64 inc = warp_incl_scan_u64(run, lane);
+    const u64 base = inc - run;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) ws.cum[k] += base;
+}
+
+// The first sorted position j < L whose running mass exceeds target (-1 if
+// none); *before gets the mass ahead of it, *cand the candidate there.
+template <int DT, bool VEC>
+__device__ __forceinline__ int warp_first_above(const Row<DT, VEC>& row, const WarpSorted& ws, int L, u64 target,
+                                                int lane, u64* before, u64* cand) {
+    int kf = 8;
+#pragma unroll
+    for (int k = 7; k >= 0; --k)
+        if (lane * 8 + k < L && ws.cum[k] > target) kf = k;
+    const unsigned who = __ballot_sync(kFull, kf < 8);
+    if (!who) return -1;
+    const int src = __ffs(who) - 1;
+    u64 cum = 0, c = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        if (k == kf) {
+            cum = ws.cum[k];
+            c = ws.c[k];
+        }
+    cum = __shfl_sync(kFull, cum, src);
+    c = __shfl_sync(kFull, c, src);
+    *before = cum - row.weight(key_value((uint32_t)(c >> 32)));
+    *cand = c;
+    return src * 8 + __shfl_sync(kFull, kf, src);
+}
+
+// the running mass through sorted position L - 1 (L >= 1)
+__device__ __forceinline__ u64 warp_mass_through(const WarpSorted& ws, int L) {
+    const int j = L - 1;
+    u64 v = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        if (k == (j & 7)) v = ws.cum[k];
+    return __shfl_sync(kFull, v, j >> 3);
+}
+
 // The bin (scanning from the top bin down) where the running sum of h(b)
 // passes target (target < the sum); *above gets the sum of the bins above it.
 template <typename H>
@@ -871,6 +970,20 @@ sample_descending(const void* x, int32_t* out, int n, int method, float t, int k
             // every number, when the floor is -inf)
             const float T = maxima_floor(sb.lmax[threadIdx.x], (k + kW - 1) / kW, sb.s);
             gather_ge(row, sb, T);
+            __syncthreads();  // every candidate is in
+            const unsigned ncand = sb.s.ncand;
+            if (ncand <= (unsigned)kWarpCand) {
+                if (threadIdx.x < 32) {  // one warp finishes the row
+                    WarpSorted ws;
+                    warp_sort_weigh(row, sb.cand, (int)ncand, row.lane, ws);
+                    const int L = min(k, (int)ncand);
+                    const u64 wk = warp_mass_through(ws, L);
+                    u64 before, c;
+                    const int q = warp_first_above(row, ws, L, scaled(ur, wk), row.lane, &before, &c);
+                    if (threadIdx.x == 0) out[blockIdx.x] = q >= 0 ? cand_index(c) : -1;
+                }
+                return;
+            }
             const int nc = sort_cand(sb);
             if (sb.s.ncand <= (unsigned)kMaxCand) {
                 const int L = min(k, nc);
@@ -918,13 +1031,42 @@ sample_descending(const void* x, int32_t* out, int n, int method, float t, int k
     const float T = maxima_floor(sb.lmax[threadIdx.x], kTopLanes / kW, sb.s);
     u64 all;
     block_exscan(mass_and_gather(row, sb, T), sb.s, &all);
-    const bool fits = sb.s.ncand <= (unsigned)kMaxCand;  // final: block_exscan's barriers follow every atomic
-    const int nc = sort_cand(sb);
+    const unsigned ncand = sb.s.ncand;  // final: block_exscan's barriers follow every atomic
+    const bool fits = ncand <= (unsigned)kMaxCand;
     const u64 cut = (u64)((double)p * (double)all);
     u64 kept = all, unused;
     int idx = -1;
     bool ok = false;
-    if (fits) {
+    if (ncand <= (unsigned)kWarpCand) {
+        // one warp settles the row when the cut and the draw fall among the
+        // gathered candidates; else every thread takes the exact path below
+        if (threadIdx.x < 32) {
+            WarpSorted ws;
+            warp_sort_weigh(row, sb.cand, (int)ncand, row.lane, ws);
+            const u64 top_mass = ncand ? warp_mass_through(ws, (int)ncand) : 0ull;
+            bool done = false;
+            u64 kp = all, before, c;
+            if (cut < all) {
+                if (cut < top_mass && warp_first_above(row, ws, (int)ncand, cut, row.lane, &kp, &c) >= 0) {
+                    if (kp == 0) kp = 1;  // a target of 0 lands on the first entry
+                    done = true;
+                }
+            } else {
+                done = true;
+            }
+            const u64 target = scaled(ur, kp);
+            if (done && target < top_mass) {
+                const int q = warp_first_above(row, ws, (int)ncand, target, row.lane, &before, &c);
+                if (threadIdx.x == 0) out[blockIdx.x] = q >= 0 ? cand_index(c) : -1;
+            } else {
+                done = false;
+            }
+            if (threadIdx.x == 0) sb.s.ri[3] = done ? 1 : 0;
+        }
+        __syncthreads();
+        if (sb.s.ri[3]) return;
+    } else if (fits) {
+        const int nc = sort_cand(sb);
         const u64 top_mass = sorted_mass(row, nc, sb);
         if (cut < all) {
             if (cut < top_mass) {

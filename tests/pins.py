@@ -371,7 +371,8 @@ def sampling_probs_f64(x, method, t=1.0, k=1, p=1.0):
     order the draw walks, the smallest margin of any keep/cut decision)."""
     x = np.asarray(x, np.float64)
     valid = ~np.isnan(x)
-    order_sorted = sorted(np.nonzero(valid)[0], key=lambda i: (-x[i], i))
+    vi = np.nonzero(valid)[0]
+    order_sorted = list(vi[np.lexsort((vi, -x[vi]))])  # descending value, then ascending index
     probs = np.zeros_like(x)
     margin = np.inf
     if method == "temperature" or method == "min_p":
