@@ -1037,35 +1037,30 @@ sample_descending(const void* x, int32_t* out, int n, int method, float t, int k
     u64 kept = all, unused;
     int idx = -1;
     bool ok = false;
+    u64 top_mass = 0;  // the gathered candidates' mass (order-free: any thread order)
     if (ncand <= (unsigned)kWarpCand) {
-        // one warp settles the row when the cut and the draw fall among the
-        // gathered candidates; else every thread takes the exact path below
+        u64 mine = 0;
+        for (int j = threadIdx.x; j < (int)ncand; j += kT) mine += row.weight(key_value((uint32_t)(sb.cand[j] >> 32)));
+        block_exscan(mine, sb.s, &top_mass);
+    }
+    // The candidates settle the row when the cut lies below their mass (the
+    // draw then does too), or, with no cut, when the draw does.
+    const bool settles = ncand <= (unsigned)kWarpCand && (cut < all ? cut < top_mass : scaled(ur, all) < top_mass);
+    if (settles) {
+        // one warp finishes the row; the others are done
         if (threadIdx.x < 32) {
             WarpSorted ws;
             warp_sort_weigh(row, sb.cand, (int)ncand, row.lane, ws);
-            const u64 top_mass = ncand ? warp_mass_through(ws, (int)ncand) : 0ull;
-            bool done = false;
             u64 kp = all, before, c;
             if (cut < all) {
-                if (cut < top_mass && warp_first_above(row, ws, (int)ncand, cut, row.lane, &kp, &c) >= 0) {
-                    if (kp == 0) kp = 1;  // a target of 0 lands on the first entry
-                    done = true;
-                }
-            } else {
-                done = true;
+                warp_first_above(row, ws, (int)ncand, cut, row.lane, &kp, &c);
+                if (kp == 0) kp = 1;  // a target of 0 lands on the first entry
             }
-            const u64 target = scaled(ur, kp);
-            if (done && target < top_mass) {
-                const int q = warp_first_above(row, ws, (int)ncand, target, row.lane, &before, &c);
-                if (threadIdx.x == 0) out[blockIdx.x] = q >= 0 ? cand_index(c) : -1;
-            } else {
-                done = false;
-            }
-            if (threadIdx.x == 0) sb.s.ri[3] = done ? 1 : 0;
+            const int q = warp_first_above(row, ws, (int)ncand, scaled(ur, kp), row.lane, &before, &c);
+            if (threadIdx.x == 0) out[blockIdx.x] = q >= 0 ? cand_index(c) : -1;
         }
-        __syncthreads();
-        if (sb.s.ri[3]) return;
-    } else if (fits) {
+        return;
+    } else if (fits && ncand > (unsigned)kWarpCand) {
         const int nc = sort_cand(sb);
         const u64 top_mass = sorted_mass(row, nc, sb);
         if (cut < all) {
