@@ -57,10 +57,16 @@ template <int TPR>
 struct RowShape {
     static constexpr int kRpc = TPR == 32 ? 4 : 1;
     static constexpr int kMaxThreads = TPR == 0 ? 1024 : TPR * kRpc;
+    // Wide rows (512 or 1024 threads each): at least two rows resident per
+    // SM, so that one row's reduction overlaps another's loads (a single
+    // 1024-thread CTA per SM left the SM's load and store phases in turn).
+    // Not for the fused add, whose second input would then spill.
+    template <bool ADD>
+    static constexpr int min_blocks() { return (TPR >= 512 && !ADD) ? 2048 / TPR : 1; }
 };
 
 template <int DT, int K, bool ADD, int TPR>
-__global__ void __launch_bounds__(RowShape<TPR>::kMaxThreads)
+__global__ void __launch_bounds__(RowShape<TPR>::kMaxThreads, RowShape<TPR>::template min_blocks<ADD>())
 rmsnorm_rows(const void* x, const void* res, const void* w, void* y, void* h, int64_t rows, int d, float eps,
              int tpr_rt) {
     using S = Store<DT>;
@@ -177,7 +183,7 @@ rmsnorm_two_pass(const void* x, const void* res, const void* w, void* y, void* h
 // RMSNorm; the row's two sums (of x, then of (x - mu)^2) each take the same
 // fixed tree, so a row's bits depend only on the row, d and the type.
 template <int DT, int K, int TPR>
-__global__ void __launch_bounds__(RowShape<TPR>::kMaxThreads)
+__global__ void __launch_bounds__(RowShape<TPR>::kMaxThreads, RowShape<TPR>::template min_blocks<false>())
 layernorm_rows(const void* x, const void* g, const void* b, void* y, int64_t rows, int d, float eps, int tpr_rt) {
     using S = Store<DT>;
     constexpr int V = S::V;
