@@ -110,6 +110,14 @@ __device__ __forceinline__ uint32_t f32_to_bf16_bits(float f) {
     return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
+// Two values rounded to bf16 (nearest, ties to even, as f32_to_bf16_bits) in
+// one conversion: lo in bits 0..15, hi in bits 16..31.
+__device__ __forceinline__ uint32_t f32x2_to_bf16x2_bits(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
 template <int DT>
 struct Store;
 
@@ -152,7 +160,7 @@ struct Store<kBF16> {
         Vec16 v;
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-            v.w[e] = f32_to_bf16_bits(f[2 * e]) | (f32_to_bf16_bits(f[2 * e + 1]) << 16);
+            v.w[e] = f32x2_to_bf16x2_bits(f[2 * e], f[2 * e + 1]);
         return v;
     }
     __device__ __forceinline__ static float load1(const void* base, int64_t i) {

@@ -28,6 +28,8 @@
 // stages the normalised rows in shared memory (so a lane can read the
 // partner of each of its entries), rotates and stores them.  Head width is
 // limited to 32 chunks (head_dim <= 128 f32 / 256 bf16).
+#include <algorithm>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -62,26 +64,67 @@ __device__ __forceinline__ void load_chunk(const char* row, int c, int D, float 
 
 // Aligned rows whose pair partners lie a whole number of chunks apart (the
 // half layout with r/2 a multiple of the vector, or the interleaved layout
-// with r a multiple of it): no shared memory.  A lane's partner chunk is
-// fetched from the partner lane with four register shuffles (half layout),
-// or sits in the lane's own chunk (interleaved).  Same arithmetic as below.
+// with r a multiple of it).  One CTA per token, one warp per chunk of R * 4
+// head rows of q or k (a warp loops when the token has more chunks than
+// warps).  The token's r/2 angles are formed once, one pair per thread,
+// while the head rows' loads are in flight, and read back from shared memory
+// after one CTA barrier.  A lane's partner chunk is fetched from the partner
+// lane with four register shuffles (half layout), or sits in the lane's own
+// chunk (interleaved).
+//
+// The four rows' sums of squares are reduced by a transposed butterfly: at
+// the step of distance W/2 a lane keeps two of its four rows and hands the
+// other two to its partner, at distance W/4 it keeps one, and the remaining
+// steps reduce that one.  Each addition is the one the per-row butterfly
+// does (own partial + partner partial, the same pairs, the same order), so
+// every total is bit-identical to gbe_rmsnorm's; each lane then takes the
+// reciprocal root of its one row and shuffles the other three in.
+constexpr int kTokWarps = 16;  // most warps of one token's CTA
+constexpr int kMaxHalf = 128;  // r/2 <= 128: head_dim <= 256
+
+// Where angle i sits in the token's cos (or sin) table.  QPL = 2 (a lane
+// reads two quads, bf16 half layout): quad s of the lane whose angles start
+// at 8a sits at s * half/2 + 4a, so the eight lanes of one shared-memory
+// phase read 128 contiguous bytes.  Otherwise angle i sits at i.
+template <int QPL>
+__device__ __forceinline__ int angle_slot(int i, int half) {
+    if (QPL == 2) return ((i & 7) >> 2) * (half >> 1) + (i >> 3) * 4 + (i & 3);
+    return i;
+}
+
+// A shared-memory load the compiler keeps where it stands (volatile): the
+// angles are re-read in every pass instead of held in sixteen registers.
+__device__ __forceinline__ float4 lds4(const float* p) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"((unsigned)__cvta_generic_to_shared(p)));
+    return v;
+}
+__device__ __forceinline__ float2 lds2(const float* p) {
+    float2 v;
+    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"((unsigned)__cvta_generic_to_shared(p)));
+    return v;
+}
+
 template <int DT, int LAYOUT, bool CACHE>
-__global__ void __launch_bounds__(kWarps * 32)
-qk_norm_rope_shfl(QkSide A, QkSide B, int nca, int ncb, float eps, const int32_t* pos, int64_t T, int D, int r,
-                  const float* inv_freq, const float2* cache, int64_t cache_len, float mu, int W) {
+__global__ void __launch_bounds__(kTokWarps * 32, 2)
+qk_norm_rope_tok(QkSide A, QkSide B, int nca, int ncb, float eps, const int32_t* pos, int D, int r,
+                 const float* inv_freq, const float2* cache, int64_t cache_len, float mu, int W) {
     using S = Store<DT>;
     constexpr int V = S::V;
     constexpr int64_t ES = sizeof(typename S::T);
     constexpr int NP = kPassesShfl;
+    constexpr int NA = LAYOUT == 0 ? V : V / 2;  // angles of one lane's chunk
+    constexpr int QPL = NA >= 8 ? 2 : 1;          // 16-byte quads of them (NA = 2: one 8-byte pair)
+    __shared__ __align__(16) float cs_cos[kMaxHalf];
+    __shared__ __align__(16) float cs_sin[kMaxHalf];
+    __shared__ __align__(16) float cs_nsin[LAYOUT == 0 ? kMaxHalf : 1];  // -sin, for first members
     pdl_begin();
     const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t item = (int64_t)blockIdx.x * kWarps + wib;
+    const int nw = blockDim.x >> 5;
+    const int64_t t = blockIdx.x;
     const int per_tok = nca + ncb;
-    const int64_t t = item / per_tok;
-    if (t >= T) return;  // whole warps leave together
-    const int ci = (int)(item - t * per_tok);
-    const bool second = ci >= nca;
-    const QkSide Q = second ? B : A;
     const int nchunks = D / V;
     const int R = 32 / W;
     const int sub = lane / W;
@@ -89,116 +132,323 @@ qk_norm_rope_shfl(QkSide A, QkSide B, int nca, int ncb, float eps, const int32_t
     const bool has = c < nchunks;
     const int half = r >> 1;
     const int G = half / V;  // chunks between pair members (half layout)
-    const int h0 = (second ? ci - nca : ci) * R * NP;
-    const char* xt = Q.x + t * Q.xs * ES;
-    char* yt = Q.y + t * Q.ys * ES;
-
-    Vec16 raw[NP];
-#pragma unroll
-    for (int k = 0; k < NP; ++k) {
-        const int h = h0 + k * R + sub;
-        raw[k] = Vec16{{0u, 0u, 0u, 0u}};
-        if (has && h < Q.H) raw[k] = ld_stream(xt + ((int64_t)h * D + (int64_t)c * V) * ES);
-    }
-    float gv[V];
-    if (has) S::unpack(ld_reuse(Q.g + (int64_t)c * 16), gv);
-    // The angles of the pairs this lane's entries belong to, each formed once
-    // per lane pair, with the same instructions in every lane (no divergent
-    // branch): interleaved, the two members of a pair sit in one lane (even
-    // entries form the angle, odd ones copy it); half layout, a first-member
-    // lane and its partner lane hold the same pairs, so each forms half of
-    // them and they swap the other half by shuffle.
-    const int src = LAYOUT == 0 ? (c < G ? lane + G : (c < 2 * G ? lane - G : lane)) : lane;
-    constexpr int HV = V / 2;
     const int32_t p = pos[t];
-    float tc[HV], ts[HV];
-    const bool low = LAYOUT == 0 ? c < G : true;
+
+    // the first item's loads go out before anything else
+    int ci = wib;
+    Vec16 raw[NP];
+    auto load_item = [&](int item) {
+        const bool second = item >= nca;
+        const QkSide& Q = second ? B : A;
+        const int h0 = (second ? item - nca : item) * R * NP;
+        const char* xt = Q.x + t * Q.xs * ES;
 #pragma unroll
-    for (int k = 0; k < HV; ++k) {
-        const int e = LAYOUT == 0 ? k + (low ? 0 : HV) : 2 * k;  // the entry whose angle this lane forms
-        const int j = c * V + e;
-        tc[k] = 1.0f;
-        ts[k] = 0.0f;
-        if (has && j < r) {
-            const int i = LAYOUT == 0 ? (j < half ? j : j - half) : (j >> 1);
-            if (CACHE && p >= 0 && p < cache_len) {
-                const float2 v = __ldg(cache + (int64_t)p * half + i);
-                tc[k] = v.x;
-                ts[k] = v.y;
-            } else {
-                sincosf(__fmul_rn((float)p, __ldg(inv_freq + i)), &ts[k], &tc[k]);
-            }
+        for (int k = 0; k < NP; ++k) {
+            const int h = h0 + k * R + sub;
+            raw[k] = Vec16{{0u, 0u, 0u, 0u}};
+            if (has && h < Q.H) raw[k] = ld_stream(xt + ((int64_t)h * D + (int64_t)c * V) * ES);
         }
+    };
+    if (ci < per_tok) load_item(ci);
+
+    // the token's angles, one pair per thread
+    for (int i = threadIdx.x; i < half; i += blockDim.x) {
+        float cv, sv;
+        if (CACHE && p >= 0 && p < cache_len) {
+            const float2 v = __ldg(cache + (int64_t)p * half + i);
+            cv = v.x;
+            sv = v.y;
+        } else {
+            sincosf(__fmul_rn((float)p, __ldg(inv_freq + i)), &sv, &cv);
+        }
+        const int slot = angle_slot<QPL>(i, half);
+        cs_cos[slot] = cv;
+        cs_sin[slot] = sv;
+        if (LAYOUT == 0) cs_nsin[slot] = -sv;
     }
-    float ca[V], sa[V];
-    if (LAYOUT == 1) {
+    __syncthreads();  // every thread of the CTA reaches it: no thread has left yet
+
+    const bool rot = has && c * V < r;  // this chunk is rotated
+    const bool first_half = LAYOUT == 0 && c < G;
+    const int src = LAYOUT == 0 ? (c < G ? lane + G : (c < 2 * G ? lane - G : lane)) : lane;
+    // the starting angle of this lane's chunk, and its quads in the table
+    const int ib = LAYOUT == 0 ? (first_half ? c : c - G) * V : c * (V / 2);
+    int slot0 = 0;
+    if (rot) slot0 = angle_slot<QPL>(ib, half);
+    const float* tc = cs_cos + slot0;
+    const float* tsn = (LAYOUT == 0 && first_half ? cs_nsin : cs_sin) + slot0;
+
+    for (; ci < per_tok; ci += nw) {
+        if (ci != wib) load_item(ci);
+        const bool second = ci >= nca;
+        const QkSide& Q = second ? B : A;
+        const int h0 = (second ? ci - nca : ci) * R * NP;
+        char* yt = Q.y + t * Q.ys * ES;
+        float gv[V];
+        if (has) S::unpack(ld_reuse(Q.g + (int64_t)c * 16), gv);
+
+        // sums of squares of the four rows this lane holds a chunk of
+        float s[NP];
 #pragma unroll
-        for (int k = 0; k < HV; ++k) {
-            ca[2 * k] = ca[2 * k + 1] = tc[k];
-            sa[2 * k] = sa[2 * k + 1] = ts[k];
-        }
-    } else {
-#pragma unroll
-        for (int k = 0; k < HV; ++k) {
-            const float pc = __shfl_sync(0xFFFFFFFFu, tc[k], src);  // the partner's entry k (low) or k + HV
-            const float ps = __shfl_sync(0xFFFFFFFFu, ts[k], src);
-            ca[k] = low ? tc[k] : pc;
-            sa[k] = low ? ts[k] : ps;
-            ca[k + HV] = low ? pc : tc[k];
-            sa[k + HV] = low ? ps : ts[k];
-        }
-    }
-    float s[NP];
-#pragma unroll
-    for (int k = 0; k < NP; ++k) {
-        s[k] = 0.0f;
-        if (has && h0 + k * R + sub < Q.H) {
+        for (int k = 0; k < NP; ++k) {
             float f[V];
-            S::unpack(raw[k], f);
+            S::unpack(raw[k], f);  // zero for absent rows and chunks
+            s[k] = 0.0f;
 #pragma unroll
             for (int e = 0; e < V; ++e) s[k] = __fmaf_rn(f[e], f[e], s[k]);
         }
+        float inv[NP];
+        if (W >= 4) {
+            const int m1 = W >> 1, m2 = W >> 2;
+            const bool b1 = (lane & m1) != 0, b2 = (lane & m2) != 0;
+            float k0 = b1 ? s[2] : s[0], k1 = b1 ? s[3] : s[1];
+            const float g0 = b1 ? s[0] : s[2], g1 = b1 ? s[1] : s[3];
+            k0 = __fadd_rn(k0, __shfl_xor_sync(0xFFFFFFFFu, g0, m1));
+            k1 = __fadd_rn(k1, __shfl_xor_sync(0xFFFFFFFFu, g1, m1));
+            float kk = b2 ? k1 : k0;
+            const float gg = b2 ? k0 : k1;
+            kk = __fadd_rn(kk, __shfl_xor_sync(0xFFFFFFFFu, gg, m2));
+            for (int m = W >> 3; m >= 1; m >>= 1) kk = __fadd_rn(kk, __shfl_xor_sync(0xFFFFFFFFu, kk, m));
+            // this lane's row is pass 2*b1 + b2
+            const float own = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(kk, (float)D), eps)));
+            const int base = sub * W;
+#pragma unroll
+            for (int k = 0; k < NP; ++k)
+                inv[k] = __shfl_sync(0xFFFFFFFFu, own, base + ((k >> 1) ? m1 : 0) + ((k & 1) ? m2 : 0));
+        } else {
+            for (int m = W >> 1; m >= 1; m >>= 1) {
+#pragma unroll
+                for (int k = 0; k < NP; ++k) s[k] = __fadd_rn(s[k], __shfl_xor_sync(0xFFFFFFFFu, s[k], m));
+            }
+#pragma unroll
+            for (int k = 0; k < NP; ++k)
+                inv[k] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(s[k], (float)D), eps)));
+        }
+
+#pragma unroll
+        for (int k = 0; k < NP; ++k) {
+            if (h0 + k * R >= Q.H) break;  // uniform across the warp
+            const int h = h0 + k * R + sub;
+            const bool live = has && h < Q.H;
+            float n[V];
+            S::unpack(raw[k], n);
+#pragma unroll
+            for (int e = 0; e < V; ++e) n[e] = __fmul_rn(__fmul_rn(n[e], inv[k]), gv[e]);
+            const Vec16 nv = S::pack(n);  // the stored (rounded) normalised chunk
+            S::unpack(nv, n);
+            float o[V], m2[V];
+            if (LAYOUT == 0) {
+                Vec16 pv;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) pv.w[q] = __shfl_sync(0xFFFFFFFFu, nv.w[q], src);
+                S::unpack(pv, m2);
+            } else {
+#pragma unroll
+                for (int e = 0; e < V; ++e) m2[e] = n[e ^ 1];
+            }
+            // The angles of this lane's entries.  Both members of a pair take
+            // one formula, out = mu * (own * cos + partner * sg), sg = -sin for
+            // the first member and +sin for the second: IEEE gives a - b ==
+            // a + (-b) and a + b == b + a exactly, so this is the same
+            // arithmetic as mu * (a cos - b sin) and mu * (a sin + b cos).  A
+            // first-half lane (half layout) reads the negated sines; in the
+            // interleaved layout the even entries are the first members.
+            float ac[NA], as[NA];
+#pragma unroll
+            for (int q = 0; q < QPL; ++q) {
+                if (NA >= 4) {
+                    const float4 vc = lds4(tc + q * (half >> 1));
+                    const float4 vs = lds4(tsn + q * (half >> 1));
+                    ac[4 * q] = vc.x; ac[4 * q + 1] = vc.y; ac[4 * q + 2] = vc.z; ac[4 * q + 3] = vc.w;
+                    as[4 * q] = vs.x; as[4 * q + 1] = vs.y; as[4 * q + 2] = vs.z; as[4 * q + 3] = vs.w;
+                } else {
+                    const float2 vc = lds2(tc);
+                    const float2 vs = lds2(tsn);
+                    ac[0] = vc.x; ac[1] = vc.y;
+                    as[0] = vs.x; as[1] = vs.y;
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < V; ++e) {
+                const float ce = LAYOUT == 0 ? ac[e] : ac[e >> 1];
+                const float se = LAYOUT == 0 ? as[e] : ((e & 1) ? as[e >> 1] : -as[e >> 1]);
+                o[e] = rot ? __fmul_rn(mu, __fadd_rn(__fmul_rn(n[e], ce), __fmul_rn(m2[e], se))) : n[e];
+            }
+            if (live) st_stream(yt + ((int64_t)h * D + (int64_t)c * V) * ES, S::pack(o));
+        }
     }
-    for (int m = W >> 1; m >= 1; m >>= 1) {
+}
+
+// Both members of one lane's pairs rotated and stored: lo = mu (a cos - b
+// sin), hi = mu (a sin + b cos), each product, sum and the scale rounded on
+// its own as gbe_rope does, one quad of pairs at a time (its cos and sin read
+// from shared memory then).  MU false: mu is 1, and 1 * x == x for every
+// value the sum can take (-0, infinities and NaN included), so the scale is
+// left out.
+template <int DT, bool MU>
+__device__ __forceinline__ void rotate_store(const float (&a)[Store<DT>::V], const float (&b)[Store<DT>::V],
+                                             const float* tc, const float* ts, int qstride, float mu, char* lo_at,
+                                             char* hi_at) {
+    using S = Store<DT>;
+    constexpr int V = S::V;
+    float lo[V], hi[V];
 #pragma unroll
-        for (int k = 0; k < NP; ++k) s[k] = __fadd_rn(s[k], __shfl_xor_sync(0xFFFFFFFFu, s[k], m));
+    for (int q = 0; q < V / 4; ++q) {
+        const float4 vc = lds4(tc + q * qstride);
+        const float4 vs = lds4(ts + q * qstride);
+        const float c4[4] = {vc.x, vc.y, vc.z, vc.w};
+        const float s4[4] = {vs.x, vs.y, vs.z, vs.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int e = 4 * q + j;
+            lo[e] = __fsub_rn(__fmul_rn(a[e], c4[j]), __fmul_rn(b[e], s4[j]));
+            hi[e] = __fadd_rn(__fmul_rn(a[e], s4[j]), __fmul_rn(b[e], c4[j]));
+            if (MU) {
+                lo[e] = __fmul_rn(mu, lo[e]);
+                hi[e] = __fmul_rn(mu, hi[e]);
+            }
+        }
     }
-    const bool rot = has && c * V < r;        // this chunk is rotated
-    // Both members of a pair take one formula, out = mu * (own * cos + partner * sg)
-    // with sg = -sin for the first member and +sin for the second: IEEE gives
-    // a - b == a + (-b) and a + b == b + a exactly, so this is the same
-    // arithmetic as mu * (a cos - b sin) and mu * (a sin + b cos).
+    st_stream(lo_at, S::pack(lo));
+    st_stream(hi_at, S::pack(hi));
+}
+
+// Half layout, the whole head rotated (r = head_dim), a power-of-two number
+// of chunks (2 to 32): a lane holds chunk c of the first half of a head row
+// and chunk c + L of the second half (L = chunks / 2), so both members of
+// every pair it rotates sit in its own registers -- no exchange between
+// lanes.  gbe_rmsnorm's tree for such a row first adds the sums of chunks c
+// and c + L (its butterfly step of distance L, chunk c's sum first): here
+// that step is an addition inside the lane, and the remaining steps run
+// over the L lanes of the row.  Rows: 32 / L per pass, two passes per warp
+// item, whose sums share the butterfly transposed (at distance L/2 a lane
+// keeps one pass and hands the other to its partner).  One CTA per token,
+// the token's angles formed once into shared memory, as in qk_norm_rope_tok.
+template <int DT, bool CACHE>
+__global__ void __launch_bounds__(kTokWarps * 32, 2)
+qk_norm_rope_pair(QkSide A, QkSide B, int nca, int ncb, float eps, const int32_t* pos, int D, int lgL,
+                  const float* inv_freq, const float2* cache, int64_t cache_len, float mu) {
+    using S = Store<DT>;
+    constexpr int V = S::V;
+    constexpr int64_t ES = sizeof(typename S::T);
+    constexpr int NP = 2;
+    constexpr int QPL = V >= 8 ? 2 : 1;  // 16-byte quads of one lane's angles
+    __shared__ __align__(16) float cs_cos[kMaxHalf];
+    __shared__ __align__(16) float cs_sin[kMaxHalf];
+    pdl_begin();
+    const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nw = blockDim.x >> 5;
+    const int64_t t = blockIdx.x;
+    const int per_tok = nca + ncb;
+    const int L = 1 << lgL;    // lanes of one head row
+    const int RP = 32 >> lgL;  // head rows per pass
+    const int sub = lane >> lgL;
+    const int c = lane & (L - 1);
+    const int half = D >> 1;  // L * V
+    const int32_t p = pos[t];
+
+    int ci = wib;
+    Vec16 raw[NP][2];
+    auto load_item = [&](int item) {
+        const bool second = item >= nca;
+        const QkSide& Q = second ? B : A;
+        const int h0 = (second ? item - nca : item) * RP * NP;
+        const char* xt = Q.x + t * Q.xs * ES + (int64_t)c * 16;
 #pragma unroll
-    for (int e = 0; e < V; ++e) {
-        const bool first_e = LAYOUT == 0 ? c < G : (e & 1) == 0;
-        sa[e] = first_e ? -sa[e] : sa[e];
+        for (int k = 0; k < NP; ++k) {
+            const int h = h0 + k * RP + sub;
+            raw[k][0] = raw[k][1] = Vec16{{0u, 0u, 0u, 0u}};
+            if (h < Q.H) {
+                const char* row = xt + (int64_t)h * D * ES;
+                raw[k][0] = ld_stream(row);
+                raw[k][1] = ld_stream(row + half * ES);
+            }
+        }
+    };
+    if (ci < per_tok) load_item(ci);
+
+    for (int i = threadIdx.x; i < half; i += blockDim.x) {
+        float cv, sv;
+        if (CACHE && p >= 0 && p < cache_len) {
+            const float2 v = __ldg(cache + (int64_t)p * half + i);
+            cv = v.x;
+            sv = v.y;
+        } else {
+            sincosf(__fmul_rn((float)p, __ldg(inv_freq + i)), &sv, &cv);
+        }
+        const int slot = angle_slot<QPL>(i, half);
+        cs_cos[slot] = cv;
+        cs_sin[slot] = sv;
     }
+    __syncthreads();  // every thread of the CTA reaches it: no thread has left yet
+    const int slot0 = angle_slot<QPL>(c * V, half);
+    const bool mu_one = mu == 1.0f;
+
+    for (; ci < per_tok; ci += nw) {
+        if (ci != wib) load_item(ci);
+        const bool second = ci >= nca;
+        const QkSide& Q = second ? B : A;
+        const int h0 = (second ? ci - nca : ci) * RP * NP;
+        const Vec16 g_lo = ld_reuse(Q.g + (int64_t)c * 16);
+        const Vec16 g_hi = ld_reuse(Q.g + (int64_t)c * 16 + half * ES);
+
+        // the sum of squares of each chunk in element order, then the
+        // butterfly step of distance L inside the lane
+        float s[NP];
 #pragma unroll
-    for (int k = 0; k < NP; ++k) {
-        if (h0 + k * R >= Q.H) break;  // uniform across the warp
-        const int h = h0 + k * R + sub;
-        const bool live = has && h < Q.H;
-        const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(s[k], (float)D), eps)));
-        float n[V];
-        S::unpack(raw[k], n);
+        for (int k = 0; k < NP; ++k) {
+            float f[V];
+            float s0 = 0.0f, s1 = 0.0f;
+            S::unpack(raw[k][0], f);
 #pragma unroll
-        for (int e = 0; e < V; ++e) n[e] = __fmul_rn(__fmul_rn(n[e], inv), gv[e]);
-        const Vec16 nv = S::pack(n);  // the stored (rounded) normalised chunk
-        S::unpack(nv, n);
-        float o[V], m2[V];
-        if (LAYOUT == 0) {
-            Vec16 pv;
+            for (int e = 0; e < V; ++e) s0 = __fmaf_rn(f[e], f[e], s0);
+            S::unpack(raw[k][1], f);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) pv.w[q] = __shfl_sync(0xFFFFFFFFu, nv.w[q], src);
-            S::unpack(pv, m2);
+            for (int e = 0; e < V; ++e) s1 = __fmaf_rn(f[e], f[e], s1);
+            s[k] = __fadd_rn(s0, s1);
+        }
+        float inv[NP];
+        if (L >= 2) {
+            const int m1 = L >> 1;
+            const bool b1 = (lane & m1) != 0;
+            float kk = b1 ? s[1] : s[0];
+            const float gg = b1 ? s[0] : s[1];
+            kk = __fadd_rn(kk, __shfl_xor_sync(0xFFFFFFFFu, gg, m1));
+            for (int m = L >> 2; m >= 1; m >>= 1) kk = __fadd_rn(kk, __shfl_xor_sync(0xFFFFFFFFu, kk, m));
+            const float own = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(kk, (float)D), eps)));
+            const int base = sub << lgL;
+            inv[0] = __shfl_sync(0xFFFFFFFFu, own, base);
+            inv[1] = __shfl_sync(0xFFFFFFFFu, own, base + m1);
         } else {
 #pragma unroll
-            for (int e = 0; e < V; ++e) m2[e] = n[e ^ 1];
+            for (int k = 0; k < NP; ++k)
+                inv[k] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(s[k], (float)D), eps)));
         }
+
 #pragma unroll
-        for (int e = 0; e < V; ++e)
-            o[e] = rot ? __fmul_rn(mu, __fadd_rn(__fmul_rn(n[e], ca[e]), __fmul_rn(m2[e], sa[e]))) : n[e];
-        if (live) st_stream(yt + ((int64_t)h * D + (int64_t)c * V) * ES, S::pack(o));
+        for (int k = 0; k < NP; ++k) {
+            if (h0 + k * RP >= Q.H) break;  // uniform across the warp
+            const int h = h0 + k * RP + sub;
+            float a[V], b[V], g[V];
+            // normalised and rounded to storage, as a stored intermediate would be
+            S::unpack(raw[k][0], a);
+            S::unpack(g_lo, g);
+#pragma unroll
+            for (int e = 0; e < V; ++e) a[e] = __fmul_rn(__fmul_rn(a[e], inv[k]), g[e]);
+            S::unpack(S::pack(a), a);
+            S::unpack(raw[k][1], b);
+            S::unpack(g_hi, g);
+#pragma unroll
+            for (int e = 0; e < V; ++e) b[e] = __fmul_rn(__fmul_rn(b[e], inv[k]), g[e]);
+            S::unpack(S::pack(b), b);
+            if (h < Q.H) {
+                char* row = Q.y + (t * Q.ys + (int64_t)h * D) * ES + (int64_t)c * 16;
+                if (mu_one)
+                    rotate_store<DT, false>(a, b, cs_cos + slot0, cs_sin + slot0, half >> 1, mu, row, row + half * ES);
+                else
+                    rotate_store<DT, true>(a, b, cs_cos + slot0, cs_sin + slot0, half >> 1, mu, row, row + half * ES);
+            }
+        }
     }
 }
 
@@ -346,6 +596,21 @@ cudaError_t launch_dt(const QkNormRopeArgs& a, bool vec, cudaStream_t st) {
         sd[k].ys = a.side[k].stride;
         sd[k].H = (int)a.side[k].H;
     }
+    int lgL = 0;
+    while ((2 << lgL) < nchunks) ++lgL;
+    const bool pair = vec && a.layout == 0 && a.r == a.D && nchunks >= 2 && (2 << lgL) == nchunks;
+    if (pair) {
+        const int rows_item = (32 >> lgL) * 2;
+        const int pa = (int)((a.side[0].H + rows_item - 1) / rows_item);
+        const int pb = (int)((a.side[1].H + rows_item - 1) / rows_item);
+        const int warps = (int)std::min<int64_t>(pa + pb, kTokWarps);
+        const float2* cs = reinterpret_cast<const float2*>(a.cos_sin);
+        if (cs != nullptr)
+            return launch(qk_norm_rope_pair<DT, true>, dim3((unsigned)a.T), dim3(warps * 32), 0, st, sd[0], sd[1], pa,
+                          pb, a.eps, a.pos, (int)a.D, lgL, a.inv_freq, cs, a.cache_len, a.mu);
+        return launch(qk_norm_rope_pair<DT, false>, dim3((unsigned)a.T), dim3(warps * 32), 0, st, sd[0], sd[1], pa, pb,
+                      a.eps, a.pos, (int)a.D, lgL, a.inv_freq, cs, a.cache_len, a.mu);
+    }
     const bool shfl = vec && a.r > 0 && (a.layout == 0 ? (a.r / 2) % V == 0 : a.r % V == 0);
     const int rows_per_item = (32 / W) * (shfl ? kPassesShfl : kPasses);  // head rows one warp handles
     const int nca = (int)((a.side[0].H + rows_per_item - 1) / rows_per_item);
@@ -358,9 +623,10 @@ cudaError_t launch_dt(const QkNormRopeArgs& a, bool vec, cudaStream_t st) {
 #define GBE_QKN(L, VV, C)                                                                                 \
     return launch(qk_norm_rope_kernel<DT, L, VV, C>, dim3(grid), dim3(kWarps * 32), 0, st, sd[0], sd[1], nca, ncb, \
                   a.eps, a.pos, a.T, Di, ri, a.inv_freq, cache, a.cache_len, a.mu, W)
-#define GBE_QKN_S(L, C)                                                                                        \
-    return launch(qk_norm_rope_shfl<DT, L, C>, dim3(grid), dim3(kWarps * 32), 0, st, sd[0], sd[1], nca, ncb, a.eps, \
-                  a.pos, a.T, Di, ri, a.inv_freq, cache, a.cache_len, a.mu, W)
+    const int tok_warps = (int)std::min<int64_t>(nca + ncb, kTokWarps);
+#define GBE_QKN_S(L, C)                                                                                  \
+    return launch(qk_norm_rope_tok<DT, L, C>, dim3((unsigned)a.T), dim3(tok_warps * 32), 0, st, sd[0], sd[1], nca, \
+                  ncb, a.eps, a.pos, Di, ri, a.inv_freq, cache, a.cache_len, a.mu, W)
     if (shfl) {
         if (a.layout == 0) {
             if (cached) GBE_QKN_S(0, true); else GBE_QKN_S(0, false);

@@ -39,12 +39,19 @@ def _unfused(q, k, gq, gk, pos, om, r, mu, layout, eps=1e-6):
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("layout", [0, 1])
 @pytest.mark.parametrize("T,Hq,Hk,D,r", [(9, 32, 8, 128, 128), (5, 4, 2, 64, 32), (3, 3, 1, 16, 16),
-                                         (4, 2, 2, 8, 8), (17, 16, 4, 96, 64)])
-def test_equals_unfused_composition(dtype, layout, T, Hq, Hk, D, r):
+                                         (4, 2, 2, 8, 8), (17, 16, 4, 96, 64),
+                                         # more chunks of head rows than warps of a token's CTA
+                                         (3, 160, 9, 128, 128),
+                                         # the widest head (256 bf16 / 128 f32 is the limit)
+                                         (2, 4, 2, 256, 256), (3, 5, 3, 128, 96)])
+@pytest.mark.parametrize("mu", [1.0, 1.1])
+def test_equals_unfused_composition(dtype, layout, T, Hq, Hk, D, r, mu):
+    if dtype == "f32" and D > 128:
+        pytest.skip("head_dim is limited to 32 chunks: 128 f32 entries")
     q, k, gq, gk, pos, om = _case(1, T, Hq, Hk, D, r, dtype)
-    qn, kn = _unfused(q, k, gq, gk, pos, om, r, 1.1, layout)
+    qn, kn = _unfused(q, k, gq, gk, pos, om, r, mu, layout)
     qd, kd = to_dev(q), to_dev(k)
-    gbe.gbe_qk_norm_rope(qd, qd, to_dev(gq), kd, kd, to_dev(gk), 1e-6, to_dev(pos), to_dev(om), r, 1.1, layout)
+    gbe.gbe_qk_norm_rope(qd, qd, to_dev(gq), kd, kd, to_dev(gk), 1e-6, to_dev(pos), to_dev(om), r, mu, layout)
     assert np.array_equal(bits(qd), bits(qn)), "q"
     assert np.array_equal(bits(kd), bits(kn)), "k"
 
@@ -66,10 +73,11 @@ def test_against_oracle(dtype, layout):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_qkv_slices_cache_and_unaligned(dtype):
+@pytest.mark.parametrize("layout", [0, 1])
+def test_qkv_slices_cache_and_unaligned(dtype, layout):
     T, Hq, Hk, D, r = 33, 8, 2, 64, 64
     q, k, gq, gk, pos, om = _case(3, T, Hq, Hk, D, r, dtype)
-    qn, kn = _unfused(q, k, gq, gk, pos, om, r, 1.0, 0)
+    qn, kn = _unfused(q, k, gq, gk, pos, om, r, 1.0, layout)
     width = (Hq + 2 * Hk) * D
     tdt = torch.float32 if dtype == "f32" else torch.bfloat16
     for extra in (0, 1):  # extra = 1: token stride not a multiple of 16 bytes -> scalar path
@@ -82,7 +90,7 @@ def test_qkv_slices_cache_and_unaligned(dtype):
         qv = buf.as_strided((T, Hq, D), (stride, D, 1))
         kv = buf.as_strided((T, Hk, D), (stride, D, 1), Hq * D)
         cache = gbe.rope_cos_sin(to_dev(om), r, 1 << 15) if extra == 0 else None  # some positions past it
-        gbe.gbe_qk_norm_rope(qv, qv, to_dev(gq), kv, kv, to_dev(gk), 1e-6, to_dev(pos), to_dev(om), r, 1.0, 0,
+        gbe.gbe_qk_norm_rope(qv, qv, to_dev(gq), kv, kv, to_dev(gk), 1e-6, to_dev(pos), to_dev(om), r, 1.0, layout,
                              cos_sin=cache)
         assert np.array_equal(bits(qv.contiguous()), bits(qn)), extra
         assert np.array_equal(bits(kv.contiguous()), bits(kn)), extra
