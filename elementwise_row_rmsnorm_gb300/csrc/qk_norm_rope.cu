@@ -21,13 +21,13 @@
 //  * the angles are float(p) * omega_i and CUDA's sincosf (or the same values
 //    from the cos/sin table), as in rope.cu.
 //
-// Map: a warp owns one chunk of head rows of one token (4 passes of 32 / W
-// rows: 8 rows for bf16 head_dim 128), so the heads of a token spread over
-// several warps.  It issues the loads of all its rows first, forms its
-// lanes' angles while they are in flight, reduces the rows side by side,
-// stages the normalised rows in shared memory (so a lane can read the
-// partner of each of its entries), rotates and stores them.  Head width is
-// limited to 32 chunks (head_dim <= 128 f32 / 256 bf16).
+// Map: one CTA per token (qk_norm_rope_pair and qk_norm_rope_tok, aligned
+// rows), a warp per chunk of the token's head rows of q or k; the token's
+// angles are formed once into shared memory.  Unaligned rows take
+// qk_norm_rope_kernel: a warp per chunk of head rows that stages the
+// normalised rows in shared memory (so a lane can read the partner of each
+// of its entries).  Head width is limited to 32 chunks (head_dim <= 128 f32
+// / 256 bf16).
 #include <algorithm>
 
 #include "common.cuh"
