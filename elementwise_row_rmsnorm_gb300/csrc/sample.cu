@@ -163,6 +163,17 @@ struct Row {
     // fixed-point weight of a logit that is not NaN
     __device__ __forceinline__ u64 weight(float v) const { return w_of(e_of(v)); }
 
+    // this lane's 16-byte vector of the tile starting at j, NaN entries past
+    // the segment (aligned rows)
+    __device__ __forceinline__ Vec16 load_raw(int j) const {
+        const int i = j + lane * V;
+        if (i < s1) return ld_reuse(static_cast<const char*>(x) + (base + i) * (int64_t)sizeof(typename Store<DT>::T));
+        Vec16 r;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) r.w[w] = DT == kBF16 ? 0x7FC07FC0u : 0x7FC00000u;
+        return r;
+    }
+
     // this lane's V entries of the tile starting at j (NaN past the segment)
     __device__ __forceinline__ void load(int j, float (&v)[V]) const {
         const int i = j + lane * V;
@@ -201,6 +212,49 @@ struct Row {
         each(f, [] {});
     }
 };
+
+// The largest number among a vector's entries, NaN only when all are NaN
+// (bf16: packed maxima, which skip NaN as fmaxf does).  Some entry is >= T
+// exactly when this maximum is.
+template <int DT>
+__device__ __forceinline__ float vec_max(const Vec16& r) {
+    if (DT == kBF16) {
+        const __nv_bfloat162 m = __hmax2(__hmax2(*reinterpret_cast<const __nv_bfloat162*>(&r.w[0]),
+                                                 *reinterpret_cast<const __nv_bfloat162*>(&r.w[1])),
+                                         __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&r.w[2]),
+                                                 *reinterpret_cast<const __nv_bfloat162*>(&r.w[3])));
+        const float2 f = __bfloat1622float2(m);
+        return fmaxf(f.x, f.y);
+    }
+    return fmaxf(fmaxf(__uint_as_float(r.w[0]), __uint_as_float(r.w[1])),
+                 fmaxf(__uint_as_float(r.w[2]), __uint_as_float(r.w[3])));
+}
+
+// bit e set for the entries v[e] >= T (NaN fails)
+template <int V>
+__device__ __forceinline__ unsigned bits_ge(const float (&v)[V], float T) {
+    unsigned in = 0;
+#pragma unroll
+    for (int e = 0; e < V; ++e) in |= (v[e] >= T ? 1u : 0u) << e;
+    return in;
+}
+
+// A unit's e summed in f32 in index order, NaN entries left out.  Every e of
+// a number lies in [0, 1], so the plain sum is NaN exactly when some entry
+// is NaN; only then is the unit summed again with those entries skipped.
+template <int DT, bool VEC>
+__device__ __forceinline__ float unit_sum(const Row<DT, VEC>& row, const float (&v)[Row<DT, VEC>::V]) {
+    constexpr int V = Row<DT, VEC>::V;
+    float s = 0.0f;
+#pragma unroll
+    for (int e = 0; e < V; ++e) s = __fadd_rn(s, row.e_of(v[e]));
+    if (s != s) {
+        s = 0.0f;
+#pragma unroll
+        for (int e = 0; e < V; ++e) s = __fadd_rn(s, fmaxf(row.e_of(v[e]), 0.0f));  // NaN gives 0
+    }
+    return s;
+}
 
 // ---- warp and block primitives ----------------------------------------------------
 
@@ -409,6 +463,7 @@ sample_index_order(const void* x, int32_t* out, int n, float t, float p, const f
     int nv;
     if (!first_pass<false>(row, out, sh, &nv)) return;
     auto unit = [&](const float (&v)[V]) -> u64 {
+        if (!MINP) return fixed40(unit_sum(row, v));
         float s = 0.0f;
 #pragma unroll
         for (int e = 0; e < V; ++e) s = __fadd_rn(s, kept_e<DT, VEC, MINP>(row, v[e], p));
@@ -898,15 +953,30 @@ __device__ void gather_ge(const Row<DT, VEC>& row, ShBig& sb, float T) {
     __syncthreads();
     if (threadIdx.x == 0) sb.s.ncand = 0;
     __syncthreads();
+    if (VEC) {
+        // the tile's maximum first; its entries only when it reaches T (rare)
+        for (int j0 = row.s0; j0 < row.s1; j0 += kTile * kU) {
+            Vec16 r[kU];
+#pragma unroll
+            for (int q = 0; q < kU; ++q) r[q] = row.load_raw(j0 + q * kTile);
+#pragma unroll
+            for (int q = 0; q < kU; ++q) {
+                if (vec_max<DT>(r[q]) >= T) {
+                    float v[V];
+                    Store<DT>::unpack(r[q], v);
+                    gather_bits(row, sb, bits_ge(v, T), j0 + q * kTile + row.lane * V);
+                }
+            }
+        }
+        return;
+    }
     for (int j0 = row.s0; j0 < row.s1; j0 += kTile * kU) {
         float v[kU][V];
 #pragma unroll
         for (int q = 0; q < kU; ++q) row.load(j0 + q * kTile, v[q]);
 #pragma unroll
         for (int q = 0; q < kU; ++q) {
-            unsigned in = 0;
-#pragma unroll
-            for (int e = 0; e < V; ++e) in |= (v[q][e] >= T ? 1u : 0u) << e;
+            const unsigned in = bits_ge(v[q], T);
             if (in) gather_bits(row, sb, in, j0 + q * kTile + row.lane * V);
         }
     }
@@ -923,25 +993,34 @@ __device__ u64 mass_and_gather(const Row<DT, VEC>& row, ShBig& sb, float T) {
     __syncthreads();
     if (threadIdx.x == 0) sb.s.ncand = 0;
     __syncthreads();
-    u64 tot = 0;
+    MassAcc acc;
     for (int j0 = row.s0; j0 < row.s1; j0 += kTile * kU) {
-        float v[kU][V];
+        if (VEC) {
+            Vec16 r[kU];
 #pragma unroll
-        for (int q = 0; q < kU; ++q) row.load(j0 + q * kTile, v[q]);
+            for (int q = 0; q < kU; ++q) r[q] = row.load_raw(j0 + q * kTile);
 #pragma unroll
-        for (int q = 0; q < kU; ++q) {
-            float s = 0.0f;
-            unsigned in = 0;  // the entries >= T, one bit each
-#pragma unroll
-            for (int e = 0; e < V; ++e) {
-                s = __fadd_rn(s, fmaxf(row.e_of(v[q][e]), 0.0f));  // NaN gives 0
-                in |= (v[q][e] >= T ? 1u : 0u) << e;
+            for (int q = 0; q < kU; ++q) {
+                float v[V];
+                Store<DT>::unpack(r[q], v);
+                acc.add(unit_sum(row, v));
+                // the tile's maximum first; its entries >= T only when it reaches T (rare)
+                if (vec_max<DT>(r[q]) >= T) gather_bits(row, sb, bits_ge(v, T), j0 + q * kTile + row.lane * V);
             }
-            tot += fixed40(s);
-            if (in) gather_bits(row, sb, in, j0 + q * kTile + row.lane * V);
+        } else {
+            float v[kU][V];
+#pragma unroll
+            for (int q = 0; q < kU; ++q) row.load(j0 + q * kTile, v[q]);
+#pragma unroll
+            for (int q = 0; q < kU; ++q) {
+                acc.add(unit_sum(row, v[q]));
+                const unsigned in = bits_ge(v[q], T);
+                if (in) gather_bits(row, sb, in, j0 + q * kTile + row.lane * V);
+            }
         }
+        acc.fold();
     }
-    return tot;
+    return acc.total();
 }
 
 template <int DT, bool VEC>
@@ -1032,7 +1111,6 @@ sample_descending(const void* x, int32_t* out, int n, int method, float t, int k
     u64 all;
     block_exscan(mass_and_gather(row, sb, T), sb.s, &all);
     const unsigned ncand = sb.s.ncand;  // final: block_exscan's barriers follow every atomic
-    const bool fits = ncand <= (unsigned)kMaxCand;
     const u64 cut = (u64)((double)p * (double)all);
     u64 kept = all, unused;
     int idx = -1;
@@ -1060,7 +1138,17 @@ sample_descending(const void* x, int32_t* out, int n, int method, float t, int k
             if (threadIdx.x == 0) out[blockIdx.x] = q >= 0 ? cand_index(c) : -1;
         }
         return;
-    } else if (fits && ncand > (unsigned)kWarpCand) {
+    }
+    unsigned nc2 = ncand;
+    if (ncand <= (unsigned)kWarpCand) {
+        // the few did not settle the row: a second, wider round, the entries
+        // >= a floor that twice as many entries per warp reach (sorted by the
+        // block, up to kMaxCand of them)
+        gather_ge(row, sb, maxima_floor(sb.lmax[threadIdx.x], 2 * (kTopLanes / kW), sb.s));
+        __syncthreads();  // every candidate is in
+        nc2 = sb.s.ncand;
+    }
+    if (nc2 <= (unsigned)kMaxCand) {
         const int nc = sort_cand(sb);
         const u64 top_mass = sorted_mass(row, nc, sb);
         if (cut < all) {

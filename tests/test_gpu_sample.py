@@ -237,6 +237,22 @@ def test_prefill_logits_sampled_rows(method, kw):
     assert np.array_equal(got[pick], sub)
 
 
+def test_top_p_rows_past_the_first_gather():
+    """Top-p 0.9 at t = 0.7 on the first 512 rows of the prefill logits (the
+    bench's setting): in about 2 % of them the first, narrow gather of the
+    row's top holds less than the cut's mass, and a wider round (or the exact
+    search) decides.  Every draw is held to the float64 distribution within
+    2e-6, and every difference from the oracle is a boundary case."""
+    kw = dict(temperature=0.7, p=0.9)
+    a, _ = W.cases(W.PREFILL)["argmax"](rows=(0, 512))
+    x = a["x"]
+    u = _u(x.shape[0], "topp.rounds")
+    got = _check(x, u, "top_p", kw, "top_p prefill rows", max_miss=1.0)
+    x32 = widen(x)
+    for r in range(x.shape[0]):
+        assert _valid_draw(x32[r], float(u[r]), "top_p", kw, int(got[r]), 2e-6), (r, u[r], got[r])
+
+
 def test_refusals_on_device():
     x = torch.randn(4, 1000, device="cuda")
     u = torch.rand(4, device="cuda")
