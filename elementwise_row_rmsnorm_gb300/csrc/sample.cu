@@ -451,8 +451,10 @@ __device__ __forceinline__ float kept_e(const Row<DT, VEC>& row, float v, float 
                 : fmaxf(e, 0.0f);         // NaN gives 0
 }
 
+// Three rows resident per SM (40 registers a thread): the tiles in flight
+// stay packed, which is what lets the aligned kernels fit without spilling.
 template <int DT, bool VEC, bool MINP>
-__global__ void __launch_bounds__(kT, 2)
+__global__ void __launch_bounds__(kT, 3)
 sample_index_order(const void* x, int32_t* out, int n, float t, float p, const float* u) {
     constexpr int V = Row<DT, VEC>::V;
     constexpr int kTile = Row<DT, VEC>::kTile;
@@ -471,11 +473,24 @@ sample_index_order(const void* x, int32_t* out, int n, float t, float p, const f
     };
     u64 mine = 0;
     for (int j0 = row.s0; j0 < row.s1; j0 += kTile * kU) {
-        float v[kU][V];
+        if (VEC) {
+            // the tiles in flight stay packed; each is unpacked as its unit is summed
+            Vec16 r[kU];
 #pragma unroll
-        for (int q = 0; q < kU; ++q) row.load(j0 + q * kTile, v[q]);
+            for (int q = 0; q < kU; ++q) r[q] = row.load_raw(j0 + q * kTile);
 #pragma unroll
-        for (int q = 0; q < kU; ++q) mine += unit(v[q]);
+            for (int q = 0; q < kU; ++q) {
+                float v[V];
+                Store<DT>::unpack(r[q], v);
+                mine += unit(v);
+            }
+        } else {
+            float v[kU][V];
+#pragma unroll
+            for (int q = 0; q < kU; ++q) row.load(j0 + q * kTile, v[q]);
+#pragma unroll
+            for (int q = 0; q < kU; ++q) mine += unit(v[q]);
+        }
     }
     u64 total;
     const u64 wmass = warp_sum_u64(mine);
@@ -551,11 +566,10 @@ struct ShBig {
 // ---- one warp over at most 256 candidates ----------------------------------------
 //
 // The common case of top-k and top-p gathers a few hundred candidates at
-// most.  One warp then sorts them in registers (8 per lane, entry
-// i = 8 lane + slot) with a bitonic network -- strides below 8 inside a
-// lane, larger ones by shuffles -- and finds the cut and the draw with warp
-// scans: no block barrier, where the block-wide sort and walks take several
-// dozen.
+// most.  The block ranks them (one barrier), then one warp holds them in
+// sorted order (8 per lane, entry i = 8 lane + slot) and finds the cut and
+// the draw with warp scans, where the block-wide sort and walks take several
+// dozen barriers.
 constexpr int kWarpCand = 256;
 
 struct WarpSorted {
@@ -563,41 +577,33 @@ struct WarpSorted {
     u64 cum[8];  // running mass through each (inclusive), in sorted order
 };
 
+// Sort the nc <= kWarpCand candidates cand[0, nc) descending into
+// sorted[0, nc): thread i counts the candidates greater than its own (all
+// reads of one step hit one shared word) and writes its own at that rank.
+// Candidates are distinct (their low words hold distinct indices), so the
+// ranks are a permutation.  The caller's barrier makes sorted visible.
+__device__ __forceinline__ void rank_sort(const u64* cand, u64* sorted, int nc) {
+    const int i = threadIdx.x;
+    if (i < nc) {
+        const u64 c = cand[i];
+        int r = 0;
+        int j = 0;
+        for (; j + 4 <= nc; j += 4)
+            r += (int)(cand[j] > c) + (int)(cand[j + 1] > c) + (int)(cand[j + 2] > c) + (int)(cand[j + 3] > c);
+        for (; j < nc; ++j) r += (int)(cand[j] > c);
+        sorted[r] = c;
+    }
+}
+
+// One warp loads the sorted candidates (8 per lane, position 8 lane + slot)
+// and their running masses.
 template <int DT, bool VEC>
-__device__ __forceinline__ void warp_sort_weigh(const Row<DT, VEC>& row, const u64* cand, int nc, int lane,
-                                                WarpSorted& ws) {
+__device__ __forceinline__ void warp_weigh(const Row<DT, VEC>& row, const u64* sorted, int nc, int lane,
+                                           WarpSorted& ws) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
         const int i = lane * 8 + k;
-        ws.c[k] = i < nc ? cand[i] : 0ull;  // pads sort last
-    }
-#pragma unroll
-    for (int ls = 1; ls <= 8; ++ls) {  // blocks of 2^ls entries
-#pragma unroll
-        for (int lt = ls - 1; lt >= 0; --lt) {  // compare entries 2^lt apart
-            const int size = 1 << ls, stride = 1 << lt;
-            if (lt >= 3) {
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const u64 o = __shfl_xor_sync(kFull, ws.c[k], stride >> 3);
-                    const int i = lane * 8 + k;
-                    const bool keep_max = ((i & stride) == 0) == ((i & size) == 0);
-                    ws.c[k] = keep_max ? (ws.c[k] > o ? ws.c[k] : o) : (ws.c[k] < o ? ws.c[k] : o);
-                }
-            } else {
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    if ((k & stride) == 0) {
-                        const int k2 = k | stride;
-                        const bool desc = ((lane * 8 + k) & size) == 0;
-                        const u64 a = ws.c[k], b = ws.c[k2];
-                        const bool swap = desc ? a < b : a > b;
-                        ws.c[k] = swap ? b : a;
-                        ws.c[k2] = swap ? a : b;
-                    }
-                }
-            }
-        }
+        ws.c[k] = i < nc ? sorted[i] : 0ull;
     }
     u64 run = 0;
 #pragma unroll
@@ -1052,9 +1058,11 @@ sample_descending(const void* x, int32_t* out, int n, int method, float t, int k
             __syncthreads();  // every candidate is in
             const unsigned ncand = sb.s.ncand;
             if (ncand <= (unsigned)kWarpCand) {
+                rank_sort(sb.cand, sb.cand + kWarpCand, (int)ncand);
+                __syncthreads();
                 if (threadIdx.x < 32) {  // one warp finishes the row
                     WarpSorted ws;
-                    warp_sort_weigh(row, sb.cand, (int)ncand, row.lane, ws);
+                    warp_weigh(row, sb.cand + kWarpCand, (int)ncand, row.lane, ws);
                     const int L = min(k, (int)ncand);
                     const u64 wk = warp_mass_through(ws, L);
                     u64 before, c;
@@ -1125,10 +1133,12 @@ sample_descending(const void* x, int32_t* out, int n, int method, float t, int k
     // draw then does too), or, with no cut, when the draw does.
     const bool settles = ncand <= (unsigned)kWarpCand && (cut < all ? cut < top_mass : scaled(ur, all) < top_mass);
     if (settles) {
+        rank_sort(sb.cand, sb.cand + kWarpCand, (int)ncand);
+        __syncthreads();
         // one warp finishes the row; the others are done
         if (threadIdx.x < 32) {
             WarpSorted ws;
-            warp_sort_weigh(row, sb.cand, (int)ncand, row.lane, ws);
+            warp_weigh(row, sb.cand + kWarpCand, (int)ncand, row.lane, ws);
             u64 kp = all, before, c;
             if (cut < all) {
                 warp_first_above(row, ws, (int)ncand, cut, row.lane, &kp, &c);
