@@ -63,6 +63,12 @@ struct RowShape {
     // Not for the fused add, whose second input would then spill.
     template <bool ADD>
     static constexpr int min_blocks() { return (TPR >= 512 && !ADD) ? 2048 / TPR : 1; }
+    // LayerNorm rows of 64 to 256 threads: 1536 threads resident per SM (40
+    // registers, no spill), as many rows as RMSNorm keeps, where the
+    // unbounded kernel took 47 registers and fit 1280.
+    static constexpr int ln_min_blocks() {
+        return (TPR >= 64 && TPR <= 256) ? 1536 / (TPR > 0 ? TPR : 1) : min_blocks<false>();
+    }
 };
 
 template <int DT, int K, bool ADD, int TPR>
@@ -183,7 +189,7 @@ rmsnorm_two_pass(const void* x, const void* res, const void* w, void* y, void* h
 // RMSNorm; the row's two sums (of x, then of (x - mu)^2) each take the same
 // fixed tree, so a row's bits depend only on the row, d and the type.
 template <int DT, int K, int TPR>
-__global__ void __launch_bounds__(RowShape<TPR>::kMaxThreads, RowShape<TPR>::template min_blocks<false>())
+__global__ void __launch_bounds__(RowShape<TPR>::kMaxThreads, RowShape<TPR>::ln_min_blocks())
 layernorm_rows(const void* x, const void* g, const void* b, void* y, int64_t rows, int d, float eps, int tpr_rt) {
     using S = Store<DT>;
     constexpr int V = S::V;
