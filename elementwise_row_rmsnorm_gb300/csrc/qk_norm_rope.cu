@@ -68,7 +68,9 @@ __device__ __forceinline__ void load_chunk(const char* row, int c, int D, float 
 // head rows of q or k (a warp loops when the token has more chunks than
 // warps).  The token's r/2 angles are formed once, one pair per thread,
 // while the head rows' loads are in flight, and read back from shared memory
-// after one CTA barrier.  A lane's partner chunk is fetched from the partner
+// after one CTA barrier, which a warp reaches once its first rows are reduced
+// (so no warp idles there while the angles are formed).  A lane's partner
+// chunk is fetched from the partner
 // lane with four register shuffles (half layout), or sits in the lane's own
 // chunk (interleaved).
 //
@@ -166,7 +168,6 @@ qk_norm_rope_tok(QkSide A, QkSide B, int nca, int ncb, float eps, const int32_t*
         cs_sin[slot] = sv;
         if (LAYOUT == 0) cs_nsin[slot] = -sv;
     }
-    __syncthreads();  // every thread of the CTA reaches it: no thread has left yet
 
     const bool rot = has && c * V < r;  // this chunk is rotated
     const bool first_half = LAYOUT == 0 && c < G;
@@ -224,6 +225,10 @@ qk_norm_rope_tok(QkSide A, QkSide B, int nca, int ncb, float eps, const int32_t*
             for (int k = 0; k < NP; ++k)
                 inv[k] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(s[k], (float)D), eps)));
         }
+        // the angles are in once every thread has passed here; each warp's
+        // first item comes through (there are no more warps than items), so
+        // every thread of the CTA arrives exactly once
+        if (ci == wib) __syncthreads();
 
 #pragma unroll
         for (int k = 0; k < NP; ++k) {
@@ -380,7 +385,6 @@ qk_norm_rope_pair(QkSide A, QkSide B, int nca, int ncb, float eps, const int32_t
         cs_cos[slot] = cv;
         cs_sin[slot] = sv;
     }
-    __syncthreads();  // every thread of the CTA reaches it: no thread has left yet
     const int slot0 = angle_slot<QPL>(c * V, half);
     const bool mu_one = mu == 1.0f;
 
@@ -424,6 +428,10 @@ qk_norm_rope_pair(QkSide A, QkSide B, int nca, int ncb, float eps, const int32_t
             for (int k = 0; k < NP; ++k)
                 inv[k] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(s[k], (float)D), eps)));
         }
+        // the angles are in once every thread has passed here; each warp's
+        // first item comes through (there are no more warps than items), so
+        // every thread of the CTA arrives exactly once
+        if (ci == wib) __syncthreads();
 
 #pragma unroll
         for (int k = 0; k < NP; ++k) {
