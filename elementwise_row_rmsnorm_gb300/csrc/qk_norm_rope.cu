@@ -304,14 +304,23 @@ __device__ __forceinline__ void rotate_store(const float (&a)[Store<DT>::V], con
         const float c4[4] = {vc.x, vc.y, vc.z, vc.w};
         const float s4[4] = {vs.x, vs.y, vs.z, vs.w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < 4; j += 2) {
+            // the products two lanes at a time; the sums scalar (a packed
+            // multiply feeding a packed add may be fused into one rounding)
             const int e = 4 * q + j;
-            lo[e] = __fsub_rn(__fmul_rn(a[e], c4[j]), __fmul_rn(b[e], s4[j]));
-            hi[e] = __fadd_rn(__fmul_rn(a[e], s4[j]), __fmul_rn(b[e], c4[j]));
+            const float2 A = make_float2(a[e], a[e + 1]), B = make_float2(b[e], b[e + 1]);
+            const float2 C = make_float2(c4[j], c4[j + 1]), Sn = make_float2(s4[j], s4[j + 1]);
+            const float2 ac = mul2_rn(A, C), bs = mul2_rn(B, Sn), as = mul2_rn(A, Sn), bc = mul2_rn(B, C);
+            float2 l = make_float2(__fsub_rn(ac.x, bs.x), __fsub_rn(ac.y, bs.y));
+            float2 h = make_float2(__fadd_rn(as.x, bc.x), __fadd_rn(as.y, bc.y));
             if (MU) {
-                lo[e] = __fmul_rn(mu, lo[e]);
-                hi[e] = __fmul_rn(mu, hi[e]);
+                l = mul2_rn(make_float2(mu, mu), l);
+                h = mul2_rn(make_float2(mu, mu), h);
             }
+            lo[e] = l.x;
+            lo[e + 1] = l.y;
+            hi[e] = h.x;
+            hi[e + 1] = h.y;
         }
     }
     st_stream(lo_at, S::pack(lo));
@@ -439,15 +448,24 @@ qk_norm_rope_pair(QkSide A, QkSide B, int nca, int ncb, float eps, const int32_t
             const int h = h0 + k * RP + sub;
             float a[V], b[V], g[V];
             // normalised and rounded to storage, as a stored intermediate would be
+            const float2 iv = make_float2(inv[k], inv[k]);
             S::unpack(raw[k][0], a);
             S::unpack(g_lo, g);
 #pragma unroll
-            for (int e = 0; e < V; ++e) a[e] = __fmul_rn(__fmul_rn(a[e], inv[k]), g[e]);
+            for (int e = 0; e < V; e += 2) {
+                const float2 u = mul2_rn(mul2_rn(make_float2(a[e], a[e + 1]), iv), make_float2(g[e], g[e + 1]));
+                a[e] = u.x;
+                a[e + 1] = u.y;
+            }
             S::unpack(S::pack(a), a);
             S::unpack(raw[k][1], b);
             S::unpack(g_hi, g);
 #pragma unroll
-            for (int e = 0; e < V; ++e) b[e] = __fmul_rn(__fmul_rn(b[e], inv[k]), g[e]);
+            for (int e = 0; e < V; e += 2) {
+                const float2 u = mul2_rn(mul2_rn(make_float2(b[e], b[e + 1]), iv), make_float2(g[e], g[e + 1]));
+                b[e] = u.x;
+                b[e + 1] = u.y;
+            }
             S::unpack(S::pack(b), b);
             if (h < Q.H) {
                 char* row = Q.y + (t * Q.ys + (int64_t)h * D) * ES + (int64_t)c * 16;
