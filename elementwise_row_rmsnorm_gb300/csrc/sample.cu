@@ -256,6 +256,35 @@ __device__ __forceinline__ float unit_sum(const Row<DT, VEC>& row, const float (
     return s;
 }
 
+// The f32 sums, in index order, of the e of two units at once: entry e of
+// unit 0 and entry e of unit 1 go through the subtraction, the scaling and
+// the running sums as the two lanes of packed instructions (each lane's
+// arithmetic is the scalar one, bit for bit; no product feeds a sum: the
+// exponential sits between).  A lane is NaN where its unit holds a NaN;
+// unit_sum then gives that unit's sum with them skipped.  (Top-p's mass
+// pass; the index-order kernel keeps the scalar form, which fits its
+// 40-register budget without spilling.)
+template <int DT, bool VEC>
+__device__ __forceinline__ float2 unit_sums2(const Row<DT, VEC>& row, const float (&v0)[Row<DT, VEC>::V],
+                                             const float (&v1)[Row<DT, VEC>::V]) {
+    constexpr int V = Row<DT, VEC>::V;
+    const float2 M = make_float2(row.mx, row.mx), C = make_float2(row.c, row.c);
+    float2 s = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int e = 0; e < V; ++e) {
+        const float2 y = mul2_rn(sub2_rn(make_float2(v0[e], v1[e]), M), C);
+        s = add2_rn(s, make_float2(ex2(y.x), ex2(y.y)));
+    }
+    return s;
+}
+
+template <int DT, bool VEC>
+__device__ __forceinline__ float unit_sum_of(const Row<DT, VEC>& row, const Vec16& r) {
+    float v[Row<DT, VEC>::V];
+    Store<DT>::unpack(r, v);
+    return unit_sum(row, v);
+}
+
 // ---- warp and block primitives ----------------------------------------------------
 
 __device__ __forceinline__ u64 warp_sum_u64(u64 v) {
@@ -1006,12 +1035,28 @@ __device__ u64 mass_and_gather(const Row<DT, VEC>& row, ShBig& sb, float T) {
 #pragma unroll
             for (int q = 0; q < kU; ++q) r[q] = row.load_raw(j0 + q * kTile);
 #pragma unroll
-            for (int q = 0; q < kU; ++q) {
-                float v[V];
-                Store<DT>::unpack(r[q], v);
-                acc.add(unit_sum(row, v));
+            for (int q = 0; q < kU; q += 2) {  // two units at a time
+                float2 su;
+                {
+                    float v0[V], v1[V];
+                    Store<DT>::unpack(r[q], v0);
+                    Store<DT>::unpack(r[q + 1], v1);
+                    su = unit_sums2<DT, VEC>(row, v0, v1);
+                }
+                // a unit holding NaN, summed again from its packed tile (rare)
+                if (su.x != su.x) su.x = unit_sum_of<DT, VEC>(row, r[q]);
+                if (su.y != su.y) su.y = unit_sum_of<DT, VEC>(row, r[q + 1]);
+                acc.add(su.x);
+                acc.add(su.y);
                 // the tile's maximum first; its entries >= T only when it reaches T (rare)
-                if (vec_max<DT>(r[q]) >= T) gather_bits(row, sb, bits_ge(v, T), j0 + q * kTile + row.lane * V);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    if (vec_max<DT>(r[q + h]) >= T) {
+                        float v[V];
+                        Store<DT>::unpack(r[q + h], v);
+                        gather_bits(row, sb, bits_ge(v, T), j0 + (q + h) * kTile + row.lane * V);
+                    }
+                }
             }
         } else {
             float v[kU][V];
