@@ -240,7 +240,8 @@ def build_extra_inputs(tokens: int = 8192):
 def build_workload_inputs(workload: str):
     """Per-op inputs of the other workloads, for --isolated: the f32 RoPE
     variants (each operand rotated in place), the wide f32 argmax and
-    RMSNorm, and the decode step's ops (T = 64, launch-latency bound)."""
+    RMSNorm, and the decode step's ops (T = 64, launch-latency bound) with
+    one draw per row of its logits by each sampling method."""
     from synth import workloads as W
     cases = W.cases(workload)
     if workload == W.ROPE_VARIANTS:
@@ -248,9 +249,13 @@ def build_workload_inputs(workload: str):
     if workload == W.WIDE:
         return {"argmax": cases["argmax"](), "rmsnorm": cases["rmsnorm"]()}
     if workload == W.DECODE:
+        import synth
         rope = combine("rope_qk_half", [cases["rope_q"](), cases["rope_k"]()])
+        al, pl = cases["argmax"]()
+        u = synth.units(W.SEEDS[W.DECODE], "sample.u", al["x"].shape[0]).astype(np.float32)
+        sampling = {op: ({"x": al["x"], "u": u}, dict(pl, method=m, kw=kw)) for op, (m, kw) in SAMPLING.items()}
         return {"add_rmsnorm": cases["add_rmsnorm"](), "rope_qk_half": rope, "silu_mul": cases["silu_mul"](),
-                "argmax": cases["argmax"]()}
+                "argmax": (al, pl), **sampling}
     raise KeyError(workload)
 
 

@@ -49,11 +49,14 @@
 //    equal logits is walked in index order by the warps.
 // No memory beyond the inputs and the outputs.
 #include <atomic>
+#include <cooperative_groups.h>
 
 #include "common.cuh"
 #include "launch.h"
 
 namespace gbe {
+
+namespace cg = cooperative_groups;
 
 namespace {
 
@@ -398,26 +401,55 @@ __device__ int warp_walk(const Row<DT, VEC>& row, u64 target, M meas) {
 
 // ---- index order: temperature and min-p -------------------------------------------
 
+// The row of this CTA (row i of CL CTAs each, rank r of them) and this
+// warp's segment: the row is cut into CL * kW segments of whole tiles, CTA r
+// owning segments r kW .. r kW + kW - 1.  Segments start at multiples of a
+// tile, so the units (V consecutive entries from the row's start) are the
+// same for every CL.
 template <int DT, bool VEC>
-__device__ __forceinline__ void setup(Row<DT, VEC>& row, const void* x, int n, float t) {
+__device__ __forceinline__ void setup(Row<DT, VEC>& row, const void* x, int n, float t, int64_t i = blockIdx.x,
+                                      int rank = 0, int cl = 1) {
     constexpr int kTile = Row<DT, VEC>::kTile;
     row.x = x;
-    row.base = (int64_t)blockIdx.x * n;
+    row.base = i * n;
     row.t = t;
     row.mx = 0.0f;
     row.c = fminf(__fdiv_rn(1.44269502f, t), 3.4028234663852886e38f);  // log2(e) / t, finite
     row.lane = threadIdx.x & 31;
-    const int per = ((n + kW - 1) / kW + kTile - 1) / kTile * kTile;
-    const int w = threadIdx.x >> 5;
+    const int nseg = kW * cl;
+    const int per = ((n + nseg - 1) / nseg + kTile - 1) / kTile * kTile;
+    const int w = rank * kW + (threadIdx.x >> 5);
     row.s0 = min(n, w * per);
     row.s1 = min(n, row.s0 + per);
+}
+
+// false (and -1 written by `writer` at out[i]) when the row has no number or
+// no finite largest x / t; a row of NaN leaves mx = -inf, not finite either
+template <int DT, bool VEC>
+__device__ __forceinline__ bool accept_max(const Row<DT, VEC>& row, int32_t* out, int64_t i, bool writer) {
+    if (!isfinite(__fdiv_rn(row.mx, row.t))) {
+        if (writer) out[i] = -1;
+        return false;
+    }
+    return true;
 }
 
 // pass 1: the largest logit (and with COUNT the count of numbers); false
 // (and -1 written) when the row has no number or no finite largest x / t
 template <bool COUNT, int DT, bool VEC>
+__device__ __forceinline__ float block_first_max(Row<DT, VEC>& row, Sh& sh, int* nv_out, float* thread_max);
+
+template <bool COUNT, int DT, bool VEC>
 __device__ __forceinline__ bool first_pass(Row<DT, VEC>& row, int32_t* out, Sh& sh, int* nv_out,
                                            float* thread_max = nullptr) {
+    row.mx = block_first_max<COUNT>(row, sh, nv_out, thread_max);
+    return accept_max(row, out, blockIdx.x, threadIdx.x == 0);
+}
+
+// The CTA's largest logit over its warps' segments (NaN skipped; -inf when
+// none is a number), with COUNT the count of numbers.
+template <bool COUNT, int DT, bool VEC>
+__device__ __forceinline__ float block_first_max(Row<DT, VEC>& row, Sh& sh, int* nv_out, float* thread_max) {
     float mx = -INFINITY;
     int nv = 0;
     if (DT == kBF16 && VEC && !COUNT) {
@@ -454,14 +486,8 @@ __device__ __forceinline__ bool first_pass(Row<DT, VEC>& row, int32_t* out, Sh& 
     if (thread_max) thread_max[threadIdx.x] = mx;  // this thread's own maximum (-inf if it has no number)
     mx = block_max(mx, sh);
     if (COUNT) nv = block_sum_int(nv, sh);
-    row.mx = mx;
     *nv_out = nv;
-    // a row of NaN leaves mx = -inf, which is not finite either
-    if (!isfinite(__fdiv_rn(mx, row.t))) {
-        if (threadIdx.x == 0) out[blockIdx.x] = -1;
-        return false;
-    }
-    return true;
+    return mx;
 }
 
 // Index order works on units: a lane's V consecutive entries of one tile.
@@ -480,19 +506,44 @@ __device__ __forceinline__ float kept_e(const Row<DT, VEC>& row, float v, float 
                 : fmaxf(e, 0.0f);         // NaN gives 0
 }
 
+// One row per CL CTAs (a thread-block cluster when CL > 1, for batches too
+// small to fill the GPU with one CTA a row).  The CTAs combine their
+// maxima and their masses through distributed shared memory after hardware
+// cluster barriers (no spin loop); a CTA leaves only after a barrier that
+// follows every read of its shared memory by the others.  Every CL gives
+// the same draw: the unit weights are the same integers, summed exactly.
+//
 // Three rows resident per SM (40 registers a thread): the tiles in flight
 // stay packed, which is what lets the aligned kernels fit without spilling.
-template <int DT, bool VEC, bool MINP>
-__global__ void __launch_bounds__(kT, 3)
-sample_index_order(const void* x, int32_t* out, int n, float t, float p, const float* u) {
+template <int DT, bool VEC, bool MINP, int CL>
+__device__ __forceinline__ void index_order_body(const void* x, int32_t* out, int n, float t, float p, const float* u) {
     constexpr int V = Row<DT, VEC>::V;
     constexpr int kTile = Row<DT, VEC>::kTile;
     pdl_begin();
     __shared__ Sh sh;
+    __shared__ float cl_max;  // this CTA's maximum, read by the cluster
+    __shared__ u64 cl_mass;   // this CTA's kept mass, read by the cluster
+    const int64_t ri = CL > 1 ? (int64_t)(blockIdx.x / CL) : (int64_t)blockIdx.x;
+    const int rank = CL > 1 ? (int)(blockIdx.x % CL) : 0;
     Row<DT, VEC> row;
-    setup(row, x, n, t);
+    setup(row, x, n, t, ri, rank, CL);
     int nv;
-    if (!first_pass<false>(row, out, sh, &nv)) return;
+    row.mx = block_first_max<false>(row, sh, &nv, nullptr);
+    if (CL > 1) {
+        cg::cluster_group cluster = cg::this_cluster();
+        if (threadIdx.x == 0) cl_max = row.mx;
+        cluster.sync();
+        float m = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < CL; ++q) m = fmaxf(m, *cluster.map_shared_rank(&cl_max, q));
+        row.mx = m;
+        if (!accept_max(row, out, ri, rank == 0 && threadIdx.x == 0)) {
+            cluster.sync();  // the others' reads of cl_max are done
+            return;
+        }
+    } else if (!accept_max(row, out, ri, threadIdx.x == 0)) {
+        return;
+    }
     auto unit = [&](const float (&v)[V]) -> u64 {
         if (!MINP) return fixed40(unit_sum(row, v));
         float s = 0.0f;
@@ -523,8 +574,23 @@ sample_index_order(const void* x, int32_t* out, int n, float t, float p, const f
     }
     u64 total;
     const u64 wmass = warp_sum_u64(mine);
-    const u64 ex = warp_exscan(wmass, sh, &total);
-    const u64 target = scaled(u[blockIdx.x], total);
+    u64 ex = warp_exscan(wmass, sh, &total);
+    if (CL > 1) {
+        cg::cluster_group cluster = cg::this_cluster();
+        if (threadIdx.x == 0) cl_mass = total;
+        cluster.sync();  // also: every CTA is done reading cl_max
+        u64 before = 0, all = 0;
+#pragma unroll
+        for (int q = 0; q < CL; ++q) {
+            const u64 m = *cluster.map_shared_rank(&cl_mass, q);
+            if (q < rank) before += m;
+            all += m;
+        }
+        cluster.sync();  // every read of cl_mass is done before any CTA leaves
+        ex += before;
+        total = all;
+    }
+    const u64 target = scaled(u[ri], total);
     if (!(wmass > 0 && ex <= target && target < ex + wmass)) return;
     // this warp holds the target: walk its tiles
     const u64 want = target - ex;
@@ -549,10 +615,49 @@ sample_index_order(const void* x, int32_t* out, int n, float t, float p, const f
             }
             const unsigned who = __ballot_sync(kFull, found >= 0);
             const int idx = __shfl_sync(kFull, found, who ? __ffs(who) - 1 : 0);
-            if (row.lane == 0) out[blockIdx.x] = idx;
+            if (row.lane == 0) out[ri] = idx;
             return;
         }
         run += tot;
+    }
+}
+
+template <int DT, bool VEC, bool MINP>
+__global__ void __launch_bounds__(kT, 3) sample_index_order(const void* x, int32_t* out, int n, float t, float p,
+                                                            const float* u) {
+    index_order_body<DT, VEC, MINP, 1>(x, out, n, t, p, u);
+}
+template <int DT, bool VEC, bool MINP>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kT, 3)
+sample_index_order2(const void* x, int32_t* out, int n, float t, float p, const float* u) {
+    index_order_body<DT, VEC, MINP, 2>(x, out, n, t, p, u);
+}
+template <int DT, bool VEC, bool MINP>
+__global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kT, 3)
+sample_index_order4(const void* x, int32_t* out, int n, float t, float p, const float* u) {
+    index_order_body<DT, VEC, MINP, 4>(x, out, n, t, p, u);
+}
+template <int DT, bool VEC, bool MINP>
+__global__ void __cluster_dims__(8, 1, 1) __launch_bounds__(kT, 3)
+sample_index_order8(const void* x, int32_t* out, int n, float t, float p, const float* u) {
+    index_order_body<DT, VEC, MINP, 8>(x, out, n, t, p, u);
+}
+
+// CTAs per row for the index-order kernels: doubled while the grid still
+// fits in one wave (three CTAs an SM) and each warp keeps two tiles.
+template <int DT, bool VEC, bool MINP>
+cudaError_t launch_index_order(const void* x, int32_t* out, int64_t rows, int n, float t, float p, const float* u,
+                               cudaStream_t st) {
+    constexpr int kTile = Row<DT, VEC>::kTile;
+    const int64_t target = 3LL * sm_count();
+    int cl = 1;
+    while (cl < 8 && rows * cl * 2 <= target && (int64_t)n >= (int64_t)kW * 2 * (2 * cl) * kTile) cl *= 2;
+    const dim3 grid((unsigned)(rows * cl)), block(kT);
+    switch (cl) {
+        case 1: return launch(sample_index_order<DT, VEC, MINP>, grid, block, 0, st, x, out, n, t, p, u);
+        case 2: return launch(sample_index_order2<DT, VEC, MINP>, grid, block, 0, st, x, out, n, t, p, u);
+        case 4: return launch(sample_index_order4<DT, VEC, MINP>, grid, block, 0, st, x, out, n, t, p, u);
+        default: return launch(sample_index_order8<DT, VEC, MINP>, grid, block, 0, st, x, out, n, t, p, u);
     }
 }
 
@@ -1003,16 +1108,16 @@ __device__ void gather_ge(const Row<DT, VEC>& row, ShBig& sb, float T) {
                 }
             }
         }
-        return;
-    }
-    for (int j0 = row.s0; j0 < row.s1; j0 += kTile * kU) {
-        float v[kU][V];
+    } else {
+        for (int j0 = row.s0; j0 < row.s1; j0 += kTile * kU) {
+            float v[kU][V];
 #pragma unroll
-        for (int q = 0; q < kU; ++q) row.load(j0 + q * kTile, v[q]);
+            for (int q = 0; q < kU; ++q) row.load(j0 + q * kTile, v[q]);
 #pragma unroll
-        for (int q = 0; q < kU; ++q) {
-            const unsigned in = bits_ge(v[q], T);
-            if (in) gather_bits(row, sb, in, j0 + q * kTile + row.lane * V);
+            for (int q = 0; q < kU; ++q) {
+                const unsigned in = bits_ge(v[q], T);
+                if (in) gather_bits(row, sb, in, j0 + q * kTile + row.lane * V);
+            }
         }
     }
 }
@@ -1240,10 +1345,8 @@ sample_descending(const void* x, int32_t* out, int n, int method, float t, int k
 template <int DT, bool VEC>
 cudaError_t launch_vec(const void* x, int32_t* out, int64_t rows, int n, int method, float t, int k, float p,
                        const float* u, cudaStream_t st) {
-    if (method == kTemperature)
-        return launch(sample_index_order<DT, VEC, false>, dim3((unsigned)rows), dim3(kT), 0, st, x, out, n, t, p, u);
-    if (method == kMinP)
-        return launch(sample_index_order<DT, VEC, true>, dim3((unsigned)rows), dim3(kT), 0, st, x, out, n, t, p, u);
+    if (method == kTemperature) return launch_index_order<DT, VEC, false>(x, out, rows, n, t, p, u, st);
+    if (method == kMinP) return launch_index_order<DT, VEC, true>(x, out, rows, n, t, p, u, st);
     const size_t smem = sizeof(ShBig);
     // the shared-memory opt-in, once per device for this kernel
     static std::atomic<uint64_t> opted{0};
