@@ -434,20 +434,9 @@ __device__ __forceinline__ bool accept_max(const Row<DT, VEC>& row, int32_t* out
     return true;
 }
 
-// pass 1: the largest logit (and with COUNT the count of numbers); false
-// (and -1 written) when the row has no number or no finite largest x / t
-template <bool COUNT, int DT, bool VEC>
-__device__ __forceinline__ float block_first_max(Row<DT, VEC>& row, Sh& sh, int* nv_out, float* thread_max);
-
-template <bool COUNT, int DT, bool VEC>
-__device__ __forceinline__ bool first_pass(Row<DT, VEC>& row, int32_t* out, Sh& sh, int* nv_out,
-                                           float* thread_max = nullptr) {
-    row.mx = block_first_max<COUNT>(row, sh, nv_out, thread_max);
-    return accept_max(row, out, blockIdx.x, threadIdx.x == 0);
-}
-
-// The CTA's largest logit over its warps' segments (NaN skipped; -inf when
-// none is a number), with COUNT the count of numbers.
+// Pass 1: the CTA's largest logit over its warps' segments (NaN skipped;
+// -inf when none is a number), with COUNT the count of numbers, and each
+// thread's own maximum in thread_max when given.
 template <bool COUNT, int DT, bool VEC>
 __device__ __forceinline__ float block_first_max(Row<DT, VEC>& row, Sh& sh, int* nv_out, float* thread_max) {
     float mx = -INFINITY;
@@ -1179,17 +1168,16 @@ __device__ u64 mass_and_gather(const Row<DT, VEC>& row, ShBig& sb, float T) {
     return acc.total();
 }
 
+// Row ri, the whole of it by this CTA (all kT threads): top-k and top-p.
 template <int DT, bool VEC>
-__global__ void __launch_bounds__(kT, 2)
-sample_descending(const void* x, int32_t* out, int n, int method, float t, int k, float p, const float* u) {
-    pdl_begin();
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    ShBig& sb = *reinterpret_cast<ShBig*>(smem_raw);
+__device__ void descending_row(const void* x, int32_t* out, int64_t ri, int n, int method, float t, int k, float p,
+                               const float* u, ShBig& sb) {
     Row<DT, VEC> row;
-    setup(row, x, n, t);
+    setup(row, x, n, t, ri, 0, 1);
     int nv;
-    if (!first_pass<false>(row, out, sb.s, &nv, sb.lmax)) return;
-    const float ur = u[blockIdx.x];
+    row.mx = block_first_max<false>(row, sb.s, &nv, sb.lmax);
+    if (!accept_max(row, out, ri, threadIdx.x == 0)) return;
+    const float ur = u[ri];
     // The head of the row: the first-digit bins from that of M - 24 / c down
     // -- every entry of weight above 2^-24 of the largest (and some below).
     // The rest of a row of n entries weighs at most n 2^-24 of the largest, so
@@ -1217,7 +1205,7 @@ sample_descending(const void* x, int32_t* out, int n, int method, float t, int k
                     const u64 wk = warp_mass_through(ws, L);
                     u64 before, c;
                     const int q = warp_first_above(row, ws, L, scaled(ur, wk), row.lane, &before, &c);
-                    if (threadIdx.x == 0) out[blockIdx.x] = q >= 0 ? cand_index(c) : -1;
+                    if (threadIdx.x == 0) out[ri] = q >= 0 ? cand_index(c) : -1;
                 }
                 return;
             }
@@ -1227,7 +1215,7 @@ sample_descending(const void* x, int32_t* out, int n, int method, float t, int k
                 const u64 wk = sorted_mass(row, L, sb);
                 u64 unused;
                 const int q = sorted_pick(row, L, scaled(ur, wk), sb, &unused);
-                if (threadIdx.x == 0) out[blockIdx.x] = q >= 0 ? cand_index(sb.cand[q]) : -1;
+                if (threadIdx.x == 0) out[ri] = q >= 0 ? cand_index(sb.cand[q]) : -1;
                 return;
             }
         }
@@ -1244,7 +1232,7 @@ sample_descending(const void* x, int32_t* out, int n, int method, float t, int k
                     const u64 wk = sorted_mass(row, k, sb);
                     u64 unused;
                     const int q = sorted_pick(row, k, scaled(ur, wk), sb, &unused);
-                    if (threadIdx.x == 0) out[blockIdx.x] = q >= 0 ? cand_index(sb.cand[q]) : -1;
+                    if (threadIdx.x == 0) out[ri] = q >= 0 ? cand_index(sb.cand[q]) : -1;
                     return;
                 }
             }
@@ -1256,7 +1244,7 @@ sample_descending(const void* x, int32_t* out, int n, int method, float t, int k
         if (k < nv) desc_search<DT, VEC, true>(row, (u64)k, sb, &kept);  // the entry past the k-th
         u64 unused;
         const int idx = desc_search<DT, VEC, false>(row, scaled(ur, kept), sb, &unused);
-        if (threadIdx.x == 0) out[blockIdx.x] = idx;
+        if (threadIdx.x == 0) out[ri] = idx;
         return;
     }
     // top-p: keep the prefix whose running mass stays <= p * W (the first
@@ -1295,7 +1283,7 @@ sample_descending(const void* x, int32_t* out, int n, int method, float t, int k
                 if (kp == 0) kp = 1;  // a target of 0 lands on the first entry
             }
             const int q = warp_first_above(row, ws, (int)ncand, scaled(ur, kp), row.lane, &before, &c);
-            if (threadIdx.x == 0) out[blockIdx.x] = q >= 0 ? cand_index(c) : -1;
+            if (threadIdx.x == 0) out[ri] = q >= 0 ? cand_index(c) : -1;
         }
         return;
     }
@@ -1339,7 +1327,16 @@ sample_descending(const void* x, int32_t* out, int n, int method, float t, int k
         }
         idx = desc_search<DT, VEC, false>(row, scaled(ur, kept), sb, &unused);
     }
-    if (threadIdx.x == 0) out[blockIdx.x] = idx;
+    if (threadIdx.x == 0) out[ri] = idx;
+}
+
+template <int DT, bool VEC>
+__global__ void __launch_bounds__(kT, 2)
+sample_descending(const void* x, int32_t* out, int n, int method, float t, int k, float p, const float* u) {
+    pdl_begin();
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    ShBig& sb = *reinterpret_cast<ShBig*>(smem_raw);
+    descending_row<DT, VEC>(x, out, blockIdx.x, n, method, t, k, p, u, sb);
 }
 
 template <int DT, bool VEC>

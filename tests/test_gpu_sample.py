@@ -237,6 +237,23 @@ def test_prefill_logits_sampled_rows(method, kw):
     assert np.array_equal(got[pick], sub)
 
 
+@pytest.mark.parametrize("method,kw", METHODS + [("top_k", dict(temperature=0.7, top_k=300))])
+def test_draws_do_not_depend_on_the_split(method, kw):
+    """Batches too small to fill the GPU split each row over a cluster of 2, 4
+    or 8 CTAs; large ones take one CTA a row.  The same rows give the same
+    draws in a batch of 320 (one CTA a row), 48, 16 and 1 (clusters), NaN
+    entries included; a few rows are also checked against the oracle."""
+    rows, n = 320, 131072
+    x = _logits(rows, n, "bf16", nan_frac=0.001, tag="split")
+    xd = to_dev(x)
+    u = torch.from_numpy(_u(rows, "split")).cuda()
+    ref = gbe.sample(xd, u, method, **kw).cpu().numpy()
+    for r0, r1 in ((0, 48), (100, 116), (7, 8), (319, 320)):
+        got = gbe.sample(xd[r0:r1].contiguous(), u[r0:r1].contiguous(), method, **kw).cpu().numpy()
+        assert np.array_equal(got, ref[r0:r1]), (r0, r1)
+    _check(x[:8], u[:8].cpu().numpy(), method, kw, f"{method} split rows", max_miss=1.0)
+
+
 def test_top_p_rows_past_the_first_gather():
     """Top-p 0.9 at t = 0.7 on the first 512 rows of the prefill logits (the
     bench's setting): in about 2 % of them the first, narrow gather of the
