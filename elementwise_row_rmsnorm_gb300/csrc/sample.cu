@@ -166,6 +166,14 @@ struct Row {
     // fixed-point weight of a logit that is not NaN
     __device__ __forceinline__ u64 weight(float v) const { return w_of(e_of(v)); }
 
+    // The start of the segment's last group of kU tiles (s0 - 1 when the
+    // segment is empty).  Later passes walk the groups backwards: the tiles
+    // pass 1 read last are the likeliest to be still in L2.  Their sums are
+    // integers and the gathers are sorted afterwards, so order is free.
+    __device__ __forceinline__ int last_group() const {
+        return s1 > s0 ? s0 + (s1 - s0 - 1) / (kTile * kU) * (kTile * kU) : s0 - 1;
+    }
+
     // this lane's 16-byte vector of the tile starting at j, NaN entries past
     // the segment (aligned rows)
     __device__ __forceinline__ Vec16 load_raw(int j) const {
@@ -541,7 +549,7 @@ __device__ __forceinline__ void index_order_body(const void* x, int32_t* out, in
         return fixed40(s);
     };
     u64 mine = 0;
-    for (int j0 = row.s0; j0 < row.s1; j0 += kTile * kU) {
+    for (int j0 = row.last_group(); j0 >= row.s0; j0 -= kTile * kU) {
         if (VEC) {
             // the tiles in flight stay packed; each is unpacked as its unit is summed
             Vec16 r[kU];
@@ -1084,7 +1092,7 @@ __device__ void gather_ge(const Row<DT, VEC>& row, ShBig& sb, float T) {
     __syncthreads();
     if (VEC) {
         // the tile's maximum first; its entries only when it reaches T (rare)
-        for (int j0 = row.s0; j0 < row.s1; j0 += kTile * kU) {
+        for (int j0 = row.last_group(); j0 >= row.s0; j0 -= kTile * kU) {
             Vec16 r[kU];
 #pragma unroll
             for (int q = 0; q < kU; ++q) r[q] = row.load_raw(j0 + q * kTile);
@@ -1098,7 +1106,7 @@ __device__ void gather_ge(const Row<DT, VEC>& row, ShBig& sb, float T) {
             }
         }
     } else {
-        for (int j0 = row.s0; j0 < row.s1; j0 += kTile * kU) {
+        for (int j0 = row.last_group(); j0 >= row.s0; j0 -= kTile * kU) {
             float v[kU][V];
 #pragma unroll
             for (int q = 0; q < kU; ++q) row.load(j0 + q * kTile, v[q]);
@@ -1123,7 +1131,7 @@ __device__ u64 mass_and_gather(const Row<DT, VEC>& row, ShBig& sb, float T) {
     if (threadIdx.x == 0) sb.s.ncand = 0;
     __syncthreads();
     MassAcc acc;
-    for (int j0 = row.s0; j0 < row.s1; j0 += kTile * kU) {
+    for (int j0 = row.last_group(); j0 >= row.s0; j0 -= kTile * kU) {
         if (VEC) {
             Vec16 r[kU];
 #pragma unroll
