@@ -230,10 +230,12 @@ layernorm_rows(const void* x, const void* g, const void* b, void* y, int64_t row
         if (c < nchunks) {
             float f[V];
             S::unpack(rx[k], f);
+            const float2 m2 = make_float2(mu, mu);
 #pragma unroll
-            for (int e = 0; e < V; ++e) {
-                const float cc = __fsub_rn(f[e], mu);
-                s2 = __fmaf_rn(cc, cc, s2);
+            for (int e = 0; e < V; e += 2) {
+                const float2 cc = sub2_rn(make_float2(f[e], f[e + 1]), m2);  // two centred entries at once
+                s2 = __fmaf_rn(cc.x, cc.x, s2);
+                s2 = __fmaf_rn(cc.y, cc.y, s2);
             }
         }
     }
@@ -247,10 +249,16 @@ layernorm_rows(const void* x, const void* g, const void* b, void* y, int64_t row
             S::unpack(rx[k], f);
             S::unpack(ld_reuse(static_cast<const char*>(g) + (int64_t)c * 16), gv);
             if (b != nullptr) S::unpack(ld_reuse(static_cast<const char*>(b) + (int64_t)c * 16), bv);
+            const float2 m2 = make_float2(mu, mu), i2 = make_float2(inv, inv);
 #pragma unroll
-            for (int e = 0; e < V; ++e) {
-                const float u = __fmul_rn(__fmul_rn(__fsub_rn(f[e], mu), inv), gv[e]);
-                f[e] = b != nullptr ? __fadd_rn(u, bv[e]) : u;
+            for (int e = 0; e < V; e += 2) {
+                // (x - mu) * inv * g for two entries per instruction; the bias
+                // added by scalar adds (a packed product feeding a packed add
+                // may be fused into one rounding)
+                const float2 u = mul2_rn(mul2_rn(sub2_rn(make_float2(f[e], f[e + 1]), m2), i2),
+                                         make_float2(gv[e], gv[e + 1]));
+                f[e] = b != nullptr ? __fadd_rn(u.x, bv[e]) : u.x;
+                f[e + 1] = b != nullptr ? __fadd_rn(u.y, bv[e + 1]) : u.y;
             }
             st_stream(static_cast<char*>(y) + boff + (int64_t)c * 16, S::pack(f));
         }
