@@ -201,7 +201,7 @@ SAMPLING = {"sample_temperature": ("temperature", dict(temperature=0.7)),
             "sample_min_p": ("min_p", dict(temperature=0.7, p=0.05))}
 
 
-def build_extra_inputs(tokens: int = 8192):
+def build_extra_inputs(tokens: int = 8192, ops=None):
     """Inputs of the ops beyond the step, at the same prefill shapes: QK-norm
     then RoPE on q [T, 32, 128] and k [T, 8, 128] (gains U(0.5, 1.5)); RoPE of
     q and k driven by a cos/sin table of 8192 positions; LayerNorm of
@@ -225,16 +225,19 @@ def build_extra_inputs(tokens: int = 8192):
     pm = np.stack([synth.randint(seed, f"rope_multi.pos{a}", (T,), 0, hi)
                    for a, hi in enumerate((64, 256, 256))], axis=1).astype(np.int32)
     fm = np.concatenate([(10000.0 ** (-2.0 * np.arange(d // 2) / d)).astype(np.float32) for d in MULTI_DIMS])
-    al, pl = cases["argmax"](rows=rows)
-    u = synth.units(seed, "sample.u", al["x"].shape[0]).astype(np.float32)
-    sampling = {op: ({"x": al["x"], "u": u}, dict(pl, method=m, kw=kw)) for op, (m, kw) in SAMPLING.items()}
-    return {
+    sampling = {}
+    if ops is None or any(op in SAMPLING for op in ops):  # the logits are 2.1 GB: only when asked for
+        al, pl = cases["argmax"](rows=rows)
+        u = synth.units(seed, "sample.u", al["x"].shape[0]).astype(np.float32)
+        sampling = {op: ({"x": al["x"], "u": u}, dict(pl, method=m, kw=kw)) for op, (m, kw) in SAMPLING.items()}
+    out = {
         "qk_norm_rope": (dict(qk, gq=gq, gk=gk), dict(pq, eps=1e-6)),
         "rope_qk_half_cached": (dict(qk), dict(pq, cache_len=8192)),
         "layernorm": ({"x": ax["x"], "g": ax["w"], "b": lb}, px),
         "rope_multi": ({"x": xm, "pos": pm, "inv_freq": fm}, {"T": T, "dims": MULTI_DIMS, "mu": 1.0, "layout": 0}),
         **sampling,
     }
+    return out if ops is None else {op: v for op, v in out.items() if op in ops}
 
 
 def build_workload_inputs(workload: str):
@@ -424,7 +427,7 @@ def run_isolated(args):
     else:
         data = build_inputs(args.tokens)
         if args.extra or (args.keep and args.keep & set(EXTRA)):
-            extra = build_extra_inputs(args.tokens)
+            extra = build_extra_inputs(args.tokens, ops=args.keep or None)
             data.update({op: v for op, v in extra.items() if not args.keep or op in args.keep})
     if args.keep:
         data = {op: v for op, v in data.items() if op in args.keep}
