@@ -23,10 +23,12 @@
 // as the equivalent e >= p, since max(e) = 1.)  Rows are limited to 2^23
 // entries so that W < 2^63.
 //
-// Map: one CTA of 512 threads (16 warps) per row.  Warp w owns a contiguous
-// segment of the row, read in coalesced tiles of 32 16-byte vectors (lane l
-// holds tile entries [l V, l V + V)), so index order is warp, tile, lane,
-// element.  The first pass reads HBM; later ones hit L2.
+// Map: one CTA of 512 threads (16 warps) per row -- or, for batches too
+// small to fill the GPU, temperature and min-p rows over a cluster of 2, 4
+// or 8 CTAs.  Warp w owns a contiguous segment of the row, read in
+// coalesced tiles of 32 16-byte vectors (lane l holds tile entries
+// [l V, l V + V)), so index order is warp, tile, lane, element.  The first
+// pass reads HBM; later ones walk the segment backwards and mostly hit L2.
 //  * temperature, min-p (index order): pass 1 the maximum, pass 2 each
 //    warp's kept mass in units of V consecutive entries (their e summed in
 //    f32, the unit sum held as a fixed-point integer); the warp holding the
@@ -36,10 +38,12 @@
 //    maximum; a floor that enough entries reach (from those maxima, sorted
 //    per warp) selects the few entries at the top of the row, which pass 2
 //    gathers into shared memory as (key, ~index) pairs -- for top-p while
-//    it sums the row's mass -- and a bitonic sort orders descending, equal
-//    logits by index (key: an order-keeping 32-bit image of the logit).
-//    Top-k draws among the first k; top-p walks the sorted prefix for the
-//    cut and the draw when the prefix's mass passes the cut.  Otherwise
+//    it sums the row's mass -- and they are ordered descending, equal
+//    logits by index (key: an order-keeping 32-bit image of the logit): up
+//    to 256 by a one-step rank sort, more by a bitonic sort in shared
+//    memory.  Top-k draws among the first k; top-p walks the sorted prefix
+//    for the cut and the draw when the prefix's mass passes the cut (else
+//    a second, wider gather is tried the same way).  Otherwise
 //    (large k, flat or heavily tied rows) an exact radix search: the key's
 //    12 / 10 / 10-bit digits, a histogram per digit (counts, and masses as
 //    exact 64-bit sums in two 32-bit words) locates the bin where the
