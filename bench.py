@@ -411,6 +411,21 @@ def run_ours(args):
     return result
 
 
+def batch_sweep(data):
+    """Each row op of `data` on its first b rows, b = 1, 2, 4, ... up to all
+    of them (keys "op@b"): the batch sweep of the row ops."""
+    out = {}
+    for op, (arrays, params) in data.items():
+        rows = params.get("rows")
+        if not rows:
+            continue
+        bs = sorted({min(rows, 1 << i) for i in range(0, 31) if (1 << i) <= 2 * rows})
+        for b in bs:
+            sl = {k: (v[:b] if getattr(v, "ndim", 0) >= 1 and v.shape[0] == rows else v) for k, v in arrays.items()}
+            out[f"{op}@{b}"] = (sl, dict(params, rows=b))
+    return out
+
+
 def run_isolated(args):
     """Each op alone, launched back to back over rotating copies of its inputs
     and outputs (together more than four times the L2), timed with one CUDA
@@ -431,10 +446,13 @@ def run_isolated(args):
             data.update({op: v for op, v in extra.items() if not args.keep or op in args.keep})
     if args.keep:
         data = {op: v for op, v in data.items() if op in args.keep}
+    if args.sweep:
+        data = batch_sweep(data)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     res = {}
-    for op in list(data):
-        arrays, params = data[op]
+    for key in list(data):
+        op = key.split("@")[0]  # "op@b": the op on the first b rows
+        arrays, params = data[key]
         nb, rows = op_bytes(op, arrays, params)
         sets = int(min(12, max(2, -(-4 * l2 // nb) + 1)))
         base = {k: to_device(torch, dev, v) for k, v in arrays.items()}
@@ -481,7 +499,8 @@ def run_isolated(args):
             e.record()
             torch.cuda.synchronize()
             ms = a.elapsed_time(e) / n
-        res[op] = {"bytes": nb, "us": round(ms * 1e3, 2), "gbs": round(nb / ms / 1e6, 1), "copies": sets}
+        res[key] = {"bytes": nb, "us": round(ms * 1e3, 2), "gbs": round(nb / ms / 1e6, 1),
+                    "rows_per_s": round(rows / ms * 1e3, 1), "copies": sets}
         del rings, base
         torch.cuda.empty_cache()
     peak, kind = peaks()
@@ -826,6 +845,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--isolated", action="store_true",
                     help="time each op alone, back to back over rotating buffers, and print that instead")
+    ap.add_argument("--sweep", action="store_true",
+                    help="with --isolated: each row op on its first b rows, b = 1, 2, 4, ... (batch sweep)")
     ap.add_argument("--graph", action="store_true",
                     help="with --isolated: capture each op's launches in a CUDA graph and time its replays")
     ap.add_argument("--workload", default="",
