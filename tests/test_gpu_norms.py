@@ -139,6 +139,26 @@ def test_batch_invariance_wide_f32():
                 "rmsnorm f32 d=16384")
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_wide_rows_batch_invariant(dtype):
+    """Wide rows (f32: 1024 threads a row, bf16: 512) give the same bits in
+    any batch, for RMSNorm and the fused add (both outputs)."""
+    rows, d = 200, 16384
+    x, w = _inputs(rows, d, dtype, seed=13)
+    r, _ = _inputs(rows, d, dtype, seed=14)
+    xd, wd, rd = to_dev(x), to_dev(w), to_dev(r)
+    ref = gbe.rmsnorm(xd, wd, 1e-5)
+    yf, hf = gbe.add_rmsnorm(xd, rd, wd, 1e-5)
+    _check_rms(x[:3], w, 1e-5, ref[:3], dtype, f"rmsnorm {dtype} wide")
+    iv = torch.int32 if dtype == "f32" else torch.int16
+    for b in (1, 5, 40, 76, 77, 150, 152, 153, 200):
+        y = gbe.rmsnorm(xd[:b].contiguous(), wd, 1e-5)
+        assert torch.equal(y.view(iv), ref[:b].view(iv)), b
+        ya, ha = gbe.add_rmsnorm(xd[:b].contiguous(), rd[:b].contiguous(), wd, 1e-5)
+        assert torch.equal(ya.view(iv), yf[:b].view(iv)), ("add y", b)
+        assert torch.equal(ha.view(iv), hf[:b].view(iv)), ("add h", b)
+
+
 def test_batch_invariance_prefill_bf16():
     """[8192, 4096] bf16: batches b = 1..4096 and rows placed at other offsets."""
     a, p = W.cases(W.PREFILL)["add_rmsnorm"]()
