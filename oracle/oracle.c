@@ -31,7 +31,10 @@
  * taken over num_heads * head_dim instead of per head); k = 17 plants a
  * LayerNorm whose variance is not centred on the mean ([Ops] section 2);
  * k = 18 drops the rule that top-p always keeps its first entry ([Ops]
- * section 8).
+ * section 8); k = 19 rotates every slice of multi-axis RoPE at the first
+ * axis's position ([Ops] section 3); k = 20 cuts min-p at p of the whole
+ * mass instead of p times the largest probability, and k = 21 orders equal
+ * logits by descending index ([Ops] section 8).
  * The tests build those variants on the CPU to show that their pins reject
  * each one.  A normal build (ORACLE_MUTANT undefined) contains none of them.
  */
@@ -256,7 +259,8 @@ int orc_rope_multi(const float *x, float *y, const int32_t *pos, int64_t T, int6
         const int64_t half = dims[a] / 2;
         for (int64_t t = 0; t < T; ++t) {
             for (int64_t j = 0; j < half; ++j) {
-                float theta = (float)((double)pos[t * A + a] * (double)inv_freq[foff + j]);
+                /* s19: every slice at the first axis's position */
+                float theta = (float)((double)pos[t * A + (MUT(19) ? 0 : a)] * (double)inv_freq[foff + j]);
                 float c = (float)cos((double)theta);
                 float s = (float)sin((double)theta);
                 for (int64_t h = 0; h < H; ++h) {
@@ -439,6 +443,7 @@ static int orc_desc_cmp(const void *pa, const void *pb) {
     float va = orc_sort_base[a], vb = orc_sort_base[b];
     if (va > vb) return -1;
     if (va < vb) return 1;
+    if (MUT(21)) return a > b ? -1 : (a < b ? 1 : 0); /* s21: equal logits by descending index */
     return a < b ? -1 : (a > b ? 1 : 0);
 }
 
@@ -483,7 +488,7 @@ static int32_t orc_sample_one(const float *x, int64_t n, int method, float t, in
         float mx = 0.0f;
         for (int64_t j = 0; j < L; ++j)
             if (buf[j] > mx) mx = buf[j];
-        float thr = p * mx;
+        float thr = MUT(20) ? p : p * mx; /* s20: the cut against the whole mass, not the maximum */
         for (int64_t j = 0; j < L; ++j)
             if (!(buf[j] >= thr)) buf[j] = 0.0f;
     }

@@ -405,7 +405,10 @@ def sampling_probs_f64(x, method, t=1.0, k=1, p=1.0):
 def _grid_counts(o, x, method, n_grid, **kw):
     u = ((np.arange(n_grid) + 0.5) / n_grid).astype(np.float32)
     rows = np.repeat(np.asarray(x, np.float32).reshape(1, -1), n_grid, axis=0)
-    return np.bincount(o.sample(rows, method, u, **kw), minlength=rows.shape[1])
+    drawn = o.sample(rows, method, u, **kw)
+    # every method keeps at least one entry of a row that holds a number
+    assert np.all(drawn >= 0), (method, "a row with numbers drew nothing")
+    return np.bincount(drawn, minlength=rows.shape[1])
 
 
 def pin_sampling_draws_in_proportion(o):
@@ -536,4 +539,7 @@ KILLS = {
     16: "qk_norm_rope_per_head",
     17: "layernorm",
     18: "sampling_limits",
+    19: "rope_multi_axis",
+    20: "sampling_draws_in_proportion",
+    21: "sampling_limits",
 }
