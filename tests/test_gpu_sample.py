@@ -254,6 +254,30 @@ def test_draws_do_not_depend_on_the_split(method, kw):
     _check(x[:8], u[:8].cpu().numpy(), method, kw, f"{method} split rows", max_miss=1.0)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_rows_without_a_maximum_in_a_split_batch(dtype):
+    """A small batch of wide rows is split over clusters (eight CTAs a row
+    for temperature and min-p at this size): a row of NaN, a row of -inf
+    and a row holding +inf still give -1, every CTA of their clusters
+    leaving together, and the other rows draw what they draw in a batch of
+    one CTA a row."""
+    n = 131072
+    x32 = widen(_logits(4, n, dtype, nan_frac=0.001, tag="split.lim"))
+    x32[1] = np.nan
+    x32[2, :] = -np.inf
+    x32[3, 5] = np.inf
+    x = to_bf16(x32) if dtype == "bf16" else x32
+    xd = to_dev(x)
+    big = torch.cat([xd] * 80)  # 320 rows: one CTA a row
+    u = torch.from_numpy(_u(4, "split.lim")).cuda()
+    ub = torch.cat([u] * 80)
+    for m, kw in METHODS:
+        got = gbe.sample(xd, u, m, **kw).cpu().numpy()
+        assert got[1] == -1 and got[2] == -1 and got[3] == -1, (m, got)
+        ref = gbe.sample(big, ub, m, **kw).cpu().numpy()
+        assert np.array_equal(got, ref[:4]), (m, got, ref[:4])
+
+
 def test_top_p_rows_past_the_first_gather():
     """Top-p 0.9 at t = 0.7 on the first 512 rows of the prefill logits (the
     bench's setting): in about 2 % of them the first, narrow gather of the
