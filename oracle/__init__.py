@@ -13,7 +13,8 @@ the definition the pages give, written out step by step in f32; the
 citations sit beside each function in ``oracle.c``.
 
 ``Oracle(mutant=k)`` loads a build with the k-th planted mistake of the
-pages' pitfalls table (s01..s15), so tests can show that the pins reject it.
+pages' pitfalls table and the further planted mistakes (s01..s24), so tests can
+show that the pins reject each one.
 """
 from __future__ import annotations
 
@@ -63,6 +64,7 @@ class Oracle:
         self.mutant = mutant
         lib = ctypes.CDLL(build(mutant))
         i64, f32, vp, i32 = ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_int
+        u64 = ctypes.c_uint64
         sig = {
             "orc_rmsnorm": [vp, vp, vp, i64, i64, f32],
             "orc_add": [vp, vp, vp, i64],
@@ -77,6 +79,11 @@ class Oracle:
             "orc_argmax": [vp, i64],
             "orc_argmax_rows": [vp, vp, i64, i64],
             "orc_sample_rows": [vp, vp, i64, i64, i32, f32, i64, f32, vp, vp, vp],
+            "orc_sample_rows_seeded": [vp, vp, i64, i64, i32, f32, i64, f32, u64, u64, vp, vp, vp],
+            "orc_pcg64_seeded_state": [u64, vp],
+            "orc_pcg64_raw": [u64, u64, u64, u64, i64, vp, vp],
+            "orc_pcg64_advance": [u64, u64, u64, u64, u64, u64, vp],
+            "orc_pcg64_uniforms": [u64, u64, i64, vp],
             "orc_bf16_widen": [vp, vp, i64],
             "orc_bf16_round": [vp, vp, i64],
             "orc_mutant": [],
@@ -85,7 +92,7 @@ class Oracle:
             fn = getattr(lib, name)
             fn.argtypes = args
             fn.restype = ctypes.c_int32 if name == "orc_argmax" else (
-                None if name.startswith("orc_bf16") else ctypes.c_int)
+                None if name.startswith(("orc_bf16", "orc_pcg64")) else ctypes.c_int)
         assert lib.orc_mutant() == mutant
         self.lib = lib
 
@@ -247,6 +254,56 @@ class Oracle:
         self._check(self.lib.orc_sample_rows(_ptr(x), _ptr(out), rows, n, m, temperature, top_k, pp, _ptr(u),
                                              _ptr(idx), _ptr(buf)), "sample")
         return out
+
+    def sample_seeded(self, x, method: str, seed: int, offset: int, temperature: float = 1.0, top_k: int = 1,
+                      top_p: float = 1.0, min_p: float = 0.0) -> np.ndarray:
+        """One draw per row of x [rows, n]; row r draws with the uniform of
+        draw offset + r of the PCG64 stream seeded with `seed`."""
+        x = _f32(x)
+        if x.ndim == 1:
+            x = x.reshape(1, -1)
+        rows, n = x.shape
+        out = np.empty(rows, dtype=np.int32)
+        u = np.empty(rows, dtype=np.float32)
+        idx = np.empty(n, dtype=np.int64)
+        buf = np.empty(n, dtype=np.float32)
+        pp = top_p if method == "top_p" else min_p
+        self._check(self.lib.orc_sample_rows_seeded(_ptr(x), _ptr(out), rows, n, self.METHODS[method], temperature,
+                                                    top_k, pp, seed, offset, _ptr(u), _ptr(idx), _ptr(buf)),
+                    "sample_seeded")
+        return out
+
+    # -- the seeded generator (PCG64) ----------------------------------------------
+    @staticmethod
+    def _split(v: int) -> tuple[int, int]:
+        v &= (1 << 128) - 1
+        return v >> 64, v & ((1 << 64) - 1)
+
+    def pcg64_seeded_state(self, seed: int) -> int:
+        """The 128-bit state the seed plants."""
+        st = np.empty(2, dtype=np.uint64)
+        self.lib.orc_pcg64_seeded_state(seed, _ptr(st))
+        return (int(st[0]) << 64) | int(st[1])
+
+    def pcg64_raw(self, state: int, inc: int, count: int) -> tuple[np.ndarray, int]:
+        """`count` 64-bit outputs from (state, inc), each after its step, and
+        the final state."""
+        out = np.empty(count, dtype=np.uint64)
+        st = np.empty(2, dtype=np.uint64)
+        self.lib.orc_pcg64_raw(*self._split(state), *self._split(inc), count, _ptr(out), _ptr(st))
+        return out, (int(st[0]) << 64) | int(st[1])
+
+    def pcg64_advance(self, state: int, inc: int, delta: int) -> int:
+        """The state `delta` steps after `state` (0 <= delta < 2^128)."""
+        st = np.empty(2, dtype=np.uint64)
+        self.lib.orc_pcg64_advance(*self._split(state), *self._split(inc), *self._split(delta), _ptr(st))
+        return (int(st[0]) << 64) | int(st[1])
+
+    def pcg64_uniforms(self, seed: int, offset: int, n: int) -> np.ndarray:
+        """The uniforms of draws offset .. offset + n - 1 of the seeded stream."""
+        u = np.empty(n, dtype=np.float32)
+        self.lib.orc_pcg64_uniforms(seed, offset, n, _ptr(u))
+        return u
 
     def argmax_one(self, x) -> int:
         """The pages' single-row routine as written, -1 for an empty row too."""

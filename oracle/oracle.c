@@ -34,7 +34,11 @@
  * section 8); k = 19 rotates every slice of multi-axis RoPE at the first
  * axis's position ([Ops] section 3); k = 20 cuts min-p at p of the whole
  * mass instead of p times the largest probability, and k = 21 orders equal
- * logits by descending index ([Ops] section 8).
+ * logits by descending index ([Ops] section 8); k = 22 takes the PCG64
+ * output rotation from the wrong bits of the state, k = 23 drops the
+ * increment's own term from the squared step of the jump-ahead, and k = 24
+ * takes an output before its step instead of after it ([Ops] section 8, the
+ * seeded generator).
  * The tests build those variants on the CPU to show that their pins reject
  * each one.  A normal build (ORACLE_MUTANT undefined) contains none of them.
  */
@@ -509,6 +513,108 @@ int orc_sample_rows(const float *x, int32_t *out, int64_t rows, int64_t n, int m
     for (int64_t r = 0; r < rows; ++r)
         out[r] = orc_sample_one(x + r * n, n, method, t, k, p, u ? u[r] : 0.0f, idx, buf);
     return ORC_OK;
+}
+
+/* ---- The seeded uniforms of sample_categorical ----------------------------------
+ * [Ops] 8 (Sample): sample_categorical draws "using a seeded RNG (Xorshift or
+ * PCG)", and the same seed with the same distribution gives the same draw.
+ * Reading: PCG64 -- the 128-bit linear congruential generator
+ * state' = state * M + INC (mod 2^128) with the XSL-RR output permutation,
+ * as O'Neill defines it ("PCG: A Family of Simple Fast Space-Efficient
+ * Statistically Good Algorithms for Random Number Generation", 2014): after
+ * each step the output is the xor of the state's two 64-bit halves, rotated
+ * right by the state's top 6 bits.  M and INC are that generator's default
+ * 128-bit multiplier and increment.  A 64-bit seed s is planted as the PCG
+ * reference seeds: state = 0, one step, state += s, one step.  Draw number j
+ * (j = 0, 1, ...) of the seeded stream is the output after j + 1 further
+ * steps, and its uniform is its top 24 bits times 2^-24 (exact in f32, in
+ * [0, 1)).  A batch drawn at stream position `offset` gives row r draw
+ * number offset + r.  The stream is entered at draw j without stepping j
+ * times by the jump-ahead of an LCG (Brown, "Random Number Generation with
+ * Arbitrary Strides", 1994): the affine map s -> M s + INC is composed with
+ * itself by repeated squaring, over the bits of the distance.                 */
+__extension__ typedef unsigned __int128 orc_u128;
+
+static orc_u128 orc_u128_of(uint64_t hi, uint64_t lo) { return ((orc_u128)hi << 64) | lo; }
+static orc_u128 orc_pcg_mult(void) { return orc_u128_of(0x2360ED051FC65DA4ULL, 0x4385DF649FCCF645ULL); }
+static orc_u128 orc_pcg_inc(void) { return orc_u128_of(0x5851F42D4C957F2DULL, 0x14057B7EF767814FULL); }
+
+static orc_u128 orc_pcg_step(orc_u128 s, orc_u128 inc) { return s * orc_pcg_mult() + inc; }
+
+static uint64_t orc_pcg_output(orc_u128 s) {
+    uint64_t x = (uint64_t)(s >> 64) ^ (uint64_t)s;
+    unsigned rot = (unsigned)(s >> 122);
+    if (MUT(22)) rot = (unsigned)(s >> 58) & 63u; /* s22: rotation taken from the wrong bits */
+    return (x >> rot) | (x << ((64u - rot) & 63u));
+}
+
+/* the state `delta` steps after s */
+static orc_u128 orc_pcg_advance(orc_u128 s, orc_u128 inc, orc_u128 delta) {
+    orc_u128 acc_m = 1, acc_c = 0;   /* the map so far: s -> acc_m s + acc_c */
+    orc_u128 m = orc_pcg_mult(), c = inc; /* the step map raised to 2^bit */
+    while (delta != 0) {
+        if (delta & 1) {
+            acc_m = acc_m * m;
+            acc_c = acc_c * m + c;
+        }
+        c = MUT(23) ? m * c : (m + 1) * c; /* s23: the squared map's increment loses its c term */
+        m = m * m;
+        delta >>= 1;
+    }
+    return acc_m * s + acc_c;
+}
+
+static orc_u128 orc_pcg_seeded(uint64_t seed) {
+    orc_u128 s = orc_pcg_step(0, orc_pcg_inc());
+    s = s + seed;
+    return orc_pcg_step(s, orc_pcg_inc());
+}
+
+/* For the pins: the seeded state, as (hi, lo). */
+void orc_pcg64_seeded_state(uint64_t seed, uint64_t *hi_lo) {
+    orc_u128 s = orc_pcg_seeded(seed);
+    hi_lo[0] = (uint64_t)(s >> 64);
+    hi_lo[1] = (uint64_t)s;
+}
+
+/* For the pins: `count` outputs from an arbitrary (state, inc), stepping
+ * first; st[0..1] receives the final state (hi, lo). */
+void orc_pcg64_raw(uint64_t s_hi, uint64_t s_lo, uint64_t inc_hi, uint64_t inc_lo, int64_t count, uint64_t *out,
+                   uint64_t *st) {
+    orc_u128 s = orc_u128_of(s_hi, s_lo), inc = orc_u128_of(inc_hi, inc_lo);
+    for (int64_t i = 0; i < count; ++i) {
+        s = MUT(24) ? s : orc_pcg_step(s, inc); /* s24: output taken before the step */
+        out[i] = orc_pcg_output(s);
+        if (MUT(24)) s = orc_pcg_step(s, inc);
+    }
+    st[0] = (uint64_t)(s >> 64);
+    st[1] = (uint64_t)s;
+}
+
+/* For the pins: the state delta (= d_hi 2^64 + d_lo) steps after (s, inc). */
+void orc_pcg64_advance(uint64_t s_hi, uint64_t s_lo, uint64_t inc_hi, uint64_t inc_lo, uint64_t d_hi,
+                       uint64_t d_lo, uint64_t *st) {
+    orc_u128 s = orc_pcg_advance(orc_u128_of(s_hi, s_lo), orc_u128_of(inc_hi, inc_lo), orc_u128_of(d_hi, d_lo));
+    st[0] = (uint64_t)(s >> 64);
+    st[1] = (uint64_t)s;
+}
+
+/* u[i] = the uniform of draw offset + i of the stream seeded with `seed`. */
+void orc_pcg64_uniforms(uint64_t seed, uint64_t offset, int64_t n, float *u) {
+    orc_u128 s = orc_pcg_advance(orc_pcg_seeded(seed), orc_pcg_inc(), offset);
+    for (int64_t i = 0; i < n; ++i) {
+        s = orc_pcg_step(s, orc_pcg_inc());
+        u[i] = (float)(orc_pcg_output(s) >> 40) * 0x1p-24f;
+    }
+}
+
+/* Sample with the seeded uniforms: row r draws with the uniform of draw
+ * offset + r of the stream seeded with `seed`.  u is scratch of `rows`. */
+int orc_sample_rows_seeded(const float *x, int32_t *out, int64_t rows, int64_t n, int method, float t, int64_t k,
+                           float p, uint64_t seed, uint64_t offset, float *u, int64_t *idx, float *buf) {
+    if (rows < 0) return ORC_ERR_ARG;
+    orc_pcg64_uniforms(seed, offset, rows, u);
+    return orc_sample_rows(x, out, rows, n, method, t, k, p, u, idx, buf);
 }
 
 int orc_argmax_rows(const float *x, int32_t *out, int64_t rows, int64_t n) {

@@ -446,6 +446,116 @@ def pin_sampling_limits(o):
                           o.sample(x, "temperature", u, temperature=0.9))
 
 
+# ---- The seeded generator of sample_categorical (PCG64) ---------------------------
+# numpy's PCG64 bit generator is the same generator (128-bit LCG with the
+# default multiplier, XSL-RR output after each step), implemented
+# independently: its state can be set to any (state, increment), stepped
+# (random_raw) and jumped (advance), which pins the oracle's step, output
+# permutation and jump-ahead.  The seeding procedure and the uniform are
+# definitions ("Operations" section 8 leaves them open); they are checked by
+# composing numpy's steps the way the definition says.
+
+PCG_INC = (0x5851F42D4C957F2D << 64) | 0x14057B7EF767814F  # the generator's default increment
+_M128 = (1 << 128) - 1
+
+
+def _numpy_pcg(state: int, inc: int):
+    bg = np.random.PCG64()
+    bg.state = {"bit_generator": "PCG64", "state": {"state": state & _M128, "inc": inc & _M128},
+                "has_uint32": 0, "uinteger": 0}
+    return bg
+
+
+def _rand128() -> int:
+    return int.from_bytes(RNG.bytes(16), "little")
+
+
+def pin_pcg64_steps_as_numpy(o):
+    """Outputs and final state from arbitrary (state, odd increment) equal
+    numpy's PCG64 random_raw from the same state."""
+    for trial in range(20):
+        state, inc = _rand128(), _rand128() | 1
+        if trial == 0:
+            state, inc = 0, PCG_INC
+        got, end = o.pcg64_raw(state, inc, 64)
+        bg = _numpy_pcg(state, inc)
+        want = bg.random_raw(64)
+        assert np.array_equal(got, want), (trial, got[:3], want[:3])
+        assert end == bg.state["state"]["state"], trial
+
+
+def pin_pcg64_jump_ahead(o):
+    """The jump of delta steps equals numpy's advance(delta), for small,
+    large and wrapping distances, and equals delta single steps."""
+    for trial in range(8):
+        state, inc = _rand128(), _rand128() | 1
+        for delta in (0, 1, 2, 3, 7, 1000, 12345677, (1 << 40) + 7, (1 << 64) - 1, (1 << 64) + 3,
+                      (1 << 127) + 5, _M128):
+            bg = _numpy_pcg(state, inc)
+            bg.advance(delta)
+            assert o.pcg64_advance(state, inc, delta) == bg.state["state"]["state"], (trial, delta)
+        _, stepped = o.pcg64_raw(state, inc, 513)
+        assert o.pcg64_advance(state, inc, 513) == stepped
+
+
+def pin_pcg64_seeding_and_uniforms(o):
+    """Seeding: state 0, a step, plus the seed, a step (numpy's steps).  Draw
+    j of the seeded stream is the output after j + 1 further steps; its
+    uniform is the top 24 bits times 2^-24.  Consecutive windows of draws
+    agree with one long run, and offsets past 2^64 continue the stream."""
+    for seed in (0, 1, 42, 2 ** 63 + 11, 2 ** 64 - 1):
+        bg = _numpy_pcg(0, PCG_INC)
+        bg.random_raw(1)
+        s1 = bg.state["state"]["state"]
+        bg = _numpy_pcg(s1 + seed, PCG_INC)
+        bg.random_raw(1)
+        seeded = bg.state["state"]["state"]
+        assert o.pcg64_seeded_state(seed) == seeded, seed
+        for offset in (0, 1, 1000, 2 ** 32 + 5, 2 ** 64 - 3):
+            bg = _numpy_pcg(seeded, PCG_INC)
+            bg.advance(offset)
+            raw = bg.random_raw(9)
+            want = ((raw >> np.uint64(40)).astype(np.float64) * 2.0 ** -24).astype(np.float32)
+            got = o.pcg64_uniforms(seed, offset, 9)
+            assert _same_bits(got, want), (seed, offset, got, want)
+            assert np.all((got >= 0) & (got < 1))
+            if offset + 4 < 2 ** 64:
+                assert _same_bits(o.pcg64_uniforms(seed, offset + 4, 5), got[4:])
+
+
+def pin_pcg64_uniformity(o):
+    """A million uniforms of one seed are flat over 256 bins (chi-square
+    within six standard deviations of its mean), multiples of 2^-24 with
+    mean 1/2; another seed's stream is uncorrelated with it."""
+    n = 1 << 20
+    u = o.pcg64_uniforms(7, 0, n).astype(np.float64)
+    assert np.all(u * 2 ** 24 == np.floor(u * 2 ** 24))
+    counts = np.bincount((u * 256).astype(np.int64), minlength=256)
+    e = n / 256
+    chi2 = float(((counts - e) ** 2 / e).sum())
+    assert abs(chi2 - 255) < 6 * np.sqrt(2 * 255), chi2
+    assert abs(u.mean() - 0.5) < 6 * np.sqrt(1 / 12 / n), u.mean()
+    v = o.pcg64_uniforms(8, 0, n).astype(np.float64)
+    assert abs(np.corrcoef(u, v)[0, 1]) < 6 / np.sqrt(n)
+
+
+def pin_sampling_seeded_draws(o):
+    """The seeded draw of row r is the draw at the uniform of stream draw
+    offset + r: the same seed gives the same draws, another seed others."""
+    x = _rand(64, 500, scale=2.0)
+    for method, kw in (("temperature", dict(temperature=0.8)), ("top_k", dict(temperature=1.1, top_k=20)),
+                       ("top_p", dict(temperature=0.9, top_p=0.8)), ("min_p", dict(temperature=1.0, min_p=0.1))):
+        for seed, offset in ((3, 0), (3, 64), (2 ** 64 - 5, 2 ** 40)):
+            bg = _numpy_pcg(o.pcg64_seeded_state(seed), PCG_INC)
+            bg.advance(offset)
+            u = ((bg.random_raw(64) >> np.uint64(40)).astype(np.float64) * 2.0 ** -24).astype(np.float32)
+            got = o.sample_seeded(x, method, seed, offset, **kw)
+            assert np.array_equal(got, o.sample(x, method, u, **kw)), (method, seed, offset)
+            assert np.array_equal(got, o.sample_seeded(x, method, seed, offset, **kw))
+        other = o.sample_seeded(x, method, 4, 0, **kw)
+        assert not np.array_equal(other, o.sample_seeded(x, method, 3, 0, **kw)), method
+
+
 # ---- Embedding / add / argmax / bf16 ---------------------------------------------
 
 def pin_embedding_gathers_rows(o):
@@ -542,4 +652,7 @@ KILLS = {
     19: "rope_multi_axis",
     20: "sampling_draws_in_proportion",
     21: "sampling_limits",
+    22: "pcg64_steps_as_numpy",
+    23: "pcg64_jump_ahead",
+    24: "pcg64_steps_as_numpy",
 }
