@@ -76,10 +76,12 @@ typedef unsigned long long u64;
 
 enum { kGreedy = 0, kTemperature = 1, kTopK = 2, kTopP = 3, kMinP = 4 };
 
-// Larger logit, larger key (the IEEE order of non-NaN floats, -0 below +0),
-// and back.
+// Larger logit, larger key (the IEEE order of non-NaN floats), and back.
+// -0 takes the key of +0: the two are equal logits, which order by index
+// like any other equal logits (as argmax ties -0 and +0 to the lower index).
 __device__ __forceinline__ uint32_t order_key(float v) {
-    const uint32_t b = __float_as_uint(v);
+    uint32_t b = __float_as_uint(v);
+    if (b == 0x80000000u) b = 0u;
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 __device__ __forceinline__ float key_value(uint32_t key) {

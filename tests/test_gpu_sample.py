@@ -380,3 +380,69 @@ def test_candidate_counts(method, kw):
     x32 = widen(x)
     for r in range(x.shape[0]):
         assert _valid_draw(x32[r], float(u[r]), method, kw, int(got[r]), 2e-6), (method, kw, r, u[r], got[r])
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_signed_zeros_are_equal_logits(dtype):
+    """-0 and +0 are equal logits, ordered by index like any other equal
+    logits ("Operations" section 8 sorts descending; equal logits keep index
+    order, and -0 equals +0 as in the argmax rule of "Elementwise kernels in
+    C" section 2.4).  Rows whose largest entries are zeros of both signs, -0
+    at lower indices than +0: top-k cuts between them and top-p walks across
+    them.  The weights of the zeros are exactly 2^40 each and every other
+    entry is far below them, so the draw is the floor(u * m)-th kept zero in
+    index order, exactly, for m kept zeros; the oracle must agree."""
+    rows, n = 16, 4096
+    x = normal(37, f"t.smp.zero.{n}", (rows, n), -40.0, 1.0)
+    x = np.minimum(x, -30.0).astype(np.float32)
+    zeros = []
+    for r in range(rows):
+        pos = np.sort(np.unique((units(37, f"t.smp.zero.pos.{r}", 8) * n).astype(np.int64)))[:6]
+        assert len(pos) == 6
+        sign = np.array([-0.0, -0.0, 0.0, -0.0, 0.0, 0.0], np.float32)
+        if r % 2:
+            sign = -sign  # +0 first on odd rows
+        x[r, pos] = sign
+        zeros.append(pos)
+    assert np.signbit(x[0, zeros[0][0]]) and not np.signbit(x[0, zeros[0][2]])
+    xx = to_bf16(x) if dtype == "bf16" else x
+    xd = to_dev(xx)
+    u = _u(rows, "zero")
+    ud = torch.from_numpy(u).cuda()
+    x32 = widen(xx)
+    for method, kw, m in (("top_k", dict(temperature=1.0, top_k=1), 1),
+                          ("top_k", dict(temperature=1.0, top_k=3), 3),
+                          ("top_k", dict(temperature=0.7, top_k=5), 5),
+                          ("top_p", dict(temperature=1.0, p=0.6), 3),
+                          ("top_p", dict(temperature=1.0, p=0.4), 2)):
+        got = gbe.sample(xd, ud, method, **kw).cpu().numpy()
+        want = np.array([zeros[r][int(np.floor(np.float64(u[r]) * m))] for r in range(rows)])
+        assert np.array_equal(got, want), (method, kw, got, want)
+        assert np.array_equal(got, _oracle(x32, u, method, kw)), (method, kw)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_many_signed_zeros_take_the_exact_search(dtype):
+    """2000 zeros of random sign among 8192 entries far below them: top-k
+    with k = 600 (past the gathered paths, so the exact radix search) and
+    top-p with p = 0.3001 (600 of 2000 equal weights) keep the first 600
+    zeros in index order, whatever their signs."""
+    rows, n, nz = 4, 8192, 2000
+    x = np.minimum(normal(41, "t.smp.zeros.many", (rows, n), -40.0, 1.0), -30.0).astype(np.float32)
+    zeros = []
+    for r in range(rows):
+        perm = np.argsort(units(41, f"t.smp.zeros.perm.{r}", n))
+        pos = np.sort(perm[:nz])
+        sgn = units(41, f"t.smp.zeros.sign.{r}", nz) < 0.5
+        x[r, pos] = np.where(sgn, np.float32(-0.0), np.float32(0.0))
+        zeros.append(pos)
+    xx = to_bf16(x) if dtype == "bf16" else x
+    xd = to_dev(xx)
+    u = _u(rows, "zeros.many")
+    ud = torch.from_numpy(u).cuda()
+    for method, kw in (("top_k", dict(temperature=1.0, top_k=600)), ("top_p", dict(temperature=1.0, p=0.3001))):
+        got = gbe.sample(xd, ud, method, **kw).cpu().numpy()
+        want = np.array([zeros[r][int(np.floor(np.float64(u[r]) * 600))] for r in range(rows)])
+        assert np.array_equal(got, want), (method, got, want)
+        assert np.array_equal(got, _oracle(widen(xx), u, method, kw)), method
+
