@@ -102,6 +102,49 @@ inline cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
     return e;
 }
 
+// ---- RoPE angles ------------------------------------------------------------------
+
+// cos and sin of a RoPE angle theta (the f32 product position * frequency).
+// sincosf on an argument beyond about 10^5 takes a long exact reduction
+// (positions near 2^20 give angles near 10^6 rad), which costs several times
+// the rest of a RoPE launch.  So the angle is first reduced by quarter turns
+// with Cody and Waite's method ("Software Manual for the Elementary
+// Functions", 1980): k = rint(theta * 2/pi), and r = theta - k pi/2 with
+// pi/2 split into three f32 parts, P1 + P2 + P3, each the f32 nearest to
+// what the parts before it leave of pi/2 (the rest, 1.1e-23, is negligible).
+// For |theta| < 2^22 the first step, fma(-k, P1, theta), is exact: theta
+// and k * P1 are both multiples of 2^-23 and their difference is below 2 in
+// magnitude; the other two steps round once each, so r carries an error of
+// about one f32 ulp of r (about 1e-7 rad).  k may be off by one (the f32
+// product theta * 2/pi rounds), which only leaves |r| a little above pi/4.
+// sincosf then takes r on its short path, and the quadrant k mod 4 maps
+// (cos r, sin r) to (cos theta, sin theta).  Angles of 2^22 and beyond go to
+// sincosf whole.  theta = 0 gives exactly (1, 0), so position 0 is the
+// identity.  Every RoPE kernel and the cos/sin table use this one function,
+// so the table-driven and the formed results agree bit for bit.
+__device__ __forceinline__ void rope_sincos(float theta, float* s, float* c) {
+    constexpr float kTwoOverPi = 0x1.45f306p-1f;
+    constexpr float kP1 = 0x1.921fb6p+0f;
+    constexpr float kP2 = -0x1.777a5cp-25f;
+    constexpr float kP3 = -0x1.ee59dap-50f;
+    if (fabsf(theta) < 4194304.0f) {
+        const float k = rintf(__fmul_rn(theta, kTwoOverPi));
+        float r = __fmaf_rn(-k, kP1, theta);
+        r = __fmaf_rn(-k, kP2, r);
+        r = __fmaf_rn(-k, kP3, r);
+        float sr, cr;
+        sincosf(r, &sr, &cr);
+        switch ((int)k & 3) {
+            case 0: *s = sr; *c = cr; break;
+            case 1: *s = cr; *c = -sr; break;
+            case 2: *s = -sr; *c = -cr; break;
+            default: *s = -cr; *c = sr; break;
+        }
+    } else {
+        sincosf(theta, s, c);
+    }
+}
+
 // ---- storage traits ------------------------------------------------------------
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b16) { return __uint_as_float(b16 << 16); }

@@ -18,7 +18,7 @@
 //    rows can share a warp;
 //  * the normalised value is rounded to the storage type before the
 //    rotation reads it, as a stored intermediate would be;
-//  * the angles are float(p) * omega_i and CUDA's sincosf (or the same values
+//  * the angles are float(p) * omega_i and rope_sincos (or the same values
 //    from the cos/sin table), as in rope.cu.
 //
 // Map: one CTA per token (qk_norm_rope_pair and qk_norm_rope_tok, aligned
@@ -161,7 +161,7 @@ qk_norm_rope_tok(QkSide A, QkSide B, int nca, int ncb, float eps, const int32_t*
             cv = v.x;
             sv = v.y;
         } else {
-            sincosf(__fmul_rn((float)p, __ldg(inv_freq + i)), &sv, &cv);
+            rope_sincos(__fmul_rn((float)p, __ldg(inv_freq + i)), &sv, &cv);
         }
         const int slot = angle_slot<QPL>(i, half);
         cs_cos[slot] = cv;
@@ -388,7 +388,7 @@ qk_norm_rope_pair(QkSide A, QkSide B, int nca, int ncb, float eps, const int32_t
             cv = v.x;
             sv = v.y;
         } else {
-            sincosf(__fmul_rn((float)p, __ldg(inv_freq + i)), &sv, &cv);
+            rope_sincos(__fmul_rn((float)p, __ldg(inv_freq + i)), &sv, &cv);
         }
         const int slot = angle_slot<QPL>(i, half);
         cs_cos[slot] = cv;
@@ -537,7 +537,7 @@ qk_norm_rope_kernel(QkSide A, QkSide B, int nca, int ncb, float eps, const int32
                 ca[e] = v.x;
                 sa[e] = v.y;
             } else {
-                sincosf(__fmul_rn((float)p, __ldg(inv_freq + i)), &sa[e], &ca[e]);
+                rope_sincos(__fmul_rn((float)p, __ldg(inv_freq + i)), &sa[e], &ca[e]);
             }
         }
     }

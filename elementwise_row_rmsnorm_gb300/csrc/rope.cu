@@ -8,8 +8,9 @@
 //
 // The angle is the f32 product float(p_t) * omega_i (the correctly rounded
 // product, equal to the double product rounded to f32 for p_t < 2^24), and
-// its cosine and sine come from CUDA's accurate sincosf (never the __sinf
-// approximation: at positions near 2^20 the angles reach 10^6 rad).  The
+// its cosine and sine come from rope_sincos: a quarter-turn reduction, then
+// CUDA's accurate sincosf on the remainder (never the __sinf approximation:
+// at positions near 2^20 the angles reach 10^6 rad).  The
 // pages' loop order is token, pair, head with one angle per (token, pair);
 // here a thread owns a group of pairs of one token and forms their angles
 // once, in registers, for a chunk of up to four heads (so an angle is formed
@@ -68,7 +69,7 @@ __device__ __forceinline__ void angle(int32_t p, int i, const float* inv_freq, c
         c = v.x;
         s = v.y;
     } else {
-        sincosf(__fmul_rn((float)p, __ldg(inv_freq + i)), &s, &c);
+        rope_sincos(__fmul_rn((float)p, __ldg(inv_freq + i)), &s, &c);
     }
 }
 
@@ -237,7 +238,7 @@ rope_multi_kernel(const void* x, void* y, const int32_t* pos, int64_t T, int H, 
         const int j = k - ax.poff[a];
         const int half = ax.poff[a + 1] - ax.poff[a];
         float c, sn;
-        sincosf(__fmul_rn((float)pos[t * ax.A + a], __ldg(inv_freq + k)), &sn, &c);
+        rope_sincos(__fmul_rn((float)pos[t * ax.A + a], __ldg(inv_freq + k)), &sn, &c);
         const int ia = ax.off[a] + (LAYOUT == 0 ? j : 2 * j);
         const int ib = ax.off[a] + (LAYOUT == 0 ? j + half : 2 * j + 1);
         for (int h = 0; h < H; ++h) {
@@ -313,7 +314,7 @@ rope_multi_vec(const char* x, char* y, const int32_t* pos, int64_t T, int H, int
     const float p = (float)pos[t * ax.A + a];
     const int k0 = ax.poff[a] + i0;
 #pragma unroll
-    for (int e = 0; e < P; ++e) sincosf(__fmul_rn(p, __ldg(inv_freq + k0 + e)), &sn[e], &c[e]);
+    for (int e = 0; e < P; ++e) rope_sincos(__fmul_rn(p, __ldg(inv_freq + k0 + e)), &sn[e], &c[e]);
 
 #pragma unroll
     for (int j = 0; j < HC; ++j) {
@@ -368,7 +369,7 @@ rope_cos_sin_table(float2* cache, int64_t len, int half, const float* inv_freq) 
     if (p >= len) return;
     const int i = (int)(gt - p * half);
     float c, s;
-    sincosf(__fmul_rn((float)p, __ldg(inv_freq + i)), &s, &c);
+    rope_sincos(__fmul_rn((float)p, __ldg(inv_freq + i)), &s, &c);
     cache[gt] = make_float2(c, s);
 }
 
