@@ -1,11 +1,13 @@
 // abi.cu -- the C entry points declared in include/gbe_elementwise.h.
 //
 // Every argument is validated here, on the host, before anything is
-// enqueued: sizes and scalars, pointer alignment, that each non-empty buffer
-// is memory the current device can address and that its extent stays inside
-// its allocation, and that outputs overlap nothing but their permitted exact
-// aliases.  Only then is the launcher of the op called.  Nothing here
-// allocates, frees or waits.
+// enqueued, in this order: sizes and scalars; pointer presence and
+// alignment; that outputs overlap nothing but their permitted exact aliases
+// (address arithmetic alone); that each non-empty buffer is memory the
+// current device can address and that its extent stays inside its
+// allocation (driver queries, one per distinct allocation of the call).
+// Only then is the launcher of the op called.  Nothing here allocates,
+// frees or waits.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -25,20 +27,30 @@ thread_local int t_last_cuda_error = 0;
 int elem_size(int dtype) { return dtype == GBE_F32 ? 4 : dtype == GBE_BF16 ? 2 : 0; }
 
 typedef CUresult (*AddressRangeFn)(CUdeviceptr*, size_t*, CUdeviceptr);
+typedef CUresult (*PointerAttributeFn)(void*, CUpointer_attribute, CUdeviceptr);
+
+// A driver entry point, looked up once (the library does not link libcuda).
+void* driver_fn(const char* name) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+        return p;
+    cudaGetLastError();
+    return nullptr;
+}
 
 AddressRangeFn address_range_fn() {
     static std::once_flag once;
     static AddressRangeFn fn = nullptr;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<AddressRangeFn>(p);
-        else
-            cudaGetLastError();
-    });
+    std::call_once(once, [] { fn = reinterpret_cast<AddressRangeFn>(driver_fn("cuMemGetAddressRange")); });
+    return fn;
+}
+
+PointerAttributeFn pointer_attribute_fn() {
+    static std::once_flag once;
+    static PointerAttributeFn fn = nullptr;
+    std::call_once(once, [] { fn = reinterpret_cast<PointerAttributeFn>(driver_fn("cuPointerGetAttribute")); });
     return fn;
 }
 
@@ -49,39 +61,95 @@ struct Buf {
     uint64_t align;
 };
 
-int check_buf(const Buf& b, int dev) {
+// The checks that need no driver: a non-empty buffer has a pointer, aligned
+// to its element size, whose extent does not wrap around the address space.
+int check_form(const Buf& b) {
     if (b.bytes == 0) return GBE_OK;
     if (b.p == nullptr) return GBE_ERR_NULL;
     if (reinterpret_cast<uintptr_t>(b.p) % b.align) return GBE_ERR_ALIGN;
-    cudaPointerAttributes a;
-    if (cudaPointerGetAttributes(&a, b.p) != cudaSuccess) {
-        cudaGetLastError();
-        return GBE_ERR_POINTER;
-    }
-    switch (a.type) {
-        case cudaMemoryTypeDevice:
-            if (a.device != dev) return GBE_ERR_POINTER;
-            break;
-        case cudaMemoryTypeManaged:
-            break;
-        case cudaMemoryTypeHost:  // pinned host memory, usable only when mapped at the same address
-            if (a.devicePointer != b.p) return GBE_ERR_POINTER;
-            break;
-        default:
-            return GBE_ERR_POINTER;
-    }
-    if (a.type != cudaMemoryTypeHost) {
-        if (AddressRangeFn fn = address_range_fn()) {
-            CUdeviceptr base = 0;
-            size_t size = 0;
-            const CUdeviceptr p = reinterpret_cast<CUdeviceptr>(b.p);
-            if (fn(&base, &size, p) == CUDA_SUCCESS) {
-                if (p + b.bytes > base + size || p + b.bytes < p) return GBE_ERR_POINTER;
-            }
-        }
-    }
+    if (reinterpret_cast<uintptr_t>(b.p) + b.bytes < reinterpret_cast<uintptr_t>(b.p)) return GBE_ERR_POINTER;
     return GBE_OK;
 }
+
+// The buffers of one call checked against the driver's record of their
+// allocations: each must be memory of the current device (or managed
+// memory, or pinned host memory mapped at the same address), and its extent
+// must lie inside its allocation.  An allocation, once found, is remembered
+// for the rest of the call, so buffers carved from one allocation (q and k
+// slices of one QKV buffer, small tensors of one caching-allocator segment)
+// take one driver query between them.  Nothing is remembered across calls:
+// memory may be freed and reused between them.
+class Checker {
+  public:
+    int begin() {
+        if (cudaGetDevice(&dev_) != cudaSuccess) {
+            t_last_cuda_error = (int)cudaGetLastError();
+            return GBE_ERR_CUDA;
+        }
+        return GBE_OK;
+    }
+
+    int check(const Buf& b) {
+        if (b.bytes == 0) return GBE_OK;
+        const uintptr_t p = reinterpret_cast<uintptr_t>(b.p);
+        for (int i = 0; i < n_; ++i)
+            if (p >= seen_[i].lo && p + b.bytes <= seen_[i].hi) return GBE_OK;
+        cudaPointerAttributes a;
+        if (cudaPointerGetAttributes(&a, b.p) != cudaSuccess) {
+            cudaGetLastError();
+            return GBE_ERR_POINTER;
+        }
+        CUdeviceptr base = 0;
+        size_t size = 0;
+        bool ranged = false;
+        switch (a.type) {
+            case cudaMemoryTypeDevice:
+                if (a.device != dev_) return GBE_ERR_POINTER;
+                [[fallthrough]];
+            case cudaMemoryTypeManaged:
+                if (AddressRangeFn fn = address_range_fn())
+                    ranged = fn(&base, &size, static_cast<CUdeviceptr>(p)) == CUDA_SUCCESS;
+                break;
+            case cudaMemoryTypeHost:
+                // pinned host memory, usable only when mapped at the same
+                // address, and only when the driver can say where its
+                // allocation ends (else a short buffer could not be told apart)
+                if (a.devicePointer != b.p) return GBE_ERR_POINTER;
+                if (!host_range(p, &base, &size)) return GBE_ERR_POINTER;
+                ranged = true;
+                break;
+            default:
+                return GBE_ERR_POINTER;
+        }
+        if (ranged) {
+            if (p < base || p + b.bytes > base + size) return GBE_ERR_POINTER;
+            if (n_ < kSeen) seen_[n_++] = {static_cast<uintptr_t>(base), static_cast<uintptr_t>(base + size)};
+        }
+        return GBE_OK;
+    }
+
+  private:
+    static bool host_range(uintptr_t p, CUdeviceptr* base, size_t* size) {
+        PointerAttributeFn fn = pointer_attribute_fn();
+        if (fn == nullptr) return false;
+        CUdeviceptr start = 0;
+        size_t len = 0;
+        if (fn(&start, CU_POINTER_ATTRIBUTE_RANGE_START_ADDR, static_cast<CUdeviceptr>(p)) != CUDA_SUCCESS ||
+            fn(&len, CU_POINTER_ATTRIBUTE_RANGE_SIZE, static_cast<CUdeviceptr>(p)) != CUDA_SUCCESS)
+            return false;
+        *base = start;
+        *size = len;
+        return len > 0;
+    }
+
+    static constexpr int kSeen = 16;
+    struct Span {
+        uintptr_t lo, hi;
+    };
+    int dev_ = 0;
+    Span seen_[kSeen];
+    int n_ = 0;
+};
 
 bool overlaps(const Buf& a, const Buf& b) {
     if (a.bytes == 0 || b.bytes == 0) return false;
@@ -146,18 +214,14 @@ int finish(cudaError_t e) {
     return GBE_OK;
 }
 
-// Validate the buffers of one call: each one alone, then every output (the
-// first n_out entries) against every other buffer; `alias_ok(o, j)` says
-// whether output o may be exactly buffer j.
+// Validate the buffers of one call: the form of each (pointer, alignment),
+// then every output (the first n_out entries) against every other buffer
+// (`alias_ok(o, j)` says whether output o may be exactly buffer j), then each
+// buffer against its allocation.
 template <int N, typename AliasOk>
 int check_all(const Buf (&bufs)[N], int n_out, AliasOk alias_ok) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
-        t_last_cuda_error = (int)cudaGetLastError();
-        return GBE_ERR_CUDA;
-    }
     for (int i = 0; i < N; ++i) {
-        const int st = check_buf(bufs[i], dev);
+        const int st = check_form(bufs[i]);
         if (st != GBE_OK) return st;
     }
     for (int o = 0; o < n_out; ++o)
@@ -165,7 +229,10 @@ int check_all(const Buf (&bufs)[N], int n_out, AliasOk alias_ok) {
             if (j == o || !overlaps(bufs[o], bufs[j])) continue;
             if (!(alias_ok(o, j) && same(bufs[o], bufs[j]))) return GBE_ERR_ALIAS;
         }
-    return GBE_OK;
+    Checker c;
+    int st = c.begin();
+    for (int i = 0; i < N && st == GBE_OK; ++i) st = c.check(bufs[i]);
+    return st;
 }
 
 cudaStream_t as_stream(gbe_stream s) { return reinterpret_cast<cudaStream_t>(s); }
@@ -290,13 +357,8 @@ static int rope_common(const void* const xs[2], void* const ys[2], const int64_t
     Buf bufs[7] = {out[0].extent(), out[1].extent(), in[0].extent(), in[1].extent(),
                    {pos, bp, 4}, {inv_freq, bf, 4}, {cos_sin, cos_sin ? bc : 0u, 8}};
     for (int k = 0; k < 4; ++k) bufs[k].align = (uint64_t)es;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
-        t_last_cuda_error = (int)cudaGetLastError();
-        return GBE_ERR_CUDA;
-    }
     for (const Buf& b : bufs) {
-        const int st = check_buf(b, dev);
+        const int st = check_form(b);
         if (st != GBE_OK) return st;
     }
     for (int o = 0; o < 2; ++o) {
@@ -306,6 +368,12 @@ static int rope_common(const void* const xs[2], void* const ys[2], const int64_t
         if (rows_overlap(out[o], in[1 - o]) || rows_overlap(out[o], out[1 - o])) return GBE_ERR_ALIAS;
         for (int j = 4; j < 7; ++j)
             if (overlaps(bufs[o], bufs[j])) return GBE_ERR_ALIAS;
+    }
+    Checker chk;
+    if (const int st = chk.begin()) return st;
+    for (const Buf& b : bufs) {
+        const int st = chk.check(b);
+        if (st != GBE_OK) return st;
     }
     const bool vec = aligned16(xs[0]) && aligned16(ys[0]) && aligned16(xs[1]) && aligned16(ys[1]) &&
                      (strides[0] * es) % 16 == 0 && (strides[1] * es) % 16 == 0;
@@ -384,13 +452,8 @@ int gbe_qk_norm_rope(const void* q, void* q_out, int64_t q_stride, int64_t Hq, c
                    {gq, Hq > 0 ? bg : 0u, (uint64_t)es}, {gk, Hk > 0 ? bg : 0u, (uint64_t)es},
                    {pos, bp, 4}, {inv_freq, half > 0 ? bf : 0u, 4}, {cos_sin, cos_sin ? bc : 0u, 8}};
     for (int j = 0; j < 4; ++j) bufs[j].align = (uint64_t)es;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
-        t_last_cuda_error = (int)cudaGetLastError();
-        return GBE_ERR_CUDA;
-    }
     for (const Buf& b : bufs) {
-        const int st = check_buf(b, dev);
+        const int st = check_form(b);
         if (st != GBE_OK) return st;
     }
     for (int o = 0; o < 2; ++o) {
@@ -398,6 +461,12 @@ int gbe_qk_norm_rope(const void* q, void* q_out, int64_t q_stride, int64_t Hq, c
         if (rows_overlap(out[o], in[1 - o]) || rows_overlap(out[o], out[1 - o])) return GBE_ERR_ALIAS;
         for (int j = 4; j < 9; ++j)
             if (overlaps(bufs[o], bufs[j])) return GBE_ERR_ALIAS;
+    }
+    Checker chk;
+    if (const int st = chk.begin()) return st;
+    for (const Buf& b : bufs) {
+        const int st = chk.check(b);
+        if (st != GBE_OK) return st;
     }
     const bool vec = aligned16(q) && aligned16(q_out) && aligned16(k) && aligned16(k_out) &&
                      (Hq == 0 || aligned16(gq)) && (Hk == 0 || aligned16(gk)) && (q_stride * es) % 16 == 0 &&

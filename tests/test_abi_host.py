@@ -148,3 +148,65 @@ def test_rejects_size_overflow(L):
     assert L.gbe_silu_mul(NULL, NULL, NULL, big, 0, S) == 2
     assert L.gbe_rmsnorm(NULL, NULL, NULL, 1 << 31, 1 << 31, 1e-5, 0, S) == 2
     assert L.gbe_rope(NULL, NULL, NULL, 1 << 31, 1 << 20, 1 << 20, 2, NULL, 1.0, 0, 0, S) == 2
+
+
+# Fake, never-dereferenced addresses: the overlap checks are address
+# arithmetic and run before any driver call, so a layout whose outputs
+# overlap is refused with GBE_ERR_ALIAS (8) on any machine; a layout that
+# passes them goes on to the driver checks, which refuse these addresses
+# (GBE_ERR_POINTER on a GPU machine, GBE_ERR_CUDA without a device).  No
+# call below can reach a launch.
+BASE, POS, FREQ = 0x7F0000000000, 0x7F1000000000, 0x7F2000000000
+PASSES_OVERLAP_CHECKS = (10, 11)
+
+
+def _rope_qk(L, q, qo, qs, hq, k, ko, ks, hk, T=16, D=128, dtype=1):
+    return L.gbe_rope_qk(q, qo, qs, hq, k, ko, ks, hk, POS, T, D, D, FREQ, NULL, 0, 1.0, 0, dtype, S)
+
+
+def _qk_norm_rope(L, q, qo, qs, hq, k, ko, ks, hk, T=16, D=128, dtype=1):
+    return L.gbe_qk_norm_rope(q, qo, qs, hq, FREQ + 4096, k, ko, ks, hk, FREQ + 8192, 1e-6, POS, T, D, D, FREQ,
+                              NULL, 0, 1.0, 0, dtype, S)
+
+
+@pytest.mark.parametrize("call", [_rope_qk, _qk_norm_rope])
+def test_strided_slice_overlap_rules(L, call):
+    es, D, Hq, Hk = 2, 128, 32, 8
+    stride = (Hq + 2 * Hk) * D          # one token row of a fused QKV buffer: [q | k | v]
+    q, k = BASE, BASE + Hq * D * es
+    out = BASE + (1 << 30)              # a second QKV buffer for out-of-place results
+    qo, ko = out, out + Hq * D * es
+    # q and k slices of one QKV row, in place: their rows interleave without sharing a byte
+    assert call(L, q, q, stride, Hq, k, k, stride, Hk) in PASSES_OVERLAP_CHECKS
+    # out of place, into the slices of another QKV buffer
+    assert call(L, q, qo, stride, Hq, k, ko, stride, Hk) in PASSES_OVERLAP_CHECKS
+    # k ahead of q in the row (negative distance from q to k)
+    assert call(L, BASE + Hk * D * es, BASE + Hk * D * es, stride, Hq, BASE, BASE, stride, Hk) \
+        in PASSES_OVERLAP_CHECKS
+    # k's output shifted one element back: its first entry is q's last, in every row
+    assert call(L, q, q, stride, Hq, k, k - es, stride, Hk) == 8
+    # q's output shifted one element forward into k
+    assert call(L, q, q + es, stride, Hq, k, k, stride, Hk) == 8
+    assert call(L, q, q, stride, Hq, k, q + stride * es, stride, Hk, T=16) == 8
+    # ... unless there is only one token
+    assert call(L, q, q, stride, Hq, k, q + stride * es, stride, Hk, T=1) in PASSES_OVERLAP_CHECKS
+    # different token strides whose extents overlap: not resolvable row by row, refused
+    assert call(L, q, q, stride, Hq, k, k, stride + 8, Hk) == 8
+    # an output that shares bytes with its own input without being it
+    assert call(L, q, q + stride * es, stride, Hq, k, k, stride, Hk, T=4) == 8
+    # an output overlapping the positions
+    assert call(L, q, POS, stride, Hq, k, k, stride, Hk) == 8
+
+
+def test_contiguous_overlap_rules_before_driver(L):
+    n, es = 1024, 4
+    a, b = BASE, BASE + n * es
+    assert L.gbe_add(a, b, a, n, 0, S) in PASSES_OVERLAP_CHECKS        # y == a
+    assert L.gbe_add(a, b, b, n, 0, S) in PASSES_OVERLAP_CHECKS        # y == b
+    assert L.gbe_add(a, b, a + es, n, 0, S) == 8                       # shifted by one element
+    assert L.gbe_add(a, b, b - es, n, 0, S) == 8
+    assert L.gbe_rmsnorm(a, b, a, 4, 256, 1e-5, 0, S) in PASSES_OVERLAP_CHECKS
+    assert L.gbe_rmsnorm(a, a + 768 * es, b, 4, 256, 1e-5, 0, S) in PASSES_OVERLAP_CHECKS  # w inside x: inputs may overlap
+    assert L.gbe_rmsnorm(a, b - 64 * es, b - 1024 * es, 4, 256, 1e-5, 0, S) == 8  # y == x, but y holds w
+    assert L.gbe_embedding(a, POS, a + (1 << 20), 4, 64, 100, NULL, 0, S) in PASSES_OVERLAP_CHECKS
+    assert L.gbe_embedding(a, POS, a + 64 * es, 4, 64, 100, NULL, 0, S) == 8  # out inside the table

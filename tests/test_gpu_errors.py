@@ -38,16 +38,20 @@ def _allocation_end(ptr: int) -> int:
 
 def test_extent_past_allocation_is_refused():
     L = gbe.lib()
+    out = torch.full((1,), 7, dtype=torch.int32, device="cuda")
     torch.cuda.empty_cache()  # so x starts a fresh segment of its own
     x = torch.ones(1 << 20, device="cuda")
-    out = torch.full((1,), 7, dtype=torch.int32, device="cuda")
-    n_fit = (_allocation_end(x.data_ptr()) - x.data_ptr()) // 4
+    end = _allocation_end(x.data_ptr())
+    n_fit = (end - x.data_ptr()) // 4
     # one row reaching exactly to the end of the allocation is accepted ...
     assert L.gbe_argmax(x.data_ptr(), out.data_ptr(), 1, n_fit, 0, _stream()) == 0
     torch.cuda.synchronize()
     out.fill_(7)
-    # ... one element more is refused and nothing runs
-    assert L.gbe_argmax(x.data_ptr(), out.data_ptr(), 1, n_fit + 1, 0, _stream()) == 10
+    # ... one element more is refused and nothing runs: GBE_ERR_POINTER, or
+    # GBE_ERR_ALIAS (checked first) when the output happens to sit right
+    # after x's allocation, inside the extent asked for
+    past = L.gbe_argmax(x.data_ptr(), out.data_ptr(), 1, n_fit + 1, 0, _stream())
+    assert past == (8 if out.data_ptr() == end else 10)
     torch.cuda.synchronize()
     assert int(out.item()) == 7
 

@@ -1,6 +1,8 @@
 """Pinned host buffers passed straight to the C ABI: the kernels read and
 write host memory in place (mapped at the same address on the device) and
 give the same bits as with device buffers; unpinned host memory is refused."""
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -53,3 +55,31 @@ def test_unpinned_host_memory_is_refused():
     assert st == 10
     with pytest.raises(ValueError):
         gbe.gbe_add(a, y, y)
+
+
+def _pinned_allocation_end(ptr: int) -> int:
+    """End address of the pinned host allocation that holds `ptr` (torch's
+    pinned allocator rounds blocks up, so a tensor may end before it)."""
+    cu = ctypes.CDLL("libcuda.so.1")
+    start, size = ctypes.c_uint64(0), ctypes.c_size_t(0)
+    assert cu.cuPointerGetAttribute(ctypes.byref(start), 11, ctypes.c_uint64(ptr)) == 0  # RANGE_START_ADDR
+    assert cu.cuPointerGetAttribute(ctypes.byref(size), 12, ctypes.c_uint64(ptr)) == 0   # RANGE_SIZE
+    return start.value + size.value
+
+
+def test_pinned_extent_past_allocation_is_refused():
+    """Pinned host memory is held to the end of its allocation like device
+    memory: a row reaching exactly to the end is accepted, one element more
+    is refused on the host and nothing runs (the output keeps its value)."""
+    L = gbe.lib()
+    s = torch.cuda.current_stream().cuda_stream
+    h = torch.ones(1024, dtype=torch.float32).pin_memory()
+    out = torch.full((1,), 7, dtype=torch.int32, device="cuda")
+    n_fit = (_pinned_allocation_end(h.data_ptr()) - h.data_ptr()) // 4
+    assert 1024 <= n_fit < (1 << 31)
+    assert L.gbe_argmax(h.data_ptr(), out.data_ptr(), 1, n_fit, 0, s) == 0
+    torch.cuda.synchronize()
+    out.fill_(7)
+    assert L.gbe_argmax(h.data_ptr(), out.data_ptr(), 1, n_fit + 1, 0, s) == 10
+    torch.cuda.synchronize()
+    assert int(out.item()) == 7
