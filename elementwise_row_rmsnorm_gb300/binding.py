@@ -55,6 +55,7 @@ def lib() -> ctypes.CDLL:
                     "(nvcc, sm_103a) first")
             L = ctypes.CDLL(LIB_PATH)
             vp, i64, f32, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int
+            u64 = ctypes.c_uint64
             sigs = {
                 "gbe_rmsnorm": [vp, vp, vp, i64, i64, f32, i32, vp],
                 "gbe_add_rmsnorm": [vp, vp, vp, vp, vp, i64, i64, f32, i32, vp],
@@ -71,6 +72,8 @@ def lib() -> ctypes.CDLL:
                 "gbe_embedding": [vp, vp, vp, i64, i64, i64, vp, i32, vp],
                 "gbe_argmax": [vp, vp, i64, i64, i32, vp],
                 "gbe_sample": [vp, vp, vp, i64, i64, i32, f32, i64, f32, i32, vp],
+                "gbe_sample_seeded": [vp, vp, i64, i64, i32, f32, i64, f32, u64, u64, i32, vp],
+                "gbe_pcg64_uniforms": [vp, i64, u64, u64, vp],
                 "gbe_version": [],
                 "gbe_last_cuda_error": [],
                 "gbe_status_string": [i32],
@@ -350,6 +353,34 @@ def gbe_sample(x, u, out, method: str, temperature: float = 1.0, top_k: int = 1,
                                           _stream(stream)))
 
 
+def gbe_sample_seeded(x, out, method: str, seed: int, offset: int = 0, temperature: float = 1.0, top_k: int = 1,
+                      p: float = 1.0, stream=None) -> None:
+    """One draw per row of x [..., n]; row r draws with the uniform of draw
+    offset + r of the PCG64 stream seeded with `seed` (0 <= seed, offset < 2^64)."""
+    if method not in SAMPLE_METHODS:
+        raise ValueError(f"sample: method is one of {sorted(SAMPLE_METHODS)}")
+    _dev(x, out)
+    n = x.shape[-1]
+    rows = math.prod(x.shape[:-1])
+    if out.dtype != torch.int32 or out.numel() != rows:
+        raise ValueError("sample: out is int32 with one entry per row")
+    if not (0 <= seed < 1 << 64 and 0 <= offset < 1 << 64):
+        raise ValueError("sample: seed and offset are unsigned 64-bit integers")
+    _check("gbe_sample_seeded", lib().gbe_sample_seeded(_ptr(x), _ptr(out), rows, n, SAMPLE_METHODS[method],
+                                                        temperature, top_k, p, seed, offset, _dt(x),
+                                                        _stream(stream)))
+
+
+def gbe_pcg64_uniforms(u, seed: int, offset: int = 0, stream=None) -> None:
+    """u (float32, any shape) <- the uniforms of draws offset .. offset + u.numel() - 1."""
+    _dev(u)
+    if u.dtype != torch.float32:
+        raise ValueError("pcg64_uniforms: u is float32")
+    if not (0 <= seed < 1 << 64 and 0 <= offset < 1 << 64):
+        raise ValueError("pcg64_uniforms: seed and offset are unsigned 64-bit integers")
+    _check("gbe_pcg64_uniforms", lib().gbe_pcg64_uniforms(_ptr(u), u.numel(), seed, offset, _stream(stream)))
+
+
 # ---- conveniences that allocate the outputs -------------------------------------------
 
 def rmsnorm(x, w, eps: float = 1e-5, out=None, stream=None):
@@ -404,6 +435,19 @@ def argmax(x, stream=None):
     out = torch.empty(x.shape[:-1], dtype=torch.int32, device=x.device)
     gbe_argmax(x, out, stream)
     return out
+
+
+def sample_seeded(x, method: str, seed: int, offset: int = 0, temperature: float = 1.0, top_k: int = 1,
+                  p: float = 1.0, stream=None):
+    out = torch.empty(x.shape[:-1], dtype=torch.int32, device=x.device)
+    gbe_sample_seeded(x, out, method, seed, offset, temperature, top_k, p, stream)
+    return out
+
+
+def pcg64_uniforms(n: int, seed: int, offset: int = 0, device="cuda", stream=None):
+    u = torch.empty(n, dtype=torch.float32, device=device)
+    gbe_pcg64_uniforms(u, seed, offset, stream)
+    return u
 
 
 def sample(x, u, method: str, temperature: float = 1.0, top_k: int = 1, p: float = 1.0, stream=None):

@@ -20,7 +20,7 @@
 
 namespace {
 
-constexpr int kVersion = 10000;  // 1.0.0
+constexpr int kVersion = 10100;  // 1.1.0
 
 thread_local int t_last_cuda_error = 0;
 
@@ -592,8 +592,10 @@ int gbe_argmax(const void* x, int32_t* out, int64_t rows, int64_t n, int dtype, 
     return finish(gbe::launch_argmax(x, out, rows, n, dtype, vec, as_stream(stream)));
 }
 
-int gbe_sample(const void* x, const float* u, int32_t* out, int64_t rows, int64_t n, int method,
-               float temperature, int64_t top_k, float p, int dtype, gbe_stream stream) {
+// Shared checks and launch of gbe_sample (the caller's uniforms d.u) and
+// gbe_sample_seeded (seeded: d.u is NULL and the seeded stream is drawn).
+static int sample_common(const void* x, gbe::Draws d, bool seeded, int32_t* out, int64_t rows, int64_t n,
+                         int method, float temperature, int64_t top_k, float p, int dtype, gbe_stream stream) {
     const int es = elem_size(dtype);
     if (!es) return GBE_ERR_DTYPE;
     if (method < GBE_SAMPLE_GREEDY || method > GBE_SAMPLE_MIN_P) return GBE_ERR_SAMPLING;
@@ -609,13 +611,36 @@ int gbe_sample(const void* x, const float* u, int32_t* out, int64_t rows, int64_
     uint64_t bx, bo, bu;
     if (!mul_ok(rows, n, &nx) || !extent(nx, es, &bx) || !extent(rows, 4, &bo) || !extent(rows, 4, &bu))
         return GBE_ERR_SHAPE;
-    if (greedy) bu = 0;  // u is not read
-    const Buf bufs[3] = {{out, bo, 4}, {x, bx, (uint64_t)es}, {u, bu, 4}};
+    if (greedy || seeded) bu = 0;  // u is not read
+    const Buf bufs[3] = {{out, bo, 4}, {x, bx, (uint64_t)es}, {d.u, bu, 4}};
     const int st = check_all(bufs, 1, [](int, int) { return false; });
     if (st != GBE_OK) return st;
     const bool vec = aligned16(x) && (n * es) % 16 == 0;
-    return finish(gbe::launch_sample(x, out, rows, n, method, temperature, top_k, p, u, dtype, vec,
+    return finish(gbe::launch_sample(x, out, rows, n, method, temperature, top_k, p, d, dtype, vec,
                                      as_stream(stream)));
+}
+
+int gbe_sample(const void* x, const float* u, int32_t* out, int64_t rows, int64_t n, int method,
+               float temperature, int64_t top_k, float p, int dtype, gbe_stream stream) {
+    const gbe::Draws d{u, 0ull, 0ull};
+    return sample_common(x, d, false, out, rows, n, method, temperature, top_k, p, dtype, stream);
+}
+
+int gbe_sample_seeded(const void* x, int32_t* out, int64_t rows, int64_t n, int method, float temperature,
+                      int64_t top_k, float p, uint64_t seed, uint64_t offset, int dtype, gbe_stream stream) {
+    const gbe::Draws d{nullptr, (unsigned long long)seed, (unsigned long long)offset};
+    return sample_common(x, d, true, out, rows, n, method, temperature, top_k, p, dtype, stream);
+}
+
+int gbe_pcg64_uniforms(float* u, int64_t n, uint64_t seed, uint64_t offset, gbe_stream stream) {
+    uint64_t bu;
+    if (n < 0 || !extent(n, 4, &bu)) return GBE_ERR_SHAPE;
+    if (n == 0) return GBE_OK;
+    const Buf bufs[1] = {{u, bu, 4}};
+    const int st = check_all(bufs, 1, [](int, int) { return false; });
+    if (st != GBE_OK) return st;
+    return finish(gbe::launch_pcg64_uniforms(u, n, (unsigned long long)seed, (unsigned long long)offset,
+                                             as_stream(stream)));
 }
 
 }  // extern "C"

@@ -84,7 +84,18 @@ cudaError_t launch_embedding(const void* table, const int32_t* ids, void* out, i
 cudaError_t launch_argmax(const void* x, int32_t* out, int64_t rows, int64_t n, int dtype, bool vec,
                           cudaStream_t st);
 
+// The uniforms of a sampling launch: u[row] when u is given, else draw
+// offset + row of the PCG64 stream seeded with `seed`.
+struct Draws {
+    const float* u;
+    unsigned long long seed, offset;
+};
+
 cudaError_t launch_sample(const void* x, int32_t* out, int64_t rows, int64_t n, int method, float t, int64_t k,
-                          float p, const float* u, int dtype, bool vec, cudaStream_t st);
+                          float p, Draws d, int dtype, bool vec, cudaStream_t st);
+
+// u[i] = the uniform of draw offset + i of the PCG64 stream seeded with `seed`.
+cudaError_t launch_pcg64_uniforms(float* u, int64_t n, unsigned long long seed, unsigned long long offset,
+                                  cudaStream_t st);
 
 }  // namespace gbe

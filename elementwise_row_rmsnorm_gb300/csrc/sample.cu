@@ -51,12 +51,16 @@
 //    entries are gathered, sorted and walked; a bin of more than 4096
 //    entries is split by the next digit, and a group of more than 4096
 //    equal logits is walked in index order by the warps.
+// The uniform of a row is the caller's u[row], or draw offset + row of the
+// seeded PCG64 stream (pcg64.cuh), formed by warp 0 at the row's start.
 // No memory beyond the inputs and the outputs.
+#include <algorithm>
 #include <atomic>
 #include <cooperative_groups.h>
 
 #include "common.cuh"
 #include "launch.h"
+#include "pcg64.cuh"
 
 namespace gbe {
 
@@ -99,7 +103,21 @@ struct Sh {
     u64 ru[4];
     int ri[4];
     unsigned ncand;
+    float useed;  // the row's uniform, when it is drawn from the seeded stream
 };
+
+// The row's uniform drawn from the seeded stream (d.u == NULL): warp 0
+// forms it at the start of the row, before its first loads, and leaves it
+// in sh.useed for row_uniform to read after the first block barrier.
+__device__ __forceinline__ void seed_uniform(const Draws& d, int64_t ri, Sh& sh) {
+    if (d.u == nullptr && threadIdx.x < 32) {
+        const float v = pcg::uniform_warp(d.seed, d.offset, (u64)ri);
+        if (threadIdx.x == 0) sh.useed = v;
+    }
+}
+__device__ __forceinline__ float row_uniform(const Draws& d, int64_t ri, const Sh& sh) {
+    return d.u ? d.u[ri] : sh.useed;
+}
 
 
 // 2^a, the hardware approximation (relative error near 2^-22; results below
@@ -519,7 +537,7 @@ __device__ __forceinline__ float kept_e(const Row<DT, VEC>& row, float v, float 
 // Three rows resident per SM (40 registers a thread): the tiles in flight
 // stay packed, which is what lets the aligned kernels fit without spilling.
 template <int DT, bool VEC, bool MINP, int CL>
-__device__ __forceinline__ void index_order_body(const void* x, int32_t* out, int n, float t, float p, const float* u) {
+__device__ __forceinline__ void index_order_body(const void* x, int32_t* out, int n, float t, float p, Draws d) {
     constexpr int V = Row<DT, VEC>::V;
     constexpr int kTile = Row<DT, VEC>::kTile;
     pdl_begin();
@@ -530,6 +548,7 @@ __device__ __forceinline__ void index_order_body(const void* x, int32_t* out, in
     const int rank = CL > 1 ? (int)(blockIdx.x % CL) : 0;
     Row<DT, VEC> row;
     setup(row, x, n, t, ri, rank, CL);
+    seed_uniform(d, ri, sh);
     int nv;
     row.mx = block_first_max<false>(row, sh, &nv, nullptr);
     if (CL > 1) {
@@ -593,7 +612,7 @@ __device__ __forceinline__ void index_order_body(const void* x, int32_t* out, in
         ex += before;
         total = all;
     }
-    const u64 target = scaled(u[ri], total);
+    const u64 target = scaled(row_uniform(d, ri, sh), total);
     if (!(wmass > 0 && ex <= target && target < ex + wmass)) return;
     // this warp holds the target: walk its tiles
     const u64 want = target - ex;
@@ -627,29 +646,29 @@ __device__ __forceinline__ void index_order_body(const void* x, int32_t* out, in
 
 template <int DT, bool VEC, bool MINP>
 __global__ void __launch_bounds__(kT, 3) sample_index_order(const void* x, int32_t* out, int n, float t, float p,
-                                                            const float* u) {
-    index_order_body<DT, VEC, MINP, 1>(x, out, n, t, p, u);
+                                                            Draws d) {
+    index_order_body<DT, VEC, MINP, 1>(x, out, n, t, p, d);
 }
 template <int DT, bool VEC, bool MINP>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kT, 3)
-sample_index_order2(const void* x, int32_t* out, int n, float t, float p, const float* u) {
-    index_order_body<DT, VEC, MINP, 2>(x, out, n, t, p, u);
+sample_index_order2(const void* x, int32_t* out, int n, float t, float p, Draws d) {
+    index_order_body<DT, VEC, MINP, 2>(x, out, n, t, p, d);
 }
 template <int DT, bool VEC, bool MINP>
 __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kT, 3)
-sample_index_order4(const void* x, int32_t* out, int n, float t, float p, const float* u) {
-    index_order_body<DT, VEC, MINP, 4>(x, out, n, t, p, u);
+sample_index_order4(const void* x, int32_t* out, int n, float t, float p, Draws d) {
+    index_order_body<DT, VEC, MINP, 4>(x, out, n, t, p, d);
 }
 template <int DT, bool VEC, bool MINP>
 __global__ void __cluster_dims__(8, 1, 1) __launch_bounds__(kT, 3)
-sample_index_order8(const void* x, int32_t* out, int n, float t, float p, const float* u) {
-    index_order_body<DT, VEC, MINP, 8>(x, out, n, t, p, u);
+sample_index_order8(const void* x, int32_t* out, int n, float t, float p, Draws d) {
+    index_order_body<DT, VEC, MINP, 8>(x, out, n, t, p, d);
 }
 
 // CTAs per row for the index-order kernels: doubled while the grid still
 // fits in one wave (three CTAs an SM) and each warp keeps two tiles.
 template <int DT, bool VEC, bool MINP>
-cudaError_t launch_index_order(const void* x, int32_t* out, int64_t rows, int n, float t, float p, const float* u,
+cudaError_t launch_index_order(const void* x, int32_t* out, int64_t rows, int n, float t, float p, Draws d,
                                cudaStream_t st) {
     constexpr int kTile = Row<DT, VEC>::kTile;
     const int64_t target = 3LL * sm_count();
@@ -657,10 +676,10 @@ cudaError_t launch_index_order(const void* x, int32_t* out, int64_t rows, int n,
     while (cl < 8 && rows * cl * 2 <= target && (int64_t)n >= (int64_t)kW * 2 * (2 * cl) * kTile) cl *= 2;
     const dim3 grid((unsigned)(rows * cl)), block(kT);
     switch (cl) {
-        case 1: return launch(sample_index_order<DT, VEC, MINP>, grid, block, 0, st, x, out, n, t, p, u);
-        case 2: return launch(sample_index_order2<DT, VEC, MINP>, grid, block, 0, st, x, out, n, t, p, u);
-        case 4: return launch(sample_index_order4<DT, VEC, MINP>, grid, block, 0, st, x, out, n, t, p, u);
-        default: return launch(sample_index_order8<DT, VEC, MINP>, grid, block, 0, st, x, out, n, t, p, u);
+        case 1: return launch(sample_index_order<DT, VEC, MINP>, grid, block, 0, st, x, out, n, t, p, d);
+        case 2: return launch(sample_index_order2<DT, VEC, MINP>, grid, block, 0, st, x, out, n, t, p, d);
+        case 4: return launch(sample_index_order4<DT, VEC, MINP>, grid, block, 0, st, x, out, n, t, p, d);
+        default: return launch(sample_index_order8<DT, VEC, MINP>, grid, block, 0, st, x, out, n, t, p, d);
     }
 }
 
@@ -1185,13 +1204,14 @@ __device__ u64 mass_and_gather(const Row<DT, VEC>& row, ShBig& sb, float T) {
 // Row ri, the whole of it by this CTA (all kT threads): top-k and top-p.
 template <int DT, bool VEC>
 __device__ void descending_row(const void* x, int32_t* out, int64_t ri, int n, int method, float t, int k, float p,
-                               const float* u, ShBig& sb) {
+                               Draws d, ShBig& sb) {
     Row<DT, VEC> row;
     setup(row, x, n, t, ri, 0, 1);
+    seed_uniform(d, ri, sb.s);
     int nv;
     row.mx = block_first_max<false>(row, sb.s, &nv, sb.lmax);
     if (!accept_max(row, out, ri, threadIdx.x == 0)) return;
-    const float ur = u[ri];
+    const float ur = row_uniform(d, ri, sb.s);
     // The head of the row: the first-digit bins from that of M - 24 / c down
     // -- every entry of weight above 2^-24 of the largest (and some below).
     // The rest of a row of n entries weighs at most n 2^-24 of the largest, so
@@ -1346,18 +1366,18 @@ __device__ void descending_row(const void* x, int32_t* out, int64_t ri, int n, i
 
 template <int DT, bool VEC>
 __global__ void __launch_bounds__(kT, 2)
-sample_descending(const void* x, int32_t* out, int n, int method, float t, int k, float p, const float* u) {
+sample_descending(const void* x, int32_t* out, int n, int method, float t, int k, float p, Draws d) {
     pdl_begin();
     extern __shared__ __align__(16) unsigned char smem_raw[];
     ShBig& sb = *reinterpret_cast<ShBig*>(smem_raw);
-    descending_row<DT, VEC>(x, out, blockIdx.x, n, method, t, k, p, u, sb);
+    descending_row<DT, VEC>(x, out, blockIdx.x, n, method, t, k, p, d, sb);
 }
 
 template <int DT, bool VEC>
 cudaError_t launch_vec(const void* x, int32_t* out, int64_t rows, int n, int method, float t, int k, float p,
-                       const float* u, cudaStream_t st) {
-    if (method == kTemperature) return launch_index_order<DT, VEC, false>(x, out, rows, n, t, p, u, st);
-    if (method == kMinP) return launch_index_order<DT, VEC, true>(x, out, rows, n, t, p, u, st);
+                       Draws d, cudaStream_t st) {
+    if (method == kTemperature) return launch_index_order<DT, VEC, false>(x, out, rows, n, t, p, d, st);
+    if (method == kMinP) return launch_index_order<DT, VEC, true>(x, out, rows, n, t, p, d, st);
     const size_t smem = sizeof(ShBig);
     // the shared-memory opt-in, once per device for this kernel
     static std::atomic<uint64_t> opted{0};
@@ -1373,24 +1393,46 @@ cudaError_t launch_vec(const void* x, int32_t* out, int64_t rows, int n, int met
         }
         opted.fetch_or(bit, std::memory_order_release);
     }
-    return launch(sample_descending<DT, VEC>, dim3((unsigned)rows), dim3(kT), smem, st, x, out, n, method, t, k, p, u);
+    return launch(sample_descending<DT, VEC>, dim3((unsigned)rows), dim3(kT), smem, st, x, out, n, method, t, k, p, d);
 }
 
 template <int DT>
 cudaError_t launch_dt(const void* x, int32_t* out, int64_t rows, int n, int method, float t, int k, float p,
-                      const float* u, bool vec, cudaStream_t st) {
-    if (vec) return launch_vec<DT, true>(x, out, rows, n, method, t, k, p, u, st);
-    return launch_vec<DT, false>(x, out, rows, n, method, t, k, p, u, st);
+                      Draws d, bool vec, cudaStream_t st) {
+    if (vec) return launch_vec<DT, true>(x, out, rows, n, method, t, k, p, d, st);
+    return launch_vec<DT, false>(x, out, rows, n, method, t, k, p, d, st);
+}
+
+// u[i] = the uniform of draw offset + i of the seeded stream: each warp jumps
+// to its first draw together, then lane l steps l draws further.
+__global__ void __launch_bounds__(256) pcg64_uniforms(float* u, int64_t n, u64 seed, u64 offset) {
+    pdl_begin();
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * 8;
+    for (int64_t w = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); w * 32 < n; w += warps) {
+        const int64_t i0 = w * 32;
+        // draw i0 is i0 + 1 steps after the seeded state
+        const pcg::Affine f = pcg::jump_warp(pcg::add128(pcg::U128{offset, 0}, pcg::U128{(u64)i0 + 1, 0}));
+        const pcg::U128 s = pcg::apply(pcg::jump_small((uint32_t)lane), pcg::apply(f, pcg::seeded(seed)));
+        if (i0 + lane < n) u[i0 + lane] = pcg::uniform_of(pcg::output(s));
+    }
 }
 
 }  // namespace
 
+cudaError_t launch_pcg64_uniforms(float* u, int64_t n, unsigned long long seed, unsigned long long offset,
+                                  cudaStream_t st) {
+    if (n == 0) return cudaSuccess;
+    const int64_t blocks = std::min<int64_t>((n + 255) / 256, (int64_t)sm_count() * 8);
+    return launch(pcg64_uniforms, dim3((unsigned)blocks), dim3(256), 0, st, u, n, (u64)seed, (u64)offset);
+}
+
 cudaError_t launch_sample(const void* x, int32_t* out, int64_t rows, int64_t n, int method, float t, int64_t k,
-                          float p, const float* u, int dtype, bool vec, cudaStream_t st) {
+                          float p, Draws d, int dtype, bool vec, cudaStream_t st) {
     if (method == kGreedy) return launch_argmax(x, out, rows, n, dtype, vec, st);
     const int ki = (int)(k > n ? n : k), ni = (int)n;
-    if (dtype == kF32) return launch_dt<kF32>(x, out, rows, ni, method, t, ki, p, u, vec, st);
-    return launch_dt<kBF16>(x, out, rows, ni, method, t, ki, p, u, vec, st);
+    if (dtype == kF32) return launch_dt<kF32>(x, out, rows, ni, method, t, ki, p, d, vec, st);
+    return launch_dt<kBF16>(x, out, rows, ni, method, t, ki, p, d, vec, st);
 }
 
 }  // namespace gbe

@@ -306,6 +306,40 @@ typedef enum gbe_sample_method {
 int gbe_sample(const void *x, const float *u, int32_t *out, int64_t rows, int64_t n, int method,
                float temperature, int64_t top_k, float p, int dtype, gbe_stream stream);
 
+/*
+ * gbe_sample_seeded -- gbe_sample with the uniforms drawn from a seeded
+ * generator on the device.
+ *   "Operations", section 8 (Sample): sample_categorical draws with a seeded
+ *   generator (Xorshift or PCG), and the same seed with the same
+ *   distribution gives the same draw.  The generator is PCG64 (as
+ *   gbe_pcg64_uniforms defines it); row r draws with the uniform of draw
+ *   number offset + r of the stream seeded with `seed`, then exactly as
+ *   gbe_sample draws at that uniform.  A caller that samples batch after
+ *   batch from one stream advances offset by the rows of each call.  The
+ *   [sampling] configuration's "seed = 0 means non-deterministic" is the
+ *   caller's to honour (by picking a fresh seed); here 0 is a seed like any
+ *   other.
+ * x, out, rows, n, method, temperature, top_k, p, dtype, stream, and the
+ * errors : as for gbe_sample (no u).
+ */
+int gbe_sample_seeded(const void *x, int32_t *out, int64_t rows, int64_t n, int method, float temperature,
+                      int64_t top_k, float p, uint64_t seed, uint64_t offset, int dtype, gbe_stream stream);
+
+/*
+ * gbe_pcg64_uniforms -- the uniforms of gbe_sample_seeded, written out.
+ *   "Operations", section 8 (Sample, the seeded RNG of sample_categorical):
+ *   PCG64 -- the 128-bit linear congruential generator
+ *   s' = s * M + INC (mod 2^128), M = 0x2360ED051FC65DA44385DF649FCCF645,
+ *   INC = 0x5851F42D4C957F2D14057B7EF767814F, with the XSL-RR output taken
+ *   after each step (the xor of the state's 64-bit halves rotated right by
+ *   its top six bits; O'Neill 2014).  Seeding: state 0, one step, plus
+ *   seed, one step.  Draw j (j = 0, 1, ...) is the output after j + 1
+ *   further steps; its uniform is its top 24 bits times 2^-24, in [0, 1).
+ * u : device f32[n], written with the uniforms of draws offset .. offset +
+ *     n - 1 (the stream continues past 2^64).  n >= 0.
+ */
+int gbe_pcg64_uniforms(float *u, int64_t n, uint64_t seed, uint64_t offset, gbe_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -31,7 +31,7 @@ def test_header_declares_the_ops():
     names = declared_functions()
     for op in ("gbe_rmsnorm", "gbe_add_rmsnorm", "gbe_rope", "gbe_rope_qk", "gbe_rope_cos_sin", "gbe_rope_multi", "gbe_qk_norm_rope", "gbe_silu_mul",
                "gbe_add", "gbe_embedding", "gbe_argmax", "gbe_sample", "gbe_layernorm", "gbe_status_string", "gbe_version",
-               "gbe_last_cuda_error"):
+               "gbe_last_cuda_error", "gbe_sample_seeded", "gbe_pcg64_uniforms"):
         assert op in names
 
 
@@ -47,7 +47,7 @@ def test_library_exports_every_declared_function(L):
 
 def test_status_strings_and_version(L):
     import elementwise_row_rmsnorm_gb300 as gbe
-    assert L.gbe_version() == 10000
+    assert L.gbe_version() == 10100
     for st in range(13):
         assert gbe.status_string(st) and gbe.status_string(st) != "unknown status"
     assert gbe.status_string(99) == "unknown status"

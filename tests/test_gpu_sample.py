@@ -446,3 +446,65 @@ def test_many_signed_zeros_take_the_exact_search(dtype):
         assert np.array_equal(got, want), (method, got, want)
         assert np.array_equal(got, _oracle(widen(xx), u, method, kw)), method
 
+
+# ---- the seeded draw ("Operations" section 8: sample_categorical with a
+# seeded PCG generator; same seed, same distribution, same draw) -----------------
+
+@pytest.mark.parametrize("seed,offset,n", [(0, 0, 1), (42, 0, 100003), (7, (1 << 40) + 3, 4097),
+                                           ((1 << 64) - 1, (1 << 64) - 50, 1000), (3, 12345, 31)])
+def test_pcg64_uniforms_match_the_oracle(seed, offset, n):
+    """The device stream equals the oracle's bit for bit, including draws
+    past 2^64 and ragged warps."""
+    got = gbe.pcg64_uniforms(n, seed, offset).cpu().numpy()
+    want = oracle.get().pcg64_uniforms(seed, offset, n)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("method,kw", METHODS)
+@pytest.mark.parametrize("rows,n", [(3, 1000), (16, 32000), (200, 4097)])
+def test_seeded_draws_are_the_draws_at_the_streams_uniforms(dtype, method, kw, rows, n):
+    """Row r of a seeded call draws exactly what gbe_sample draws at the
+    uniform of stream draw offset + r (the kernel forms that uniform itself);
+    against the oracle's seeded sampler, the usual boundary rule."""
+    x = _logits(rows, n, dtype, nan_frac=0.01, tag="seeded")
+    xd = to_dev(x)
+    for seed, offset in ((11, 0), (11, 1 << 33), ((1 << 64) - 2, 17)):
+        got = gbe.sample_seeded(xd, method, seed, offset, **kw).cpu().numpy()
+        u = oracle.get().pcg64_uniforms(seed, offset, rows)
+        ref = gbe.sample(xd, torch.from_numpy(u).cuda(), method, **kw).cpu().numpy()
+        assert np.array_equal(got, ref), (method, seed, offset)
+        _check(x, u, method, kw, f"seeded {method} {dtype} [{rows},{n}]")
+
+
+@pytest.mark.parametrize("method,kw", METHODS)
+def test_seeded_reproducible_and_batch_invariant(method, kw):
+    """The same seed and offset give the same draws; rows [r0, r1) drawn
+    alone at offset + r0 equal those rows of the whole batch; another seed
+    gives other draws."""
+    rows, n = 64, 32000
+    x = _logits(rows, n, "bf16", tag="seeded.inv")
+    xd = to_dev(x)
+    a = gbe.sample_seeded(xd, method, 5, 1000, **kw).cpu().numpy()
+    assert np.array_equal(a, gbe.sample_seeded(xd, method, 5, 1000, **kw).cpu().numpy())
+    for r0, r1 in ((0, 1), (7, 30), (63, 64)):
+        part = gbe.sample_seeded(xd[r0:r1], method, 5, 1000 + r0, **kw).cpu().numpy()
+        assert np.array_equal(part, a[r0:r1]), (r0, r1)
+    b = gbe.sample_seeded(xd, method, 6, 1000, **kw).cpu().numpy()
+    assert (a != b).sum() > rows // 4, method
+
+
+def test_seeded_greedy_and_refusals():
+    x = to_dev(_logits(4, 1000, "f32", tag="seeded.g"))
+    assert torch.equal(gbe.sample_seeded(x, "greedy", 1, 0), gbe.argmax(x))
+    with pytest.raises(gbe.GbeError) as e:
+        gbe.sample_seeded(x, "top_k", 1, 0, top_k=0)
+    assert e.value.status == 12
+    L = gbe.lib()
+    s = torch.cuda.current_stream().cuda_stream
+    u = torch.full((8,), 7.0, device="cuda")
+    assert L.gbe_pcg64_uniforms(u.data_ptr(), -1, 1, 0, s) == 2
+    assert L.gbe_pcg64_uniforms(None, 8, 1, 0, s) == 1
+    assert L.gbe_pcg64_uniforms(u.data_ptr(), 0, 1, 0, s) == 0
+    torch.cuda.synchronize()
+    assert torch.all(u == 7.0)
