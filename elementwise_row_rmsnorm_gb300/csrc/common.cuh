@@ -107,21 +107,24 @@ inline cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
 // cos and sin of a RoPE angle theta (the f32 product position * frequency).
 // sincosf on an argument beyond about 10^5 takes a long exact reduction
 // (positions near 2^20 give angles near 10^6 rad), which costs several times
-// the rest of a RoPE launch.  So the angle is first reduced by quarter turns
-// with Cody and Waite's method ("Software Manual for the Elementary
-// Functions", 1980): k = rint(theta * 2/pi), and r = theta - k pi/2 with
-// pi/2 split into three f32 parts, P1 + P2 + P3, each the f32 nearest to
-// what the parts before it leave of pi/2 (the rest, 1.1e-23, is negligible).
-// For |theta| < 2^22 the first step, fma(-k, P1, theta), is exact: theta
-// and k * P1 are both multiples of 2^-23 and their difference is below 2 in
+// the rest of a RoPE launch.  So the angle is reduced by quarter turns with
+// Cody and Waite's method ("Software Manual for the Elementary Functions",
+// 1980): k = rint(theta * 2/pi), and r = theta - k pi/2 with pi/2 split
+// into three f32 parts, P1 + P2 + P3, each the f32 nearest to what the
+// parts before it leave of pi/2 (the rest, 1.1e-23, is negligible).  For
+// |theta| < 2^22 the first step, fma(-k, P1, theta), is exact: theta and
+// k * P1 are both multiples of 2^-23 and their difference is below 2 in
 // magnitude; the other two steps round once each, so r carries an error of
 // about one f32 ulp of r (about 1e-7 rad).  k may be off by one (the f32
-// product theta * 2/pi rounds), which only leaves |r| a little above pi/4.
-// sincosf then takes r on its short path, and the quadrant k mod 4 maps
-// (cos r, sin r) to (cos theta, sin theta).  Angles of 2^22 and beyond go to
-// sincosf whole.  theta = 0 gives exactly (1, 0), so position 0 is the
-// identity.  Every RoPE kernel and the cos/sin table use this one function,
-// so the table-driven and the formed results agree bit for bit.
+// product theta * 2/pi rounds), which leaves |r| below 0.86 rather than
+// pi/4.  On that interval sin and cos are their Taylor series to the
+// r^13 and r^14 terms (the first terms left out stay below 7e-14 and
+// 6e-15), evaluated by Horner's rule in r^2 with coefficients 1/n!
+// rounded to f32 -- a few f32 ulps in all.  The quadrant k mod 4 maps
+// (cos r, sin r) to (cos theta, sin theta).  Angles of 2^22 and beyond go
+// to sincosf whole.  theta = 0 gives exactly (1, 0), so position 0 is the
+// identity.  Every RoPE kernel and the cos/sin table use this one
+// function, so the table-driven and the formed results agree bit for bit.
 __device__ __forceinline__ void rope_sincos(float theta, float* s, float* c) {
     constexpr float kTwoOverPi = 0x1.45f306p-1f;
     constexpr float kP1 = 0x1.921fb6p+0f;
@@ -132,8 +135,24 @@ __device__ __forceinline__ void rope_sincos(float theta, float* s, float* c) {
         float r = __fmaf_rn(-k, kP1, theta);
         r = __fmaf_rn(-k, kP2, r);
         r = __fmaf_rn(-k, kP3, r);
-        float sr, cr;
-        sincosf(r, &sr, &cr);
+        const float r2 = __fmul_rn(r, r);
+        // sin r = r + r^3 (-1/3! + r^2 (1/5! - ... + r^2 / 13!))
+        float ps = 1.0f / 6227020800.0f;
+        ps = __fmaf_rn(ps, r2, -1.0f / 39916800.0f);
+        ps = __fmaf_rn(ps, r2, 1.0f / 362880.0f);
+        ps = __fmaf_rn(ps, r2, -1.0f / 5040.0f);
+        ps = __fmaf_rn(ps, r2, 1.0f / 120.0f);
+        ps = __fmaf_rn(ps, r2, -1.0f / 6.0f);
+        const float sr = __fmaf_rn(__fmul_rn(ps, r2), r, r);
+        // cos r = 1 + r^2 (-1/2! + r^2 (1/4! - ... + r^2 / 14!))
+        float pc = -1.0f / 87178291200.0f;
+        pc = __fmaf_rn(pc, r2, 1.0f / 479001600.0f);
+        pc = __fmaf_rn(pc, r2, -1.0f / 3628800.0f);
+        pc = __fmaf_rn(pc, r2, 1.0f / 40320.0f);
+        pc = __fmaf_rn(pc, r2, -1.0f / 720.0f);
+        pc = __fmaf_rn(pc, r2, 1.0f / 24.0f);
+        pc = __fmaf_rn(pc, r2, -0.5f);
+        const float cr = __fmaf_rn(pc, r2, 1.0f);
         switch ((int)k & 3) {
             case 0: *s = sr; *c = cr; break;
             case 1: *s = cr; *c = -sr; break;

@@ -39,6 +39,26 @@ def test_silu_workload_full(workload):
     _silu_check(a["gate"], a["up"], "bf16", f"silu {workload}")
 
 
+def test_silu_dense_sweep_of_the_f32_range():
+    """Every 64th f32 bit pattern of the gate over [-104, 90] (about 35
+    million values, up = 1): the hardware exponential and reciprocal stay
+    within the f32 bar of the oracle's libm quotient everywhere, including
+    the exponent overflow edge near g = -88.7 where the exact value is
+    tiny (the bar's 1e-30 floor) and beyond it, where both give -0."""
+    neg = np.arange(0, np.float32(104.0).view(np.uint32), 64, dtype=np.uint32) | np.uint32(0x80000000)
+    pos = np.arange(0, np.float32(90.0).view(np.uint32), 64, dtype=np.uint32)
+    g = np.concatenate([neg, pos]).view(np.float32)
+    u = np.ones_like(g)
+    got = to_f32(gbe.silu_mul(to_dev(g), to_dev(u)))
+    want = oracle.get().silu_mul(g, u)
+    assert not np.isnan(got).any()
+    assert_rel(got, want, "f32", "silu sweep")
+    w = np.asarray(want, np.float64)
+    big = np.abs(w) > 1e-30
+    worst = np.max(np.abs(np.asarray(got, np.float64)[big] - w[big]) / np.abs(w[big]))
+    print(f"silu f32 sweep: {g.size} gates, largest relative error {worst:.3g}")
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("n", [1, 3, 7, 8, 9, 1000, 1023, 4096 * 4 + 5, 1 << 20])
 def test_silu_and_add_ragged(dtype, n):

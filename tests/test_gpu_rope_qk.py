@@ -95,6 +95,19 @@ def test_cos_sin_table_against_oracle(r):
     assert np.all(tab[0, :, 0] == 1.0) and np.all(tab[0, :, 1] == 0.0)
 
 
+def test_cos_sin_of_large_angles_against_oracle():
+    """Angles up to 2^23 rad: frequencies 1 and 8 at every position below
+    2^20 + 3 (the quarter-turn reduction up to 2^22, sincosf whole beyond),
+    plus frequencies whose products land on and near multiples of pi/2."""
+    om = np.array([1.0, 8.0, 0.7853982, 1.5707964], np.float32)
+    r, L = 8, (1 << 20) + 3
+    tab = gbe.rope_cos_sin(to_dev(om), r, L).cpu().numpy()
+    want = oracle.get().rope_cos_sin(om, r, L)
+    err = np.abs(tab.astype(np.float64) - want)
+    assert np.all(err <= 4e-7), (err.max(), np.unravel_index(err.argmax(), err.shape))
+    assert np.all(tab[0, :, 0] == 1.0) and np.all(tab[0, :, 1] == 0.0)
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("layout", [0, 1])
 def test_cached_equals_formed(dtype, layout):
