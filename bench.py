@@ -1,19 +1,23 @@
 """Throughput of the elementwise / row-op library on one GB300.
 
-One step is one pass of every op of the library over one batch of synthetic
-inputs at Llama-3-8B prefill shapes (T = 8192 tokens, bf16 storage, f32
-math):  embedding gather (table [128256, 4096]), fused residual add + RMSNorm
-[8192, 4096], RoPE half layout on q [8192, 32, 128] and k [8192, 8, 128],
-the same in the interleaved layout (separate copies, so no call reads what
-another left in L2), SiLU-mul [8192, 14336], residual add [8192, 4096], RMSNorm
-[8192, 4096] and greedy argmax over logits [8192, 128256].  Every op reads
-its inputs from HBM once and writes its outputs once; a step moves ~3.9 GB,
-so the inputs are far larger than the 129 MB L2.
+One step is one pass of the ops that the Llama-3-8B prefill workload names
+(T = 8192 tokens, bf16 storage, f32 math), in a layer's order: embedding
+gather (table [128256, 4096]), fused residual add + RMSNorm [8192, 4096],
+RoPE half layout on q [8192, 32, 128] and k [8192, 8, 128] in one launch,
+SiLU-mul [8192, 14336].  Every op reads its inputs from HBM once and writes
+its outputs once; a step moves ~1.28 GB through distinct buffers, far more
+than the 129 MB L2.
 
-The metric is achieved HBM GB/s: the algorithmic bytes of the step (what the
-ops must read plus what they must write) over the measured time.  Printed as
-one JSON line (rank 0).  `--impl reference` times the CPU oracle instead, on
-a bounded sample of the same workload.
+The metric is achieved HBM GB/s: the algorithmic bytes (what the ops must
+read plus what they must write) over the measured time, with rows/s beside
+it.  The line also carries `per_config`: every op of every large workload
+-- the prefill ops beyond the step (interleaved RoPE, residual add, RMSNorm,
+argmax over [8192, 128256] logits), the f32 in-place RoPE variants, the
+wide f32 argmax and RMSNorm -- and the decode ops, each timed alone, back to
+back over rotating copies of its buffers (more than four times the L2
+together), from a CUDA graph and from the stream.  Printed as one JSON line
+(rank 0).  `--impl reference` times the CPU oracle instead, on a bounded
+sample of the same workload.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
        (N > 1: one process per GPU under torch.distributed.run; each rank runs
@@ -40,17 +44,23 @@ WORKLOAD = "llama3-8b-prefill-T8192-bf16"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
-# op name -> the workload cases it runs on, in step order
+# op name -> the workload cases it runs on, in step order: the ops the
+# prefill workload names
 STEP = [
     ("embedding", ("embedding",)),
     ("add_rmsnorm", ("add_rmsnorm",)),
     ("rope_qk_half", ("rope_q", "rope_k")),
-    ("rope_qk_interleaved", ("rope_q_interleaved", "rope_k_interleaved")),
     ("silu_mul", ("silu_mul",)),
+]
+# the other Llama-3-8B prefill ops of the library, at the same shapes (timed
+# alone for per_config)
+PREFILL_MORE = [
+    ("rope_qk_interleaved", ("rope_q_interleaved", "rope_k_interleaved")),
     ("add", ("add",)),
     ("rmsnorm", ("rmsnorm",)),
     ("argmax", ("argmax",)),
 ]
+ALL_PREFILL = STEP + PREFILL_MORE
 KERNEL_OF = {  # op -> the kernel it launches (names as ncu lists them)
     "embedding": "embedding_rows", "add_rmsnorm": "rmsnorm_rows", "rope_qk_half": "rope_vec",
     "rope_qk_interleaved": "rope_vec", "silu_mul": "pointwise_vec", "add": "pointwise_vec",
@@ -262,13 +272,14 @@ def build_workload_inputs(workload: str):
     raise KeyError(workload)
 
 
-def build_inputs(tokens: int = 8192):
-    """The step's inputs; `tokens` < 8192 takes the first rows of every op (a
-    smaller case of the same kernels, for profiling)."""
+def build_inputs(tokens: int = 8192, ops=None):
+    """Inputs of the prefill ops (the step's by default); `tokens` < 8192
+    takes the first rows of every op (a smaller case of the same kernels,
+    for profiling)."""
     from synth import workloads as W
     cases = W.cases(W.PREFILL)
     rows = None if tokens >= 8192 else (0, tokens)
-    return {op: combine(op, [cases[c](rows=rows) for c in names]) for op, names in STEP}
+    return {op: combine(op, [cases[c](rows=rows) for c in names]) for op, names in (ops or STEP)}
 
 
 def max_over_ranks(value: float, world: int, device) -> float:
@@ -368,6 +379,8 @@ def run_ours(args):
 
     # e2e: the same step from pinned host buffers, copies inside the timed region
     e2e = run_e2e(args, gbe, torch, dev, data, bufs, out, call, nbytes, step_bytes) if not args.no_e2e else None
+    # every op of every large workload, each alone (rank 0 of a single-GPU run)
+    configs = per_config(torch, gbe, dev) if (world == 1 and not args.no_configs) else None
 
     peak, peak_kind = peaks()
     for op in per_op:
@@ -389,15 +402,19 @@ def run_ours(args):
             "config": {"workload": WORKLOAD if args.tokens >= 8192 else f"{WORKLOAD} (first {args.tokens} tokens)",
                        "storage": "bf16", "tokens": min(args.tokens, 8192), "hidden": 4096,
                        "ffn": 14336, "heads_q": 32, "heads_kv": 8, "head_dim": 128, "vocab": 128256,
-                       "bytes_per_step": step_bytes,
-                       "l2": "inputs larger than L2 (each step moves ~3.9 GB through distinct buffers)",
+                       "step_ops": [op for op, _ in STEP], "bytes_per_step": step_bytes,
+                       "l2": "inputs larger than L2 (each step moves ~1.28 GB through distinct buffers)",
                        "parallelism": f"replicas{world}"},
             "roofline": {"bound": "hbm", "kernel": KERNEL_OF[dom], "op": dom,
                          "achieved": per_op[dom]["gbs"], "peak": peak, "unit": "GB/s",
                          "frac": round(per_op[dom]["gbs"] / peak, 4), "peak_source": peak_kind,
                          "traffic": traffic},
             "per_op": per_op,
-            "per_op_timing": f"{op_steps} further steps with a CUDA event pair around every launch",
+            "per_op_timing": f"{op_steps} further steps with a CUDA event pair around every launch (each op "
+                             "also pays the write-back of the previous op's dirty L2 lines)",
+            "per_config": configs,
+            "per_config_timing": "each op alone, back to back over rotating copies of its buffers (> 4x L2); "
+                                 "us/gbs from CUDA graph replays, *_stream from launches on the stream",
             "e2e": e2e,
             "gpu_launches": len(STEP) * args.steps,
             "launch": "programmatic dependent launch (each kernel overlaps the previous one's tail)",
@@ -426,29 +443,14 @@ def batch_sweep(data):
     return out
 
 
-def run_isolated(args):
-    """Each op alone, launched back to back over rotating copies of its inputs
-    and outputs (together more than four times the L2), timed with one CUDA
-    event pair around the loop: the op's sustained rate when it streams."""
-    import torch
-
-    import elementwise_row_rmsnorm_gb300 as gbe
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
-    torch.cuda.set_device(dev)
-    gbe.lib()
-    workload = args.workload or WORKLOAD
-    if workload != WORKLOAD:
-        data = build_workload_inputs(workload)
-    else:
-        data = build_inputs(args.tokens)
-        if args.extra or (args.keep and args.keep & set(EXTRA)):
-            extra = build_extra_inputs(args.tokens, ops=args.keep or None)
-            data.update({op: v for op, v in extra.items() if not args.keep or op in args.keep})
-    if args.keep:
-        data = {op: v for op, v in data.items() if op in args.keep}
-    if args.sweep:
-        data = batch_sweep(data)
+def time_isolated(torch, gbe, dev, data: dict, graph: bool) -> dict:
+    """Each op of `data` alone, launched back to back over rotating copies of
+    its inputs and outputs (together more than four times the L2, so every
+    launch reads from HBM), timed with one CUDA event pair around the loop:
+    the op's sustained rate.  With `graph` the launches are captured once in
+    a CUDA graph and timed over its replays (no per-call host cost)."""
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    peak, _kind = peaks()
     res = {}
     for key in list(data):
         op = key.split("@")[0]  # "op@b": the op on the first b rows
@@ -463,50 +465,103 @@ def run_isolated(args):
         for _ in range(sets):
             b = {k: (v if k in shared else v.clone()) for k, v in base.items()}
             rings.append((b, make_outputs(torch, dev, op, b)))
-        p = params
 
-        def go(b, o):
-            run_op(gbe, op, p, b, o)
+        def go(i, p=params, op=op):
+            run_op(gbe, op, p, *rings[i % sets])
         for i in range(3 * sets):
-            go(*rings[i % sets])
+            go(i)
         torch.cuda.synchronize()
         n = max(50, 4 * sets)
         a = torch.cuda.Event(enable_timing=True)
         e = torch.cuda.Event(enable_timing=True)
-        if args.graph:
-            # the n launches captured once into a CUDA graph, timed over replays
-            side = torch.cuda.Stream()
+        if graph:
+            side = torch.cuda.Stream(dev)
             side.wait_stream(torch.cuda.current_stream())
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph, stream=side):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
                 for i in range(n):
-                    go(*rings[i % sets])
+                    go(i)
             for _ in range(3):
-                graph.replay()
+                g.replay()
             torch.cuda.synchronize()
             reps = 10
             a.record()
             for _ in range(reps):
-                graph.replay()
+                g.replay()
             e.record()
             torch.cuda.synchronize()
             ms = a.elapsed_time(e) / (n * reps)
-            del graph
+            del g
         else:
             a.record()
             for i in range(n):
-                go(*rings[i % sets])
+                go(i)
             e.record()
             torch.cuda.synchronize()
             ms = a.elapsed_time(e) / n
-        res[key] = {"bytes": nb, "us": round(ms * 1e3, 2), "gbs": round(nb / ms / 1e6, 1),
-                    "rows_per_s": round(rows / ms * 1e3, 1), "copies": sets}
+        gbs = nb / ms / 1e6
+        res[key] = {"bytes": nb, "us": round(ms * 1e3, 2), "gbs": round(gbs, 1), "rows_per_s": round(rows / ms * 1e3, 1),
+                    "frac_of_peak": round(gbs / peak, 4), "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
+                    "copies": sets}
         del rings, base
         torch.cuda.empty_cache()
+    return res
+
+
+def workload_ops(workload: str, tokens: int = 8192, extra: bool = False, keep=None):
+    """The per-op inputs of a workload for the isolated timings (with
+    `extra`, also the prefill-shaped ops beyond the workload's list, or those
+    of them in `keep`)."""
+    from synth import workloads as W
+    if workload == W.PREFILL:
+        data = build_inputs(tokens, ALL_PREFILL)
+        if extra:
+            data.update(build_extra_inputs(tokens, ops=keep or None))
+        return data
+    return build_workload_inputs(workload)
+
+
+def per_config(torch, gbe, dev) -> dict:
+    """Every op of every large workload (and the decode ops), timed alone
+    from a CUDA graph and from the stream.  The headline figure of each op
+    is the graph one; the stream one adds the per-call host cost of the
+    Python binding and the C checks, which the small ops cannot hide."""
+    from synth import workloads as W
+    out = {}
+    for wl, note in ((W.PREFILL, "the step's ops and the other prefill ops at the same shapes"),
+                     (W.ROPE_VARIANTS, "f32 RoPE in place: q interleaved r=64, k half r=128 mu=1.2"),
+                     (W.WIDE, "f32 argmax [1024,152064] (5% tied rows, 1% NaN) and RMSNorm [1024,16384]"),
+                     (W.DECODE, "T=64, L2-resident and launch-bound: reported, not held to the bar")):
+        data = workload_ops(wl)
+        g = time_isolated(torch, gbe, dev, data, graph=True)
+        st = time_isolated(torch, gbe, dev, data, graph=False)
+        ops = {}
+        for op in g:
+            ops[op] = dict(g[op], us_stream=st[op]["us"], gbs_stream=st[op]["gbs"],
+                           frac_of_peak_stream=st[op]["frac_of_peak"])
+        out[wl] = {"note": note, "ops": ops}
+        del data
+    return out
+
+
+def run_isolated(args):
+    """`--isolated`: each op of one workload alone (see time_isolated), one
+    JSON line."""
+    import torch
+
+    import elementwise_row_rmsnorm_gb300 as gbe
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    gbe.lib()
+    workload = args.workload or WORKLOAD
+    data = workload_ops(workload, args.tokens, extra=args.extra or bool(args.keep and args.keep & set(EXTRA)),
+                        keep=args.keep)
+    if args.keep:
+        data = {op: v for op, v in data.items() if op in args.keep}
+    if args.sweep:
+        data = batch_sweep(data)
+    res = time_isolated(torch, gbe, dev, data, graph=args.graph)
     peak, kind = peaks()
-    for v in res.values():
-        v["frac_of_peak"] = round(v["gbs"] / peak, 4)
-        v["frac_of_8tbs"] = round(v["gbs"] / NOMINAL_HBM_GBS, 4)
     name = workload if workload != WORKLOAD or args.tokens >= 8192 else f"{WORKLOAD} (first {args.tokens} tokens)"
     line = {"mode": "isolated" + (" (CUDA graph)" if args.graph else ""), "workload": name,
             "unit": "GB/s", "peak": peak, "peak_source": kind, "per_op": res}
@@ -843,6 +898,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="leave out the per_config timings")
     ap.add_argument("--isolated", action="store_true",
                     help="time each op alone, back to back over rotating buffers, and print that instead")
     ap.add_argument("--sweep", action="store_true",
@@ -860,12 +916,12 @@ def main(argv=None):
     keep = None
     if args.ops:
         keep = set(args.ops.split(","))
-        unknown = keep - {op for op, _ in STEP} - set(EXTRA) - {"rope_q_inplace", "rope_k_inplace"}
+        unknown = keep - {op for op, _ in ALL_PREFILL} - set(EXTRA) - {"rope_q_inplace", "rope_k_inplace"}
         if unknown:
             ap.error(f"unknown ops {sorted(unknown)}")
         if keep & set(EXTRA) and not args.isolated:
-            ap.error("the ops beyond the step run with --isolated only")
-        STEP[:] = [(op, c) for op, c in STEP if op in keep]
+            ap.error("the ops beyond the prefill list run with --isolated only")
+        STEP[:] = [(op, c) for op, c in ALL_PREFILL if op in keep]
     args.keep = keep
     if args.impl == "reference":
         return run_reference(args)
