@@ -96,6 +96,9 @@ def op_bytes(op: str, arrays: dict, params: dict) -> tuple[int, int]:
         return 2 * nb(arrays["x"]) + nb(arrays["g"]) + nb(arrays["b"]), params["rows"]
     if op == "rope_multi":
         return 2 * nb(arrays["x"]) + nb(arrays["pos"]) + nb(arrays["inv_freq"]), params["T"]
+    if op == "rope_pair_inplace":  # q and k in place, each over its own rotated width
+        moved = sum(arrays[k].shape[0] * arrays[k].shape[1] * params[k][0] * arrays[k].itemsize for k in ("q", "k"))
+        return 2 * moved + nb(arrays["pos"]) + nb(arrays["fq"]) + nb(arrays["fk"]), params["T"]
     if op == "rope_qk_half_cached":
         T, r = params["T"], params["r"]
         return 2 * (nb(arrays["q"]) + nb(arrays["k"])) + nb(arrays["pos"]) + T * (r // 2) * 8, T
@@ -258,7 +261,10 @@ def build_workload_inputs(workload: str):
     from synth import workloads as W
     cases = W.cases(workload)
     if workload == W.ROPE_VARIANTS:
-        return {"rope_q_inplace": cases["rope_q"](), "rope_k_inplace": cases["rope_k"]()}
+        (aq, pq), (ak, pk) = cases["rope_q"](), cases["rope_k"]()
+        pair = ({"q": aq["x"], "k": ak["x"], "pos": aq["pos"], "fq": aq["inv_freq"], "fk": ak["inv_freq"]},
+                {"T": pq["T"], "q": (pq["r"], pq["mu"], pq["layout"]), "k": (pk["r"], pk["mu"], pk["layout"])})
+        return {"rope_q_inplace": (aq, pq), "rope_k_inplace": (ak, pk), "rope_pair_inplace": pair}
     if workload == W.WIDE:
         return {"argmax": cases["argmax"](), "rmsnorm": cases["rmsnorm"]()}
     if workload == W.DECODE:
@@ -458,7 +464,7 @@ def time_isolated(torch, gbe, dev, data: dict, graph: bool) -> dict:
         nb, rows = op_bytes(op, arrays, params)
         sets = int(min(12, max(2, -(-4 * l2 // nb) + 1)))
         base = {k: to_device(torch, dev, v) for k, v in arrays.items()}
-        shared = ("table", "w", "g", "gq", "gk", "inv_freq", "pos", "ids", "cos_sin", "u")
+        shared = ("table", "w", "g", "gq", "gk", "inv_freq", "fq", "fk", "pos", "ids", "cos_sin", "u")
         if op == "rope_qk_half_cached":
             base["cos_sin"] = gbe.rope_cos_sin(base["inv_freq"], params["r"], params["cache_len"])
         rings = []
@@ -529,7 +535,8 @@ def per_config(torch, gbe, dev) -> dict:
     from synth import workloads as W
     out = {}
     for wl, note in ((W.PREFILL, "the step's ops and the other prefill ops at the same shapes"),
-                     (W.ROPE_VARIANTS, "f32 RoPE in place: q interleaved r=64, k half r=128 mu=1.2"),
+                     (W.ROPE_VARIANTS, "f32 RoPE in place: q interleaved r=64, k half r=128 mu=1.2, each alone "
+                                       "and both in one launch (gbe_rope_pair)"),
                      (W.WIDE, "f32 argmax [1024,152064] (5% tied rows, 1% NaN) and RMSNorm [1024,16384]"),
                      (W.DECODE, "T=64, L2-resident and launch-bound: reported, not held to the bar")):
         data = workload_ops(wl)
@@ -583,6 +590,8 @@ def make_outputs(torch, dev, op, b):
         return (torch.empty_like(b["x"]), torch.empty_like(b["x"]))
     if op.startswith("rope_qk") or op == "qk_norm_rope":
         return (torch.empty_like(b["q"]), torch.empty_like(b["k"]))
+    if op == "rope_pair_inplace":
+        return None
     if op.endswith("_inplace"):
         return b["x"]
     if op == "argmax" or op.startswith("sample_"):
@@ -611,6 +620,8 @@ def run_op(gbe, op, p, b, o):
         gbe.gbe_rmsnorm(b["x"], b["w"], o, p["eps"])
     elif op == "layernorm":
         gbe.gbe_layernorm(b["x"], b["g"], b["b"], o, p["eps"])
+    elif op == "rope_pair_inplace":
+        gbe.gbe_rope_pair((b["q"], b["q"], b["fq"], *p["q"]), (b["k"], b["k"], b["fk"], *p["k"]), b["pos"])
     elif op.startswith("rope") and op.endswith("_inplace"):
         gbe.gbe_rope(b["x"], b["x"], b["pos"], b["inv_freq"], p["r"], p["mu"], p["layout"])
     elif op == "rope_multi":
@@ -916,7 +927,8 @@ def main(argv=None):
     keep = None
     if args.ops:
         keep = set(args.ops.split(","))
-        unknown = keep - {op for op, _ in ALL_PREFILL} - set(EXTRA) - {"rope_q_inplace", "rope_k_inplace"}
+        unknown = keep - {op for op, _ in ALL_PREFILL} - set(EXTRA) - {"rope_q_inplace", "rope_k_inplace",
+                                                                         "rope_pair_inplace"}
         if unknown:
             ap.error(f"unknown ops {sorted(unknown)}")
         if keep & set(EXTRA) and not args.isolated:

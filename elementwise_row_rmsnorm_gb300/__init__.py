@@ -10,7 +10,7 @@ kernel each, in ``lib/libgbe_elementwise.so`` (declared in
 """
 from .binding import (GBE_BF16, GBE_F32, GbeError, LibraryMissing, add, add_rmsnorm, argmax, embedding,
                       gbe_add, gbe_add_rmsnorm, gbe_argmax, gbe_embedding, gbe_layernorm, gbe_pcg64_uniforms,
-                      gbe_qk_norm_rope, gbe_rmsnorm, gbe_rope, gbe_rope_cos_sin, gbe_rope_multi, gbe_rope_qk,
+                      gbe_qk_norm_rope, gbe_rmsnorm, gbe_rope, gbe_rope_cos_sin, gbe_rope_multi, gbe_rope_pair, gbe_rope_qk,
                       gbe_sample, gbe_sample_seeded, gbe_silu_mul, layernorm, lib, pcg64_uniforms, rmsnorm, rope,
                       rope_cos_sin, sample, sample_seeded, silu_mul, status_string)
 
@@ -24,7 +24,7 @@ def build(force: bool = False) -> str:
 __all__ = [
     "GBE_BF16", "GBE_F32", "GbeError", "LibraryMissing", "add", "add_rmsnorm", "argmax", "build",
     "embedding", "gbe_add", "gbe_add_rmsnorm", "gbe_argmax", "gbe_embedding", "gbe_layernorm",
-    "gbe_pcg64_uniforms", "gbe_qk_norm_rope", "gbe_rmsnorm", "gbe_rope", "gbe_rope_cos_sin", "gbe_rope_multi",
+    "gbe_pcg64_uniforms", "gbe_qk_norm_rope", "gbe_rmsnorm", "gbe_rope", "gbe_rope_cos_sin", "gbe_rope_multi", "gbe_rope_pair",
     "gbe_rope_qk", "gbe_sample", "gbe_sample_seeded", "gbe_silu_mul", "layernorm", "lib", "pcg64_uniforms",
     "rmsnorm", "rope", "rope_cos_sin", "sample", "sample_seeded", "silu_mul", "status_string",
 ]

@@ -64,6 +64,7 @@ def lib() -> ctypes.CDLL:
                 "gbe_rope_qk": [vp, vp, i64, i64, vp, vp, i64, i64, vp, i64, i64, i64, vp, vp, i64, f32, i32,
                                 i32, vp],
                 "gbe_rope_cos_sin": [vp, i64, i64, vp, vp],
+                "gbe_rope_pair": [vp, vp, vp, i64, i64, i32, vp],
                 "gbe_rope_multi": [vp, vp, vp, i64, i64, i64, i64, vp, vp, f32, i32, i32, vp],
                 "gbe_qk_norm_rope": [vp, vp, i64, i64, vp, vp, vp, i64, i64, vp, f32, vp, i64, i64, i64, vp, vp,
                                      i64, f32, i32, i32, vp],
@@ -225,6 +226,48 @@ def gbe_rope_qk(q, q_out, k, k_out, pos, inv_freq, r: int, mu: float = 1.0, layo
     (qx, qy, qs, hq), (kx, ky, ks, hk) = sides
     _check("gbe_rope_qk", lib().gbe_rope_qk(qx, qy, qs, hq, kx, ky, ks, hk, _ptr(pos), T, D, r, _ptr(inv_freq),
                                             _ptr(cos_sin), cache_len, mu, layout, _dt(*floats), _stream(stream)))
+
+
+class RopeOperand(ctypes.Structure):
+    """gbe_rope_operand of the C header."""
+    _fields_ = [("x", ctypes.c_void_p), ("y", ctypes.c_void_p), ("stride", ctypes.c_int64), ("H", ctypes.c_int64),
+                ("r", ctypes.c_int64), ("inv_freq", ctypes.c_void_p), ("mu", ctypes.c_float), ("layout", ctypes.c_int)]
+
+
+def gbe_rope_pair(a, b, pos, stream=None) -> None:
+    """RoPE of two operands in one launch.  a and b (b may be None) are
+    tuples (x, y, inv_freq, r, mu, layout): x and y [T, H, D] views with
+    contiguous heads whose token stride may exceed H * D (y is x: in place),
+    inv_freq float32[r/2]; the operands share pos (int32[T]), T, D and dtype."""
+    ops, floats = [], []
+    T = D = None
+    for o in (a, b):
+        if o is None:
+            ops.append(None)
+            continue
+        x, y, inv_freq, r, mu, layout = o
+        for t in (x, y, inv_freq):
+            if not _on_device(t):
+                raise ValueError("tensors must be on the CUDA device or in pinned host memory")
+        D = x.shape[2] if D is None else D
+        Tx, H, sx = _rows_view(x, D)
+        _, _, sy = _rows_view(y, D)
+        T = Tx if T is None else T
+        if Tx != T or y.shape != x.shape or sx != sy:
+            raise ValueError("rope_pair: the operands share T and D; an output has its input's shape and stride")
+        if inv_freq.dtype != torch.float32 or inv_freq.numel() < r // 2 or not inv_freq.is_contiguous():
+            raise ValueError("rope_pair: inv_freq is float32[r/2]")
+        ops.append(RopeOperand(x.data_ptr(), y.data_ptr(), sx, H, r, inv_freq.data_ptr(), mu, layout))
+        floats += [x, y]
+    if ops[0] is None:
+        raise ValueError("rope_pair: the first operand is required")
+    if pos.dtype != torch.int32 or pos.numel() != T or not pos.is_contiguous() or not _on_device(pos):
+        raise ValueError("rope_pair: pos is int32[T]")
+    pa = ctypes.byref(ops[0])
+    pb = ctypes.byref(ops[1]) if ops[1] is not None else None
+    _check("gbe_rope_pair", lib().gbe_rope_pair(ctypes.cast(pa, ctypes.c_void_p), ctypes.cast(pb, ctypes.c_void_p)
+                                                if pb is not None else None, _ptr(pos), T, D, _dt(*floats),
+                                                _stream(stream)))
 
 
 def gbe_qk_norm_rope(q, q_out, gq, k, k_out, gk, eps: float, pos, inv_freq, r: int, mu: float = 1.0,

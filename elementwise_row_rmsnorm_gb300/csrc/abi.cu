@@ -322,40 +322,56 @@ int gbe_add_rmsnorm(const void* x, const void* residual, const void* w, void* y,
     return finish(gbe::launch_rmsnorm(x, residual, w, y, h, rows, d, eps, dtype, vec, as_stream(stream)));
 }
 
-// Shared checks and launch of gbe_rope and gbe_rope_qk.  Operand k of the
-// call: input xs[k], output ys[k], H[k] heads, token stride strides[k].
-static int rope_common(const void* const xs[2], void* const ys[2], const int64_t H[2], const int64_t strides[2],
-                       const int32_t* pos, int64_t T, int64_t D, int64_t r, const float* inv_freq,
-                       const float* cos_sin, int64_t cache_len, float mu, int layout, int dtype,
-                       gbe_stream stream) {
+// One operand of a RoPE launch, as the entry points describe it.
+struct RopeSide {
+    const void* x;
+    void* y;
+    int64_t stride, H, r;
+    const float* inv_freq;
+    float mu;
+    int layout;
+};
+
+// Shared checks and launch of gbe_rope, gbe_rope_qk and gbe_rope_pair: two
+// operands (H = 0: absent) sharing positions, T, D and dtype, each with its
+// own token stride, width, frequencies, scale and layout; a cos/sin table
+// only when they share the last four.
+static int rope_common(const RopeSide (&sd)[2], const int32_t* pos, int64_t T, int64_t D, const float* cos_sin,
+                       int64_t cache_len, int dtype, gbe_stream stream) {
     const int es = elem_size(dtype);
     if (!es) return GBE_ERR_DTYPE;
-    if (layout != 0 && layout != 1) return GBE_ERR_LAYOUT;
+    for (const RopeSide& o : sd)
+        if (o.layout != 0 && o.layout != 1) return GBE_ERR_LAYOUT;
     if (T < 0 || D <= 0 || T > INT32_MAX || D > INT32_MAX) return GBE_ERR_SHAPE;
-    for (int k = 0; k < 2; ++k) {
+    for (const RopeSide& o : sd) {
         int64_t hd;
-        if (H[k] < 0 || !mul_ok(H[k], D, &hd) || hd > INT32_MAX / 2) return GBE_ERR_SHAPE;
-        if (H[k] > 0 && (strides[k] < hd || strides[k] > INT64_MAX / (T > 0 ? T : 1) / es)) return GBE_ERR_SHAPE;
+        if (o.H < 0 || !mul_ok(o.H, D, &hd) || hd > INT32_MAX / 2) return GBE_ERR_SHAPE;
+        if (o.H > 0 && (o.stride < hd || o.stride > INT64_MAX / (T > 0 ? T : 1) / es)) return GBE_ERR_SHAPE;
     }
-    if (r < 0 || r > D || (r & 1) || !std::isfinite(mu)) return GBE_ERR_ROTARY;
+    for (const RopeSide& o : sd)
+        if (o.r < 0 || o.r > D || (o.r & 1) || !std::isfinite(o.mu)) return GBE_ERR_ROTARY;
     if (cos_sin != nullptr && cache_len < 0) return GBE_ERR_SHAPE;
-    const int64_t half = r / 2;
     Rows in[2], out[2];
-    bool any = false;
+    bool any = false, work = false;
     for (int k = 0; k < 2; ++k) {
-        const int64_t rows = H[k] > 0 ? T : 0;
-        in[k] = {xs[k], rows, strides[k] * es, H[k] * D * es};
-        out[k] = {ys[k], rows, strides[k] * es, H[k] * D * es};
-        any = any || (rows > 0 && D > 0);
+        const int64_t rows = sd[k].H > 0 ? T : 0;
+        in[k] = {sd[k].x, rows, sd[k].stride * es, sd[k].H * D * es};
+        out[k] = {sd[k].y, rows, sd[k].stride * es, sd[k].H * D * es};
+        any = any || rows > 0;
+        work = work || (rows > 0 && !(sd[k].x == sd[k].y && sd[k].r == 0));  // in place with r = 0: nothing
     }
     if (!any) return GBE_OK;
-    uint64_t bp, bf, bc = 0;
-    int64_t nc = 0;
-    if (!extent(T, 4, &bp) || !extent(half, 4, &bf)) return GBE_ERR_SHAPE;
-    if (cos_sin != nullptr && (!mul_ok(cache_len, half, &nc) || !extent(nc, 8, &bc))) return GBE_ERR_SHAPE;
-    // 0, 1 = outputs; 2, 3 = inputs; 4 = pos; 5 = inv_freq; 6 = cos/sin table
-    Buf bufs[7] = {out[0].extent(), out[1].extent(), in[0].extent(), in[1].extent(),
-                   {pos, bp, 4}, {inv_freq, bf, 4}, {cos_sin, cos_sin ? bc : 0u, 8}};
+    uint64_t bp, bf[2], bc = 0;
+    if (!extent(T, 4, &bp)) return GBE_ERR_SHAPE;
+    for (int k = 0; k < 2; ++k)
+        if (!extent(sd[k].H > 0 ? sd[k].r / 2 : 0, 4, &bf[k])) return GBE_ERR_SHAPE;
+    if (cos_sin != nullptr) {
+        int64_t nc = 0;
+        if (!mul_ok(cache_len, sd[0].r / 2, &nc) || !extent(nc, 8, &bc)) return GBE_ERR_SHAPE;
+    }
+    // 0, 1 = outputs; 2, 3 = inputs; 4 = pos; 5, 6 = the operands' frequencies; 7 = cos/sin table
+    Buf bufs[8] = {out[0].extent(), out[1].extent(), in[0].extent(), in[1].extent(), {pos, bp, 4},
+                   {sd[0].inv_freq, bf[0], 4}, {sd[1].inv_freq, bf[1], 4}, {cos_sin, cos_sin ? bc : 0u, 8}};
     for (int k = 0; k < 4; ++k) bufs[k].align = (uint64_t)es;
     for (const Buf& b : bufs) {
         const int st = check_form(b);
@@ -366,7 +382,7 @@ static int rope_common(const void* const xs[2], void* const ys[2], const int64_t
         // the other operand (input or output) nor with the small arrays
         if (rows_overlap(out[o], in[o]) && !rows_same(out[o], in[o])) return GBE_ERR_ALIAS;
         if (rows_overlap(out[o], in[1 - o]) || rows_overlap(out[o], out[1 - o])) return GBE_ERR_ALIAS;
-        for (int j = 4; j < 7; ++j)
+        for (int j = 4; j < 8; ++j)
             if (overlaps(bufs[o], bufs[j])) return GBE_ERR_ALIAS;
     }
     Checker chk;
@@ -375,44 +391,47 @@ static int rope_common(const void* const xs[2], void* const ys[2], const int64_t
         const int st = chk.check(b);
         if (st != GBE_OK) return st;
     }
-    const bool vec = aligned16(xs[0]) && aligned16(ys[0]) && aligned16(xs[1]) && aligned16(ys[1]) &&
-                     (strides[0] * es) % 16 == 0 && (strides[1] * es) % 16 == 0;
+    if (!work) return GBE_OK;  // every operand in place with nothing to rotate
+    bool vec = true;
+    for (const RopeSide& o : sd)
+        vec = vec && aligned16(o.x) && aligned16(o.y) && (o.stride * es) % 16 == 0;
     gbe::RopeArgs a;
-    for (int k = 0; k < 2; ++k) a.side[k] = {xs[k], ys[k], strides[k], H[k] > 0 ? H[k] : 0};
+    for (int k = 0; k < 2; ++k)
+        a.side[k] = {sd[k].x, sd[k].y, sd[k].stride, sd[k].H > 0 ? sd[k].H : 0, sd[k].r, sd[k].inv_freq, sd[k].mu,
+                     sd[k].layout};
     a.pos = pos;
     a.T = T;
     a.D = D;
-    a.r = r;
-    a.inv_freq = inv_freq;
     a.cos_sin = cos_sin;
     a.cache_len = cos_sin ? cache_len : 0;
-    a.mu = mu;
-    a.layout = layout;
-    if (xs[0] == ys[0] && xs[1] == ys[1] && r == 0) return GBE_OK;  // in place, nothing to rotate
     return finish(gbe::launch_rope(a, dtype, vec, as_stream(stream)));
 }
 
 int gbe_rope(const void* x, void* y, const int32_t* pos, int64_t T, int64_t H, int64_t D, int64_t r,
              const float* inv_freq, float mu, int layout, int dtype, gbe_stream stream) {
-    const void* xs[2] = {x, nullptr};
-    void* ys[2] = {y, nullptr};
     int64_t hd = 0;
     if (H > 0 && D > 0 && !mul_ok(H, D, &hd)) return GBE_ERR_SHAPE;
-    const int64_t Hs[2] = {H, 0};
-    const int64_t strides[2] = {hd, 0};
-    return rope_common(xs, ys, Hs, strides, pos, T, D, r, inv_freq, nullptr, 0, mu, layout, dtype, stream);
+    const RopeSide sd[2] = {{x, y, hd, H, r, inv_freq, mu, layout}, {nullptr, nullptr, 0, 0, r, inv_freq, mu, layout}};
+    return rope_common(sd, pos, T, D, nullptr, 0, dtype, stream);
 }
 
 int gbe_rope_qk(const void* q, void* q_out, int64_t q_stride, int64_t Hq, const void* k, void* k_out,
                 int64_t k_stride, int64_t Hk, const int32_t* pos, int64_t T, int64_t D, int64_t r,
                 const float* inv_freq, const float* cos_sin, int64_t cache_len, float mu, int layout, int dtype,
                 gbe_stream stream) {
-    const void* xs[2] = {q, k};
-    void* ys[2] = {q_out, k_out};
-    const int64_t Hs[2] = {Hq, Hk};
-    const int64_t strides[2] = {q_stride, k_stride};
-    return rope_common(xs, ys, Hs, strides, pos, T, D, r, inv_freq, cos_sin, cache_len, mu, layout, dtype,
-                       stream);
+    const RopeSide sd[2] = {{q, q_out, q_stride, Hq, r, inv_freq, mu, layout},
+                            {k, k_out, k_stride, Hk, r, inv_freq, mu, layout}};
+    return rope_common(sd, pos, T, D, cos_sin, cache_len, dtype, stream);
+}
+
+int gbe_rope_pair(const gbe_rope_operand* a, const gbe_rope_operand* b, const int32_t* pos, int64_t T, int64_t D,
+                  int dtype, gbe_stream stream) {
+    if (a == nullptr) return GBE_ERR_NULL;
+    const gbe_rope_operand none = {nullptr, nullptr, 0, 0, 0, nullptr, 1.0f, 0};
+    const gbe_rope_operand& o2 = b ? *b : none;
+    const RopeSide sd[2] = {{a->x, a->y, a->stride, a->H, a->r, a->inv_freq, a->mu, a->layout},
+                            {o2.x, o2.y, o2.stride, o2.H, o2.r, o2.inv_freq, o2.mu, o2.layout}};
+    return rope_common(sd, pos, T, D, nullptr, 0, dtype, stream);
 }
 
 int gbe_qk_norm_rope(const void* q, void* q_out, int64_t q_stride, int64_t Hq, const void* gq, const void* k,

@@ -17,22 +17,25 @@ cudaError_t launch_layernorm(const void* x, const void* g, const void* b, void* 
                              float eps, int dtype, bool vec, cudaStream_t st);
 
 // RoPE over one or two [T, H, D] operands (q and k) that share positions and
-// frequencies; each operand has a token stride (elements) used for its input
-// and its output.  cos_sin: NULL, or a [cache_len, r/2] table of (cos, sin).
+// head_dim; each operand has a token stride (elements) used for its input
+// and its output, and its own rotated width, frequencies, scale and layout.
+// cos_sin: NULL, or a [cache_len, r/2] table of (cos, sin), given only when
+// both operands share r, inv_freq and layout.
 struct RopeArgs {
     struct Side {
         const void* x;
         void* y;
         int64_t stride;
         int64_t H;
+        int64_t r;
+        const float* inv_freq;
+        float mu;
+        int layout;
     } side[2];
     const int32_t* pos;
-    int64_t T, D, r;
-    const float* inv_freq;
+    int64_t T, D;
     const float* cos_sin;
     int64_t cache_len;
-    float mu;
-    int layout;
 };
 
 cudaError_t launch_rope(const RopeArgs& a, int dtype, bool vec, cudaStream_t st);

@@ -43,12 +43,17 @@ constexpr int kThreads = 256;
 constexpr int kHeadsPerThread = 4;  // heads a thread rotates with one set of angles
 
 // One [T, H, D] operand of a launch: input and output bases, their token
-// strides (in elements), and the number of threads this operand takes.
+// strides (in elements), its own rotated width, frequencies and scale (the
+// layout is a template parameter of the kernel), and the number of threads
+// this operand takes.
 struct Operand {
     const char* x;
     char* y;
     int64_t xs, ys;
     int H;
+    int r;                  // rotated width (even)
+    const float* inv_freq;  // f32[r / 2]
+    float mu;
     int NC;           // head chunks of kHeadsPerThread (vector path)
     int copy_tail;    // out of place with r < D: entries r .. D-1 are copied
     int64_t threads;  // threads of the launch that serve this operand
@@ -57,6 +62,18 @@ struct Operand {
 __device__ __forceinline__ void rotate(float a, float b, float c, float s, float mu, float& a2, float& b2) {
     a2 = __fmul_rn(mu, __fsub_rn(__fmul_rn(a, c), __fmul_rn(b, s)));
     b2 = __fmul_rn(mu, __fadd_rn(__fmul_rn(a, s), __fmul_rn(b, c)));
+}
+
+// rotate() for two pairs at once, (a.x, b.x) by (c.x, s.x) and (a.y, b.y)
+// by (c.y, s.y): the products and the scale two lanes at a time (packed
+// f32x2 multiplies, each lane rounded as the scalar product), the sums
+// scalar -- a packed multiply feeding a packed add may be fused into one
+// rounding -- so the bits are rotate()'s.
+__device__ __forceinline__ void rotate2(float2 a, float2 b, float2 c, float2 s, float mu, float2& a2, float2& b2) {
+    const float2 ac = mul2_rn(a, c), bs = mul2_rn(b, s), as = mul2_rn(a, s), bc = mul2_rn(b, c);
+    const float2 m = make_float2(mu, mu);
+    a2 = mul2_rn(m, make_float2(__fsub_rn(ac.x, bs.x), __fsub_rn(ac.y, bs.y)));
+    b2 = mul2_rn(m, make_float2(__fadd_rn(as.x, bc.x), __fadd_rn(as.y, bc.y)));
 }
 
 // cos / sin of the angle of pair i at position p: from the table when one is
@@ -73,29 +90,25 @@ __device__ __forceinline__ void angle(int32_t p, int i, const float* inv_freq, c
     }
 }
 
-// Aligned path.  A thread owns one group of P consecutive pairs (one 16-byte
-// vector of each pair member) of one token, for a chunk of up to HC heads
+// Aligned path, one thread's work.  A thread owns one group of P consecutive
+// pairs (one 16-byte vector of each pair member) of one token of operand R,
+// for a chunk of up to HC heads
 // (4, or 1 when the launch would otherwise hold too few threads to fill the
 // GPU, as at decode sizes):
 // it issues the loads of all its heads first, gets the P angles' cos / sin
 // into registers while those loads are in flight, then rotates and stores
 // every head.  Threads of one token and head chunk cover consecutive 16-byte
-// vectors, so each warp-wide access is contiguous.  The launch's threads
-// serve operand A first, then operand B.
+// vectors, so each warp-wide access is contiguous.
 template <int DT, int LAYOUT, bool CACHE, int HC>
-__global__ void __launch_bounds__(kThreads)
-rope_vec(Operand A, Operand B, const int32_t* pos, int64_t T, int D, int r, const float* inv_freq,
-         const float2* cache, int64_t cache_len, float mu) {
+__device__ __forceinline__ void rope_vec_item(const Operand& R, int64_t gt, const int32_t* pos, int D,
+                                              const float2* cache, int64_t cache_len) {
     using S = Store<DT>;
     constexpr int V = S::V;
     constexpr int P = LAYOUT == 0 ? V : V / 2;  // pairs per 16-byte item
     constexpr int64_t ES = sizeof(typename S::T);
-    pdl_begin();
-    int64_t gt = (int64_t)blockIdx.x * kThreads + threadIdx.x;
-    const bool second = gt >= A.threads;
-    const Operand R = second ? B : A;
-    if (second) gt -= A.threads;
-    if (gt >= R.threads) return;
+    const int r = R.r;
+    const float* inv_freq = R.inv_freq;
+    const float mu = R.mu;
     const int half = r >> 1;
     const int G = LAYOUT == 0 ? half / V : r / V;  // items per head
     const int g = (int)(gt % G);
@@ -110,6 +123,8 @@ rope_vec(Operand A, Operand B, const int32_t* pos, int64_t T, int D, int r, cons
     const int64_t hb = (int64_t)half * ES;        // byte distance to the b member (layout 0)
     const int64_t hd = (int64_t)D * ES;           // byte distance between heads
 
+    // the position first: the angles wait for it while the data loads fly
+    const int32_t p = pos[t];
     Vec16 va[HC], vb[HC];
 #pragma unroll
     for (int j = 0; j < HC; ++j) {
@@ -120,7 +135,6 @@ rope_vec(Operand A, Operand B, const int32_t* pos, int64_t T, int D, int r, cons
     }
     // this thread's pairs, once for all its heads
     float c[P], sn[P];
-    const int32_t p = pos[t];
     const int i0 = g * P;
 #pragma unroll
     for (int e = 0; e < P; ++e) angle<CACHE>(p, i0 + e, inv_freq, cache, cache_len, half, c[e], sn[e]);
@@ -135,21 +149,27 @@ rope_vec(Operand A, Operand B, const int32_t* pos, int64_t T, int D, int r, cons
                 float fb[V];
                 S::unpack(vb[j], fb);
 #pragma unroll
-                for (int e = 0; e < V; ++e) {
-                    float a2, b2;
-                    rotate(fa[e], fb[e], c[e], sn[e], mu, a2, b2);
-                    fa[e] = a2;
-                    fb[e] = b2;
+                for (int e = 0; e < V; e += 2) {
+                    float2 a2, b2;
+                    rotate2(make_float2(fa[e], fa[e + 1]), make_float2(fb[e], fb[e + 1]),
+                            make_float2(c[e], c[e + 1]), make_float2(sn[e], sn[e + 1]), mu, a2, b2);
+                    fa[e] = a2.x;
+                    fa[e + 1] = a2.y;
+                    fb[e] = b2.x;
+                    fb[e + 1] = b2.y;
                 }
                 st_stream(q, S::pack(fa));
                 st_stream(q + hb, S::pack(fb));
             } else {
 #pragma unroll
-                for (int e = 0; e < P; ++e) {
-                    float a2, b2;
-                    rotate(fa[2 * e], fa[2 * e + 1], c[e], sn[e], mu, a2, b2);
-                    fa[2 * e] = a2;
-                    fa[2 * e + 1] = b2;
+                for (int e = 0; e < P; e += 2) {
+                    float2 a2, b2;
+                    rotate2(make_float2(fa[2 * e], fa[2 * e + 2]), make_float2(fa[2 * e + 1], fa[2 * e + 3]),
+                            make_float2(c[e], c[e + 1]), make_float2(sn[e], sn[e + 1]), mu, a2, b2);
+                    fa[2 * e] = a2.x;
+                    fa[2 * e + 2] = a2.y;
+                    fa[2 * e + 1] = b2.x;
+                    fa[2 * e + 3] = b2.y;
                 }
                 st_stream(q, S::pack(fa));
             }
@@ -167,21 +187,30 @@ rope_vec(Operand A, Operand B, const int32_t* pos, int64_t T, int D, int r, cons
     }
 }
 
+// The launch's threads serve operand A first, then operand B, each with its
+// own layout (LA, LB), width, frequencies and scale.
+template <int DT, int LA, int LB, bool CACHE, int HC>
+__global__ void __launch_bounds__(kThreads)
+rope_vec(Operand A, Operand B, const int32_t* pos, int D, const float2* cache, int64_t cache_len) {
+    pdl_begin();
+    const int64_t gt = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    if (gt < A.threads)
+        rope_vec_item<DT, LA, CACHE, HC>(A, gt, pos, D, cache, cache_len);
+    else if (gt - A.threads < B.threads)
+        rope_vec_item<DT, LB, CACHE, HC>(B, gt - A.threads, pos, D, cache, cache_len);
+}
+
 // Unaligned path (or widths that do not split into 16-byte vectors): a
 // thread owns one pair of one token, gets its angle once and rotates that
 // pair in every head; tail threads copy one entry per head.
 template <int DT, int LAYOUT, bool CACHE>
-__global__ void __launch_bounds__(kThreads)
-rope_scalar(Operand A, Operand B, const int32_t* pos, int64_t T, int D, int r, const float* inv_freq,
-            const float2* cache, int64_t cache_len, float mu) {
+__device__ __forceinline__ void rope_scalar_item(const Operand& R, int64_t gt, const int32_t* pos, int D,
+                                                 const float2* cache, int64_t cache_len) {
     using S = Store<DT>;
     constexpr int64_t ES = sizeof(typename S::T);
-    pdl_begin();
-    int64_t gt = (int64_t)blockIdx.x * kThreads + threadIdx.x;
-    const bool second = gt >= A.threads;
-    const Operand R = second ? B : A;
-    if (second) gt -= A.threads;
-    if (gt >= R.threads) return;
+    const int r = R.r;
+    const float* inv_freq = R.inv_freq;
+    const float mu = R.mu;
     const int half = r >> 1;
     const int per_tok = half + (R.copy_tail ? D - r : 0);
     const int64_t t = gt / per_tok;
@@ -209,6 +238,17 @@ rope_scalar(Operand A, Operand B, const int32_t* pos, int64_t T, int D, int r, c
                 reinterpret_cast<uint16_t*>(R.y)[yo] = reinterpret_cast<const uint16_t*>(R.x)[xo];
         }
     }
+}
+
+template <int DT, int LA, int LB, bool CACHE>
+__global__ void __launch_bounds__(kThreads)
+rope_scalar(Operand A, Operand B, const int32_t* pos, int D, const float2* cache, int64_t cache_len) {
+    pdl_begin();
+    const int64_t gt = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    if (gt < A.threads)
+        rope_scalar_item<DT, LA, CACHE>(A, gt, pos, D, cache, cache_len);
+    else if (gt - A.threads < B.threads)
+        rope_scalar_item<DT, LB, CACHE>(B, gt - A.threads, pos, D, cache, cache_len);
 }
 
 // Multi-axis RoPE ("Operations", section 3): head_dim is cut into per-axis
@@ -326,21 +366,27 @@ rope_multi_vec(const char* x, char* y, const int32_t* pos, int64_t T, int H, int
                 float fb[V];
                 S::unpack(vb[j], fb);
 #pragma unroll
-                for (int e = 0; e < V; ++e) {
-                    float a2, b2;
-                    rotate(fa[e], fb[e], c[e], sn[e], mu, a2, b2);
-                    fa[e] = a2;
-                    fb[e] = b2;
+                for (int e = 0; e < V; e += 2) {
+                    float2 a2, b2;
+                    rotate2(make_float2(fa[e], fa[e + 1]), make_float2(fb[e], fb[e + 1]),
+                            make_float2(c[e], c[e + 1]), make_float2(sn[e], sn[e + 1]), mu, a2, b2);
+                    fa[e] = a2.x;
+                    fa[e + 1] = a2.y;
+                    fb[e] = b2.x;
+                    fb[e + 1] = b2.y;
                 }
                 st_stream(q, S::pack(fa));
                 st_stream(q + hb, S::pack(fb));
             } else {
 #pragma unroll
-                for (int e = 0; e < P; ++e) {
-                    float a2, b2;
-                    rotate(fa[2 * e], fa[2 * e + 1], c[e], sn[e], mu, a2, b2);
-                    fa[2 * e] = a2;
-                    fa[2 * e + 1] = b2;
+                for (int e = 0; e < P; e += 2) {
+                    float2 a2, b2;
+                    rotate2(make_float2(fa[2 * e], fa[2 * e + 2]), make_float2(fa[2 * e + 1], fa[2 * e + 3]),
+                            make_float2(c[e], c[e + 1]), make_float2(sn[e], sn[e + 1]), mu, a2, b2);
+                    fa[2 * e] = a2.x;
+                    fa[2 * e + 2] = a2.y;
+                    fa[2 * e + 1] = b2.x;
+                    fa[2 * e + 3] = b2.y;
                 }
                 st_stream(q, S::pack(fa));
             }
@@ -373,13 +419,34 @@ rope_cos_sin_table(float2* cache, int64_t len, int half, const float* inv_freq) 
     cache[gt] = make_float2(c, s);
 }
 
+template <int DT, int LA, int LB, bool CACHE>
+cudaError_t launch_shape(bool vec, bool one_head, unsigned grid, const Operand (&op)[2], const RopeArgs& a,
+                         const float2* cache, cudaStream_t st) {
+    const int Di = (int)a.D;
+    if (vec && one_head)
+        return launch(rope_vec<DT, LA, LB, CACHE, 1>, dim3(grid), dim3(kThreads), 0, st, op[0], op[1], a.pos, Di,
+                      cache, a.cache_len);
+    if (vec)
+        return launch(rope_vec<DT, LA, LB, CACHE, kHeadsPerThread>, dim3(grid), dim3(kThreads), 0, st, op[0], op[1],
+                      a.pos, Di, cache, a.cache_len);
+    return launch(rope_scalar<DT, LA, LB, CACHE>, dim3(grid), dim3(kThreads), 0, st, op[0], op[1], a.pos, Di, cache,
+                  a.cache_len);
+}
+
 template <int DT>
 cudaError_t launch_dt(const RopeArgs& a, bool vec, cudaStream_t st) {
     constexpr int V = Store<DT>::V;
-    const int64_t half = a.r / 2;
-    const bool cached = a.cos_sin != nullptr;
     const float2* cache = reinterpret_cast<const float2*>(a.cos_sin);
-    vec = vec && a.r > 0 && a.D % V == 0 && (a.layout == 0 ? half % V == 0 : a.r % V == 0);
+    bool used[2];
+    int64_t G[2];
+    vec = vec && a.D % V == 0;
+    for (int k = 0; k < 2; ++k) {
+        const RopeArgs::Side& sd = a.side[k];
+        // in place with nothing to rotate: nothing to do for this operand
+        used[k] = sd.H > 0 && a.T > 0 && !(sd.x == sd.y && sd.r == 0);
+        G[k] = sd.layout == 0 ? sd.r / 2 / V : sd.r / V;  // 16-byte items per head (vector path)
+        if (used[k]) vec = vec && sd.r > 0 && (sd.layout == 0 ? (sd.r / 2) % V == 0 : sd.r % V == 0);
+    }
     Operand op[2];
     for (int k = 0; k < 2; ++k) {
         const RopeArgs::Side& sd = a.side[k];
@@ -388,57 +455,41 @@ cudaError_t launch_dt(const RopeArgs& a, bool vec, cudaStream_t st) {
         op[k].xs = sd.stride;
         op[k].ys = sd.stride;
         op[k].H = (int)sd.H;
-        op[k].copy_tail = (sd.x != sd.y && a.r < a.D) ? 1 : 0;
+        op[k].r = (int)sd.r;
+        op[k].inv_freq = sd.inv_freq;
+        op[k].mu = sd.mu;
+        op[k].copy_tail = (sd.x != sd.y && sd.r < a.D) ? 1 : 0;
         op[k].NC = (int)((sd.H + kHeadsPerThread - 1) / kHeadsPerThread);
-        if (sd.H == 0 || a.T == 0) {
+        if (!used[k])
             op[k].threads = 0;
-        } else if (vec) {
-            const int64_t G = a.layout == 0 ? half / V : a.r / V;
-            op[k].threads = a.T * op[k].NC * G;
-        } else {
-            op[k].threads = a.T * (half + (op[k].copy_tail ? a.D - a.r : 0));
-        }
+        else if (vec)
+            op[k].threads = a.T * op[k].NC * G[k];
+        else
+            op[k].threads = a.T * (sd.r / 2 + (op[k].copy_tail ? a.D - sd.r : 0));
     }
     // few threads (decode sizes): one head per thread instead of four
     const bool one_head = vec && op[0].threads + op[1].threads < (int64_t)sm_count() * 256;
-    if (one_head) {
-        const int64_t G = a.layout == 0 ? half / V : a.r / V;
+    if (one_head)
         for (int k = 0; k < 2; ++k) {
             op[k].NC = op[k].H;
-            op[k].threads = op[k].threads ? a.T * op[k].NC * G : 0;
+            op[k].threads = op[k].threads ? a.T * op[k].NC * G[k] : 0;
         }
-    }
     const int64_t threads = op[0].threads + op[1].threads;
     if (threads == 0) return cudaSuccess;
     const unsigned grid = (unsigned)((threads + kThreads - 1) / kThreads);
-    const int Di = (int)a.D, ri = (int)a.r;
-#define GBE_ROPE(KERNEL, L, C)                                                                              \
-    return launch(KERNEL<DT, L, C>, dim3(grid), dim3(kThreads), 0, st, op[0], op[1], a.pos, a.T, Di, ri,    \
-                  a.inv_freq, cache, a.cache_len, a.mu)
-#define GBE_ROPE_VEC(L, C, HC)                                                                              \
-    return launch(rope_vec<DT, L, C, HC>, dim3(grid), dim3(kThreads), 0, st, op[0], op[1], a.pos, a.T, Di,  \
-                  ri, a.inv_freq, cache, a.cache_len, a.mu)
-    if (vec && one_head) {
-        if (a.layout == 0) {
-            if (cached) GBE_ROPE_VEC(0, true, 1); else GBE_ROPE_VEC(0, false, 1);
-        } else {
-            if (cached) GBE_ROPE_VEC(1, true, 1); else GBE_ROPE_VEC(1, false, 1);
-        }
-    } else if (vec) {
-        if (a.layout == 0) {
-            if (cached) GBE_ROPE_VEC(0, true, kHeadsPerThread); else GBE_ROPE_VEC(0, false, kHeadsPerThread);
-        } else {
-            if (cached) GBE_ROPE_VEC(1, true, kHeadsPerThread); else GBE_ROPE_VEC(1, false, kHeadsPerThread);
-        }
-    } else {
-        if (a.layout == 0) {
-            if (cached) GBE_ROPE(rope_scalar, 0, true); else GBE_ROPE(rope_scalar, 0, false);
-        } else {
-            if (cached) GBE_ROPE(rope_scalar, 1, true); else GBE_ROPE(rope_scalar, 1, false);
-        }
+    // an operand with no threads takes the other's layout (one kernel fewer)
+    const int la = used[0] ? a.side[0].layout : a.side[1].layout;
+    const int lb = used[1] ? a.side[1].layout : la;
+    if (cache != nullptr) {  // one table: both operands share r, frequencies and layout
+        if (la == 0) return launch_shape<DT, 0, 0, true>(vec, one_head, grid, op, a, cache, st);
+        return launch_shape<DT, 1, 1, true>(vec, one_head, grid, op, a, cache, st);
     }
-#undef GBE_ROPE
-#undef GBE_ROPE_VEC
+    if (la == 0) {
+        if (lb == 0) return launch_shape<DT, 0, 0, false>(vec, one_head, grid, op, a, cache, st);
+        return launch_shape<DT, 0, 1, false>(vec, one_head, grid, op, a, cache, st);
+    }
+    if (lb == 0) return launch_shape<DT, 1, 0, false>(vec, one_head, grid, op, a, cache, st);
+    return launch_shape<DT, 1, 1, false>(vec, one_head, grid, op, a, cache, st);
 }
 
 }  // namespace

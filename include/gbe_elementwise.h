@@ -167,6 +167,39 @@ int gbe_rope_qk(const void *q, void *q_out, int64_t q_stride, int64_t Hq, const 
                 const float *inv_freq, const float *cos_sin, int64_t cache_len, float mu, int layout, int dtype,
                 gbe_stream stream);
 
+/* One operand of gbe_rope_pair. */
+typedef struct gbe_rope_operand {
+    const void *x;          /* [T, H, D], consecutive tokens `stride` elements apart */
+    void *y;                /* the same shape and stride; y == x: in place */
+    int64_t stride;         /* elements from one token to the next, >= H * D */
+    int64_t H;              /* heads; 0: the operand is absent */
+    int64_t r;              /* rotated width: even, 0 <= r <= D */
+    const float *inv_freq;  /* device f32[r / 2] */
+    float mu;               /* scale of the rotated pairs, finite (1 unless YaRN) */
+    int layout;             /* 0: half, 1: interleaved */
+} gbe_rope_operand;
+
+/*
+ * gbe_rope_pair -- RoPE of two operands in one launch, each with its own
+ * rotated width, frequencies, scale and layout.
+ *   The rotation of gbe_rope ("Elementwise kernels in C", sections 2.2 and
+ *   4: partial rotary width r, the attention scale mu, the half and the
+ *   interleaved pairing; "Operations", section 3), applied to two operands
+ *   that share only the positions, T, head_dim D and dtype -- for instance
+ *   a query with interleaved pairs over r = 64 and a key with half pairs
+ *   over r = 128 and mu = 1.2.  Each operand's result equals gbe_rope of it
+ *   alone, bit for bit; one launch pays the fixed cost of a kernel once.
+ * a : HOST pointer to the first operand's description (read during the
+ *     call); b : likewise, or NULL for a single operand.
+ * pos : device int32[T], 0 <= pos < 2^24.  T, D, dtype, stream : as for
+ *     gbe_rope.
+ * Alias: an operand's y == x allowed; the operands may interleave in one
+ * buffer (rows sharing no byte), as for gbe_rope_qk.
+ * Errors: as for gbe_rope_qk, per operand; a == NULL is GBE_ERR_NULL.
+ */
+int gbe_rope_pair(const gbe_rope_operand *a, const gbe_rope_operand *b, const int32_t *pos, int64_t T, int64_t D,
+                  int dtype, gbe_stream stream);
+
 /*
  * gbe_qk_norm_rope -- QK-norm, then RoPE, of q and k in one pass.
  *   "Operations", section 5 (QK-norm): each head of q and of k is

@@ -210,3 +210,32 @@ def test_contiguous_overlap_rules_before_driver(L):
     assert L.gbe_rmsnorm(a, b - 64 * es, b - 1024 * es, 4, 256, 1e-5, 0, S) == 8  # y == x, but y holds w
     assert L.gbe_embedding(a, POS, a + (1 << 20), 4, 64, 100, NULL, 0, S) in PASSES_OVERLAP_CHECKS
     assert L.gbe_embedding(a, POS, a + 64 * es, 4, 64, 100, NULL, 0, S) == 8  # out inside the table
+
+
+def test_rope_pair_rejects_bad_operands(L):
+    """gbe_rope_pair checks each operand as gbe_rope_qk does; none of these
+    calls reaches the driver (fake addresses, refused by the argument or the
+    overlap checks)."""
+    import ctypes
+
+    from elementwise_row_rmsnorm_gb300.binding import RopeOperand
+
+    def op(**kw):
+        d = dict(x=BASE, y=BASE, stride=64, H=2, r=32, inv_freq=FREQ, mu=1.0, layout=0)
+        d.update(kw)
+        return RopeOperand(**d)
+
+    def call(a, b, T=4, D=32, dtype=0):
+        ref = lambda o: ctypes.cast(ctypes.byref(o), ctypes.c_void_p) if o is not None else None
+        return L.gbe_rope_pair(ref(a), ref(b), POS, T, D, dtype, S)
+    assert call(None, op()) == 1
+    assert call(op(), op(layout=3)) == 4 and call(op(layout=-1), None) == 4
+    assert call(op(), op(r=31)) == 6 and call(op(r=34), None) == 6 and call(op(), op(mu=float("inf"))) == 6
+    assert call(op(), op(stride=63)) == 2 and call(op(H=-1), None) == 2
+    assert call(op(), None, dtype=7) == 3
+    assert call(op(), None, T=0) == 0 and call(op(H=0), op(H=0)) == 0
+    second = BASE + (1 << 20)
+    # two operands in place in separate buffers pass the overlap checks
+    assert call(op(), op(x=second, y=second)) in PASSES_OVERLAP_CHECKS
+    # the second operand writing over the first one's rows
+    assert call(op(), op(x=second, y=BASE + 8)) == 8
