@@ -188,9 +188,10 @@ def gbe_rope(x, y, pos, inv_freq, r: int, mu: float = 1.0, layout: int = 0, stre
 def _rows_view(t: torch.Tensor, D: int):
     """(T, H, token stride) of a [T, H, D] view whose heads and entries are
     contiguous but whose tokens may be strided (a slice of a QKV buffer)."""
-    if t.dim() != 3 or t.shape[2] != D or t.stride(2) != 1 or (t.shape[1] > 1 and t.stride(1) != D):
+    shape, st = t.shape, t.stride()  # one query each (the per-call host cost matters at decode sizes)
+    if len(shape) != 3 or shape[2] != D or st[2] != 1 or (shape[1] > 1 and st[1] != D):
         raise ValueError("rope_qk: operands are [T, H, D] views with contiguous heads")
-    return t.shape[0], t.shape[1], t.stride(0) if t.shape[0] > 1 else t.shape[1] * D
+    return shape[0], shape[1], st[0] if shape[0] > 1 else shape[1] * D
 
 
 def gbe_rope_qk(q, q_out, k, k_out, pos, inv_freq, r: int, mu: float = 1.0, layout: int = 0,
