@@ -441,7 +441,7 @@ int gbe_qk_norm_rope(const void* q, void* q_out, int64_t q_stride, int64_t Hq, c
     const int es = elem_size(dtype);
     if (!es) return GBE_ERR_DTYPE;
     if (layout != 0 && layout != 1) return GBE_ERR_LAYOUT;
-    if (T < 0 || D <= 0 || T > INT32_MAX || D > 32 * (16 / es)) return GBE_ERR_SHAPE;  // head_dim <= 32 chunks
+    if (T < 0 || D <= 0 || T > INT32_MAX || D > 64 * (16 / es)) return GBE_ERR_SHAPE;  // head_dim <= 64 chunks
     if (!std::isfinite(eps) || eps < 0.0f) return GBE_ERR_EPS;
     const int64_t Hs[2] = {Hq, Hk}, strides[2] = {q_stride, k_stride};
     for (int j = 0; j < 2; ++j) {

@@ -26,8 +26,8 @@
 // angles are formed once into shared memory.  Unaligned rows take
 // qk_norm_rope_kernel: a warp per chunk of head rows that stages the
 // normalised rows in shared memory (so a lane can read the partner of each
-// of its entries).  Head width is limited to 32 chunks (head_dim <= 128 f32
-// / 256 bf16).
+// of its entries).  Head rows of 33 to 64 chunks (f32 head_dim up to 256,
+// bf16 up to 512) take qk_norm_rope_wide: a warp per row, two chunks a lane.
 #include <algorithm>
 
 #include "common.cuh"
@@ -606,6 +606,120 @@ qk_norm_rope_kernel(QkSide A, QkSide B, int nca, int ncb, float eps, const int32
     }
 }
 
+// Head rows of 33 to 64 chunks (f32 head_dim up to 256, bf16 up to 512):
+// one warp per head row, a lane holding chunks c and c + 32 -- the map and
+// the tree gbe_rmsnorm takes for such a row (32 threads, two slots each,
+// summed slot by slot in element order, then the warp butterfly), so the
+// result equals gbe_rmsnorm then gbe_rope_qk bit for bit as on the other
+// paths.  The normalised row is staged in shared memory for the pair
+// partners; each entry's angle is formed (or read from the table) by the
+// lane that writes it.
+constexpr int kWideSlots = 2;
+constexpr int kMaxWideRow = 32 * kWideSlots * 8;  // floats: 64 chunks of <= 8 entries
+
+template <int DT, int LAYOUT, bool VEC, bool CACHE>
+__global__ void __launch_bounds__(kWarps * 32)
+qk_norm_rope_wide(QkSide A, QkSide B, int nha, int nhb, float eps, const int32_t* pos, int64_t T, int D, int r,
+                  const float* inv_freq, const float2* cache, int64_t cache_len, float mu) {
+    using S = Store<DT>;
+    constexpr int V = S::V;
+    constexpr int64_t ES = sizeof(typename S::T);
+    __shared__ float stage[kWarps][kMaxWideRow];
+    pdl_begin();
+    const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t item = (int64_t)blockIdx.x * kWarps + wib;  // (token, head row of q or k)
+    const int per_tok = nha + nhb;
+    const int64_t t = item / per_tok;
+    if (t >= T) return;  // whole warps leave together: no CTA barrier follows
+    const int hi = (int)(item - t * per_tok);
+    const bool second = hi >= nha;
+    const QkSide Q = second ? B : A;
+    const int h = second ? hi - nha : hi;
+    const int nchunks = (D + V - 1) / V;
+    const int half = r >> 1;
+    const char* xr = Q.x + (t * Q.xs + (int64_t)h * D) * ES;
+    char* yr = Q.y + (t * Q.ys + (int64_t)h * D) * ES;
+    float f[kWideSlots][V], gv[kWideSlots][V];
+#pragma unroll
+    for (int q = 0; q < kWideSlots; ++q) {
+        const int c = lane + 32 * q;
+#pragma unroll
+        for (int e = 0; e < V; ++e) f[q][e] = gv[q][e] = 0.0f;
+        if (c < nchunks) {
+            load_chunk<DT, VEC>(xr, c, D, f[q]);
+            if (VEC)
+                S::unpack(ld_reuse(Q.g + (int64_t)c * 16), gv[q]);
+            else
+#pragma unroll
+                for (int e = 0; e < V; ++e) gv[q][e] = c * V + e < D ? S::load1(Q.g, (int64_t)c * V + e) : 0.0f;
+        }
+    }
+    // the row's sum of squares: slot by slot, element order, then the butterfly
+    float s = 0.0f;
+#pragma unroll
+    for (int q = 0; q < kWideSlots; ++q)
+        if (lane + 32 * q < nchunks)
+#pragma unroll
+            for (int e = 0; e < V; ++e) s = __fmaf_rn(f[q][e], f[q][e], s);
+    s = warp_sum(s);
+    const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(s, (float)D), eps)));
+    // normalised, rounded to the storage type, staged for the partners
+    float* row = stage[wib];
+#pragma unroll
+    for (int q = 0; q < kWideSlots; ++q) {
+        const int c = lane + 32 * q;
+        if (c < nchunks)
+#pragma unroll
+            for (int e = 0; e < V; ++e) {
+                f[q][e] = S::round(__fmul_rn(__fmul_rn(f[q][e], inv), gv[q][e]));
+                if (c * V + e < D) row[c * V + e] = f[q][e];
+            }
+    }
+    __syncwarp();
+    const int32_t p = pos[t];
+#pragma unroll
+    for (int q = 0; q < kWideSlots; ++q) {
+        const int c = lane + 32 * q;
+        if (c >= nchunks) continue;
+        float o[V];
+#pragma unroll
+        for (int e = 0; e < V; ++e) {
+            const int j = c * V + e;
+            const float n = f[q][e];
+            o[e] = n;
+            if (j < r) {
+                const int i = LAYOUT == 0 ? (j < half ? j : j - half) : (j >> 1);
+                float ca, sa;
+                if (CACHE && p >= 0 && p < cache_len) {
+                    const float2 v = __ldg(cache + (int64_t)p * half + i);
+                    ca = v.x;
+                    sa = v.y;
+                } else {
+                    rope_sincos(__fmul_rn((float)p, __ldg(inv_freq + i)), &sa, &ca);
+                }
+                float a, b;
+                bool first;
+                if (LAYOUT == 0) {
+                    first = j < half;
+                    a = first ? n : row[j - half];
+                    b = first ? row[j + half] : n;
+                } else {
+                    first = (j & 1) == 0;
+                    a = first ? n : row[j - 1];
+                    b = first ? row[j + 1] : n;
+                }
+                o[e] = first ? __fmul_rn(mu, __fsub_rn(__fmul_rn(a, ca), __fmul_rn(b, sa)))
+                             : __fmul_rn(mu, __fadd_rn(__fmul_rn(a, sa), __fmul_rn(b, ca)));
+            }
+        }
+        if (VEC) {
+            st_stream(yr + (int64_t)c * 16, S::pack(o));
+        } else {
+            for (int e = 0; e < V && c * V + e < D; ++e) S::store1(yr, (int64_t)c * V + e, o[e]);
+        }
+    }
+}
+
 template <int DT>
 cudaError_t launch_dt(const QkNormRopeArgs& a, bool vec, cudaStream_t st) {
     constexpr int V = Store<DT>::V;
@@ -621,6 +735,22 @@ cudaError_t launch_dt(const QkNormRopeArgs& a, bool vec, cudaStream_t st) {
         sd[k].xs = a.side[k].stride;
         sd[k].ys = a.side[k].stride;
         sd[k].H = (int)a.side[k].H;
+    }
+    if (nchunks > 32) {  // head rows of 33 to 64 chunks: a warp per row, two chunks a lane
+        const int64_t rows_all = a.T * (a.side[0].H + a.side[1].H);
+        const unsigned grid = (unsigned)((rows_all + kWarps - 1) / kWarps);
+        const float2* cache = reinterpret_cast<const float2*>(a.cos_sin);
+        const int nha = (int)a.side[0].H, nhb = (int)a.side[1].H, Di = (int)a.D, ri = (int)a.r;
+#define GBE_QKW(L, VV, C)                                                                                      \
+    return launch(qk_norm_rope_wide<DT, L, VV, C>, dim3(grid), dim3(kWarps * 32), 0, st, sd[0], sd[1], nha, nhb, \
+                  a.eps, a.pos, a.T, Di, ri, a.inv_freq, cache, a.cache_len, a.mu)
+        if (a.layout == 0) {
+            if (vec) { if (cache) GBE_QKW(0, true, true); else GBE_QKW(0, true, false); }
+            if (cache) GBE_QKW(0, false, true); else GBE_QKW(0, false, false);
+        }
+        if (vec) { if (cache) GBE_QKW(1, true, true); else GBE_QKW(1, true, false); }
+        if (cache) GBE_QKW(1, false, true); else GBE_QKW(1, false, false);
+#undef GBE_QKW
     }
     int lgL = 0;
     while ((2 << lgL) < nchunks) ++lgL;

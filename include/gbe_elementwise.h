@@ -212,7 +212,7 @@ int gbe_rope_pair(const gbe_rope_operand *a, const gbe_rope_operand *b, const in
  * cos_sin, cache_len, mu, layout, dtype : as for gbe_rope_qk.
  * gq, gk : device gains of D entries in dtype (ignored when Hq / Hk is 0).
  * eps    : finite and >= 0.
- * D      : at most 32 16-byte chunks (128 f32 or 256 bf16), else GBE_ERR_SHAPE.
+ * D      : at most 64 16-byte chunks (256 f32 or 512 bf16), else GBE_ERR_SHAPE.
  * Alias: q_out == q and k_out == k allowed.
  */
 int gbe_qk_norm_rope(const void *q, void *q_out, int64_t q_stride, int64_t Hq, const void *gq, const void *k,

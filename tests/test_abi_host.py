@@ -122,8 +122,8 @@ def test_qk_norm_rope_rejects_bad_arguments(L):
                                   NULL, 0, mu, layout, dtype, S)
     assert call(layout=2) == 4 and call(dtype=5) == 3
     assert call(eps=-1.0) == 5 and call(eps=float("inf")) == 5
-    assert call(D=264) == 2                 # bf16 head rows of more than 32 chunks
-    assert call(D=256, dtype=0, qs=2048, ks=512, r=256) == 2   # f32: 64 chunks
+    assert call(D=520, qs=8 * 520, ks=2 * 520, r=520) == 2     # bf16 head rows of more than 64 chunks
+    assert call(D=264, dtype=0, qs=8 * 264, ks=2 * 264, r=264) == 2   # f32: 66 chunks
     assert call(r=130) == 6 and call(r=7) == 6
     assert call(qs=1000) == 2
     assert call(T=0) == 0 and call(hq=0, hk=0) == 0

@@ -42,13 +42,18 @@ def _unfused(q, k, gq, gk, pos, om, r, mu, layout, eps=1e-6):
                                          (4, 2, 2, 8, 8), (17, 16, 4, 96, 64),
                                          # more chunks of head rows than warps of a token's CTA
                                          (3, 160, 9, 128, 128),
-                                         # the widest head (256 bf16 / 128 f32 is the limit)
-                                         (2, 4, 2, 256, 256), (3, 5, 3, 128, 96)])
+                                         # wide heads: up to 64 chunks (256 f32 / 512 bf16)
+                                         (2, 4, 2, 256, 256), (3, 5, 3, 128, 96), (3, 3, 2, 200, 160),
+                                         (2, 2, 1, 512, 512), (2, 3, 2, 384, 320)])
 @pytest.mark.parametrize("mu", [1.0, 1.1])
 def test_equals_unfused_composition(dtype, layout, T, Hq, Hk, D, r, mu):
-    if dtype == "f32" and D > 128:
-        pytest.skip("head_dim is limited to 32 chunks: 128 f32 entries")
     q, k, gq, gk, pos, om = _case(1, T, Hq, Hk, D, r, dtype)
+    if dtype == "f32" and D > 256:  # past 64 chunks: refused before anything runs
+        qd = to_dev(q)
+        with pytest.raises(gbe.GbeError) as e:
+            gbe.gbe_qk_norm_rope(qd, qd, to_dev(gq), None, None, None, 1e-6, to_dev(pos), to_dev(om), r, mu, layout)
+        assert e.value.status == 2
+        return
     qn, kn = _unfused(q, k, gq, gk, pos, om, r, mu, layout)
     qd, kd = to_dev(q), to_dev(k)
     gbe.gbe_qk_norm_rope(qd, qd, to_dev(gq), kd, kd, to_dev(gk), 1e-6, to_dev(pos), to_dev(om), r, mu, layout)
@@ -70,6 +75,40 @@ def test_against_oracle(dtype, layout):
         want = o.qk_norm_rope(xw, gw, 1e-6, pos, om, r, 1.0, layout, n_bf16=(dtype == "bf16"))
         n = o.rmsnorm(xw.reshape(-1, D), gw, 1e-6).reshape(xw.shape)
         assert_rope_close(to_f32(y), want, n, r, 1.0, layout, dtype, what)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("layout", [0, 1])
+def test_wide_heads_against_oracle_slices_and_cache(dtype, layout):
+    """Head rows of 33 to 64 chunks (f32 head_dim 256, bf16 512): against the
+    oracle; on QKV slices with a token stride off the 16-byte grid (the
+    scalar path) and with the cos/sin table, equal to the composition."""
+    D = 256 if dtype == "f32" else 512
+    T, Hq, Hk, r = 6, 4, 2, D
+    q, k, gq, gk, pos, om = _case(4, T, Hq, Hk, D, r, dtype)
+    qd, kd = to_dev(q), to_dev(k)
+    qo, ko = torch.empty_like(qd), torch.empty_like(kd)
+    gbe.gbe_qk_norm_rope(qd, qo, to_dev(gq), kd, ko, to_dev(gk), 1e-6, to_dev(pos), to_dev(om), r, 1.0, layout)
+    o = oracle.get()
+    for x, g, y, what in ((q, gq, qo, "q"), (k, gk, ko, "k")):
+        xw, gw = widen(x), widen(g)
+        want = o.qk_norm_rope(xw, gw, 1e-6, pos, om, r, 1.0, layout, n_bf16=(dtype == "bf16"))
+        n = o.rmsnorm(xw.reshape(-1, D), gw, 1e-6).reshape(xw.shape)
+        assert_rope_close(to_f32(y), want, n, r, 1.0, layout, dtype, what)
+    qn, kn = _unfused(q, k, gq, gk, pos, om, r, 1.0, layout)
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    for extra in (0, 1):
+        stride = (Hq + Hk) * D + extra
+        buf = torch.zeros(T * stride, dtype=tdt, device="cuda")
+        buf.view(T, stride)[:, :Hq * D] = to_dev(q).view(T, Hq * D)
+        buf.view(T, stride)[:, Hq * D:(Hq + Hk) * D] = to_dev(k).view(T, Hk * D)
+        qv = buf.as_strided((T, Hq, D), (stride, D, 1))
+        kv = buf.as_strided((T, Hk, D), (stride, D, 1), Hq * D)
+        cache = gbe.rope_cos_sin(to_dev(om), r, 1 << 15) if extra == 0 else None
+        gbe.gbe_qk_norm_rope(qv, qv, to_dev(gq), kv, kv, to_dev(gk), 1e-6, to_dev(pos), to_dev(om), r, 1.0, layout,
+                             cos_sin=cache)
+        assert np.array_equal(bits(qv.contiguous()), bits(qn)), extra
+        assert np.array_equal(bits(kv.contiguous()), bits(kn)), extra
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -106,4 +145,4 @@ def test_head_dim_limit():
     om = torch.ones(256, device="cuda")
     st = L.gbe_qk_norm_rope(x.data_ptr(), x.data_ptr(), 4 * 512, 4, g.data_ptr(), None, None, 0, 0, None, 1e-6,
                             pos.data_ptr(), 2, 512, 512, om.data_ptr(), None, 0, 1.0, 0, 0, s)
-    assert st == 2  # 512 f32 entries = 128 chunks > 32
+    assert st == 2  # 512 f32 entries = 128 chunks > 64
