@@ -191,13 +191,7 @@ qk_norm_rope_tok(QkSide A, QkSide B, int nca, int ncb, float eps, const int32_t*
         // sums of squares of the four rows this lane holds a chunk of
         float s[NP];
 #pragma unroll
-        for (int k = 0; k < NP; ++k) {
-            float f[V];
-            S::unpack(raw[k], f);  // zero for absent rows and chunks
-            s[k] = 0.0f;
-#pragma unroll
-            for (int e = 0; e < V; ++e) s[k] = __fmaf_rn(f[e], f[e], s[k]);
-        }
+        for (int k = 0; k < NP; ++k) s[k] = vec_sq_acc<DT>(raw[k], 0.0f);  // zero for absent rows and chunks
         float inv[NP];
         if (W >= 4) {
             const int m1 = W >> 1, m2 = W >> 2;
@@ -411,13 +405,7 @@ qk_norm_rope_pair(QkSide A, QkSide B, int nca, int ncb, float eps, const int32_t
 #pragma unroll
         for (int k = 0; k < NP; ++k) {
             float f[V];
-            float s0 = 0.0f, s1 = 0.0f;
-            S::unpack(raw[k][0], f);
-#pragma unroll
-            for (int e = 0; e < V; ++e) s0 = __fmaf_rn(f[e], f[e], s0);
-            S::unpack(raw[k][1], f);
-#pragma unroll
-            for (int e = 0; e < V; ++e) s1 = __fmaf_rn(f[e], f[e], s1);
+            const float s0 = vec_sq_acc<DT>(raw[k][0], 0.0f), s1 = vec_sq_acc<DT>(raw[k][1], 0.0f);
             s[k] = __fadd_rn(s0, s1);
         }
         float inv[NP];

@@ -107,19 +107,16 @@ rmsnorm_rows(const void* x, const void* res, const void* w, void* y, void* h, in
     for (int k = 0; k < K; ++k) {
         const int c = k * tpr + t;
         if (c < nchunks) {
-            float f[V];
-            S::unpack(rx[k], f);
             if (ADD) {
-                float g[V];
+                float f[V], g[V];
+                S::unpack(rx[k], f);
                 S::unpack(rr[k], g);
 #pragma unroll
                 for (int e = 0; e < V; ++e) f[e] = __fadd_rn(f[e], g[e]);
                 rx[k] = S::pack(f);
                 st_stream(static_cast<char*>(h) + boff + (int64_t)c * 16, rx[k]);
-                S::unpack(rx[k], f);
             }
-#pragma unroll
-            for (int e = 0; e < V; ++e) s = __fmaf_rn(f[e], f[e], s);
+            s = vec_sq_acc<DT>(rx[k], s);  // the stored values' squares, element order
         }
     }
     // 3) the row's sum, fixed order
