@@ -332,18 +332,27 @@ __device__ __forceinline__ void rotate_store(const float (&a)[Store<DT>::V], con
 // item, whose sums share the butterfly transposed (at distance L/2 a lane
 // keeps one pass and hands the other to its partner).  One CTA per token,
 // the token's angles formed once into shared memory, as in qk_norm_rope_tok.
-template <int DT, bool CACHE>
+//
+// D = 2 L V is a power of two here, so the mean of squares s / D is taken as
+// s * 2^-log2(D): both are the correctly rounded value of the same real
+// number, so the bits are those of gbe_rmsnorm's division.  LGL >= 0 fixes
+// log2(L) at compile time (the common head sizes); -1 reads it from lgL_arg.
+template <int DT, bool CACHE, int LGL>
 __global__ void __launch_bounds__(kTokWarps * 32, 2)
-qk_norm_rope_pair(QkSide A, QkSide B, int nca, int ncb, float eps, const int32_t* pos, int D, int lgL,
+qk_norm_rope_pair(QkSide A, QkSide B, int nca, int ncb, float eps, const int32_t* pos, int lgL_arg,
                   const float* inv_freq, const float2* cache, int64_t cache_len, float mu) {
     using S = Store<DT>;
     constexpr int V = S::V;
+    constexpr int LGV = V == 8 ? 3 : 2;
     constexpr int64_t ES = sizeof(typename S::T);
     constexpr int NP = 2;
     constexpr int QPL = V >= 8 ? 2 : 1;  // 16-byte quads of one lane's angles
     __shared__ __align__(16) float cs_cos[kMaxHalf];
     __shared__ __align__(16) float cs_sin[kMaxHalf];
     pdl_begin();
+    const int lgL = LGL >= 0 ? LGL : lgL_arg;
+    const int D = V << (lgL + 1);
+    const float rD = __int_as_float((127 - (LGV + 1 + lgL)) << 23);  // 1 / D, exact
     const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nw = blockDim.x >> 5;
     const int64_t t = blockIdx.x;
@@ -415,15 +424,16 @@ qk_norm_rope_pair(QkSide A, QkSide B, int nca, int ncb, float eps, const int32_t
             float kk = b1 ? s[1] : s[0];
             const float gg = b1 ? s[0] : s[1];
             kk = __fadd_rn(kk, __shfl_xor_sync(0xFFFFFFFFu, gg, m1));
+#pragma unroll
             for (int m = L >> 2; m >= 1; m >>= 1) kk = __fadd_rn(kk, __shfl_xor_sync(0xFFFFFFFFu, kk, m));
-            const float own = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(kk, (float)D), eps)));
+            const float own = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fmul_rn(kk, rD), eps)));
             const int base = sub << lgL;
             inv[0] = __shfl_sync(0xFFFFFFFFu, own, base);
             inv[1] = __shfl_sync(0xFFFFFFFFu, own, base + m1);
         } else {
 #pragma unroll
             for (int k = 0; k < NP; ++k)
-                inv[k] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(s[k], (float)D), eps)));
+                inv[k] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fmul_rn(s[k], rD), eps)));
         }
         // the angles are in once every thread has passed here; each warp's
         // first item comes through (there are no more warps than items), so
@@ -749,11 +759,20 @@ cudaError_t launch_dt(const QkNormRopeArgs& a, bool vec, cudaStream_t st) {
         const int pb = (int)((a.side[1].H + rows_item - 1) / rows_item);
         const int warps = (int)std::min<int64_t>(pa + pb, kTokWarps);
         const float2* cs = reinterpret_cast<const float2*>(a.cos_sin);
-        if (cs != nullptr)
-            return launch(qk_norm_rope_pair<DT, true>, dim3((unsigned)a.T), dim3(warps * 32), 0, st, sd[0], sd[1], pa,
-                          pb, a.eps, a.pos, (int)a.D, lgL, a.inv_freq, cs, a.cache_len, a.mu);
-        return launch(qk_norm_rope_pair<DT, false>, dim3((unsigned)a.T), dim3(warps * 32), 0, st, sd[0], sd[1], pa, pb,
-                      a.eps, a.pos, (int)a.D, lgL, a.inv_freq, cs, a.cache_len, a.mu);
+#define GBE_QKP(C, G)                                                                                              \
+    return launch(qk_norm_rope_pair<DT, C, G>, dim3((unsigned)a.T), dim3(warps * 32), 0, st, sd[0], sd[1], pa, pb, \
+                  a.eps, a.pos, lgL, a.inv_freq, cs, a.cache_len, a.mu)
+#define GBE_QKP_L(C)                      \
+    switch (lgL) {                        \
+        case 2: GBE_QKP(C, 2);            \
+        case 3: GBE_QKP(C, 3);            \
+        case 4: GBE_QKP(C, 4);            \
+        default: GBE_QKP(C, -1);          \
+    }
+        if (cs != nullptr) GBE_QKP_L(true)
+        GBE_QKP_L(false)
+#undef GBE_QKP_L
+#undef GBE_QKP
     }
     const bool shfl = vec && a.r > 0 && (a.layout == 0 ? (a.r / 2) % V == 0 : a.r % V == 0);
     const int rows_per_item = (32 / W) * (shfl ? kPassesShfl : kPasses);  // head rows one warp handles

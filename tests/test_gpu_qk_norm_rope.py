@@ -146,3 +146,29 @@ def test_head_dim_limit():
     st = L.gbe_qk_norm_rope(x.data_ptr(), x.data_ptr(), 4 * 512, 4, g.data_ptr(), None, None, 0, 0, None, 1e-6,
                             pos.data_ptr(), 2, 512, 512, om.data_ptr(), None, 0, 1.0, 0, 0, s)
     assert st == 2  # 512 f32 entries = 128 chunks > 64
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("Hq,Hk,D,mu,cached,extra", [(32, 8, 128, 1.0, False, 0), (12, 3, 64, 1.1, True, 0),
+                                                     (8, 2, 128, 1.0, True, 8)])
+def test_many_tokens_equal_unfused_composition(dtype, Hq, Hk, D, mu, cached, extra):
+    """Many tokens (20011) in the half-layout, whole-head case: equal bit for
+    bit to the composition, with ragged head counts, mu != 1, the cos/sin
+    table and q, k as slices of one buffer (a token stride past the heads)."""
+    T, r = 20011, D
+    q, k, gq, gk, pos, om = _case(5, T, Hq, Hk, D, r, dtype)
+    qn, kn = _unfused(q, k, gq, gk, pos, om, r, mu, 0)
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    stride = (Hq + Hk) * D + extra
+    buf = torch.full((T * stride,), 7.0, dtype=tdt, device="cuda")
+    rows = buf.view(T, stride)
+    rows[:, :Hq * D] = to_dev(q).view(T, Hq * D)
+    rows[:, Hq * D:(Hq + Hk) * D] = to_dev(k).view(T, Hk * D)
+    qv = buf.as_strided((T, Hq, D), (stride, D, 1))
+    kv = buf.as_strided((T, Hk, D), (stride, D, 1), Hq * D)
+    cache = gbe.rope_cos_sin(to_dev(om), r, 1 << 15) if cached else None  # some positions past it
+    gbe.gbe_qk_norm_rope(qv, qv, to_dev(gq), kv, kv, to_dev(gk), 1e-6, to_dev(pos), to_dev(om), r, mu, 0,
+                         cos_sin=cache)
+    assert np.array_equal(bits(qv.contiguous()), bits(qn)), "q"
+    assert np.array_equal(bits(kv.contiguous()), bits(kn)), "k"
+    assert torch.all(rows[:, (Hq + Hk) * D:] == 7.0), "past the heads untouched"
