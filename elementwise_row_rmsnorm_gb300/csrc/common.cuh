@@ -261,8 +261,12 @@ struct Store<kBF16> {
     __device__ __forceinline__ static void store1(void* base, int64_t i, float f) {
         static_cast<uint16_t*>(base)[i] = (uint16_t)f32_to_bf16_bits(f);
     }
+    // one conversion: packing f with a zero low half leaves exactly the f32
+    // bits of bf16(f) (the same rounding as f32_to_bf16_bits)
     __device__ __forceinline__ static float round(float f) {
-        return bf16_bits_to_f32(f32_to_bf16_bits(f));
+        uint32_t d;
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(f), "f"(0.0f));
+        return __uint_as_float(d);
     }
 };
 

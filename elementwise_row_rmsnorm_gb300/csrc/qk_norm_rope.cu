@@ -364,21 +364,20 @@ qk_norm_rope_pair(QkSide A, QkSide B, int nca, int ncb, float eps, const int32_t
     const int half = D >> 1;  // L * V
     const int32_t p = pos[t];
 
+    constexpr int64_t kPassBytes = 64 * V * ES;  // RP * D entries: the rows of one pass
     int ci = wib;
     Vec16 raw[NP][2];
     auto load_item = [&](int item) {
         const bool second = item >= nca;
-        const QkSide& Q = second ? B : A;
-        const int h0 = (second ? item - nca : item) * RP * NP;
-        const char* xt = Q.x + t * Q.xs * ES + (int64_t)c * 16;
+        const int H = second ? B.H : A.H;
+        const int h = (second ? item - nca : item) * RP * NP + sub;
+        const char* row = (second ? B.x : A.x) + (t * (second ? B.xs : A.xs) + (int64_t)h * D) * ES + c * 16;
 #pragma unroll
         for (int k = 0; k < NP; ++k) {
-            const int h = h0 + k * RP + sub;
             raw[k][0] = raw[k][1] = Vec16{{0u, 0u, 0u, 0u}};
-            if (h < Q.H) {
-                const char* row = xt + (int64_t)h * D * ES;
-                raw[k][0] = ld_stream(row);
-                raw[k][1] = ld_stream(row + half * ES);
+            if (h + k * RP < H) {
+                raw[k][0] = ld_stream(row + k * kPassBytes);
+                raw[k][1] = ld_stream(row + k * kPassBytes + half * ES);
             }
         }
     };
@@ -403,17 +402,16 @@ qk_norm_rope_pair(QkSide A, QkSide B, int nca, int ncb, float eps, const int32_t
     for (; ci < per_tok; ci += nw) {
         if (ci != wib) load_item(ci);
         const bool second = ci >= nca;
-        const QkSide& Q = second ? B : A;
+        const int H = second ? B.H : A.H;
         const int h0 = (second ? ci - nca : ci) * RP * NP;
-        const Vec16 g_lo = ld_reuse(Q.g + (int64_t)c * 16);
-        const Vec16 g_hi = ld_reuse(Q.g + (int64_t)c * 16 + half * ES);
+        const char* gp = (second ? B.g : A.g) + c * 16;
+        char* const yrow = (second ? B.y : A.y) + (t * (second ? B.ys : A.ys) + (int64_t)(h0 + sub) * D) * ES + c * 16;
 
         // the sum of squares of each chunk in element order, then the
         // butterfly step of distance L inside the lane
         float s[NP];
 #pragma unroll
         for (int k = 0; k < NP; ++k) {
-            float f[V];
             const float s0 = vec_sq_acc<DT>(raw[k][0], 0.0f), s1 = vec_sq_acc<DT>(raw[k][1], 0.0f);
             s[k] = __fadd_rn(s0, s1);
         }
@@ -426,14 +424,14 @@ qk_norm_rope_pair(QkSide A, QkSide B, int nca, int ncb, float eps, const int32_t
             kk = __fadd_rn(kk, __shfl_xor_sync(0xFFFFFFFFu, gg, m1));
 #pragma unroll
             for (int m = L >> 2; m >= 1; m >>= 1) kk = __fadd_rn(kk, __shfl_xor_sync(0xFFFFFFFFu, kk, m));
-            const float own = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fmul_rn(kk, rD), eps)));
+            const float own = __frcp_rn(__fsqrt_rn(__fadd_rn(__fmul_rn(kk, rD), eps)));
             const int base = sub << lgL;
             inv[0] = __shfl_sync(0xFFFFFFFFu, own, base);
             inv[1] = __shfl_sync(0xFFFFFFFFu, own, base + m1);
         } else {
 #pragma unroll
             for (int k = 0; k < NP; ++k)
-                inv[k] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fmul_rn(s[k], rD), eps)));
+                inv[k] = __frcp_rn(__fsqrt_rn(__fadd_rn(__fmul_rn(s[k], rD), eps)));
         }
         // the angles are in once every thread has passed here; each warp's
         // first item comes through (there are no more warps than items), so
@@ -442,31 +440,28 @@ qk_norm_rope_pair(QkSide A, QkSide B, int nca, int ncb, float eps, const int32_t
 
 #pragma unroll
         for (int k = 0; k < NP; ++k) {
-            if (h0 + k * RP >= Q.H) break;  // uniform across the warp
-            const int h = h0 + k * RP + sub;
+            if (h0 + k * RP >= H) break;  // uniform across the warp
             float a[V], b[V], g[V];
             // normalised and rounded to storage, as a stored intermediate would be
             const float2 iv = make_float2(inv[k], inv[k]);
             S::unpack(raw[k][0], a);
-            S::unpack(g_lo, g);
+            S::unpack(ld_reuse(gp), g);
 #pragma unroll
             for (int e = 0; e < V; e += 2) {
                 const float2 u = mul2_rn(mul2_rn(make_float2(a[e], a[e + 1]), iv), make_float2(g[e], g[e + 1]));
-                a[e] = u.x;
-                a[e + 1] = u.y;
+                a[e] = S::round(u.x);
+                a[e + 1] = S::round(u.y);
             }
-            S::unpack(S::pack(a), a);
             S::unpack(raw[k][1], b);
-            S::unpack(g_hi, g);
+            S::unpack(ld_reuse(gp + half * ES), g);
 #pragma unroll
             for (int e = 0; e < V; e += 2) {
                 const float2 u = mul2_rn(mul2_rn(make_float2(b[e], b[e + 1]), iv), make_float2(g[e], g[e + 1]));
-                b[e] = u.x;
-                b[e + 1] = u.y;
+                b[e] = S::round(u.x);
+                b[e + 1] = S::round(u.y);
             }
-            S::unpack(S::pack(b), b);
-            if (h < Q.H) {
-                char* row = Q.y + (t * Q.ys + (int64_t)h * D) * ES + (int64_t)c * 16;
+            if (h0 + k * RP + sub < H) {
+                char* row = yrow + k * kPassBytes;
                 if (mu_one)
                     rotate_store<DT, false>(a, b, cs_cos + slot0, cs_sin + slot0, half >> 1, mu, row, row + half * ES);
                 else
