@@ -62,6 +62,17 @@ __device__ __forceinline__ void load_chunk(const char* row, int c, int D, float 
     }
 }
 
+// A load kept in L1 for a second read by the same warp (ld.global.ca: a
+// coherent load, so rows written in place by this kernel are never read
+// stale -- each address is read twice and then written once, by one warp).
+__device__ __forceinline__ Vec16 ld_twice(const void* p) {
+    Vec16 v;
+    asm volatile("ld.global.ca.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
+                 : "l"(p));
+    return v;
+}
+
 // Aligned rows whose pair partners lie a whole number of chunks apart (the
 // half layout with r/2 a multiple of the vector, or the interleaved layout
 // with r a multiple of it).  One CTA per token, one warp per chunk of R * 4
@@ -328,16 +339,27 @@ __device__ __forceinline__ void rotate_store(const float (&a)[Store<DT>::V], con
 // lanes.  gbe_rmsnorm's tree for such a row first adds the sums of chunks c
 // and c + L (its butterfly step of distance L, chunk c's sum first): here
 // that step is an addition inside the lane, and the remaining steps run
-// over the L lanes of the row.  Rows: 32 / L per pass, two passes per warp
-// item, whose sums share the butterfly transposed (at distance L/2 a lane
-// keeps one pass and hands the other to its partner).  One CTA per token,
-// the token's angles formed once into shared memory, as in qk_norm_rope_tok.
+// over the L lanes of the row.  Rows: 32 / L per pass, NP passes per warp
+// item, whose sums share the butterfly transposed (NP = 2: at distance L/2
+// a lane keeps one pass and hands the other to its partner; NP = 4, L >= 4:
+// at L/2 it keeps two of four, at L/4 one, as in qk_norm_rope_tok), so one
+// reciprocal root per lane serves NP rows.  One CTA per token, the token's
+// angles formed once into shared memory, as in qk_norm_rope_tok.
+//
+// NP = 4 (the compile-time row sizes) halves the per-item work of the two-pass
+// form (addresses, the root, the butterfly): 1987 warp instructions per
+// token against 2325 at [8192, 32+8, 128] bf16.  Four passes of rows do not
+// fit beside the angle code in the 64 registers a thread has here (bounds
+// of two 512-thread CTAs an SM: more registers cost more in occupancy than
+// they save), so these loads go out after the angles are formed, kept in L1
+// (ld_twice), and each pass reads its rows again from L1 for the
+// normalisation instead of holding them from the sums.
 //
 // D = 2 L V is a power of two here, so the mean of squares s / D is taken as
 // s * 2^-log2(D): both are the correctly rounded value of the same real
 // number, so the bits are those of gbe_rmsnorm's division.  LGL >= 0 fixes
 // log2(L) at compile time (the common head sizes); -1 reads it from lgL_arg.
-template <int DT, bool CACHE, int LGL>
+template <int DT, bool CACHE, int LGL, int NP>
 __global__ void __launch_bounds__(kTokWarps * 32, 2)
 qk_norm_rope_pair(QkSide A, QkSide B, int nca, int ncb, float eps, const int32_t* pos, int lgL_arg,
                   const float* inv_freq, const float2* cache, int64_t cache_len, float mu) {
@@ -345,7 +367,6 @@ qk_norm_rope_pair(QkSide A, QkSide B, int nca, int ncb, float eps, const int32_t
     constexpr int V = S::V;
     constexpr int LGV = V == 8 ? 3 : 2;
     constexpr int64_t ES = sizeof(typename S::T);
-    constexpr int NP = 2;
     constexpr int QPL = V >= 8 ? 2 : 1;  // 16-byte quads of one lane's angles
     __shared__ __align__(16) float cs_cos[kMaxHalf];
     __shared__ __align__(16) float cs_sin[kMaxHalf];
@@ -365,6 +386,7 @@ qk_norm_rope_pair(QkSide A, QkSide B, int nca, int ncb, float eps, const int32_t
     const int32_t p = pos[t];
 
     constexpr int64_t kPassBytes = 64 * V * ES;  // RP * D entries: the rows of one pass
+    static_assert(NP == 2 || (NP == 4 && LGL >= 2), "four passes need four or more lanes per row");
     int ci = wib;
     Vec16 raw[NP][2];
     auto load_item = [&](int item) {
@@ -376,12 +398,17 @@ qk_norm_rope_pair(QkSide A, QkSide B, int nca, int ncb, float eps, const int32_t
         for (int k = 0; k < NP; ++k) {
             raw[k][0] = raw[k][1] = Vec16{{0u, 0u, 0u, 0u}};
             if (h + k * RP < H) {
-                raw[k][0] = ld_stream(row + k * kPassBytes);
-                raw[k][1] = ld_stream(row + k * kPassBytes + half * ES);
+                if (NP == 4) {
+                    raw[k][0] = ld_twice(row + k * kPassBytes);
+                    raw[k][1] = ld_twice(row + k * kPassBytes + half * ES);
+                } else {
+                    raw[k][0] = ld_stream(row + k * kPassBytes);
+                    raw[k][1] = ld_stream(row + k * kPassBytes + half * ES);
+                }
             }
         }
     };
-    if (ci < per_tok) load_item(ci);
+    if (NP == 2 && ci < per_tok) load_item(ci);  // four passes: after the angles
 
     for (int i = threadIdx.x; i < half; i += blockDim.x) {
         float cv, sv;
@@ -400,12 +427,13 @@ qk_norm_rope_pair(QkSide A, QkSide B, int nca, int ncb, float eps, const int32_t
     const bool mu_one = mu == 1.0f;
 
     for (; ci < per_tok; ci += nw) {
-        if (ci != wib) load_item(ci);
+        if (NP == 4 || ci != wib) load_item(ci);
         const bool second = ci >= nca;
         const int H = second ? B.H : A.H;
         const int h0 = (second ? ci - nca : ci) * RP * NP;
         const char* gp = (second ? B.g : A.g) + c * 16;
         char* const yrow = (second ? B.y : A.y) + (t * (second ? B.ys : A.ys) + (int64_t)(h0 + sub) * D) * ES + c * 16;
+        const char* const xrow = (second ? B.x : A.x) + (t * (second ? B.xs : A.xs) + (int64_t)(h0 + sub) * D) * ES + c * 16;
 
         // the sum of squares of each chunk in element order, then the
         // butterfly step of distance L inside the lane
@@ -416,18 +444,36 @@ qk_norm_rope_pair(QkSide A, QkSide B, int nca, int ncb, float eps, const int32_t
             s[k] = __fadd_rn(s0, s1);
         }
         float inv[NP];
-        if (L >= 2) {
+        if (NP == 4) {  // L >= 4
+            const int m1 = L >> 1, m2 = L >> 2;
+            const bool b1 = (lane & m1) != 0, b2 = (lane & m2) != 0;
+            float k0 = b1 ? s[2 % NP] : s[0], k1 = b1 ? s[3 % NP] : s[1];
+            const float g0 = b1 ? s[0] : s[2 % NP], g1 = b1 ? s[1] : s[3 % NP];
+            k0 = __fadd_rn(k0, __shfl_xor_sync(0xFFFFFFFFu, g0, m1));
+            k1 = __fadd_rn(k1, __shfl_xor_sync(0xFFFFFFFFu, g1, m1));
+            float kk = b2 ? k1 : k0;
+            const float gg = b2 ? k0 : k1;
+            kk = __fadd_rn(kk, __shfl_xor_sync(0xFFFFFFFFu, gg, m2));
+#pragma unroll
+            for (int m = L >> 3; m >= 1; m >>= 1) kk = __fadd_rn(kk, __shfl_xor_sync(0xFFFFFFFFu, kk, m));
+            // this lane's row is pass 2 * b1 + b2
+            const float own = __frcp_rn(__fsqrt_rn(__fadd_rn(__fmul_rn(kk, rD), eps)));
+            const int base = sub << lgL;
+#pragma unroll
+            for (int k = 0; k < NP; ++k)
+                inv[k] = __shfl_sync(0xFFFFFFFFu, own, base + ((k >> 1) ? m1 : 0) + ((k & 1) ? m2 : 0));
+        } else if (L >= 2) {
             const int m1 = L >> 1;
             const bool b1 = (lane & m1) != 0;
-            float kk = b1 ? s[1] : s[0];
-            const float gg = b1 ? s[0] : s[1];
+            float kk = b1 ? s[1 % NP] : s[0];
+            const float gg = b1 ? s[0] : s[1 % NP];
             kk = __fadd_rn(kk, __shfl_xor_sync(0xFFFFFFFFu, gg, m1));
 #pragma unroll
             for (int m = L >> 2; m >= 1; m >>= 1) kk = __fadd_rn(kk, __shfl_xor_sync(0xFFFFFFFFu, kk, m));
             const float own = __frcp_rn(__fsqrt_rn(__fadd_rn(__fmul_rn(kk, rD), eps)));
             const int base = sub << lgL;
             inv[0] = __shfl_sync(0xFFFFFFFFu, own, base);
-            inv[1] = __shfl_sync(0xFFFFFFFFu, own, base + m1);
+            inv[1 % NP] = __shfl_sync(0xFFFFFFFFu, own, base + m1);
         } else {
 #pragma unroll
             for (int k = 0; k < NP; ++k)
@@ -444,7 +490,16 @@ qk_norm_rope_pair(QkSide A, QkSide B, int nca, int ncb, float eps, const int32_t
             float a[V], b[V], g[V];
             // normalised and rounded to storage, as a stored intermediate would be
             const float2 iv = make_float2(inv[k], inv[k]);
-            S::unpack(raw[k][0], a);
+            // four passes: the rows are read again (from L1) rather than held;
+            // a row past H contributes nothing and is not stored
+            const bool here = h0 + k * RP + sub < H;
+            Vec16 r0 = raw[k][0], r1 = raw[k][1];
+            if (NP == 4) r0 = r1 = Vec16{{0u, 0u, 0u, 0u}};
+            if (NP == 4 && here) {
+                r0 = ld_twice(xrow + k * kPassBytes);
+                r1 = ld_twice(xrow + k * kPassBytes + half * ES);
+            }
+            S::unpack(r0, a);
             S::unpack(ld_reuse(gp), g);
 #pragma unroll
             for (int e = 0; e < V; e += 2) {
@@ -452,7 +507,7 @@ qk_norm_rope_pair(QkSide A, QkSide B, int nca, int ncb, float eps, const int32_t
                 a[e] = S::round(u.x);
                 a[e + 1] = S::round(u.y);
             }
-            S::unpack(raw[k][1], b);
+            S::unpack(r1, b);
             S::unpack(ld_reuse(gp + half * ES), g);
 #pragma unroll
             for (int e = 0; e < V; e += 2) {
@@ -749,20 +804,21 @@ cudaError_t launch_dt(const QkNormRopeArgs& a, bool vec, cudaStream_t st) {
     while ((2 << lgL) < nchunks) ++lgL;
     const bool pair = vec && a.layout == 0 && a.r == a.D && nchunks >= 2 && (2 << lgL) == nchunks;
     if (pair) {
-        const int rows_item = (32 >> lgL) * 2;
+        const int np = lgL >= 2 && lgL <= 4 ? 4 : 2;  // passes per warp item
+        const int rows_item = (32 >> lgL) * np;
         const int pa = (int)((a.side[0].H + rows_item - 1) / rows_item);
         const int pb = (int)((a.side[1].H + rows_item - 1) / rows_item);
         const int warps = (int)std::min<int64_t>(pa + pb, kTokWarps);
         const float2* cs = reinterpret_cast<const float2*>(a.cos_sin);
-#define GBE_QKP(C, G)                                                                                              \
-    return launch(qk_norm_rope_pair<DT, C, G>, dim3((unsigned)a.T), dim3(warps * 32), 0, st, sd[0], sd[1], pa, pb, \
+#define GBE_QKP(C, G, N)                                                                                              \
+    return launch(qk_norm_rope_pair<DT, C, G, N>, dim3((unsigned)a.T), dim3(warps * 32), 0, st, sd[0], sd[1], pa, pb, \
                   a.eps, a.pos, lgL, a.inv_freq, cs, a.cache_len, a.mu)
 #define GBE_QKP_L(C)                      \
     switch (lgL) {                        \
-        case 2: GBE_QKP(C, 2);            \
-        case 3: GBE_QKP(C, 3);            \
-        case 4: GBE_QKP(C, 4);            \
-        default: GBE_QKP(C, -1);          \
+        case 2: GBE_QKP(C, 2, 4);         \
+        case 3: GBE_QKP(C, 3, 4);         \
+        case 4: GBE_QKP(C, 4, 4);         \
+        default: GBE_QKP(C, -1, 2);       \
     }
         if (cs != nullptr) GBE_QKP_L(true)
         GBE_QKP_L(false)
