@@ -62,6 +62,11 @@ __device__ __forceinline__ void load_chunk(const char* row, int c, int D, float 
     }
 }
 
+// A hint: the 128-byte line at p is fetched into L2 (no register holds it).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // A load kept in L1 for a second read by the same warp (ld.global.ca: a
 // coherent load, so rows written in place by this kernel are never read
 // stale -- each address is read twice and then written once, by one warp).
@@ -353,7 +358,10 @@ __device__ __forceinline__ void rotate_store(const float (&a)[Store<DT>::V], con
 // of two 512-thread CTAs an SM: more registers cost more in occupancy than
 // they save), so these loads go out after the angles are formed, kept in L1
 // (ld_twice), and each pass reads its rows again from L1 for the
-// normalisation instead of holding them from the sums.
+// normalisation instead of holding them from the sums.  So that the loads
+// do not start only after the position's load and the angles, every lane
+// first asks for one 128-byte line of the item's rows to be fetched into
+// L2 (a prefetch holds no register): 29.3 -> 27.6 us at that shape.
 //
 // D = 2 L V is a power of two here, so the mean of squares s / D is taken as
 // s * 2^-log2(D): both are the correctly rounded value of the same real
@@ -409,6 +417,16 @@ qk_norm_rope_pair(QkSide A, QkSide B, int nca, int ncb, float eps, const int32_t
         }
     };
     if (NP == 2 && ci < per_tok) load_item(ci);  // four passes: after the angles
+    if (NP == 4 && ci < per_tok) {
+        // the first item's rows (16 whole rows, contiguous: 4 KB, one
+        // 128-byte line a lane) start coming into L2 while the angles form,
+        // so the loads after them wait for L2 rather than for DRAM
+        const bool second = ci >= nca;
+        const int h0 = (second ? ci - nca : ci) * RP * NP;
+        const int64_t off = (int64_t)lane * 128;
+        if (off < (int64_t)((second ? B.H : A.H) - h0) * D * ES)
+            prefetch_l2((second ? B.x : A.x) + (t * (second ? B.xs : A.xs) + (int64_t)h0 * D) * ES + off);
+    }
 
     for (int i = threadIdx.x; i < half; i += blockDim.x) {
         float cv, sv;
