@@ -55,6 +55,12 @@ __device__ __forceinline__ Vec16 ld_once(const void* p) {
     return v;
 }
 
+// A hint: the 128-byte line holding p is fetched into L2 (no register holds
+// it, and nothing waits for it).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ void st_once(void* p, const Vec16& v) {
     asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]),
                  "r"(v.w[3])

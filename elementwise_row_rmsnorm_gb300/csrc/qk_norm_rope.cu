@@ -62,11 +62,6 @@ __device__ __forceinline__ void load_chunk(const char* row, int c, int D, float 
     }
 }
 
-// A hint: the 128-byte line at p is fetched into L2 (no register holds it).
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
-
 // A load kept in L1 for a second read by the same warp (ld.global.ca: a
 // coherent load, so rows written in place by this kernel are never read
 // stale -- each address is read twice and then written once, by one warp).

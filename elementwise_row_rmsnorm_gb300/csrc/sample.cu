@@ -320,6 +320,51 @@ __device__ __forceinline__ float unit_sum_of(const Row<DT, VEC>& row, const Vec1
     return unit_sum(row, v);
 }
 
+// rn(rn(v - M) * c) for the two bf16 values of a packed word, low half
+// first, with no unpacking: the subtraction is the mixed-precision add of
+// -M (the bf16 operand widened exactly, then one rounding -- the bits of
+// __fsub_rn on the widened value), the two products one packed multiply.
+__device__ __forceinline__ float2 scaled_bf16x2(uint32_t w, float neg_m, float c) {
+    float d0, d1;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "add.rn.f32.bf16 %0, lo, %3;\n\tadd.rn.f32.bf16 %1, hi, %3;\n\t}"
+        : "=f"(d0), "=f"(d1) : "r"(w), "f"(neg_m));
+    return mul2_rn(make_float2(d0, d1), make_float2(c, c));
+}
+
+// unit_sum of a packed bf16 unit (the same bits): e of each entry from the
+// packed word, summed in index order; a unit holding NaN is summed again,
+// unpacked, with those entries skipped.  MINP: e counts only where e >= p
+// (NaN fails), the sum of kept_e.
+template <int DT, bool VEC, bool MINP>
+__device__ __forceinline__ float unit_sum_bf16(const Row<DT, VEC>& row, const Vec16& r, float p) {
+    float s = 0.0f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        const float2 y = scaled_bf16x2(r.w[w], -row.mx, row.c);
+        const float e0 = ex2(y.x), e1 = ex2(y.y);
+        s = __fadd_rn(s, MINP ? (e0 >= p ? e0 : 0.0f) : e0);
+        s = __fadd_rn(s, MINP ? (e1 >= p ? e1 : 0.0f) : e1);
+    }
+    if (!MINP && s != s) s = unit_sum_of(row, r);
+    return s;
+}
+
+// unit_sums2 of two packed bf16 units (the same bits): entry e of unit 0 and
+// of unit 1 summed as the two lanes of packed additions.
+template <int DT, bool VEC>
+__device__ __forceinline__ float2 unit_sums2_bf16(const Row<DT, VEC>& row, const Vec16& r0, const Vec16& r1) {
+    float2 s = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        const float2 y0 = scaled_bf16x2(r0.w[w], -row.mx, row.c);
+        const float2 y1 = scaled_bf16x2(r1.w[w], -row.mx, row.c);
+        s = add2_rn(s, make_float2(ex2(y0.x), ex2(y1.x)));
+        s = add2_rn(s, make_float2(ex2(y0.y), ex2(y1.y)));
+    }
+    return s;
+}
+
 // ---- warp and block primitives ----------------------------------------------------
 
 __device__ __forceinline__ u64 warp_sum_u64(u64 v) {
@@ -582,9 +627,13 @@ __device__ __forceinline__ void index_order_body(const void* x, int32_t* out, in
             for (int q = 0; q < kU; ++q) r[q] = row.load_raw(j0 + q * kTile);
 #pragma unroll
             for (int q = 0; q < kU; ++q) {
-                float v[V];
-                Store<DT>::unpack(r[q], v);
-                mine += unit(v);
+                if (DT == kBF16) {
+                    mine += fixed40(unit_sum_bf16<DT, VEC, MINP>(row, r[q], p));
+                } else {
+                    float v[V];
+                    Store<DT>::unpack(r[q], v);
+                    mine += unit(v);
+                }
             }
         } else {
             float v[kU][V];
@@ -1164,7 +1213,9 @@ __device__ u64 mass_and_gather(const Row<DT, VEC>& row, ShBig& sb, float T) {
 #pragma unroll
             for (int q = 0; q < kU; q += 2) {  // two units at a time
                 float2 su;
-                {
+                if (DT == kBF16) {
+                    su = unit_sums2_bf16<DT, VEC>(row, r[q], r[q + 1]);
+                } else {
                     float v0[V], v1[V];
                     Store<DT>::unpack(r[q], v0);
                     Store<DT>::unpack(r[q + 1], v1);
