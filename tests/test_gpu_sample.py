@@ -278,6 +278,35 @@ def test_rows_without_a_maximum_in_a_split_batch(dtype):
         assert np.array_equal(got, ref[:4]), (m, got, ref[:4])
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_rows_walked_by_resident_ctas(dtype):
+    """A batch larger than the resident CTAs (1500 rows: several waves),
+    with rows of NaN, of -inf, holding +inf, of equal logits and with one
+    dominant entry in among them: every row draws what it draws alone or in
+    a small batch, the rows without a maximum give -1, and some are checked
+    against the oracle."""
+    rows, n = 1500, 8192
+    x32 = widen(_logits(rows, n, dtype, nan_frac=0.002, tag="resident"))
+    x32[5] = np.nan
+    x32[306, :] = -np.inf
+    x32[457, 17] = np.inf
+    x32[700] = 1.5
+    x32[1499, 4000] = 60.0
+    x = to_bf16(x32) if dtype == "bf16" else x32
+    xd = to_dev(x)
+    u = torch.from_numpy(_u(rows, "resident")).cuda()
+    for m, kw in METHODS + [("top_k", dict(temperature=0.7, top_k=300))]:
+        got = gbe.sample(xd, u, m, **kw).cpu().numpy()
+        assert got[5] == -1 and got[306] == -1 and got[457] == -1, (m, got[[5, 306, 457]])
+        assert got[1499] == 4000, m
+        for r0, r1 in ((0, 1), (5, 6), (300, 320), (699, 701), (1490, 1500)):
+            ref = gbe.sample(xd[r0:r1].contiguous(), u[r0:r1].contiguous(), m, **kw).cpu().numpy()
+            assert np.array_equal(got[r0:r1], ref), (m, r0, r1)
+        pick = np.array([0, 1, 303, 304, 455, 456, 700, 1200])
+        sub = _check(x[pick], u[pick].cpu().numpy(), m, kw, f"{m} resident rows", max_miss=1.0)
+        assert np.array_equal(got[pick], sub), m
+
+
 def test_top_p_rows_past_the_first_gather():
     """Top-p 0.9 at t = 0.7 on the first 512 rows of the prefill logits (the
     bench's setting): in about 2 % of them the first, narrow gather of the
