@@ -8,14 +8,15 @@
 //
 // The angle is the f32 product float(p_t) * omega_i (the correctly rounded
 // product, equal to the double product rounded to f32 for p_t < 2^24), and
-// its cosine and sine come from rope_sincos: a quarter-turn reduction, then
-// CUDA's accurate sincosf on the remainder (never the __sinf approximation:
-// at positions near 2^20 the angles reach 10^6 rad).  The
-// pages' loop order is token, pair, head with one angle per (token, pair);
-// here a thread owns a group of pairs of one token and forms their angles
-// once, in registers, for a chunk of up to four heads (so an angle is formed
-// once per token for every four heads), with no shared memory and no
-// barrier.
+// its cosine and sine come from rope_sincos (common.cuh: a quarter-turn
+// reduction and Taylor series; never the __sinf approximation: at positions
+// near 2^20 the angles reach 10^6 rad).  The pages' loop order is token,
+// pair, head with one angle per (token, pair); here a thread owns a group of
+// pairs of one token and has their angles in registers for a chunk of up to
+// four heads, with no shared memory and no barrier -- formed by itself, or,
+// where K chunks of a token sit in one warp, one K-th of them formed by each
+// of K lanes and exchanged by shuffles (an angle formed once per token for
+// every 4 K heads).
 //
 // Both members of a pair are loaded (all loads of a thread, in fact) before
 // either is stored, and no two threads touch the same entry, so the call may
@@ -99,7 +100,16 @@ __device__ __forceinline__ void angle(int32_t p, int i, const float* inv_freq, c
 // into registers while those loads are in flight, then rotates and stores
 // every head.  Threads of one token and head chunk cover consecutive 16-byte
 // vectors, so each warp-wide access is contiguous.
-template <int DT, int LAYOUT, bool CACHE, int HC>
+//
+// K > 1 (angles formed, not read from a table): the launch guarantees that
+// the G K consecutive lanes holding items 0..G-1 of K head chunks of one
+// token lie in one warp (K divides the operand's chunks, G K divides 32, the
+// operand starts on a warp).  Those lanes share the token's angles: lane
+// (item g, chunk kq = hc mod K) forms the P / K angles of item g with
+// e = kq (mod K), and takes each of its item's P from the lane that formed
+// it -- lane g + G (e mod K) of the group, its value e / K -- by register
+// shuffles: K times fewer sin/cos evaluations, the same values.
+template <int DT, int LAYOUT, bool CACHE, int HC, int K>
 __device__ __forceinline__ void rope_vec_item(const Operand& R, int64_t gt, const int32_t* pos, int D,
                                               const float2* cache, int64_t cache_len) {
     using S = Store<DT>;
@@ -136,8 +146,26 @@ __device__ __forceinline__ void rope_vec_item(const Operand& R, int64_t gt, cons
     // this thread's pairs, once for all its heads
     float c[P], sn[P];
     const int i0 = g * P;
+    if (K > 1) {
+        constexpr int PK = P / K > 0 ? P / K : 1;
+        const int kq = hc % K;
+        float mc[PK], ms[PK];
 #pragma unroll
-    for (int e = 0; e < P; ++e) angle<CACHE>(p, i0 + e, inv_freq, cache, cache_len, half, c[e], sn[e]);
+        for (int m = 0; m < PK; ++m) rope_sincos(__fmul_rn((float)p, __ldg(inv_freq + i0 + kq + m * K)), &ms[m], &mc[m]);
+        // the lanes of this warp that serve the operand (whole groups)
+        const int lane = (int)(gt & 31);
+        const int64_t live = R.threads - (gt - lane);
+        const unsigned mask = live >= 32 ? 0xFFFFFFFFu : (1u << live) - 1u;
+#pragma unroll
+        for (int e = 0; e < P; ++e) {
+            const int src = g + G * (e % K);
+            c[e] = __shfl_sync(mask, mc[e / K], src, G * K);
+            sn[e] = __shfl_sync(mask, ms[e / K], src, G * K);
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < P; ++e) angle<CACHE>(p, i0 + e, inv_freq, cache, cache_len, half, c[e], sn[e]);
+    }
 
 #pragma unroll
     for (int j = 0; j < HC; ++j) {
@@ -189,15 +217,15 @@ __device__ __forceinline__ void rope_vec_item(const Operand& R, int64_t gt, cons
 
 // The launch's threads serve operand A first, then operand B, each with its
 // own layout (LA, LB), width, frequencies and scale.
-template <int DT, int LA, int LB, bool CACHE, int HC>
+template <int DT, int LA, int LB, bool CACHE, int HC, int K = 1>
 __global__ void __launch_bounds__(kThreads)
 rope_vec(Operand A, Operand B, const int32_t* pos, int D, const float2* cache, int64_t cache_len) {
     pdl_begin();
     const int64_t gt = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     if (gt < A.threads)
-        rope_vec_item<DT, LA, CACHE, HC>(A, gt, pos, D, cache, cache_len);
+        rope_vec_item<DT, LA, CACHE, HC, K>(A, gt, pos, D, cache, cache_len);
     else if (gt - A.threads < B.threads)
-        rope_vec_item<DT, LB, CACHE, HC>(B, gt - A.threads, pos, D, cache, cache_len);
+        rope_vec_item<DT, LB, CACHE, HC, K>(B, gt - A.threads, pos, D, cache, cache_len);
 }
 
 // Unaligned path (or widths that do not split into 16-byte vectors): a
@@ -420,12 +448,18 @@ rope_cos_sin_table(float2* cache, int64_t len, int half, const float* inv_freq) 
 }
 
 template <int DT, int LA, int LB, bool CACHE>
-cudaError_t launch_shape(bool vec, bool one_head, unsigned grid, const Operand (&op)[2], const RopeArgs& a,
+cudaError_t launch_shape(bool vec, bool one_head, int K, unsigned grid, const Operand (&op)[2], const RopeArgs& a,
                          const float2* cache, cudaStream_t st) {
     const int Di = (int)a.D;
     if (vec && one_head)
         return launch(rope_vec<DT, LA, LB, CACHE, 1>, dim3(grid), dim3(kThreads), 0, st, op[0], op[1], a.pos, Di,
                       cache, a.cache_len);
+    if (vec && !CACHE && K == 4)
+        return launch(rope_vec<DT, LA, LB, false, kHeadsPerThread, 4>, dim3(grid), dim3(kThreads), 0, st, op[0],
+                      op[1], a.pos, Di, cache, a.cache_len);
+    if (vec && !CACHE && K == 2)
+        return launch(rope_vec<DT, LA, LB, false, kHeadsPerThread, 2>, dim3(grid), dim3(kThreads), 0, st, op[0],
+                      op[1], a.pos, Di, cache, a.cache_len);
     if (vec)
         return launch(rope_vec<DT, LA, LB, CACHE, kHeadsPerThread>, dim3(grid), dim3(kThreads), 0, st, op[0], op[1],
                       a.pos, Di, cache, a.cache_len);
@@ -477,19 +511,33 @@ cudaError_t launch_dt(const RopeArgs& a, bool vec, cudaStream_t st) {
     const int64_t threads = op[0].threads + op[1].threads;
     if (threads == 0) return cudaSuccess;
     const unsigned grid = (unsigned)((threads + kThreads - 1) / kThreads);
+    // K chunks of a token share its angles (rope_vec_item) where the lane
+    // groups fit whole in warps, for every operand of the launch
+    int K = 1;
+    if (vec && !one_head && cache == nullptr) {
+        for (int kk = 4; kk >= 2 && K == 1; kk >>= 1) {
+            bool ok = !(used[0] && used[1]) || op[0].threads % 32 == 0;
+            for (int k = 0; k < 2; ++k) {
+                if (!used[k]) continue;
+                const int P = a.side[k].layout == 0 ? V : V / 2;
+                ok = ok && op[k].NC % kk == 0 && P % kk == 0 && 32 % (G[k] * kk) == 0;
+            }
+            if (ok) K = kk;
+        }
+    }
     // an operand with no threads takes the other's layout (one kernel fewer)
     const int la = used[0] ? a.side[0].layout : a.side[1].layout;
     const int lb = used[1] ? a.side[1].layout : la;
     if (cache != nullptr) {  // one table: both operands share r, frequencies and layout
-        if (la == 0) return launch_shape<DT, 0, 0, true>(vec, one_head, grid, op, a, cache, st);
-        return launch_shape<DT, 1, 1, true>(vec, one_head, grid, op, a, cache, st);
+        if (la == 0) return launch_shape<DT, 0, 0, true>(vec, one_head, K, grid, op, a, cache, st);
+        return launch_shape<DT, 1, 1, true>(vec, one_head, K, grid, op, a, cache, st);
     }
     if (la == 0) {
-        if (lb == 0) return launch_shape<DT, 0, 0, false>(vec, one_head, grid, op, a, cache, st);
-        return launch_shape<DT, 0, 1, false>(vec, one_head, grid, op, a, cache, st);
+        if (lb == 0) return launch_shape<DT, 0, 0, false>(vec, one_head, K, grid, op, a, cache, st);
+        return launch_shape<DT, 0, 1, false>(vec, one_head, K, grid, op, a, cache, st);
     }
-    if (lb == 0) return launch_shape<DT, 1, 0, false>(vec, one_head, grid, op, a, cache, st);
-    return launch_shape<DT, 1, 1, false>(vec, one_head, grid, op, a, cache, st);
+    if (lb == 0) return launch_shape<DT, 1, 0, false>(vec, one_head, K, grid, op, a, cache, st);
+    return launch_shape<DT, 1, 1, false>(vec, one_head, K, grid, op, a, cache, st);
 }
 
 }  // namespace
