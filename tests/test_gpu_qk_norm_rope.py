@@ -41,7 +41,10 @@ def _unfused(q, k, gq, gk, pos, om, r, mu, layout, eps=1e-6):
 @pytest.mark.parametrize("T,Hq,Hk,D,r", [(9, 32, 8, 128, 128), (5, 4, 2, 64, 32), (3, 3, 1, 16, 16),
                                          (4, 2, 2, 8, 8), (17, 16, 4, 96, 64),
                                          # more chunks of head rows than warps of a token's CTA
-                                         (3, 160, 9, 128, 128),
+                                         (3, 160, 9, 128, 128), (2, 300, 20, 128, 128),
+                                         # four-pass items of 4 lanes a row (f32 head_dim 32, bf16 64),
+                                         # head counts ragged in 16-row items
+                                         (7, 20, 5, 32, 32), (6, 33, 3, 64, 64),
                                          # wide heads: up to 64 chunks (256 f32 / 512 bf16)
                                          (2, 4, 2, 256, 256), (3, 5, 3, 128, 96), (3, 3, 2, 200, 160),
                                          (2, 2, 1, 512, 512), (2, 3, 2, 384, 320)])
