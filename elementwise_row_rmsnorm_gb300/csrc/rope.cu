@@ -335,7 +335,12 @@ rope_multi_kernel(const void* x, void* y, const int32_t* pos, int64_t T, int H, 
 // to four heads, loads all of them first, forms the P angles from its
 // slice's position and frequencies while they are in flight, then rotates
 // and stores.  Item g belongs to the slice whose item range holds it.
-template <int DT, int LAYOUT>
+//
+// HC heads a thread; K > 1: the G K lanes of K head chunks of one token (one
+// warp: the launch checks that K divides NC and G K divides 32) share the
+// angles as in rope_vec_item, lane (g, kq) forming the P / K of item g with
+// e = kq (mod K) from its item's slice.
+template <int DT, int LAYOUT, int HC, int K>
 __global__ void __launch_bounds__(kThreads)
 rope_multi_vec(const char* x, char* y, const int32_t* pos, int64_t T, int H, int D,
                const __grid_constant__ MultiAxis ax,
@@ -344,7 +349,6 @@ rope_multi_vec(const char* x, char* y, const int32_t* pos, int64_t T, int H, int
     constexpr int V = S::V;
     constexpr int P = LAYOUT == 0 ? V : V / 2;  // pairs per 16-byte item
     constexpr int64_t ES = sizeof(typename S::T);
-    constexpr int HC = kHeadsPerThread;
     pdl_begin();
     const int64_t gt = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     const int g = (int)(gt % G);
@@ -381,8 +385,25 @@ rope_multi_vec(const char* x, char* y, const int32_t* pos, int64_t T, int H, int
     float c[P], sn[P];
     const float p = (float)pos[t * ax.A + a];
     const int k0 = ax.poff[a] + i0;
+    if (K > 1) {
+        constexpr int PK = P / K > 0 ? P / K : 1;
+        const int kq = hc % K;
+        float mc[PK], ms[PK];
 #pragma unroll
-    for (int e = 0; e < P; ++e) rope_sincos(__fmul_rn(p, __ldg(inv_freq + k0 + e)), &sn[e], &c[e]);
+        for (int m = 0; m < PK; ++m) rope_sincos(__fmul_rn(p, __ldg(inv_freq + k0 + kq + m * K)), &ms[m], &mc[m]);
+        const int lane = (int)(gt & 31);
+        const int64_t live = T * NC * G - (gt - lane);
+        const unsigned mask = live >= 32 ? 0xFFFFFFFFu : (1u << live) - 1u;
+#pragma unroll
+        for (int e = 0; e < P; ++e) {
+            const int src = g + G * (e % K);
+            c[e] = __shfl_sync(mask, mc[e / K], src, G * K);
+            sn[e] = __shfl_sync(mask, ms[e / K], src, G * K);
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < P; ++e) rope_sincos(__fmul_rn(p, __ldg(inv_freq + k0 + e)), &sn[e], &c[e]);
+    }
 
 #pragma unroll
     for (int j = 0; j < HC; ++j) {
@@ -567,17 +588,33 @@ cudaError_t launch_rope_multi(const void* x, void* y, const int32_t* pos, int64_
         G += half / P;
     }
     if (vec) {
-        const int NC = (Hi + kHeadsPerThread - 1) / kHeadsPerThread;
+        // heads a thread and the chunks that share a token's angles: three
+        // heads and four chunks where the lane groups fit (the angles formed
+        // once per token for every 12 heads), else four heads and two, else
+        // four heads alone
+        const int P = layout == 0 ? V : V / 2;
+        auto fits = [&](int hc, int k) {
+            const int nc = (Hi + hc - 1) / hc;
+            return nc % k == 0 && P % k == 0 && 32 % (G * k) == 0;
+        };
+        const int hc = fits(3, 4) ? 3 : 4;
+        const int K = hc == 3 ? 4 : (fits(4, 2) ? 2 : 1);
+        const int NC = (Hi + hc - 1) / hc;
         const dim3 grid((unsigned)((T * NC * G + kThreads - 1) / kThreads));
         const char* xc = static_cast<const char*>(x);
         char* yc = static_cast<char*>(y);
-#define GBE_MULTI(D_, L_)                                                                                        \
-    return launch(rope_multi_vec<D_, L_>, grid, dim3(kThreads), 0, st, xc, yc, pos, T, Hi, Di, ax, inv_freq, mu, \
-                  copy_tail, G, NC)
+#define GBE_MULTI(D_, L_, H_, K_)                                                                              \
+    return launch(rope_multi_vec<D_, L_, H_, K_>, grid, dim3(kThreads), 0, st, xc, yc, pos, T, Hi, Di, ax,     \
+                  inv_freq, mu, copy_tail, G, NC)
+#define GBE_MULTI_K(D_, L_)                            \
+    if (K == 4) GBE_MULTI(D_, L_, 3, 4);               \
+    if (K == 2) GBE_MULTI(D_, L_, kHeadsPerThread, 2); \
+    GBE_MULTI(D_, L_, kHeadsPerThread, 1)
         if (dtype == kF32) {
-            if (layout == 0) GBE_MULTI(kF32, 0); else GBE_MULTI(kF32, 1);
+            if (layout == 0) { GBE_MULTI_K(kF32, 0); } else { GBE_MULTI_K(kF32, 1); }
         }
-        if (layout == 0) GBE_MULTI(kBF16, 0); else GBE_MULTI(kBF16, 1);
+        if (layout == 0) { GBE_MULTI_K(kBF16, 0); } else { GBE_MULTI_K(kBF16, 1); }
+#undef GBE_MULTI_K
 #undef GBE_MULTI
     }
     const dim3 grid((unsigned)((T * per_tok + kThreads - 1) / kThreads));

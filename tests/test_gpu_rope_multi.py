@@ -70,12 +70,16 @@ def test_bad_axes_are_refused():
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("layout", [0, 1])
-def test_vector_path_equals_scalar(dtype, layout):
-    """The (t, h, w) = (32, 48, 48) split of head_dim 128 at 24 heads takes the
-    16-byte vector kernel; the same data one element off alignment takes the
-    scalar one: the two agree bit for bit, in place and out of place."""
-    T, H, D, dims = 50, 6, 128, [32, 48, 48]
-    x = normal(33, "rm.vec", (T, H, D), 0.0, 1.0)
+@pytest.mark.parametrize("H", [6, 24, 12, 7])
+def test_vector_path_equals_scalar(dtype, layout, H):
+    """The (t, h, w) = (32, 48, 48) split of head_dim 128 takes the 16-byte
+    vector kernel (at 24 and 12 heads, bf16 half layout: three heads a thread
+    and four head chunks sharing the angles; at 6 and 7 heads, or f32: four
+    heads and two chunks, or none); the same data one element off alignment
+    takes the scalar one: the two agree bit for bit, in place and out of
+    place."""
+    T, D, dims = 50, 128, [32, 48, 48]
+    x = normal(33, f"rm.vec.{H}", (T, H, D), 0.0, 1.0)
     if dtype == "bf16":
         x = to_bf16(x)
     pos = randint(33, "rm.vec.pos", (T, 3), 0, 300)
