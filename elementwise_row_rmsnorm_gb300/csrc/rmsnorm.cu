@@ -31,6 +31,9 @@
 // two-pass kernel with the same map.  The row's sum is complete before the
 // first write, so y may be x (and h may be residual).  Launches overlap the
 // previous kernel's tail (programmatic dependent launch, see common.cuh).
+#include <algorithm>
+#include <atomic>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -136,6 +139,100 @@ rmsnorm_rows(const void* x, const void* res, const void* w, void* y, void* h, in
             for (int e = 0; e < V; ++e) f[e] = __fmul_rn(__fmul_rn(f[e], inv), wv[e]);
             st_stream(static_cast<char*>(y) + boff + (int64_t)c * 16, S::pack(f));
         }
+    }
+}
+
+// Aligned rows of 1024 threads (more than 3072 chunks: f32 d up to 16384,
+// bf16 up to 32768), plain RMSNorm, when the call holds more rows than two
+// per SM: rmsnorm_rows keeps two such rows resident per SM, so a batch of R
+// rows takes ceil(R / 2 SMs) waves of one row each, the last partly empty.
+// Here one CTA per SM walks the rows blockIdx.x, + gridDim.x, ... with the
+// next two rows' chunks already in flight into a ring of shared memory
+// (cp.async, 16 bytes per copy).  Each thread copies exactly the chunks it
+// will read, so its own wait_group (a hardware wait, not a loop) is the only
+// wait before it reads them, and it refills a ring slot only after it has
+// read that slot itself.  The map, the per-thread order and the reduction
+// tree are rmsnorm_rows<DT, 4, false, 1024>'s, so the bits are the same.
+constexpr int kStreamSlots = 3;  // rows a CTA holds: the one it works on and two in flight
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((unsigned)__cvta_generic_to_shared(smem)),
+                 "l"(gmem)
+                 : "memory");
+}
+
+template <int DT>
+__global__ void __launch_bounds__(1024, 1)
+rmsnorm_stream(const void* x, const void* w, void* y, int64_t rows, int d, float eps) {
+    using S = Store<DT>;
+    constexpr int V = S::V;
+    constexpr int K = kMaxSlots;
+    constexpr int TPR = 1024;
+    constexpr int NS = kStreamSlots;
+    constexpr int64_t ES = sizeof(typename S::T);
+    extern __shared__ Vec16 ring[];  // [NS][K][TPR]
+    __shared__ float red[2][32];
+    pdl_begin();
+    const int t = threadIdx.x;
+    const int warp = t >> 5, lane = t & 31;
+    const int nchunks = d / V;
+    const int64_t rb = (int64_t)d * ES;
+    const int64_t G = gridDim.x;
+    auto issue = [&](int64_t r, int slot) {
+        if (r < rows) {
+            const char* src = static_cast<const char*>(x) + r * rb;
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                const int c = k * TPR + t;
+                if (c < nchunks) cp_async16(&ring[(slot * K + k) * TPR + t], src + (int64_t)c * 16);
+            }
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");  // empty past the last row: the count stays even
+    };
+    int64_t r = blockIdx.x;
+#pragma unroll
+    for (int q = 0; q < NS - 1; ++q) issue(r + q * G, q);
+    // this thread's gains, the same for every row
+    Vec16 wv[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const int c = k * TPR + t;
+        if (c < nchunks) wv[k] = ld_reuse(static_cast<const char*>(w) + (int64_t)c * 16);
+    }
+    int slot = 0, fill = NS - 1;
+    for (int it = 0; r < rows; ++it, r += G) {  // r depends on blockIdx only: the CTA stays together
+        issue(r + (NS - 1) * G, fill);
+        asm volatile("cp.async.wait_group %0;" ::"n"(NS - 1) : "memory");  // this thread's chunks of row r
+        Vec16 rx[K];
+        float s = 0.0f;
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            const int c = k * TPR + t;
+            if (c < nchunks) {
+                rx[k] = ring[(slot * K + k) * TPR + t];
+                s = vec_sq_acc<DT>(rx[k], s);
+            }
+        }
+        // the reduction's words alternate between rows: a row's are rewritten
+        // two rows later, after every thread has passed the barrier between
+        const float total = row_sum(s, red[it & 1], warp, lane, TPR >> 5);
+        const float ms = __fdiv_rn(total, (float)d);
+        const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+        char* yr = static_cast<char*>(y) + r * rb;
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            const int c = k * TPR + t;
+            if (c < nchunks) {
+                float f[V], g[V];
+                S::unpack(rx[k], f);
+                S::unpack(wv[k], g);
+#pragma unroll
+                for (int e = 0; e < V; ++e) f[e] = __fmul_rn(__fmul_rn(f[e], inv), g[e]);
+                st_stream(yr + (int64_t)c * 16, S::pack(f));
+            }
+        }
+        slot = slot + 1 == NS ? 0 : slot + 1;
+        fill = fill + 1 == NS ? 0 : fill + 1;
     }
 }
 
@@ -326,6 +423,28 @@ cudaError_t launch_ln(const void* x, const void* g, const void* b, void* y, int6
 #undef GBE_LN
 }
 
+// rmsnorm_stream with one CTA per SM, after the shared-memory opt-in (once
+// per device); cudaErrorNotReady when the opt-in is refused, and the caller
+// takes rmsnorm_rows.
+template <int DT>
+cudaError_t launch_stream(const void* x, const void* w, void* y, int64_t rows, int d, float eps, cudaStream_t st) {
+    const size_t smem = (size_t)kStreamSlots * kMaxSlots * 1024 * sizeof(Vec16);
+    static std::atomic<uint64_t> opted{0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaGetLastError();
+    const uint64_t bit = dev >= 0 && dev < 64 ? 1ull << dev : 0ull;
+    if (!(opted.load(std::memory_order_acquire) & bit) || bit == 0) {
+        if (cudaFuncSetAttribute(rmsnorm_stream<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return cudaErrorNotReady;
+        }
+        opted.fetch_or(bit, std::memory_order_release);
+    }
+    const int64_t grid = std::min<int64_t>(rows, sm_count());
+    return launch(rmsnorm_stream<DT>, dim3((unsigned)grid), dim3(1024), smem, st, x, w, y, rows, d, eps);
+}
+
 template <int DT, bool ADD>
 cudaError_t launch_dt(const void* x, const void* res, const void* w, void* y, void* h, int64_t rows, int64_t d,
                       float eps, bool vec, cudaStream_t st) {
@@ -338,6 +457,10 @@ cudaError_t launch_dt(const void* x, const void* res, const void* w, void* y, vo
     if (wide || !vec) {
         return launch(rmsnorm_two_pass<DT, ADD>, dim3((unsigned)rows), dim3((unsigned)tpr), 0, st, x, res, w, y, h,
                       rows, di, eps);
+    }
+    if (!ADD && tpr == 1024 && rows > 2LL * sm_count()) {
+        const cudaError_t e = launch_stream<DT>(x, w, y, rows, di, eps, st);
+        if (e != cudaErrorNotReady) return e;
     }
     const int64_t slots = (nchunks + tpr - 1) / tpr;
     const dim3 one((unsigned)rows), four((unsigned)((rows + 3) / 4));

@@ -159,6 +159,26 @@ def test_wide_rows_batch_invariant(dtype):
         assert torch.equal(ha.view(iv), hf[:b].view(iv)), ("add h", b)
 
 
+@pytest.mark.parametrize("dtype,d", [("f32", 16384), ("f32", 16000), ("bf16", 32768), ("bf16", 31000)])
+def test_rows_of_1024_threads_many_rows(dtype, d):
+    """Rows of 1024 threads in a batch of more rows than two per SM (700):
+    the whole batch and slices of it small enough to take the kernel that
+    keeps rows in registers give the same bits; some rows match the oracle."""
+    rows = 700
+    x, w = _inputs(rows, d, dtype, seed=17)
+    xd, wd = to_dev(x), to_dev(w)
+    ref = gbe.rmsnorm(xd, wd, 1e-5)
+    iv = torch.int32 if dtype == "f32" else torch.int16
+    for r0, r1 in ((0, 100), (299, 400), (600, 700), (699, 700)):
+        y = gbe.rmsnorm(xd[r0:r1].contiguous(), wd, 1e-5)
+        assert torch.equal(y.view(iv), ref[r0:r1].view(iv)), (r0, r1)
+    pick = [0, 151, 152, 350, 699]
+    _check_rms(x[pick], w, 1e-5, ref[pick], dtype, f"rmsnorm {dtype} d={d} many rows")
+    y2 = xd.clone()
+    gbe.gbe_rmsnorm(y2, wd, y2, 1e-5)  # in place
+    assert torch.equal(y2.view(iv), ref.view(iv)), "in place"
+
+
 def test_batch_invariance_prefill_bf16():
     """[8192, 4096] bf16: batches b = 1..4096 and rows placed at other offsets."""
     a, p = W.cases(W.PREFILL)["add_rmsnorm"]()
