@@ -177,6 +177,20 @@ def test_rows_of_1024_threads_many_rows(dtype, d):
     y2 = xd.clone()
     gbe.gbe_rmsnorm(y2, wd, y2, 1e-5)  # in place
     assert torch.equal(y2.view(iv), ref.view(iv)), "in place"
+    # rows of zeros, with an infinity, with a NaN and of huge values: the same
+    # bits in the large batch as alone
+    x2 = widen(x).copy()
+    x2[3] = 0.0
+    x2[310, 17] = np.inf
+    x2[460, 5] = np.nan
+    x2[611] = 3.0e38
+    x2 = to_bf16(x2) if dtype == "bf16" else x2.astype(np.float32)
+    xd2 = to_dev(x2)
+    ref2 = gbe.rmsnorm(xd2, wd, 1e-5)
+    for r in (3, 310, 460, 611):
+        y = gbe.rmsnorm(xd2[r:r + 1].contiguous(), wd, 1e-5)
+        assert torch.equal(y.view(iv), ref2[r:r + 1].view(iv)), r
+    assert torch.all(ref2[3] == 0), "a zero row stays zero"
 
 
 def test_batch_invariance_prefill_bf16():

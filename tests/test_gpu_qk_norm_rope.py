@@ -175,3 +175,29 @@ def test_many_tokens_equal_unfused_composition(dtype, Hq, Hk, D, mu, cached, ext
     assert np.array_equal(bits(qv.contiguous()), bits(qn)), "q"
     assert np.array_equal(bits(kv.contiguous()), bits(kn)), "k"
     assert torch.all(rows[:, (Hq + Hk) * D:] == 7.0), "past the heads untouched"
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_special_values_equal_unfused_composition(dtype):
+    """Head rows of zeros (1/rms = 1/sqrt(eps)), with an infinity, with a NaN,
+    and of values near the top of the range, in the whole-head half layout
+    (four-pass items) and at a partial r: the fused call gives the
+    composition's bits."""
+    for T, Hq, Hk, D, r in ((9, 32, 8, 128, 128), (5, 8, 2, 64, 32)):
+        q, k, gq, gk, pos, om = _case(6, T, Hq, Hk, D, r, dtype)
+        q, k = widen(q).copy(), widen(k).copy()
+        q[0, 3] = 0.0
+        q[1, 5, 7] = np.inf
+        k[2, 1, 0] = np.nan
+        q[3, 0] = 1.0e30
+        k[4, 0] = -2.0e-30
+        if dtype == "bf16":
+            q, k = to_bf16(q), to_bf16(k)
+        else:
+            q, k = q.astype(np.float32), k.astype(np.float32)
+        qn, kn = _unfused(q, k, gq, gk, pos, om, r, 1.0, 0)
+        qd, kd = to_dev(q), to_dev(k)
+        gbe.gbe_qk_norm_rope(qd, qd, to_dev(gq), kd, kd, to_dev(gk), 1e-6, to_dev(pos), to_dev(om), r, 1.0, 0)
+        assert np.array_equal(bits(qd), bits(qn)), (T, D, r, "q")
+        assert np.array_equal(bits(kd), bits(kn)), (T, D, r, "k")
+
