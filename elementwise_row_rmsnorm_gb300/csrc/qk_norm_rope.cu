@@ -413,9 +413,10 @@ qk_norm_rope_pair(QkSide A, QkSide B, int nca, int ncb, float eps, const int32_t
     };
     if (NP == 2 && ci < per_tok) load_item(ci);  // four passes: after the angles
     if (NP == 4 && ci < per_tok) {
-        // the first item's rows (16 whole rows, contiguous: 4 KB, one
-        // 128-byte line a lane) start coming into L2 while the angles form,
-        // so the loads after them wait for L2 rather than for DRAM
+        // the first item's rows (RP NP whole rows, contiguous: 256 V ES =
+        // 4 KB, one 128-byte line a lane; those past H left out) start coming
+        // into L2 while the angles form, so the loads after them wait for L2
+        // rather than for DRAM
         const bool second = ci >= nca;
         const int h0 = (second ? ci - nca : ci) * RP * NP;
         const int64_t off = (int64_t)lane * 128;
