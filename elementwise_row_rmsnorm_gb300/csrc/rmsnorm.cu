@@ -43,6 +43,27 @@ namespace {
 
 constexpr int kMaxSlots = 4;
 
+// (x_lo + c_lo, x_hi + c_hi) for the two bf16 values of a packed word by the
+// mixed-precision add (the bf16 operand widened exactly, then one rounding:
+// the bits of __fadd_rn on the widened value), with no unpacking.
+__device__ __forceinline__ float2 bf16x2_plus(uint32_t w, float c_lo, float c_hi) {
+    float d0, d1;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "add.rn.f32.bf16 %0, lo, %3;\n\tadd.rn.f32.bf16 %1, hi, %4;\n\t}"
+        : "=f"(d0), "=f"(d1) : "r"(w), "f"(c_lo), "f"(c_hi));
+    return make_float2(d0, d1);
+}
+
+// s + x_lo + x_hi, in that order, for the two bf16 values of a packed word
+// (the same mixed-precision add: the bits of two __fadd_rn).
+__device__ __forceinline__ float bf16x2_sum_acc(uint32_t w, float s) {
+    float d;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+        "add.rn.f32.bf16 %0, lo, %2;\n\tadd.rn.f32.bf16 %0, hi, %0;\n\t}"
+        : "=f"(d) : "r"(w), "f"(s));
+    return d;
+}
+
 // Threads per row for a row of `nchunks` 16-byte chunks: enough that each
 // owns at most kMaxSlots chunks.  A function of (d, dtype) only.
 inline int64_t threads_per_row(int64_t nchunks) {
@@ -310,10 +331,15 @@ layernorm_rows(const void* x, const void* g, const void* b, void* y, int64_t row
     for (int k = 0; k < K; ++k) {
         const int c = k * tpr + t;
         if (c < nchunks) {
-            float f[V];
-            S::unpack(rx[k], f);
+            if (DT == kBF16) {  // the packed words added as they are: the same sums
 #pragma unroll
-            for (int e = 0; e < V; ++e) s = __fadd_rn(s, f[e]);
+                for (int w = 0; w < 4; ++w) s = bf16x2_sum_acc(rx[k].w[w], s);
+            } else {
+                float f[V];
+                S::unpack(rx[k], f);
+#pragma unroll
+                for (int e = 0; e < V; ++e) s = __fadd_rn(s, f[e]);
+            }
         }
     }
     const float mu = __fdiv_rn((TPR == 32) ? warp_sum(s) : row_sum(s, red[0], warp, lane, tpr >> 5), (float)d);
@@ -322,14 +348,23 @@ layernorm_rows(const void* x, const void* g, const void* b, void* y, int64_t row
     for (int k = 0; k < K; ++k) {
         const int c = k * tpr + t;
         if (c < nchunks) {
-            float f[V];
-            S::unpack(rx[k], f);
-            const float2 m2 = make_float2(mu, mu);
+            if (DT == kBF16) {
 #pragma unroll
-            for (int e = 0; e < V; e += 2) {
-                const float2 cc = sub2_rn(make_float2(f[e], f[e + 1]), m2);  // two centred entries at once
-                s2 = __fmaf_rn(cc.x, cc.x, s2);
-                s2 = __fmaf_rn(cc.y, cc.y, s2);
+                for (int w = 0; w < 4; ++w) {
+                    const float2 cc = bf16x2_plus(rx[k].w[w], -mu, -mu);  // x - mu == x + (-mu)
+                    s2 = __fmaf_rn(cc.x, cc.x, s2);
+                    s2 = __fmaf_rn(cc.y, cc.y, s2);
+                }
+            } else {
+                float f[V];
+                S::unpack(rx[k], f);
+                const float2 m2 = make_float2(mu, mu);
+#pragma unroll
+                for (int e = 0; e < V; e += 2) {
+                    const float2 cc = sub2_rn(make_float2(f[e], f[e + 1]), m2);
+                    s2 = __fmaf_rn(cc.x, cc.x, s2);
+                    s2 = __fmaf_rn(cc.y, cc.y, s2);
+                }
             }
         }
     }
@@ -338,7 +373,23 @@ layernorm_rows(const void* x, const void* g, const void* b, void* y, int64_t row
 #pragma unroll
     for (int k = 0; k < K; ++k) {
         const int c = k * tpr + t;
-        if (c < nchunks) {
+        if (c < nchunks && DT == kBF16) {
+            // x - mu and the bias added to the packed words as they are (the
+            // bits of the unpacked form below; b + u == u + b)
+            float f[V], gv[V];
+            const Vec16 bw = b != nullptr ? ld_reuse(static_cast<const char*>(b) + (int64_t)c * 16) : Vec16{};
+            S::unpack(ld_reuse(static_cast<const char*>(g) + (int64_t)c * 16), gv);
+            const float2 i2 = make_float2(inv, inv);
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const float2 u = mul2_rn(mul2_rn(bf16x2_plus(rx[k].w[w], -mu, -mu), i2),
+                                         make_float2(gv[2 * w], gv[2 * w + 1]));
+                const float2 o = b != nullptr ? bf16x2_plus(bw.w[w], u.x, u.y) : u;
+                f[2 * w] = o.x;
+                f[2 * w + 1] = o.y;
+            }
+            st_stream(static_cast<char*>(y) + boff + (int64_t)c * 16, S::pack(f));
+        } else if (c < nchunks) {
             float f[V], gv[V], bv[V];
             S::unpack(rx[k], f);
             S::unpack(ld_reuse(static_cast<const char*>(g) + (int64_t)c * 16), gv);
