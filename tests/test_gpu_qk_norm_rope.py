@@ -195,9 +195,10 @@ def test_special_values_equal_unfused_composition(dtype):
             q, k = to_bf16(q), to_bf16(k)
         else:
             q, k = q.astype(np.float32), k.astype(np.float32)
-        qn, kn = _unfused(q, k, gq, gk, pos, om, r, 1.0, 0)
-        qd, kd = to_dev(q), to_dev(k)
-        gbe.gbe_qk_norm_rope(qd, qd, to_dev(gq), kd, kd, to_dev(gk), 1e-6, to_dev(pos), to_dev(om), r, 1.0, 0)
-        assert np.array_equal(bits(qd), bits(qn)), (T, D, r, "q")
-        assert np.array_equal(bits(kd), bits(kn)), (T, D, r, "k")
+        for eps in (1e-6, 0.0):  # eps = 0: the zero head's 1/rms is infinite, its output NaN
+            qn, kn = _unfused(q, k, gq, gk, pos, om, r, 1.0, 0, eps=eps)
+            qd, kd = to_dev(q), to_dev(k)
+            gbe.gbe_qk_norm_rope(qd, qd, to_dev(gq), kd, kd, to_dev(gk), eps, to_dev(pos), to_dev(om), r, 1.0, 0)
+            assert np.array_equal(bits(qd), bits(qn)), (T, D, r, eps, "q")
+            assert np.array_equal(bits(kd), bits(kn)), (T, D, r, eps, "k")
 
